@@ -1,0 +1,420 @@
+"""Benchmark: quantized Muon optimizer steps on one GB300 (replicas for N > 1).
+
+One step = the whole hot path: the blockwise 8-bit momentum update over every
+matrix, grouped Frobenius norms, batched Newton-Schulz (5 quintic
+iterations) and the weight update, with the MuonBP schedule (block NS on
+1 x 8 column tiles, full NS every 5th step).  Default workload: 4 layers of a
+Llama-8B-shaped model (q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096,
+down 4096x14336), 872,415,232 parameters, synthetic seeded gradients.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  ``value`` = parameters processed per second (Mparams/s)
+over K timed steps, inputs resident in HBM, timed with CUDA events and taken
+as the max over ranks.  Every step first copies that step's gradient batch
+into the gradient buffers (device-to-device copies, part of the timed
+region), because the step overwrites them.  The inputs (1.75 GB of gradients
+per step) are larger than L2.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "qMuon update HBM GB/s + Newton-Schulz TFLOP/s; Mparams/s per optimizer step"
+UPDATE_BYTES_PER_ELEM = 1 + 2 + 1 + 2 + 8.0 / 256   # q8 r/w, bf16 grad r/w, absmax r/w
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def ns_flops_of(rows, cols, iters):
+    m, n = min(rows, cols), max(rows, cols)
+    return iters * 2.0 * (2.0 * n * m * m + float(m) ** 3)
+
+
+def step_ns_flops(w, full):
+    tr, tc = (1, 1) if full else w.tile
+    tot = 0.0
+    for m in w.matrices:
+        tot += tr * tc * ns_flops_of(m.rows // tr, m.cols // tc, w.iters)
+    return tot
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle leg (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, budget_s=15.0):
+    """Time the oracle on a bounded sample of the workload's block step.
+
+    The momentum update (numpy, fp32 codec) runs on one whole matrix of each
+    shape and the Newton-Schulz (numpy, fp64) on one tile of each shape; the
+    per-parameter costs are added, weighted by how many parameters of the
+    workload have that shape.  Returns (Mparams/s, sample, cores, seconds)."""
+    import numpy as np
+    from oracle import codec, ns as ons
+
+    shapes = {}
+    for m in w.matrices:
+        shapes[(m.rows, m.cols)] = shapes.get((m.rows, m.cols), 0) + m.numel
+    tr, tc = w.tile if w.P != 1 else (1, 1)
+    rng = np.random.default_rng(0)
+    t_start = time.perf_counter()
+    sec_per_param = 0.0
+    done = []
+    for (rows, cols), weight in sorted(shapes.items(), key=lambda kv: kv[0][0] * kv[0][1]):
+        n = rows * cols
+        q8 = np.zeros(n, np.int8)
+        a = np.zeros((n + 255) // 256, np.float32)
+        g = codec.bf16_bits_from_f32(rng.standard_normal(n).astype(np.float32))
+        t0 = time.perf_counter()
+        r = codec.momentum_update(q8, a, g, w.beta)
+        t_upd = (time.perf_counter() - t0) / n
+        th, tw = rows // tr, cols // tc
+        M = codec.f32_from_bf16_bits(r.grad).reshape(rows, cols)[:th, :tw].astype(np.float64)
+        t0 = time.perf_counter()
+        ons.newton_schulz(M, iters=w.iters)
+        t_ns = (time.perf_counter() - t0) / (th * tw)
+        sec_per_param += (t_upd + t_ns) * weight / w.numel
+        done.append(f"{rows}x{cols} (update) / {th}x{tw} (NS)")
+        if time.perf_counter() - t_start > budget_s:
+            break
+    dt = time.perf_counter() - t_start
+    sample = ("block step, per shape: numpy fp32 codec on one whole matrix + fp64 Newton-Schulz on one "
+              f"{tr}x{tc} tile, per-parameter costs weighted by the workload's shape mix: " + "; ".join(done))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return 1.0 / sec_per_param / 1e6, sample, cores, dt
+
+
+# --------------------------------------------------------------------------
+# the GPU leg
+# --------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import memory_reduced_muon_gb300 as q
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workloads.get(args.workload)
+    if args.scale > 1:
+        w = workloads.scaled(w, args.scale)
+    mats = w.matrices
+    n_params = w.numel
+    stream = torch.cuda.current_stream()
+
+    states = [workloads.zero_state(m, w.q8_kind, device=dev) for m in mats]
+    grads = [torch.empty(m.rows, m.cols, dtype=torch.bfloat16, device=dev) for m in mats]
+    weights = [workloads.make_weight(w, i, device=dev) for i in range(len(mats))]
+    pool = [[workloads.make_grad(w, i, s + 1, device=dev) for i in range(len(mats))] for s in range(2)]
+    plan = q.qmuon_plan_create([(s[0], s[1], g, m.rows, m.cols) for s, g, m in zip(states, grads, mats)],
+                               w.q8_kind, "bf16", tile=w.tile)
+    info = q.qmuon_plan_info(plan)
+    ws = torch.empty(q.qmuon_workspace_size(plan, q.QMUON_WS_STEP), dtype=torch.uint8, device=dev)
+    sums = torch.zeros(max(info["n_full_groups"], info["n_block_groups"]), dtype=torch.float32, device=dev)
+
+    def refill(t):
+        src = pool[t % 2]
+        for g, s in zip(grads, src):
+            g.copy_(s, non_blocking=True)
+
+    def step(t):
+        q.qmuon_step(plan, t, w.P, w.beta, w.eta_full, w.eta_block, weights, w.coeffs, w.iters, sums, ws,
+                     stream=stream)
+
+    # warm-up (also builds the Newton-Schulz tables of both step kinds)
+    t = 0
+    for _ in range(max(args.warmup, 1)):
+        t += 1
+        refill(t)
+        step(t)
+    if w.P > 1 and not any((t0 % w.P) == 0 for t0 in range(1, t + 1)):
+        step(w.P)   # make sure a full step has been seen before timing
+    q.qmuon_sync_status(ws, stream)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ----
+    t_first = t + 1
+    n_full = sum(1 for k in range(t_first, t_first + args.steps) if w.P and k % w.P == 0)
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+        sel = f"{torch.cuda.get_device_properties(local).pci_domain_id:08X}:{bus:02X}:{torch.cuda.get_device_properties(local).pci_device_id:02X}.0"
+    except Exception:
+        sel = str(local)
+    sampler = ClockSampler(sel)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        refill(t)
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    q.qmuon_sync_status(ws, stream)
+    ms_max = max_over_ranks(ms, world)
+    value = world * n_params * args.steps / (ms_max / 1e3) / 1e6
+
+    # ---- per-kernel timing: the update alone and the Newton-Schulz engine alone ----
+    plan_u = q.qmuon_plan_create([(s[0], s[1], g, m.rows, m.cols) for s, g, m in zip(states, grads, mats)],
+                                 w.q8_kind, "bf16")
+    ws_u = torch.empty(q.qmuon_workspace_size(plan_u), dtype=torch.uint8, device=dev)
+    inv_u = torch.zeros(len(mats), dtype=torch.float32, device=dev)
+    reps = max(3, args.steps)
+    for _ in range(2):
+        q.qmuon_update_multi_normalize_groups(plan_u, w.beta, 2, None, inv_u, ws_u, stream=stream)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    u0.record(stream)
+    for _ in range(reps):
+        q.qmuon_update_multi_normalize_groups(plan_u, w.beta, 2, None, inv_u, ws_u, stream=stream)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    upd_ms = u0.elapsed_time(u1) / reps
+    upd_bytes = UPDATE_BYTES_PER_ELEM * n_params
+    upd_gbs = upd_bytes / (upd_ms / 1e3) / 1e9
+
+    def ns_problems(full):
+        tr, tc = (1, 1) if full else w.tile
+        probs = []
+        k = 0
+        for m, g in zip(mats, grads):
+            th, tw = m.rows // tr, m.cols // tc
+            for i in range(tr):
+                for j in range(tc):
+                    off = (i * th * m.cols + j * tw) * 2
+                    probs.append(q.ns_problem(g.data_ptr() + off, th, tw, ld=m.cols,
+                                              inv_norm=inv_u.data_ptr() + 4 * (k % len(mats))))
+                    k += 1
+        return probs
+
+    ns_ms, ns_flop = {}, {}
+    for full in ([False, True] if w.P != 1 else [True]):
+        probs = ns_problems(full)
+        ws_n = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device=dev)
+        q.qmuon_newton_schulz_batched(probs, w.iters, w.coeffs, ws_n, stream=stream)
+        torch.cuda.synchronize()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nrep = 3
+        n0.record(stream)
+        for _ in range(nrep):
+            q.qmuon_newton_schulz_batched(probs, w.iters, w.coeffs, ws_n, stream=stream)
+        n1.record(stream)
+        torch.cuda.synchronize()
+        q.qmuon_sync_status(ws_n, stream)
+        key = "full" if full else "block"
+        ns_ms[key] = n0.elapsed_time(n1) / nrep
+        ns_flop[key] = step_ns_flops(w, full)
+        del ws_n
+
+    # e2e: host gradients in pinned memory, copied in every step; the group
+    # sums (the step's metric) read back every step
+    host_pool = [[g.cpu().pin_memory() for g in batch] for batch in pool]
+    torch.cuda.synchronize()
+    e2e_steps = max(2, min(args.steps, 5))
+    h2d = sum(g.numel() * g.element_size() for g in grads)
+    ngr = info["n_block_groups"] if w.P != 1 else info["n_full_groups"]
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        t += 1
+        for g, hsrc in zip(grads, host_pool[t % 2]):
+            g.copy_(hsrc, non_blocking=True)
+        step(t)
+        _ = sums.cpu()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e_value = world * n_params * e2e_steps / e2e_s / 1e6
+
+    # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
+    launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
+    return dict(value=value, ms=ms_max, clocks=clocks, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
+                ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=4 * ngr, n_full=n_full,
+                launches=launches_per_step * args.steps, n_params=n_params, w=w)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=4)
+    ap.add_argument("--scale", type=int, default=1, help="divide matrix sizes (profiling captures only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    w = workloads.get(args.workload)
+    wl_name = {4: "llama8b_x4_muonbp", 1: "single_512", 2: "decoder2048_x24_update", 3: "qkv_mlp_grouped",
+               5: "llama8b_x4_mxfp8"}[args.workload]
+    config = {"workload": wl_name, "description": w.name, "params": w.numel, "matrices": len(w.matrices),
+              "P": w.P, "tile": list(w.tile), "ns_iters": w.iters, "beta": w.beta,
+              "l2": "inputs larger than L2 (1.75 GB of bf16 gradients per step)", "parallelism": f"replicas x{world}"}
+    if args.scale > 1:
+        config["scale"] = f"1/{args.scale} (profiling only)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, sample, cores, dt = oracle_sample(w, budget_s=20.0)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "Mparams/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.numel / (v * 1e6) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 codec / f64 NS",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "Mparams/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": v, "unit": "Mparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    r = run_gpu(args, world, rank, local)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    traffic = load_traffic()
+    w = r["w"]
+    # dominant kernel family: the Newton-Schulz GEMMs (block steps dominate a P=5 schedule)
+    key = "block" if "block" in r["ns_ms"] else "full"
+    ns_tflops = {k: r["ns_flop"][k] / (r["ns_ms"][k] / 1e3) / 1e12 for k in r["ns_ms"]}
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    roof = {"bound": "tensor", "kernel": f"ns_gemm ({key} step, 15 launches per call)",
+            "achieved": ns_tflops[key], "peak": peak_t, "unit": "TFLOP/s", "frac": ns_tflops[key] / peak_t,
+            "peak_source": f"bf16_tflops_sustained of {peak_src}",
+            "traffic": traffic.get(f"ns_{key}_bytes_per_call"),
+            "flops_per_call": r["ns_flop"][key], "ms_per_call": r["ns_ms"][key]}
+    upd_roof = {"bound": "hbm", "achieved": r["upd_gbs"], "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": r["upd_gbs"] / float(peaks["hbm_gbs"]), "frac_of_8000": r["upd_gbs"] / 8000.0,
+                "bytes_per_launch": r["upd_bytes"], "ms_per_launch": r["upd_ms"],
+                "traffic": traffic.get("update_bytes_per_launch")}
+    line = {"metric": METRIC, "value": r["value"], "unit": "Mparams/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (NS operands, fp32 accumulate); int8 state, fp32 codec",
+            "data": "synthetic (seeded gradients, zero initial state, N(0,0.02^2) weights)", "config": config,
+            "full_steps_timed": r["n_full"],
+            "update_gbs": r["upd_gbs"], "ns_tflops": ns_tflops,
+            "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
+            "e2e": {"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"]}
+    if not args.no_cpu_baseline:
+        v, sample, cores, dt = oracle_sample(w, budget_s=15.0)
+        line["cpu_baseline"] = {"value": v, "unit": "Mparams/s", "cores": cores, "kind": "oracle", "sample": sample,
+                                "seconds": dt}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+/*
+ * qmuon -- quantized Muon optimizer step for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is either a host pointer (H) or a device
+ * pointer (D), as marked.  All device memory is owned by the caller except
+ * the small metadata tables a qmuon_plan owns.  Every entry that takes a
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
+ * only enqueues work on it and returns; results are ready when the stream
+ * reaches that point.  Every entry validates its arguments on the host first
+ * and launches nothing when validation fails; no entry aborts or throws.
+ *
+ * Layouts: tensors are dense, row-major and contiguous.  q8 codes and
+ * gradients must start on a 16-byte boundary; absmax on a 4-byte boundary.
+ * A tensor has rows*cols elements, split into 256-element quantization
+ * blocks in flat order; the last block may be partial.
+ *
+ * Concurrency: calls that share a workspace must not overlap on the GPU
+ * (enqueue them on one stream).  Distinct plans/workspaces are independent.
+ */
+#ifndef QMUON_H_
+#define QMUON_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QMUON_API __attribute__((visibility("default")))
+#else
+#define QMUON_API
+#endif
+
+#define QMUON_BLOCK 256          /* elements per quantization block          */
+#define QMUON_SCALE_BLOCK 32     /* elements per MXFP8 carrier scale (a row) */
+
+typedef enum {
+  QMUON_OK = 0,
+  QMUON_ERR_INVALID_ARGUMENT = 1,   /* NULL/misaligned pointer, bad size or enum */
+  QMUON_ERR_MISALIGNED_SEGMENT = 2, /* norm segment not on 256-element blocks   */
+  QMUON_ERR_UNSUPPORTED = 3,        /* valid request this build does not serve   */
+  QMUON_ERR_WORKSPACE_TOO_SMALL = 4,
+  QMUON_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed         */
+  QMUON_ERR_TIMEOUT = 6             /* a kernel's bounded wait expired (see qmuon_sync_status) */
+} qmuon_status;
+
+typedef enum { QMUON_Q8_INT8 = 0, QMUON_Q8_UINT8 = 1 } qmuon_q8_kind;
+typedef enum { QMUON_BF16 = 0, QMUON_FP16 = 1, QMUON_FP32 = 2 } qmuon_dtype;
+
+/* One optimizer tensor (a matrix of momentum state).
+ *   q8     D  rows*cols codes: int8 q, or uint8 q+128 (offset binary)
+ *   absmax D  ceil(rows*cols/256) fp32 block maxima
+ *   grad   D  rows*cols gradient elements of the plan's dtype; IN: gradient,
+ *             OUT: the new momentum m (update entries) or the orthogonalised
+ *             update U (qmuon_step)
+ * State format: "Quantized Muon Momentum", section "What Exists". */
+typedef struct {
+  void* q8;
+  float* absmax;
+  void* grad;
+  int64_t rows;
+  int64_t cols;
+} qmuon_tensor;
+
+/* A run of one tensor's flat elements that belongs to a norm group
+ * ("Quantized Muon Momentum", section "Grouped QKV And Sharding").
+ * `start` must be a multiple of 256 and `start + length` a multiple of 256
+ * or the tensor's element count; otherwise QMUON_ERR_MISALIGNED_SEGMENT.
+ * Group ids are dense in [0, n_groups).  A block may belong to at most one
+ * segment; blocks in no segment are updated but not summed. */
+typedef struct {
+  int32_t tensor_index;
+  int32_t group_id;
+  int64_t start;
+  int64_t length;
+} qmuon_norm_segment;
+
+typedef struct qmuon_plan qmuon_plan;
+
+/* Build a reusable plan over `n_tensors` tensors (H array, copied).
+ *   segments/n_segments  H  norm groups for qmuon_update_multi_normalize_groups;
+ *                           NULL/0 = one group per tensor (n_groups must then
+ *                           equal n_tensors, or be 0 to mean that)
+ *   tile_r, tile_c          MuonBP block tiling used by qmuon_step's block
+ *                           steps: every tensor is cut into tile_r x tile_c
+ *                           tiles of (rows/tile_r) x (cols/tile_c); with
+ *                           tile_c > 1 the tile width must be a multiple of
+ *                           256, with tile_c == 1 each tile's element count
+ *   out                  H  receives the plan (freed by qmuon_plan_destroy)
+ * The plan uploads its tables once (one H2D copy) to the current device and
+ * is tied to that device.  Allocates device memory (small tables) only. */
+QMUON_API qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n_tensors,
+                               qmuon_q8_kind q8_kind, qmuon_dtype grad_dtype,
+                               const qmuon_norm_segment* segments, int32_t n_segments,
+                               int32_t n_groups, int32_t tile_r, int32_t tile_c,
+                               qmuon_plan** out);
+QMUON_API void qmuon_plan_destroy(qmuon_plan* plan);
+
+/* Counts a caller needs to size outputs: the plan's segment groups, the
+ * full-step groups (one per tensor) and block-step groups (tiles). */
+QMUON_API qmuon_status qmuon_plan_info(const qmuon_plan* plan, int64_t* n_blocks, int32_t* n_groups,
+                             int32_t* n_full_groups, int32_t* n_block_groups);
+
+/* Which entry a workspace is sized for. */
+typedef enum { QMUON_WS_UPDATE = 0, QMUON_WS_STEP = 1 } qmuon_ws_kind;
+
+/* Bytes of device workspace the entry needs (0 on a NULL plan).  The
+ * workspace is scratch: its contents between calls are unspecified, except
+ * that it must not be shared by calls in flight at the same time. */
+QMUON_API size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind which);
+
+/* The blockwise 8-bit momentum update over every tensor of the plan in one
+ * launch ("Quantized Muon Momentum", section "Algorithm", steps 1-9):
+ * dequantize, m = beta*old + (1-beta)*grad in fp32, m written over grad,
+ * new absmax, symmetric nearest requantization to [-127, 127], and the
+ * per-group sum of m*m reduced across the grid in the same launch.
+ *   normalize_mode  0: no normalisation (sums/inverse norms still written to
+ *                      the non-NULL outputs)
+ *                   1: in place -- every grouped block of grad is then
+ *                      scaled by its group's inverse norm (second pass)
+ *                   2: deferred -- inverse norms only, for a later
+ *                      qmuon_newton_schulz_batched (group_inv_norm required)
+ *   group_sumsq     D  [n_groups] fp32 sum of m*m per group, or NULL
+ *   group_inv_norm  D  [n_groups] fp32 1/(sqrt(sum)+1e-7), or NULL
+ *   ws, ws_bytes    D  workspace of qmuon_workspace_size(plan, QMUON_WS_UPDATE)
+ * q8 codes and absmax are bit-exact with the reference arithmetic (no FMA
+ * contraction); sums are accumulated in fp64 across blocks. */
+QMUON_API qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* plan, float beta,
+                                                 int32_t normalize_mode, float* group_sumsq,
+                                                 float* group_inv_norm, void* ws,
+                                                 size_t ws_bytes, void* stream);
+
+/* Workspace bytes of qmuon_update_mxfp8_carrier for a rows x cols tensor. */
+QMUON_API size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols);
+
+/* q8 state + grad -> q8 state + normalised rowwise MXFP8 carrier
+ * ("Quantized Muon Momentum", section "Wave18B MXFP8 Carrier Probe").
+ *   tensor     H  one tensor (q8/absmax D, updated in place; grad D, READ ONLY)
+ *   payload    D  rows x cols uint8 E4M3 codes of m / 2^(scale-127)
+ *   scale_inv  D  rows x (cols/32) uint8 E8M0 exponents: the smallest power
+ *                 of two with amax/2^(e-127) <= 448 per 32 row elements
+ *   inv_norm   D  one fp32, 1/(sqrt(sum m*m)+1e-7)
+ * cols must be a multiple of 32 (else QMUON_ERR_UNSUPPORTED). */
+QMUON_API qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
+                                        qmuon_dtype grad_dtype, float beta, uint8_t* payload,
+                                        uint8_t* scale_inv, float* inv_norm, void* ws,
+                                        size_t ws_bytes, void* stream);
+
+/* Input of one Newton-Schulz problem. */
+typedef enum { QMUON_NS_BF16 = 0, QMUON_NS_MXFP8 = 1 } qmuon_ns_input;
+
+/* One matrix to orthogonalise.
+ *   x          D  bf16 rows x cols, row stride ld elements (ld >= cols,
+ *                 ld % 8 == 0, x 16-byte aligned); IN: M, OUT: NS(inv*M)
+ *                 (MXFP8 input: OUT only)
+ *   inv_norm   D  fp32 scalar applied to the input, or NULL for 1
+ *   input      QMUON_NS_BF16, or QMUON_NS_MXFP8 with payload/scale_inv:
+ *   payload    D  rows x cols E4M3 codes (row stride cols), cols % 32 == 0
+ *   scale_inv  D  rows x (cols/32) E8M0 bytes */
+typedef struct {
+  void* x;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+  const float* inv_norm;
+  int32_t input;
+  int32_t reserved;
+  const uint8_t* payload;
+  const uint8_t* scale_inv;
+} qmuon_ns_problem;
+
+/* Workspace bytes for qmuon_newton_schulz_batched on these problems. */
+QMUON_API size_t qmuon_ns_workspace_size(const qmuon_ns_problem* problems, int32_t n_problems);
+
+/* Quintic Newton-Schulz on a batch of independent matrices, in place:
+ * per iteration A = X X^T, B = b*A + c*A*A, X <- a*X + B*X (three products,
+ * "NVIDIA impulsa optimizadores avanzados ... con Megatron", section
+ * "Newton-Schulz distribuido"; the first two are symmetric, section "SYRK y
+ * reducción fusionada").  A matrix with rows > cols is processed as its
+ * transpose.  tcgen05 tensor cores, bf16 operands, fp32 accumulation.
+ *   problems  H  n_problems entries (copied)
+ *   iters     >= 1
+ *   coeffs    H  (a, b, c) */
+QMUON_API qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* problems, int32_t n_problems,
+                                         int32_t iters, const float coeffs[3], void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/* One MuonBP quantized Muon step over every tensor of the plan ("MuonBP:
+ * Faster Muon via Block-Periodic Orthogonalization", section "整体框架"):
+ * the momentum update of qmuon_update_multi_normalize_groups, then, when
+ * t mod P == 0 (a full step; P == 1 is plain Muon), Newton-Schulz on each
+ * whole matrix with one norm group per tensor and W <- W - eta_full*U;
+ * otherwise (a block step; P == 0 means never full, i.e. BlockMuon)
+ * Newton-Schulz on every tile of the plan's tiling, each with its own norm,
+ * and W <- W - eta_block*U.  U (bf16) is left in each grad buffer.
+ *   t          1-based step index
+ *   weights    H  n_tensors device pointers (D) to fp32 rows x cols master
+ *                 weights, updated in place
+ *   group_sumsq D [n groups of this step] fp32 sums of m*m, or NULL */
+QMUON_API qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
+                        float eta_full, float eta_block, float* const* weights,
+                        const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Synchronise `stream` and report a kernel-side error recorded in `ws`
+ * (QMUON_ERR_TIMEOUT when a bounded wait expired), then clear it. */
+QMUON_API qmuon_status qmuon_sync_status(void* ws, void* stream);
+
+/* Static description of a status code (never NULL). */
+QMUON_API const char* qmuon_status_string(qmuon_status status);
+
+/* Library version, e.g. "qmuon 0.1 sm_103a". */
+QMUON_API const char* qmuon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMUON_H_ */

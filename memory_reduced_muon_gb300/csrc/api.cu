@@ -1,0 +1,531 @@
+// C-ABI entry points of qmuon (declared in include/qmuon.h).
+//
+// Host side only: argument validation (before any CUDA call), plan tables,
+// workspace carving and launches.  Every device computation happens in the
+// kernels of update.cu and ns_gemm.cu.
+#include <algorithm>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <vector>
+
+#include "qm_internal.h"
+#include "qm_ns.h"
+
+using namespace qm;
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t nblocks(int64_t numel) { return (numel + kBlock - 1) / kBlock; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool valid_q8(int v) { return v == QMUON_Q8_INT8 || v == QMUON_Q8_UINT8; }
+inline bool valid_dtype(int v) { return v == QMUON_BF16 || v == QMUON_FP16 || v == QMUON_FP32; }
+
+// Host copy of one group layout (uploaded into the plan's device table).
+struct HostLayout {
+  int32_t n_groups = 0;
+  std::vector<int32_t> block_group;     // [nb]
+  std::vector<int32_t> cta_slot_begin;  // [grid+1]
+  std::vector<int32_t> slot_group;      // [n_slots]
+  std::vector<int32_t> grp_ptr;         // [n_groups+1]
+  std::vector<int32_t> grp_slots;       // [n_slots]
+};
+
+// Slots: for every CTA, one per distinct group among its blocks (ascending).
+void build_slots(HostLayout& L, int32_t grid, int64_t chunk, int64_t nb) {
+  L.cta_slot_begin.assign(grid + 1, 0);
+  L.slot_group.clear();
+  std::vector<std::vector<int32_t>> per_group(L.n_groups);
+  std::vector<int32_t> seen;
+  for (int32_t c = 0; c < grid; ++c) {
+    L.cta_slot_begin[c] = (int32_t)L.slot_group.size();
+    const int64_t b0 = (int64_t)c * chunk, b1 = std::min(nb, b0 + chunk);
+    seen.clear();
+    for (int64_t b = b0; b < b1; ++b) {
+      const int32_t g = L.block_group[b];
+      if (g >= 0 && (seen.empty() || seen.back() != g)) seen.push_back(g);
+    }
+    std::sort(seen.begin(), seen.end());
+    seen.erase(std::unique(seen.begin(), seen.end()), seen.end());
+    for (int32_t g : seen) {
+      per_group[g].push_back((int32_t)L.slot_group.size());
+      L.slot_group.push_back(g);
+    }
+  }
+  L.cta_slot_begin[grid] = (int32_t)L.slot_group.size();
+  L.grp_ptr.assign(L.n_groups + 1, 0);
+  L.grp_slots.clear();
+  for (int32_t g = 0; g < L.n_groups; ++g) {
+    L.grp_ptr[g] = (int32_t)L.grp_slots.size();
+    L.grp_slots.insert(L.grp_slots.end(), per_group[g].begin(), per_group[g].end());
+  }
+  L.grp_ptr[L.n_groups] = (int32_t)L.grp_slots.size();
+}
+
+qmuon_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMUON_OK : QMUON_ERR_CUDA; }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// the plan
+// ---------------------------------------------------------------------------
+struct qmuon_plan {
+  int device = 0;
+  int num_sms = 0;
+  std::vector<qmuon_tensor> tensors;
+  qmuon_q8_kind q8 = QMUON_Q8_INT8;
+  qmuon_dtype dt = QMUON_BF16;
+  int32_t tile_r = 1, tile_c = 1;
+  int64_t nb_total = 0;
+  std::vector<int64_t> tensor_begin;  // [n+1]
+  int32_t grid = 0;
+  int64_t chunk = 0;
+  // layouts: 0 = segments (qmuon_update_multi_normalize_groups), 1 = one group
+  // per tensor (full steps), 2 = tiles (block steps)
+  GroupLayout layout[3];
+  int32_t n_slots_max = 0;
+  void* d_table = nullptr;            // one device allocation for every table
+  UpdTensor* d_tensors = nullptr;
+  int64_t* d_tensor_begin = nullptr;
+  ns::StepTables* ns_full = nullptr;  // Newton-Schulz problem sets of qmuon_step
+  ns::StepTables* ns_block = nullptr;
+};
+
+namespace {
+
+qmuon_status validate_tensor(const qmuon_tensor& t, qmuon_dtype dt) {
+  if (t.rows < 0 || t.cols < 0) return QMUON_ERR_INVALID_ARGUMENT;
+  if (t.rows > 0 && t.cols > (((int64_t)1 << 40) / t.rows)) return QMUON_ERR_INVALID_ARGUMENT;
+  const int64_t n = t.rows * t.cols;
+  if (n == 0) return QMUON_OK;
+  if (!t.q8 || !t.absmax || !t.grad) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(t.q8, 16) || !aligned(t.grad, 16) || !aligned(t.absmax, 4)) return QMUON_ERR_INVALID_ARGUMENT;
+  (void)dt;
+  return QMUON_OK;
+}
+
+// Update launch geometry: whole waves of resident CTAs, at most kMaxChunk
+// blocks per CTA and at least 16 (one per half-warp).
+void update_geometry(int64_t nb, int sms, int per_sm, int32_t* grid, int64_t* chunk) {
+  const int64_t wave = (int64_t)std::max(1, sms) * std::max(1, per_sm);
+  int64_t g;
+  if (nb <= wave * 16) {
+    g = std::max<int64_t>(1, (nb + 15) / 16);
+  } else {
+    const int64_t waves = (nb + wave * kMaxChunk - 1) / (wave * kMaxChunk);
+    g = wave * waves;
+  }
+  int64_t c = (nb + g - 1) / g;
+  if (c < 1) c = 1;
+  g = (nb + c - 1) / c;
+  if (g < 1) g = 1;
+  *grid = (int32_t)g;
+  *chunk = c;
+}
+
+}  // namespace
+
+extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n_tensors,
+                                          qmuon_q8_kind q8_kind, qmuon_dtype grad_dtype,
+                                          const qmuon_norm_segment* segments, int32_t n_segments,
+                                          int32_t n_groups, int32_t tile_r, int32_t tile_c,
+                                          qmuon_plan** out) {
+  // ---- host validation: nothing below touches CUDA until it all passes ----
+  if (!out) return QMUON_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  if (!tensors || n_tensors <= 0) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!valid_q8(q8_kind) || !valid_dtype(grad_dtype)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (tile_r < 1 || tile_c < 1) return QMUON_ERR_INVALID_ARGUMENT;
+  if (n_segments < 0 || (n_segments > 0 && !segments)) return QMUON_ERR_INVALID_ARGUMENT;
+  const bool per_tensor = (segments == nullptr || n_segments == 0);
+  if (per_tensor && n_groups != 0 && n_groups != n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!per_tensor && n_groups <= 0) return QMUON_ERR_INVALID_ARGUMENT;
+  std::vector<int64_t> begin(n_tensors + 1, 0);
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const qmuon_status s = validate_tensor(tensors[i], grad_dtype);
+    if (s != QMUON_OK) return s;
+    begin[i + 1] = begin[i] + nblocks(tensors[i].rows * tensors[i].cols);
+  }
+  const int64_t nb = begin[n_tensors];
+  if (nb == 0 || nb > ((int64_t)1 << 31) - 1) return QMUON_ERR_INVALID_ARGUMENT;
+  // tiles of the MuonBP block steps must be whole 256-element runs
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t R = tensors[i].rows, C = tensors[i].cols;
+    if (R * C == 0) continue;
+    if (R % tile_r || C % tile_c) return QMUON_ERR_INVALID_ARGUMENT;
+    if (tile_c > 1) {
+      if (C % kBlock || (C / tile_c) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
+    } else if (tile_r > 1) {
+      if (((R / tile_r) * C) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
+    }
+  }
+
+  std::unique_ptr<qmuon_plan> P(new (std::nothrow) qmuon_plan);
+  if (!P) return QMUON_ERR_INVALID_ARGUMENT;
+  P->tensors.assign(tensors, tensors + n_tensors);
+  P->q8 = q8_kind;
+  P->dt = grad_dtype;
+  P->tile_r = tile_r;
+  P->tile_c = tile_c;
+  P->nb_total = nb;
+  P->tensor_begin = begin;
+
+  // ---- group layouts (host) ----
+  HostLayout H[3];
+  H[1].n_groups = n_tensors;
+  H[1].block_group.resize(nb);
+  for (int32_t i = 0; i < n_tensors; ++i)
+    std::fill(H[1].block_group.begin() + begin[i], H[1].block_group.begin() + begin[i + 1], i);
+  if (per_tensor) {
+    H[0].n_groups = n_tensors;
+    H[0].block_group = H[1].block_group;
+  } else {
+    H[0].n_groups = n_groups;
+    H[0].block_group.assign(nb, -1);
+    for (int32_t s = 0; s < n_segments; ++s) {
+      const qmuon_norm_segment& g = segments[s];
+      if (g.tensor_index < 0 || g.tensor_index >= n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
+      if (g.group_id < 0 || g.group_id >= n_groups) return QMUON_ERR_INVALID_ARGUMENT;
+      const int64_t n = tensors[g.tensor_index].rows * tensors[g.tensor_index].cols;
+      if (g.start < 0 || g.length <= 0 || g.start + g.length > n) return QMUON_ERR_INVALID_ARGUMENT;
+      const int64_t end = g.start + g.length;
+      if (g.start % kBlock || (end % kBlock && end != n)) return QMUON_ERR_MISALIGNED_SEGMENT;
+      for (int64_t b = begin[g.tensor_index] + g.start / kBlock,
+                   e = begin[g.tensor_index] + nblocks(end); b < e; ++b) {
+        if (H[0].block_group[b] >= 0) return QMUON_ERR_INVALID_ARGUMENT;  // overlap
+        H[0].block_group[b] = g.group_id;
+      }
+    }
+  }
+  {
+    int32_t gbase = 0;
+    H[2].block_group.assign(nb, -1);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const int64_t R = tensors[i].rows, C = tensors[i].cols;
+      if (R * C == 0) continue;
+      const int64_t th = R / tile_r, tw = C / tile_c;
+      for (int64_t r = 0; r < R; ++r)
+        for (int64_t c0 = 0; c0 < C; c0 += tw) {
+          const int32_t g = gbase + (int32_t)((r / th) * tile_c + c0 / tw);
+          const int64_t e0 = r * C + c0, e1 = e0 + tw;
+          for (int64_t b = e0 / kBlock; b < nblocks(e1); ++b) H[2].block_group[begin[i] + b] = g;
+        }
+      gbase += tile_r * tile_c;
+    }
+    H[2].n_groups = gbase;
+  }
+
+  // ---- device properties and geometry ----
+  if (cudaGetDevice(&P->device) != cudaSuccess) return QMUON_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
+    return QMUON_ERR_CUDA;
+  const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
+  if (per_sm <= 0) return QMUON_ERR_CUDA;
+  update_geometry(nb, P->num_sms, per_sm, &P->grid, &P->chunk);
+  for (auto& h : H) build_slots(h, P->grid, P->chunk, nb);
+
+  // ---- one device allocation for every table, one H2D copy ----
+  std::vector<UpdTensor> ut(n_tensors);
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    ut[i].q8 = tensors[i].q8;
+    ut[i].absmax = tensors[i].absmax;
+    ut[i].grad = tensors[i].grad;
+    ut[i].payload = nullptr;
+    ut[i].scale = nullptr;
+    ut[i].numel = tensors[i].rows * tensors[i].cols;
+    ut[i].block_begin = begin[i];
+  }
+  std::vector<unsigned char> blob;
+  auto put = [&blob](const void* src, size_t bytes) {
+    const size_t off = align_up(blob.size(), 256);
+    blob.resize(off + bytes);
+    if (bytes) std::memcpy(blob.data() + off, src, bytes);
+    return off;
+  };
+  const size_t o_t = put(ut.data(), ut.size() * sizeof(UpdTensor));
+  const size_t o_b = put(begin.data(), begin.size() * sizeof(int64_t));
+  size_t o_l[3][5];
+  for (int l = 0; l < 3; ++l) {
+    o_l[l][0] = put(H[l].block_group.data(), H[l].block_group.size() * 4);
+    o_l[l][1] = put(H[l].cta_slot_begin.data(), H[l].cta_slot_begin.size() * 4);
+    o_l[l][2] = put(H[l].slot_group.data(), H[l].slot_group.size() * 4);
+    o_l[l][3] = put(H[l].grp_ptr.data(), H[l].grp_ptr.size() * 4);
+    o_l[l][4] = put(H[l].grp_slots.data(), H[l].grp_slots.size() * 4);
+  }
+  if (cudaMalloc(&P->d_table, blob.size()) != cudaSuccess) return QMUON_ERR_CUDA;
+  if (cudaMemcpy(P->d_table, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(P->d_table);
+    return QMUON_ERR_CUDA;
+  }
+  unsigned char* base = static_cast<unsigned char*>(P->d_table);
+  P->d_tensors = reinterpret_cast<UpdTensor*>(base + o_t);
+  P->d_tensor_begin = reinterpret_cast<int64_t*>(base + o_b);
+  for (int l = 0; l < 3; ++l) {
+    GroupLayout& G = P->layout[l];
+    G.n_groups = H[l].n_groups;
+    G.n_slots = (int32_t)H[l].slot_group.size();
+    G.block_group = reinterpret_cast<const int32_t*>(base + o_l[l][0]);
+    G.cta_slot_begin = reinterpret_cast<const int32_t*>(base + o_l[l][1]);
+    G.slot_group = reinterpret_cast<const int32_t*>(base + o_l[l][2]);
+    G.grp_ptr = reinterpret_cast<const int32_t*>(base + o_l[l][3]);
+    G.grp_slots = reinterpret_cast<const int32_t*>(base + o_l[l][4]);
+    P->n_slots_max = std::max(P->n_slots_max, G.n_slots);
+  }
+  *out = P.release();
+  return QMUON_OK;
+}
+
+extern "C" void qmuon_plan_destroy(qmuon_plan* plan) {
+  if (!plan) return;
+  if (plan->d_table) cudaFree(plan->d_table);
+  ns::destroy_step_tables(plan->ns_full);
+  ns::destroy_step_tables(plan->ns_block);
+  delete plan;
+}
+
+extern "C" qmuon_status qmuon_plan_info(const qmuon_plan* plan, int64_t* n_blocks, int32_t* n_groups,
+                                        int32_t* n_full_groups, int32_t* n_block_groups) {
+  if (!plan) return QMUON_ERR_INVALID_ARGUMENT;
+  if (n_blocks) *n_blocks = plan->nb_total;
+  if (n_groups) *n_groups = plan->layout[0].n_groups;
+  if (n_full_groups) *n_full_groups = plan->layout[1].n_groups;
+  if (n_block_groups) *n_block_groups = plan->layout[2].n_groups;
+  return QMUON_OK;
+}
+
+namespace {
+
+// Workspace carving: [header | partials | group sums | group inverse norms | NS]
+struct UpdWs {
+  WsHeader* header;
+  double* partials;
+  float* sumsq;
+  float* inv;
+  unsigned char* ns;
+  size_t ns_bytes;
+};
+
+size_t update_ws_bytes(const qmuon_plan* p) {
+  int32_t gmax = 0;
+  for (const auto& l : p->layout) gmax = std::max(gmax, l.n_groups);
+  return kWsHeader + align_up((size_t)std::max(p->n_slots_max, 1) * 8, 256) +
+         2 * align_up((size_t)std::max(gmax, 1) * 4, 256);
+}
+
+UpdWs carve(const qmuon_plan* p, void* ws, size_t ws_bytes) {
+  int32_t gmax = 0;
+  for (const auto& l : p->layout) gmax = std::max(gmax, l.n_groups);
+  unsigned char* b = static_cast<unsigned char*>(ws);
+  UpdWs w;
+  w.header = reinterpret_cast<WsHeader*>(b);
+  size_t off = kWsHeader;
+  w.partials = reinterpret_cast<double*>(b + off);
+  off += align_up((size_t)std::max(p->n_slots_max, 1) * 8, 256);
+  w.sumsq = reinterpret_cast<float*>(b + off);
+  off += align_up((size_t)std::max(gmax, 1) * 4, 256);
+  w.inv = reinterpret_cast<float*>(b + off);
+  off += align_up((size_t)std::max(gmax, 1) * 4, 256);
+  w.ns = b + off;
+  w.ns_bytes = ws_bytes > off ? ws_bytes - off : 0;
+  return w;
+}
+
+UpdLaunch make_launch(const qmuon_plan* p, int layout, float beta, const UpdWs& w,
+                      float* sumsq, float* inv) {
+  UpdLaunch L{};
+  L.tensors = p->d_tensors;
+  L.tensor_begin = p->d_tensor_begin;
+  L.n_tensors = (int32_t)p->tensors.size();
+  L.nb_total = p->nb_total;
+  L.chunk = p->chunk;
+  L.grid = p->grid;
+  L.beta = beta;
+  L.layout = p->layout[layout];
+  L.partials = w.partials;
+  L.header = w.header;
+  L.group_sumsq = sumsq;
+  L.group_inv = inv;
+  return L;
+}
+
+}  // namespace
+
+extern "C" size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind which) {
+  if (!plan) return 0;
+  size_t b = update_ws_bytes(plan);
+  if (which == QMUON_WS_STEP) {
+    const size_t a = ns::step_workspace_bytes(plan->tensors.data(), (int32_t)plan->tensors.size(), 1, 1);
+    const size_t c = ns::step_workspace_bytes(plan->tensors.data(), (int32_t)plan->tensors.size(),
+                                              plan->tile_r, plan->tile_c);
+    b += std::max(a, c);
+  }
+  return b;
+}
+
+extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* plan, float beta,
+                                                            int32_t normalize_mode,
+                                                            float* group_sumsq, float* group_inv_norm,
+                                                            void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+  if (normalize_mode < 0 || normalize_mode > 2) return QMUON_ERR_INVALID_ARGUMENT;
+  if (normalize_mode == 2 && !group_inv_norm) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < update_ws_bytes(plan)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  if ((group_sumsq && !aligned(group_sumsq, 4)) || (group_inv_norm && !aligned(group_inv_norm, 4)))
+    return QMUON_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const UpdWs w = carve(plan, ws, ws_bytes);
+  float* inv = group_inv_norm;
+  if (normalize_mode == 1 && !inv) inv = w.inv;
+  const bool reduce = group_sumsq || inv;
+  UpdLaunch L = make_launch(plan, 0, beta, w, group_sumsq, inv);
+  if (!reduce) L.layout.n_groups = 0;
+  cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
+  if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
+  if (e == cudaSuccess && normalize_mode == 1) e = launch_scale_groups(L, plan->dt, inv, s);
+  return cuda_status(e);
+}
+
+extern "C" size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return kWsHeader;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int per_sm = std::max(1, update_blocks_per_sm(QMUON_Q8_INT8, QMUON_BF16, true));
+  int32_t grid = 0;
+  int64_t chunk = 0;
+  update_geometry(nblocks(rows * cols), sms, per_sm, &grid, &chunk);
+  return kWsHeader + align_up((size_t)grid * 8, 256);
+}
+
+extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
+                                                   qmuon_dtype grad_dtype, float beta, uint8_t* payload,
+                                                   uint8_t* scale_inv, float* inv_norm, void* ws,
+                                                   size_t ws_bytes, void* stream) {
+  if (!tensor || !payload || !scale_inv || !inv_norm || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!valid_q8(q8_kind) || !valid_dtype(grad_dtype)) return QMUON_ERR_INVALID_ARGUMENT;
+  const qmuon_status vs = validate_tensor(*tensor, grad_dtype);
+  if (vs != QMUON_OK) return vs;
+  const int64_t n = tensor->rows * tensor->cols;
+  if (n == 0) return QMUON_ERR_INVALID_ARGUMENT;
+  if (tensor->cols % QMUON_SCALE_BLOCK) return QMUON_ERR_UNSUPPORTED;
+  if (!aligned(payload, 16) || !aligned(ws, 256) || !aligned(inv_norm, 4)) return QMUON_ERR_INVALID_ARGUMENT;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QMUON_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMUON_ERR_CUDA;
+  const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, true);
+  if (per_sm <= 0) return QMUON_ERR_CUDA;
+  int32_t grid = 0;
+  int64_t chunk = 0;
+  update_geometry(nblocks(n), sms, per_sm, &grid, &chunk);
+  if (ws_bytes < kWsHeader + align_up((size_t)grid * 8, 256)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  unsigned char* b = static_cast<unsigned char*>(ws);
+  UpdLaunch L{};
+  L.tensors = nullptr;
+  L.single.q8 = tensor->q8;
+  L.single.absmax = tensor->absmax;
+  L.single.grad = tensor->grad;
+  L.single.payload = payload;
+  L.single.scale = scale_inv;
+  L.single.numel = n;
+  L.single.block_begin = 0;
+  L.n_tensors = 1;
+  L.nb_total = nblocks(n);
+  L.chunk = chunk;
+  L.grid = grid;
+  L.beta = beta;
+  L.layout.n_groups = 1;   // block_group == null: one group, one slot per CTA
+  L.header = reinterpret_cast<WsHeader*>(b);
+  L.partials = reinterpret_cast<double*>(b + kWsHeader);
+  L.group_sumsq = nullptr;
+  L.group_inv = inv_norm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
+  if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, true, s);
+  return cuda_status(e);
+}
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz and the MuonBP step
+// ---------------------------------------------------------------------------
+extern "C" size_t qmuon_ns_workspace_size(const qmuon_ns_problem* problems, int32_t n_problems) {
+  if (!problems || n_problems <= 0) return 0;
+  return kWsHeader + ns::batch_workspace_bytes(problems, n_problems);
+}
+
+extern "C" qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* problems, int32_t n_problems,
+                                                    int32_t iters, const float coeffs[3], void* ws,
+                                                    size_t ws_bytes, void* stream) {
+  if (!problems || n_problems <= 0 || iters < 1 || !coeffs || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  for (int32_t i = 0; i < n_problems; ++i) {
+    const qmuon_status s = ns::validate_problem(problems[i]);
+    if (s != QMUON_OK) return s;
+  }
+  if (ws_bytes < kWsHeader + ns::batch_workspace_bytes(problems, n_problems))
+    return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  unsigned char* b = static_cast<unsigned char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(b, 0, kWsHeader, s) != cudaSuccess) return QMUON_ERR_CUDA;
+  return ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
+                       b + kWsHeader, ws_bytes - kWsHeader, s);
+}
+
+extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
+                                   float eta_full, float eta_block, float* const* weights,
+                                   const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!plan || !weights || !coeffs || !ws || t < 1 || P < 0 || iters < 1) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
+  const int32_t n = (int32_t)plan->tensors.size();
+  for (int32_t i = 0; i < n; ++i) {
+    const qmuon_tensor& T = plan->tensors[i];
+    if (T.rows * T.cols == 0) continue;
+    if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
+  }
+  if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  const bool full = (P != 0) && (t % P == 0);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const UpdWs w = carve(plan, ws, ws_bytes);
+  qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
+  ns::StepTables*& tabs = full ? mp->ns_full : mp->ns_block;
+  const qmuon_status ts = ns::ensure_step_tables(&tabs, plan->tensors.data(), n, full ? 1 : plan->tile_r,
+                                                 full ? 1 : plan->tile_c, weights, w.inv, w.ns, w.ns_bytes);
+  if (ts != QMUON_OK) return ts;
+  UpdLaunch L = make_launch(plan, full ? 1 : 2, beta, w, group_sumsq ? group_sumsq : w.sumsq, w.inv);
+  cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
+  if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
+  if (e != cudaSuccess) return QMUON_ERR_CUDA;
+  return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+}
+
+extern "C" qmuon_status qmuon_sync_status(void* ws, void* stream) {
+  if (!ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QMUON_ERR_CUDA;
+  unsigned int err = 0;
+  if (cudaMemcpy(&err, ws, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return QMUON_ERR_CUDA;
+  if (err != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return (qmuon_status)err;
+  }
+  return QMUON_OK;
+}
+
+extern "C" const char* qmuon_status_string(qmuon_status status) {
+  switch (status) {
+    case QMUON_OK: return "ok";
+    case QMUON_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case QMUON_ERR_MISALIGNED_SEGMENT: return "norm segment not aligned to 256-element blocks";
+    case QMUON_ERR_UNSUPPORTED: return "unsupported request";
+    case QMUON_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case QMUON_ERR_CUDA: return "CUDA error";
+    case QMUON_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* qmuon_version(void) { return "qmuon 0.1 sm_103a"; }

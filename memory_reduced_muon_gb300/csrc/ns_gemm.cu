@@ -1,0 +1,715 @@
+// Quintic Newton-Schulz orthogonalisation on tcgen05 tensor cores (sm_103a).
+//
+// One iteration is three matrix products ("NVIDIA impulsa optimizadores
+// avanzados ... con Megatron", section "Newton-Schulz distribuido"):
+//   G_GRAM   A = s1 * X X^T            (s1 = inv^2 on the first iteration)
+//   G_POLY   B = b A + c A A
+//   G_UPDATE X <- s3 * (a X + B X)     (s3 = inv on the first iteration;
+//                                       the last one may also apply W -= eta U)
+// A matrix stored with more rows than columns (S, n x m) is orthogonalised as
+// its transpose without moving data: A = S^T S and S <- a S + S B, since
+// (B X)^T = X^T B for the symmetric B.  Operands are bf16, accumulation fp32
+// in tensor memory.
+//
+// Kernel: one CTA per 128 x 256 output tile of one problem of a batch.
+// 6 warps: warp 0 issues TMA loads (64 x 64 bf16 boxes, 128-byte swizzle)
+// into a 4-stage shared-memory ring, warp 1 allocates 256 TMEM columns and
+// issues tcgen05.mma (M=128, N=256, K=16) from one thread, warps 2-5 read the
+// accumulator back with tcgen05.ld and run the fused epilogue.  K-major and
+// MN-major operands are both read straight from the row-major buffers; the
+// instruction descriptor says which.  Every mbarrier wait is bounded: on
+// expiry it records QMUON_ERR_TIMEOUT in the workspace header and the CTA
+// winds down instead of hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "qm_ns.h"
+
+namespace qm {
+namespace ns {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kBox = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16 = 8 KB
+constexpr uint32_t kStageA = 2 * kBox;          // 128 rows (or columns) x 64
+constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kTmemCols = 256;
+constexpr size_t kSmemBytes = STAGES * kStageBytes + 1024 + 256;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2 };
+
+struct alignas(128) NsProb {
+  CUtensorMap map_x[3];   // X buffers: 0 = caller's matrix, 1/2 = workspace ping-pong
+  CUtensorMap map_a;      // m x m Gram
+  CUtensorMap map_b;      // m x m polynomial
+  __nv_bfloat16* x[3];
+  int64_t x_ld[3];
+  __nv_bfloat16* a;
+  __nv_bfloat16* b;
+  float* w;               // fp32 weights (stored orientation) or null
+  int64_t w_ld;
+  const float* inv;       // inverse norm applied on the first iteration, or null
+  int32_t rows, cols;     // stored shape
+  int32_t m, n;           // m = min(rows, cols), n = max
+  int32_t tall;           // rows > cols
+  int32_t tiles_n[3];     // output tile columns per product kind
+  int32_t tiles[3];       // output tiles per product kind
+};
+
+struct GemmArgs {
+  const NsProb* probs;
+  const int32_t* tile_start;  // [n_probs + 1] prefix of tiles for this kind
+  int32_t n_probs;
+  int32_t src, dst;           // X buffer indices read / written (G_UPDATE); src for G_GRAM
+  int32_t first;              // apply inv (first iteration)
+  int32_t apply_w;            // W -= eta * U (last iteration of a step)
+  float ca, cb, cc, eta;
+  WsHeader* hdr;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void record_error(WsHeader* h, unsigned code, unsigned where) {
+  if (atomicCAS(&h->error, 0u, code) == 0u) h->error_info = where;
+}
+// Bounded wait: false when the phase did not complete in time (or another
+// CTA already gave up), after recording the timeout.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WsHeader* h, unsigned where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*reinterpret_cast<volatile unsigned*>(&h->error) != 0u) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        record_error(h, QMUON_ERR_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Make tensor maps written through the generic proxy (host copies into global
+// memory) visible to the tensor-map proxy before the first TMA that uses them.
+__device__ __forceinline__ void fence_tensormap(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading- and
+// stride-dimension byte offsets (all >> 4), descriptor version 1 at bit 46,
+// 128-byte swizzle (layout type 2) at bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// K-major tile (rows of 64 K-elements = 128 B, 8-row swizzle atoms of 1 KB):
+// the k-th 16-wide slice starts 32 B further in.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) { return smem_desc(tile + kk * 32, 16, 1024); }
+// MN-major tile (one 8 KB box per 64 MN-elements, a K row = 128 B): the k-th
+// 16-row slice starts 16 rows (2 KB) further in; MN atoms are 8 KB apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) { return smem_desc(tile + kk * 2048, kBox, 1024); }
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B
+// major-ness, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t make_idesc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+// Load 32 bf16 starting at p (valid elements only when n < 32) as fp32.
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* p, int n, float (&v)[32]) {
+  if (n >= 32) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = q[i];
+      v[8 * i + 0] = bf16_lo(u.x); v[8 * i + 1] = bf16_hi(u.x);
+      v[8 * i + 2] = bf16_lo(u.y); v[8 * i + 3] = bf16_hi(u.y);
+      v[8 * i + 4] = bf16_lo(u.z); v[8 * i + 5] = bf16_hi(u.z);
+      v[8 * i + 6] = bf16_lo(u.w); v[8 * i + 7] = bf16_hi(u.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = (i < n) ? __bfloat162float(p[i]) : 0.0f;
+  }
+}
+__device__ __forceinline__ void store_row32(__nv_bfloat16* p, int n, const float (&v)[32]) {
+  if (n >= 32) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      q[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                        pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < n) p[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), done_bar = smem_u32(bars + 2 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- which problem and which output tile ----
+  const int tile = blockIdx.x;
+  int lo = 0, hi = args.n_probs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(args.tile_start + mid) <= tile) lo = mid; else hi = mid - 1;
+  }
+  const NsProb& P = args.probs[lo];
+  const int local = tile - __ldg(args.tile_start + lo);
+  const int tn = P.tiles_n[KIND];
+  const int row0 = (local / tn) * BM, col0 = (local % tn) * BN;
+
+  int M_, N_, K_;
+  bool a_mn, b_mn;
+  const CUtensorMap* mapA;
+  const CUtensorMap* mapB;
+  if (KIND == G_GRAM) {
+    M_ = P.m; N_ = P.m; K_ = P.n;
+    mapA = mapB = &P.map_x[args.src];
+    a_mn = b_mn = (P.tall != 0);
+  } else if (KIND == G_POLY) {
+    M_ = P.m; N_ = P.m; K_ = P.m;
+    mapA = mapB = &P.map_a;
+    a_mn = b_mn = false;
+  } else if (!P.tall) {
+    M_ = P.m; N_ = P.n; K_ = P.m;
+    mapA = &P.map_b; a_mn = false;
+    mapB = &P.map_x[args.src]; b_mn = true;
+  } else {
+    M_ = P.n; N_ = P.m; K_ = P.m;
+    mapA = &P.map_x[args.src]; a_mn = false;
+    mapB = &P.map_b; b_mn = false;
+  }
+  const int num_kb = (K_ + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      fence_tensormap(mapA);
+      if (mapB != mapA) fence_tensormap(mapB);
+      int issued = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES, round = kb / STAGES;
+        if (round > 0 && !mbar_wait(empty0 + 8 * s, (round - 1) & 1, args.hdr, 0x100u | KIND)) break;
+        const uint32_t bar = full0 + 8 * s;
+        mbar_expect_tx(bar, kStageBytes);
+        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+        const int k0 = kb * BK;
+        if (!a_mn) {
+          tma_load_2d(sa, mapA, bar, k0, row0);
+          tma_load_2d(sa + kBox, mapA, bar, k0, row0 + 64);
+        } else {
+          tma_load_2d(sa, mapA, bar, row0, k0);
+          tma_load_2d(sa + kBox, mapA, bar, row0 + 64, k0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (!b_mn) tma_load_2d(sb + j * kBox, mapB, bar, k0, col0 + 64 * j);
+          else       tma_load_2d(sb + j * kBox, mapB, bar, col0 + 64 * j, k0);
+        }
+        ++issued;
+      }
+      // every load this thread issued has landed before the CTA may exit
+      for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+        mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1, args.hdr, 0x200u | KIND);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      const uint32_t idesc = make_idesc(a_mn, b_mn);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES, round = kb / STAGES;
+        if (!mbar_wait(full0 + 8 * s, round & 1, args.hdr, 0x300u | KIND)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
+          const uint64_t bd = b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
+          mma_bf16(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(empty0 + 8 * s);   // frees the stage once these MMAs are done
+      }
+      mma_commit(done_bar);           // accumulator complete (also on the error path)
+    }
+  } else {
+    // ---- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----
+    const int quarter = warp & 3;
+    const int r = row0 + quarter * 32 + lane;
+    const bool ok = mbar_wait(done_bar, 0, args.hdr, 0x400u | KIND);
+    tc_fence_after();
+    if (ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u) {
+      float s_first = 1.0f;
+      if (args.first && P.inv) {
+        const float iv = *P.inv;
+        s_first = (KIND == G_GRAM) ? iv * iv : iv;
+      }
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(c * 32), acc);
+        const int cb = col0 + c * 32;
+        if (r >= M_ || cb >= N_) continue;
+        const int nv = N_ - cb;
+        float out[32];
+        if (KIND == G_GRAM) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(acc[i]);
+          store_row32(P.a + (int64_t)r * P.m + cb, nv, out);
+        } else if (KIND == G_POLY) {
+          float av[32];
+          load_row32(P.a + (int64_t)r * P.m + cb, nv, av);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = args.cb * av[i] + args.cc * __uint_as_float(acc[i]);
+          store_row32(P.b + (int64_t)r * P.m + cb, nv, out);
+        } else {
+          float xv[32];
+          load_row32(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + cb, nv, xv);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(acc[i]));
+          store_row32(P.x[args.dst] + (int64_t)r * P.x_ld[args.dst] + cb, nv, out);
+          if (args.apply_w && P.w) {
+            float* wp = P.w + (int64_t)r * P.w_ld + cb;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i < nv) {
+                const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
+                wp[i] = __fsub_rn(wp[i], __fmul_rn(args.eta, u));
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: the accumulator is idle once done_bar has fired ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Copy the workspace result back to the caller's matrix (single-iteration runs).
+__global__ void copy_back_kernel(const NsProb* probs, int32_t p, int32_t from) {
+  const NsProb& P = probs[p];
+  const int64_t total = (int64_t)P.rows * P.cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / P.cols, c = i % P.cols;
+    P.x[0][r * P.x_ld[0] + c] = P.x[from][r * P.x_ld[from] + c];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map (rows x cols, row stride ld elements), 64 x 64 boxes, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shape of one problem's scratch: A and B (m x m) and two X buffers (rows x cols, compact).
+struct Shape {
+  int64_t rows, cols;
+};
+size_t scratch_bytes(const Shape& s) {
+  const int64_t m = std::min(s.rows, s.cols);
+  return 2 * align_up((size_t)(m * m) * 2, 256) + 2 * align_up((size_t)(s.rows * s.cols) * 2, 256);
+}
+size_t table_bytes(int32_t n) { return align_up((size_t)n * sizeof(NsProb), 256) + align_up((size_t)3 * (n + 1) * 4, 256); }
+
+// Fill one problem: x0 is the caller's matrix (row stride ld), scratch is carved from `ws`.
+bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, const float* inv, float* w,
+                  int64_t w_ld, unsigned char*& ws) {
+  std::memset(&P, 0, sizeof(P));
+  P.rows = (int32_t)rows;
+  P.cols = (int32_t)cols;
+  P.tall = rows > cols;
+  P.m = (int32_t)std::min(rows, cols);
+  P.n = (int32_t)std::max(rows, cols);
+  const int64_t m = P.m;
+  P.a = reinterpret_cast<__nv_bfloat16*>(ws);
+  ws += align_up((size_t)(m * m) * 2, 256);
+  P.b = reinterpret_cast<__nv_bfloat16*>(ws);
+  ws += align_up((size_t)(m * m) * 2, 256);
+  P.x[0] = static_cast<__nv_bfloat16*>(x0);
+  P.x_ld[0] = ld;
+  for (int i = 1; i < 3; ++i) {
+    P.x[i] = reinterpret_cast<__nv_bfloat16*>(ws);
+    P.x_ld[i] = cols;
+    ws += align_up((size_t)(rows * cols) * 2, 256);
+  }
+  P.inv = inv;
+  P.w = w;
+  P.w_ld = w_ld;
+  for (int i = 0; i < 3; ++i)
+    if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
+  if (!encode_bf16(&P.map_a, P.a, m, m, m) || !encode_bf16(&P.map_b, P.b, m, m, m)) return false;
+  const int64_t tm = (m + BM - 1) / BM, tnm = (m + BN - 1) / BN;
+  P.tiles_n[G_GRAM] = P.tiles_n[G_POLY] = (int32_t)tnm;
+  P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)(tm * tnm);
+  const int64_t um = P.tall ? P.n : P.m, un = P.tall ? P.m : P.n;   // G_UPDATE output (stored orientation)
+  P.tiles_n[G_UPDATE] = (int32_t)((un + BN - 1) / BN);
+  P.tiles[G_UPDATE] = (int32_t)(((um + BM - 1) / BM) * P.tiles_n[G_UPDATE]);
+  return true;
+}
+
+struct Launchable {
+  NsProb* d_probs = nullptr;
+  int32_t* d_tile_start = nullptr;  // [3][n+1]
+  int32_t n = 0;
+  int32_t total[3] = {0, 0, 0};
+};
+
+void prefix(const std::vector<NsProb>& probs, std::vector<int32_t>& ts, int32_t total[3]) {
+  const int32_t n = (int32_t)probs.size();
+  ts.assign(3 * (n + 1), 0);
+  for (int k = 0; k < 3; ++k) {
+    for (int32_t i = 0; i < n; ++i) ts[k * (n + 1) + i + 1] = ts[k * (n + 1) + i] + probs[i].tiles[k];
+    total[k] = ts[k * (n + 1) + n];
+  }
+}
+
+bool configure_kernels() {
+  static bool done = false, ok = false;
+  if (!done) {
+    ok = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess;
+    done = true;
+  }
+  return ok;
+}
+
+cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
+  if (L.total[kind] == 0) return cudaSuccess;
+  GemmArgs a = a0;
+  a.tile_start = L.d_tile_start + kind * (L.n + 1);
+  void* args[] = {&a};
+  void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM>
+           : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY> : (void*)ns_gemm_kernel<G_UPDATE>;
+  return cudaLaunchKernel(fn, dim3(L.total[kind]), dim3(kThreads), args, kSmemBytes, s);
+}
+
+// The iteration schedule over X buffers: 0 -> 1 -> 2 -> 1 -> ... and the last
+// iteration writes back into buffer 0 (its source is never 0 when iters >= 2).
+qmuon_status run_iterations(const Launchable& L, int32_t iters, const float coeffs[3], float eta, bool apply_w,
+                            WsHeader* hdr, cudaStream_t s, const std::vector<NsProb>& host_probs) {
+  if (!configure_kernels()) return QMUON_ERR_CUDA;
+  GemmArgs a{};
+  a.probs = L.d_probs;
+  a.n_probs = L.n;
+  a.ca = coeffs[0];
+  a.cb = coeffs[1];
+  a.cc = coeffs[2];
+  a.eta = eta;
+  a.hdr = hdr;
+  int src = 0;
+  for (int32_t it = 0; it < iters; ++it) {
+    const bool last = (it == iters - 1);
+    const int dst = (last && iters >= 2) ? 0 : 1 + (it % 2);
+    a.src = src;
+    a.dst = dst;
+    a.first = (it == 0);
+    a.apply_w = (last && apply_w) ? 1 : 0;
+    cudaError_t e = launch_gemm(G_GRAM, L, a, s);
+    if (e == cudaSuccess) e = launch_gemm(G_POLY, L, a, s);
+    if (e == cudaSuccess) e = launch_gemm(G_UPDATE, L, a, s);
+    if (e != cudaSuccess) return QMUON_ERR_CUDA;
+    src = dst;
+  }
+  if (src != 0) {
+    for (int32_t p = 0; p < L.n; ++p) {
+      copy_back_kernel<<<256, 256, 0, s>>>(L.d_probs, p, src);
+    }
+    if (cudaGetLastError() != cudaSuccess) return QMUON_ERR_CUDA;
+  }
+  (void)host_probs;
+  return QMUON_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// qmuon_newton_schulz_batched
+// ---------------------------------------------------------------------------
+qmuon_status validate_problem(const qmuon_ns_problem& p) {
+  if (p.rows <= 0 || p.cols <= 0 || p.rows > (1 << 30) || p.cols > (1 << 30)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (p.input != QMUON_NS_BF16 && p.input != QMUON_NS_MXFP8) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!p.x || (reinterpret_cast<uintptr_t>(p.x) & 15)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (p.ld < p.cols) return QMUON_ERR_INVALID_ARGUMENT;
+  if (p.ld % 8 || p.cols % 8) return QMUON_ERR_UNSUPPORTED;
+  if (p.inv_norm && (reinterpret_cast<uintptr_t>(p.inv_norm) & 3)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (p.input == QMUON_NS_MXFP8) return QMUON_ERR_UNSUPPORTED;
+  return QMUON_OK;
+}
+
+size_t batch_workspace_bytes(const qmuon_ns_problem* probs, int32_t n) {
+  size_t b = table_bytes(n);
+  for (int32_t i = 0; i < n; ++i) b += scratch_bytes({probs[i].rows, probs[i].cols});
+  return b;
+}
+
+qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, const float coeffs[3],
+                       WsHeader* hdr, unsigned char* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!encoder()) return QMUON_ERR_CUDA;
+  std::vector<NsProb> hp(n);
+  unsigned char* table = ws;
+  unsigned char* scratch = ws + table_bytes(n);
+  for (int32_t i = 0; i < n; ++i) {
+    if (!fill_problem(hp[i], probs[i].x, probs[i].rows, probs[i].cols, probs[i].ld, probs[i].inv_norm, nullptr, 0,
+                      scratch))
+      return QMUON_ERR_CUDA;
+  }
+  if ((size_t)(scratch - ws) > ws_bytes) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  Launchable L;
+  L.n = n;
+  L.d_probs = reinterpret_cast<NsProb*>(table);
+  L.d_tile_start = reinterpret_cast<int32_t*>(table + align_up((size_t)n * sizeof(NsProb), 256));
+  std::vector<int32_t> ts;
+  prefix(hp, ts, L.total);
+  if (cudaMemcpyAsync(L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QMUON_ERR_CUDA;
+  const qmuon_status st = run_iterations(L, iters, coeffs, 0.0f, false, hdr, s, hp);
+  // the pageable host vectors are staged by the copies above before they return
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// qmuon_step's problem sets
+// ---------------------------------------------------------------------------
+struct StepTables {
+  Launchable L;
+  void* d_mem = nullptr;
+  size_t d_bytes = 0;
+  std::vector<NsProb> host;
+  // what the cached tables were built for
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  const float* inv = nullptr;
+  std::vector<float*> weights;
+  int32_t tile_r = 0, tile_c = 0;
+};
+
+size_t step_workspace_bytes(const qmuon_tensor* t, int32_t n, int32_t tile_r, int32_t tile_c) {
+  size_t b = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (t[i].rows * t[i].cols == 0) continue;
+    const Shape sh{t[i].rows / tile_r, t[i].cols / tile_c};
+    b += (size_t)tile_r * tile_c * scratch_bytes(sh);
+  }
+  return b;
+}
+
+qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_t n, int32_t tile_r, int32_t tile_c,
+                                float* const* weights, const float* inv, unsigned char* ws, size_t ws_bytes) {
+  StepTables* T = *tabs;
+  if (T && T->ws == ws && T->ws_bytes == ws_bytes && T->inv == inv && T->tile_r == tile_r && T->tile_c == tile_c &&
+      std::equal(T->weights.begin(), T->weights.end(), weights))
+    return QMUON_OK;
+  if (!encoder()) return QMUON_ERR_CUDA;
+  std::vector<NsProb> hp;
+  unsigned char* scratch = ws;
+  int32_t g = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t R = t[i].rows, C = t[i].cols;
+    if (R * C == 0) continue;
+    const int64_t th = R / tile_r, tw = C / tile_c;
+    for (int32_t bi = 0; bi < tile_r; ++bi)
+      for (int32_t bj = 0; bj < tile_c; ++bj, ++g) {
+        NsProb P;
+        const int64_t off = bi * th * C + bj * tw;
+        void* x0 = static_cast<__nv_bfloat16*>(t[i].grad) + off;
+        if (!fill_problem(P, x0, th, tw, C, inv + g, weights[i] + off, C, scratch)) return QMUON_ERR_CUDA;
+        hp.push_back(P);
+      }
+  }
+  if ((size_t)(scratch - ws) > ws_bytes) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  if (!T) {
+    T = new StepTables;
+    *tabs = T;
+  }
+  const int32_t np = (int32_t)hp.size();
+  const size_t need = table_bytes(np);
+  if (T->d_bytes < need) {
+    if (T->d_mem) cudaFree(T->d_mem);
+    T->d_mem = nullptr;
+    T->d_bytes = 0;
+    if (cudaMalloc(&T->d_mem, need) != cudaSuccess) return QMUON_ERR_CUDA;
+    T->d_bytes = need;
+  }
+  T->L.n = np;
+  T->L.d_probs = static_cast<NsProb*>(T->d_mem);
+  T->L.d_tile_start = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(T->d_mem) +
+                                                 align_up((size_t)np * sizeof(NsProb), 256));
+  std::vector<int32_t> ts;
+  prefix(hp, ts, T->L.total);
+  if (cudaMemcpy(T->L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(T->L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return QMUON_ERR_CUDA;
+  T->host = std::move(hp);
+  T->ws = ws;
+  T->ws_bytes = ws_bytes;
+  T->inv = inv;
+  T->weights.assign(weights, weights + n);
+  T->tile_r = tile_r;
+  T->tile_c = tile_c;
+  return QMUON_OK;
+}
+
+qmuon_status run_step(StepTables* tabs, int32_t iters, const float coeffs[3], float eta, WsHeader* hdr,
+                      cudaStream_t s) {
+  if (!tabs) return QMUON_ERR_INVALID_ARGUMENT;
+  return run_iterations(tabs->L, iters, coeffs, eta, true, hdr, s, tabs->host);
+}
+
+void destroy_step_tables(StepTables* t) {
+  if (!t) return;
+  if (t->d_mem) cudaFree(t->d_mem);
+  delete t;
+}
+
+}  // namespace ns
+}  // namespace qm

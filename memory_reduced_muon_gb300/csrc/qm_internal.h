@@ -1,0 +1,77 @@
+// Internal declarations shared by the qmuon translation units (not part of
+// the public C ABI in include/qmuon.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "qmuon.h"
+
+namespace qm {
+
+constexpr int kBlock = QMUON_BLOCK;   // elements per quantization block
+constexpr int kUpdThreads = 256;      // 8 warps = 16 half-warps, one block per half-warp
+constexpr int kMaxChunk = 2048;       // quantization blocks per CTA (shared-memory bound)
+constexpr double kEps = 1e-7;         // added to the Frobenius norm
+
+// Workspace header: the first kWsHeader bytes of every workspace.
+struct WsHeader {
+  unsigned int error;      // 0 = ok, else a qmuon_status recorded by a kernel
+  unsigned int error_info; // where it happened (kernel-specific)
+  unsigned int ticket;     // last-CTA counter of the update kernel (self-resetting)
+  unsigned int pad[61];
+};
+constexpr size_t kWsHeader = sizeof(WsHeader);
+static_assert(kWsHeader == 256, "workspace header is 256 bytes");
+
+// One tensor as the update kernel sees it (device table entry).
+struct UpdTensor {
+  void* q8;
+  float* absmax;
+  void* grad;
+  uint8_t* payload;     // carrier only
+  uint8_t* scale;       // carrier only
+  int64_t numel;
+  int64_t block_begin;  // global index of the tensor's first quantization block
+};
+
+// Group layout of one launch: which norm group every block feeds, how the
+// grid's CTAs map onto (CTA, group) partial-sum slots, and the per-group list
+// of slots for the final deterministic reduction.  With block_group null the
+// launch has one group holding every block and one slot per CTA.
+struct GroupLayout {
+  int32_t n_groups = 0;
+  int32_t n_slots = 0;
+  const int32_t* block_group = nullptr;     // [nb_total], -1 = no group
+  const int32_t* cta_slot_begin = nullptr;  // [grid+1]
+  const int32_t* slot_group = nullptr;      // [n_slots], ascending within a CTA
+  const int32_t* grp_ptr = nullptr;         // [n_groups+1]
+  const int32_t* grp_slots = nullptr;       // slots of each group, CTA order
+};
+
+struct UpdLaunch {
+  const UpdTensor* tensors;   // device table, or null: use `single`
+  const int64_t* tensor_begin;  // device [n_tensors+1] block_begin, last = nb_total
+  UpdTensor single;           // the only tensor when `tensors` is null
+  int32_t n_tensors;
+  int64_t nb_total;
+  int64_t chunk;              // blocks per CTA
+  int32_t grid;
+  float beta;
+  GroupLayout layout;         // n_groups == 0: no reduction
+  double* partials;           // workspace [n_slots]
+  WsHeader* header;           // workspace header
+  float* group_sumsq;         // D or null
+  float* group_inv;           // D or null
+};
+
+// Host-side launchers (update.cu).  Return a cudaError_t from the launch.
+cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, bool carrier,
+                          cudaStream_t stream);
+cudaError_t launch_scale_groups(const UpdLaunch& L, qmuon_dtype dt, const float* inv,
+                                cudaStream_t stream);
+int update_blocks_per_sm(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier);
+
+}  // namespace qm

@@ -1,0 +1,463 @@
+// Blockwise 8-bit Muon momentum update for sm_103a.
+//
+// Implements "Quantized Muon Momentum", section "Algorithm", steps 1-9, over
+// many tensors in one launch (section "What Exists": the multi-tensor in-place
+// update, the fused sum of squares, the grouped normalisation of section
+// "Grouped QKV And Sharding"), and the MXFP8 carrier of section "Wave18B
+// MXFP8 Carrier Probe".
+//
+// Layout on the GPU: a CTA of 256 threads owns a contiguous chunk of
+// quantization blocks (the grid is a whole number of waves of resident CTAs).
+// A half-warp (16 lanes) handles one 256-element block; a lane owns 16
+// consecutive elements, so one 16-byte load brings its q8 codes and two
+// (bf16/fp16) or four (fp32) 16-byte loads its gradient.  Each half-warp
+// keeps two blocks in flight.  absmax and the block sum of squares are
+// shuffle reductions inside the half-warp.  The codec arithmetic uses the
+// round-to-nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn,
+// __float2int_rn), which the compiler never contracts into FMAs, in exactly
+// the order of the page's steps.
+//
+// Group sums without a second pass over HBM: every CTA writes its block sums
+// into shared memory, folds them per norm group into one partial per
+// (CTA, group) slot, and takes a ticket; the CTA that takes the last ticket
+// adds the slots of every group in a fixed order (fp64) and writes the sums
+// and inverse norms.  No CTA waits on another, and the result does not depend
+// on scheduling.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qm_internal.h"
+
+namespace qm {
+namespace {
+
+// ---------------------------------------------------------------------------
+// gradient element I/O: 16 consecutive elements per lane
+// ---------------------------------------------------------------------------
+template <int DT> struct Grad;
+
+template <> struct Grad<QMUON_BF16> {
+  static constexpr int kVecs = 2;   // 16 x 2 B = 2 x 16 B
+  __device__ __forceinline__ static float get(const uint4* v, int i) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(v)[i >> 1];
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+  __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+  }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+template <> struct Grad<QMUON_FP16> {
+  static constexpr int kVecs = 2;
+  __device__ __forceinline__ static float get(const uint4* v, int i) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(v)[i >> 1];
+    return __half2float(__ushort_as_half((unsigned short)((i & 1) ? (w >> 16) : (w & 0xFFFFu))));
+  }
+  __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+    return (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+  }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return __half2float(reinterpret_cast<const __half*>(p)[i]);
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
+  }
+};
+
+template <> struct Grad<QMUON_FP32> {
+  static constexpr int kVecs = 4;
+  __device__ __forceinline__ static float get(const uint4* v, int i) {
+    return __uint_as_float(reinterpret_cast<const uint32_t*>(v)[i]);
+  }
+  __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+    return reinterpret_cast<const float*>(p)[i];
+  }
+  __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+    reinterpret_cast<float*>(p)[i] = v;
+  }
+};
+
+template <int QK>
+__device__ __forceinline__ int decode_q(uint32_t w, int b) {
+  if (QK == QMUON_Q8_INT8) return (int)(int8_t)((w >> (8 * b)) & 0xFFu);
+  return (int)((w >> (8 * b)) & 0xFFu) - 128;
+}
+
+template <int QK>
+__device__ __forceinline__ uint32_t encode_q(int q, int b) {
+  const uint32_t u = (QK == QMUON_Q8_INT8) ? (uint32_t)(q & 0xFF) : (uint32_t)((q + 128) & 0xFF);
+  return u << (8 * b);
+}
+
+// E8M0 exponent byte of a 32-element block: 127 + e with e the smallest
+// integer such that amax <= 448 * 2^e (448 = 1.75 * 2^8 is the largest E4M3
+// value), clamped to [0, 254]; 127 for amax == 0, 254 for amax == inf.
+__device__ __forceinline__ int e8m0_of_amax(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const uint32_t ef = (b >> 23) & 0xFFu, mant = b & 0x7FFFFFu;
+  if (amax == 0.0f) return 127;
+  if (ef == 0xFFu) return 254;
+  int E;          // amax = f * 2^E with f in [1, 2)
+  bool above;     // f > 1.75
+  if (ef != 0) {
+    E = (int)ef - 127;
+    above = mant > 0x600000u;
+  } else {        // subnormal: amax = mant * 2^-149
+    const int p = 31 - __clz((int)mant);
+    E = p - 149;
+    above = ((uint64_t)mant << 2) > ((uint64_t)7u << p);
+  }
+  const int e = E - 8 + (above ? 1 : 0);
+  const int byte = 127 + e;
+  return byte < 0 ? 0 : (byte > 254 ? 254 : byte);
+}
+
+// 2^(127 - byte) as an fp32 (byte in [0, 254]: exponent in [-127, 127]).
+__device__ __forceinline__ float pow2_from_e8m0(int byte) {
+  const int k = 127 - byte;
+  if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
+  return __uint_as_float(0x00400000u);  // 2^-127 (subnormal, exact)
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Input of one block held by a lane between its loads and its compute.
+template <int DT>
+struct LaneIn {
+  uint4 q;
+  uint4 g[Grad<DT>::kVecs];
+  float amax_old;
+  int valid;   // elements of this lane inside the tensor (16 for a full block)
+};
+
+template <int QK, int DT>
+__device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, int64_t lb, int hl) {
+  const int64_t e0 = lb * kBlock + hl * 16;
+  in.amax_old = __ldcs(T.absmax + lb);
+  const int64_t rem = T.numel - e0;
+  in.valid = rem >= 16 ? 16 : (rem > 0 ? (int)rem : 0);
+  if (in.valid == 16) {
+    in.q = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(T.q8) + e0));
+    constexpr int esz = (DT == QMUON_FP32) ? 4 : 2;
+    const uint4* gp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(T.grad) + e0 * esz);
+#pragma unroll
+    for (int v = 0; v < Grad<DT>::kVecs; ++v) in.g[v] = __ldcs(gp + v);
+  } else {
+    // tail of a tensor whose size is not a multiple of 256: element loads
+    uint32_t qw[4] = {0u, 0u, 0u, 0u};
+    uint32_t gw[4 * Grad<DT>::kVecs];
+#pragma unroll
+    for (int i = 0; i < 4 * Grad<DT>::kVecs; ++i) gw[i] = 0u;
+    const uint8_t* qp = static_cast<const uint8_t*>(T.q8) + e0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i >= in.valid) continue;
+      qw[i >> 2] |= (uint32_t)qp[i] << (8 * (i & 3));
+      const float gv = Grad<DT>::load1(T.grad, e0 + i);
+      if (DT == QMUON_FP32) {
+        gw[i] = __float_as_uint(gv);
+      } else {
+        const uint32_t bits = (DT == QMUON_BF16)
+            ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(gv))
+            : (uint32_t)__half_as_ushort(__float2half_rn(gv));
+        gw[i >> 1] |= bits << (16 * (i & 1));
+      }
+    }
+    in.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+#pragma unroll
+    for (int v = 0; v < Grad<DT>::kVecs; ++v)
+      in.g[v] = make_uint4(gw[4 * v], gw[4 * v + 1], gw[4 * v + 2], gw[4 * v + 3]);
+  }
+}
+
+// Steps 1-9 for one lane's 16 elements; returns the block's sum of m*m
+// (identical in all 16 lanes of the half-warp).
+template <int QK, int DT, bool CARRIER>
+__device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTensor& T, int64_t lb,
+                                              int hl, float beta, float omb) {
+  const int64_t e0 = lb * kBlock + hl * 16;
+  const uint32_t* qw = reinterpret_cast<const uint32_t*>(&in.q);
+  // (1)-(2) dequantise: one division per block, one multiply per element
+  const float s_old = __fdiv_rn(in.amax_old, 127.0f);
+  float m[16];
+  float amax = 0.0f, ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float old = __fmul_rn(__int2float_rn(decode_q<QK>(qw[i >> 2], i & 3)), s_old);
+    const float g = Grad<DT>::get(in.g, i);
+    // (4) m = beta * old + (1 - beta) * g: two rounded products, one rounded sum
+    float mi = __fadd_rn(__fmul_rn(beta, old), __fmul_rn(omb, g));
+    if (i >= in.valid) mi = 0.0f;
+    m[i] = mi;
+    amax = fmaxf(amax, fabsf(mi));
+    ss = fmaf(mi, mi, ss);
+  }
+  // (6) block absmax and (9) block sum of squares across the half-warp
+  float amax_l = amax;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  }
+  // (7) requantise: sc = 127 / amax, q = clamp(rint(m * sc), -127, 127)
+  const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
+  uint32_t qo[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    int q = __float2int_rn(__fmul_rn(m[i], sc));
+    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+    if (amax == 0.0f) q = 0;
+    qo[i >> 2] |= encode_q<QK>(q, i & 3);
+  }
+  uint8_t* q8p = static_cast<uint8_t*>(T.q8) + e0;
+  if (in.valid == 16) {
+    __stcs(reinterpret_cast<uint4*>(q8p), make_uint4(qo[0], qo[1], qo[2], qo[3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < in.valid) q8p[i] = (uint8_t)((qo[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+  }
+  if (hl == 0) __stcs(T.absmax + lb, amax);  // (8)
+
+  if constexpr (!CARRIER) {
+    // (5) the momentum overwrites the gradient
+    if (in.valid == 16) {
+      constexpr int esz = (DT == QMUON_FP32) ? 4 : 2;
+      uint4* gp = reinterpret_cast<uint4*>(static_cast<uint8_t*>(T.grad) + e0 * esz);
+      if constexpr (DT == QMUON_FP32) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          __stcs(gp + v, make_uint4(__float_as_uint(m[4 * v]), __float_as_uint(m[4 * v + 1]),
+                                    __float_as_uint(m[4 * v + 2]), __float_as_uint(m[4 * v + 3])));
+      } else {
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          __stcs(gp + v, make_uint4(Grad<DT>::pack2(m[8 * v], m[8 * v + 1]),
+                                    Grad<DT>::pack2(m[8 * v + 2], m[8 * v + 3]),
+                                    Grad<DT>::pack2(m[8 * v + 4], m[8 * v + 5]),
+                                    Grad<DT>::pack2(m[8 * v + 6], m[8 * v + 7])));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i < in.valid) Grad<DT>::store1(T.grad, e0 + i, m[i]);
+    }
+  } else {
+    // MXFP8 carrier: a 32-element row block is two neighbouring lanes (the
+    // tensor's columns are a multiple of 32, so flat 32-groups are row blocks)
+    const float amax32 = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, 1));
+    const int byte = e8m0_of_amax(amax32);
+    const float mult = pow2_from_e8m0(byte);
+    uint32_t pw[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(m[4 * v], mult), __fmul_rn(m[4 * v + 1], mult));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(m[4 * v + 2], mult), __fmul_rn(m[4 * v + 3], mult));
+      pw[v] = lo | (hi << 16);
+    }
+    if (in.valid == 16) {
+      __stcs(reinterpret_cast<uint4*>(T.payload + e0), make_uint4(pw[0], pw[1], pw[2], pw[3]));
+      if ((hl & 1) == 0) T.scale[e0 >> 5] = (uint8_t)byte;
+    }
+    // valid is 0 or 16 here: the element count is a multiple of 32
+  }
+  return ss;
+}
+
+template <int QK, int DT, bool CARRIER>
+__global__ void __launch_bounds__(kUpdThreads, 3) update_kernel(UpdLaunch L) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* s_bsum = reinterpret_cast<float*>(smem_raw);
+  int32_t* s_bgrp = reinterpret_cast<int32_t*>(smem_raw + kMaxChunk * sizeof(float));
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int hw = tid >> 4, hl = tid & 15;
+  const int64_t kb = (int64_t)blockIdx.x * L.chunk;
+  const int64_t ke = (kb + L.chunk < L.nb_total) ? kb + L.chunk : L.nb_total;
+  const bool reduce = L.layout.n_groups > 0;
+  const float beta = L.beta;
+  const float omb = __fsub_rn(1.0f, beta);
+
+  const bool single = (L.tensors == nullptr);
+  // tensor holding this half-warp's first block (tensor_begin is ascending)
+  int t = 0;
+  if (!single) {
+    const int64_t k0 = kb + hw;
+    int lo = 0, hi = L.n_tensors - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(L.tensor_begin + mid) <= k0) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+  }
+
+  for (int64_t k = kb + hw; k < ke; k += 32) {
+    const int64_t k2 = k + 16;
+    const bool has2 = k2 < ke;
+    int t2 = t;
+    if (!single) {
+      while (k >= __ldg(L.tensor_begin + t + 1)) ++t;
+      t2 = t;
+      if (has2) while (k2 >= __ldg(L.tensor_begin + t2 + 1)) ++t2;
+    }
+    const UpdTensor T0 = single ? L.single : L.tensors[t];
+    const UpdTensor T1 = single ? L.single : L.tensors[t2];
+    LaneIn<DT> in0, in1;
+    load_lane<QK, DT>(in0, T0, k - T0.block_begin, hl);
+    if (has2) load_lane<QK, DT>(in1, T1, k2 - T1.block_begin, hl);
+    int32_t g0 = 0, g1 = 0;
+    if (reduce && hl == 0 && L.layout.block_group) {
+      g0 = __ldg(L.layout.block_group + k);
+      if (has2) g1 = __ldg(L.layout.block_group + k2);
+    }
+    const float ss0 = compute_lane<QK, DT, CARRIER>(in0, T0, k - T0.block_begin, hl, beta, omb);
+    if (reduce && hl == 0) { s_bsum[k - kb] = ss0; s_bgrp[k - kb] = g0; }
+    if (has2) {
+      const float ss1 = compute_lane<QK, DT, CARRIER>(in1, T1, k2 - T1.block_begin, hl, beta, omb);
+      if (reduce && hl == 0) { s_bsum[k2 - kb] = ss1; s_bgrp[k2 - kb] = g1; }
+    }
+    t = t2;
+  }
+  if (!reduce) return;
+
+  // ---- per-(CTA, group) partial sums, fixed order ----
+  __syncthreads();
+  const int nloc = (int)(ke - kb);
+  const bool one_group = (L.layout.block_group == nullptr);
+  const int s0 = one_group ? (int)blockIdx.x : __ldg(L.layout.cta_slot_begin + blockIdx.x);
+  const int s1 = one_group ? (int)blockIdx.x + 1 : __ldg(L.layout.cta_slot_begin + blockIdx.x + 1);
+  for (int s = s0 + warp; s < s1; s += kUpdThreads / 32) {
+    const int g = one_group ? 0 : __ldg(L.layout.slot_group + s);
+    float sum = 0.0f, comp = 0.0f;   // compensated fp32 sum per lane
+    for (int i = lane; i < nloc; i += 32) {
+      if (s_bgrp[i] == g) {
+        const float y = s_bsum[i] - comp;
+        const float tt = sum + y;
+        comp = (tt - sum) - y;
+        sum = tt;
+      }
+    }
+    const double v = warp_sum((double)sum - (double)comp);
+    if (lane == 0) L.partials[s] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&L.header->ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+
+  // ---- the last CTA: per-group totals in slot order ----
+  __threadfence();
+  for (int g = warp; g < L.layout.n_groups; g += kUpdThreads / 32) {
+    const int j0 = one_group ? 0 : __ldg(L.layout.grp_ptr + g);
+    const int j1 = one_group ? (int)gridDim.x : __ldg(L.layout.grp_ptr + g + 1);
+    double acc = 0.0;
+    for (int j = j0 + lane; j < j1; j += 32)
+      acc += __ldcg(L.partials + (one_group ? j : __ldg(L.layout.grp_slots + j)));
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      if (L.group_sumsq) L.group_sumsq[g] = (float)acc;
+      if (L.group_inv) L.group_inv[g] = (float)(1.0 / (sqrt(acc) + kEps));
+    }
+  }
+  if (tid == 0) L.header->ticket = 0u;
+}
+
+// In-place normalisation (second pass): grad <- store(float(grad) * inv[group]).
+template <int DT>
+__global__ void __launch_bounds__(kUpdThreads) scale_groups_kernel(UpdLaunch L, const float* inv) {
+  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
+  const bool single = (L.tensors == nullptr);
+  int t = 0;   // k only grows, so the tensor index only grows
+  for (int64_t k = (int64_t)blockIdx.x * 16 + hw; k < L.nb_total; k += (int64_t)gridDim.x * 16) {
+    if (!single) while (k >= __ldg(L.tensor_begin + t + 1)) ++t;
+    const int32_t g = L.layout.block_group ? __ldg(L.layout.block_group + k) : 0;
+    if (g < 0) continue;
+    const float s = __ldg(inv + g);
+    const UpdTensor T = single ? L.single : L.tensors[t];
+    const int64_t e0 = (k - T.block_begin) * kBlock + hl * 16;
+    const int64_t rem = T.numel - e0;
+    const int valid = rem >= 16 ? 16 : (rem > 0 ? (int)rem : 0);
+    for (int i = 0; i < valid; ++i)
+      Grad<DT>::store1(T.grad, e0 + i, __fmul_rn(Grad<DT>::load1(T.grad, e0 + i), s));
+  }
+}
+
+template <int QK, int DT, bool C>
+void* kernel_ptr() { return reinterpret_cast<void*>(&update_kernel<QK, DT, C>); }
+
+void* pick_kernel(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
+#define QM_PICK(QK, DT)                                                        \
+  if (q8 == QK && dt == DT) return carrier ? kernel_ptr<QK, DT, true>() : kernel_ptr<QK, DT, false>();
+  QM_PICK(QMUON_Q8_INT8, QMUON_BF16)
+  QM_PICK(QMUON_Q8_INT8, QMUON_FP16)
+  QM_PICK(QMUON_Q8_UINT8, QMUON_BF16)
+  QM_PICK(QMUON_Q8_UINT8, QMUON_FP16)
+#undef QM_PICK
+  if (dt == QMUON_FP32 && !carrier)
+    return q8 == QMUON_Q8_INT8 ? kernel_ptr<QMUON_Q8_INT8, QMUON_FP32, false>()
+                               : kernel_ptr<QMUON_Q8_UINT8, QMUON_FP32, false>();
+  if (dt == QMUON_FP32 && carrier)
+    return q8 == QMUON_Q8_INT8 ? kernel_ptr<QMUON_Q8_INT8, QMUON_FP32, true>()
+                               : kernel_ptr<QMUON_Q8_UINT8, QMUON_FP32, true>();
+  return nullptr;
+}
+
+constexpr size_t kUpdSmem = kMaxChunk * (sizeof(float) + sizeof(int32_t));
+
+}  // namespace
+
+int update_blocks_per_sm(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
+  void* k = pick_kernel(q8, dt, carrier);
+  if (!k) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kUpdThreads, kUpdSmem) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, bool carrier,
+                          cudaStream_t stream) {
+  void* k = pick_kernel(q8, dt, carrier);
+  if (!k) return cudaErrorInvalidValue;
+  UpdLaunch arg = L;
+  void* args[] = {&arg};
+  return cudaLaunchKernel(k, dim3(L.grid), dim3(kUpdThreads), args, kUpdSmem, stream);
+}
+
+cudaError_t launch_scale_groups(const UpdLaunch& L, qmuon_dtype dt, const float* inv,
+                                cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t want = (L.nb_total + 15) / 16;
+  int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  if (grid < 1) grid = 1;
+  switch (dt) {
+    case QMUON_BF16: scale_groups_kernel<QMUON_BF16><<<grid, kUpdThreads, 0, stream>>>(L, inv); break;
+    case QMUON_FP16: scale_groups_kernel<QMUON_FP16><<<grid, kUpdThreads, 0, stream>>>(L, inv); break;
+    case QMUON_FP32: scale_groups_kernel<QMUON_FP32><<<grid, kUpdThreads, 0, stream>>>(L, inv); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qm

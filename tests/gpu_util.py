@@ -1,0 +1,49 @@
+"""Helpers shared by the GPU parity tests (device <-> oracle representations)."""
+
+import numpy as np
+import torch
+
+TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+def to_oracle_grad(t: torch.Tensor, dtype: str) -> np.ndarray:
+    """A device gradient as the oracle stores it (bf16 as uint16 bits)."""
+    t = t.detach().contiguous().cpu().reshape(-1)
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    if dtype == "f16":
+        return t.numpy().copy()
+    return t.numpy().astype(np.float32).copy()
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def min_row_cos(a: np.ndarray, b: np.ndarray) -> float:
+    na = np.linalg.norm(a, axis=1)
+    nb = np.linalg.norm(b, axis=1)
+    keep = nb > 0
+    return float(np.min(np.sum(a[keep] * b[keep], axis=1) / (na[keep] * nb[keep])))
+
+
+def ulp_diff_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> int:
+    """Largest distance in bf16 ulps between two arrays of bf16 bit patterns."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, 0x8000 - (x & 0x7FFF), 0x8000 + x)
+    return int(np.max(np.abs(ordered(a_bits) - ordered(b_bits)))) if a_bits.size else 0
+
+
+def random_grad(n: int, dtype: str, seed: int, device="cuda") -> torch.Tensor:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    nb = (n + 255) // 256
+    scale = torch.exp(torch.empty(nb, device=device).uniform_(-8.0, 4.0, generator=g)).repeat_interleave(256)[:n]
+    x = torch.randn(n, generator=g, device=device) * scale
+    x[torch.rand(n, generator=g, device=device) < 0.02] = 0.0
+    return x.to(TORCH_DT[dtype]).contiguous()

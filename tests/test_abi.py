@@ -1,0 +1,143 @@
+"""The C ABI on the CPU: the library loads, exports every symbol the header
+declares, and rejects invalid arguments on the host (status codes, nothing
+launched) -- none of these calls needs a GPU."""
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import memory_reduced_muon_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmuon.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(q.LIB_PATH):
+        from memory_reduced_muon_gb300 import build
+        build.build()
+    return q.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QMUON_API\s+[\w\s\*]+?\b(qmuon_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for must in ["qmuon_update_multi_normalize_groups", "qmuon_update_mxfp8_carrier",
+                 "qmuon_newton_schulz_batched", "qmuon_step", "qmuon_plan_create"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", q.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(q.exported_symbols()) <= set(declared_symbols())
+
+
+def test_status_strings_and_version(lib):
+    assert q.qmuon_version().startswith("qmuon")
+    for code in range(7):
+        s = q.status_string(code)
+        assert s and s != "unknown status"
+    assert q.status_string(99) == "unknown status"
+
+
+FAKE = 0x7F0000000000  # a 16-byte-aligned address that is never dereferenced
+
+
+def _tensor(rows, cols, base=FAKE):
+    return q.qmuon_tensor(base, base + 0x100000, base + 0x200000, rows, cols)
+
+
+def _plan_status(tensors, segments=None, n_groups=0, tile=(1, 1), q8=0, dt=0):
+    arr = (q.qmuon_tensor * max(1, len(tensors)))(*tensors)
+    segs = None
+    if segments:
+        segs = (q.qmuon_norm_segment * len(segments))(*[q.qmuon_norm_segment(t, g, s, l) for t, s, l, g in segments])
+    out = C.c_void_p()
+    return q.lib().qmuon_plan_create(arr, len(tensors), q8, dt, segs, len(segments or []), n_groups,
+                                     tile[0], tile[1], C.byref(out))
+
+
+def test_plan_create_rejects_on_host(lib):
+    INV, MIS = q.QMUON_ERR_INVALID_ARGUMENT, q.QMUON_ERR_MISALIGNED_SEGMENT
+    assert _plan_status([]) == INV
+    assert _plan_status([_tensor(16, 16)], q8=7) == INV                      # bad enum
+    assert _plan_status([_tensor(16, 16)], dt=9) == INV
+    assert _plan_status([q.qmuon_tensor(FAKE + 8, FAKE, FAKE, 16, 16)]) == INV   # q8 not 16-byte aligned
+    assert _plan_status([q.qmuon_tensor(0, FAKE, FAKE, 16, 16)]) == INV          # null pointer
+    assert _plan_status([_tensor(-1, 16)]) == INV
+    # norm segments ("Grouped QKV And Sharding"): 256-element alignment
+    t = [_tensor(8, 512)]
+    assert _plan_status(t, segments=[(0, 100, 256, 0)], n_groups=1) == MIS
+    assert _plan_status(t, segments=[(0, 0, 300, 0)], n_groups=1) == MIS
+    assert _plan_status(t, segments=[(0, 0, 512, 0), (0, 256, 512, 1)], n_groups=2) == INV  # overlap
+    assert _plan_status(t, segments=[(0, 0, 512, 3)], n_groups=2) == INV                    # group id
+    assert _plan_status(t, segments=[(1, 0, 512, 0)], n_groups=1) == INV                    # tensor index
+    assert _plan_status(t, segments=[(0, 0, 5000, 0)], n_groups=1) == INV                   # past the end
+    # MuonBP tiling: must divide the matrix, column tiles must be 256-aligned
+    assert _plan_status([_tensor(8, 512)], tile=(3, 1)) == INV
+    assert _plan_status([_tensor(8, 512)], tile=(1, 4)) == MIS
+    assert _plan_status([_tensor(8, 512)], tile=(0, 1)) == INV
+    assert _plan_status([_tensor(8, 512)], n_groups=5) == INV  # per-tensor groups need n_groups == n
+
+
+def test_entries_reject_null_plan_and_bad_args(lib):
+    L = q.lib()
+    INV = q.QMUON_ERR_INVALID_ARGUMENT
+    assert L.qmuon_update_multi_normalize_groups(None, 0.9, 0, None, None, FAKE, 1 << 20, None) == INV
+    assert L.qmuon_workspace_size(None, 0) == 0
+    cf = (C.c_float * 3)(3.4445, -4.775, 2.0315)
+    w = (C.c_void_p * 1)(FAKE)
+    assert L.qmuon_step(None, 1, 5, 0.9, 0.02, 0.01, w, cf, 5, None, FAKE, 1 << 20, None) == INV
+    assert L.qmuon_sync_status(None, None) == INV
+    assert L.qmuon_sync_status(FAKE + 16, None) == INV   # not 256-byte aligned
+
+
+def test_carrier_rejects_on_host(lib):
+    L = q.lib()
+    t = _tensor(4, 48)   # 48 columns: not a multiple of 32
+    r = L.qmuon_update_mxfp8_carrier(C.byref(t), 0, 0, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert r == q.QMUON_ERR_UNSUPPORTED
+    t = _tensor(4, 64)
+    r = L.qmuon_update_mxfp8_carrier(C.byref(t), 0, 0, 0.9, FAKE + 4, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert r == q.QMUON_ERR_INVALID_ARGUMENT   # payload not 16-byte aligned
+    r = L.qmuon_update_mxfp8_carrier(C.byref(t), 3, 0, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert r == q.QMUON_ERR_INVALID_ARGUMENT
+
+
+def test_newton_schulz_rejects_on_host(lib):
+    L = q.lib()
+    cf = (C.c_float * 3)(3.4445, -4.775, 2.0315)
+
+    def call(probs, iters=5, ws_bytes=1 << 30):
+        arr = (q.qmuon_ns_problem * len(probs))(*probs)
+        return L.qmuon_newton_schulz_batched(arr, len(probs), iters, cf, FAKE, ws_bytes, None)
+
+    ok = q.ns_problem(FAKE, 64, 64)
+    assert call([q.ns_problem(FAKE, 0, 64)]) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert call([q.ns_problem(FAKE, 64, 60)]) == q.QMUON_ERR_UNSUPPORTED       # cols % 8
+    assert call([q.ns_problem(FAKE, 64, 64, ld=32)]) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert call([q.ns_problem(FAKE + 8, 64, 64)]) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert call([ok], iters=0) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert call([ok], ws_bytes=100) == q.QMUON_ERR_WORKSPACE_TOO_SMALL
+    need = q.qmuon_ns_workspace_size([ok])
+    # A, B (64x64 bf16) and two 64x64 scratch copies, plus the problem table
+    assert need >= 4 * 64 * 64 * 2
+
+
+def test_binding_raises_when_library_missing(monkeypatch):
+    monkeypatch.setattr(q, "LIB_PATH", "/nonexistent/libqmuon.so")
+    monkeypatch.setattr(q, "_lib_handle", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        q.lib()

@@ -1,0 +1,166 @@
+"""GPU parity of the Newton-Schulz engine (tcgen05) and of the MuonBP step.
+
+Single-iteration runs with one coefficient switched on at a time check each
+of the three tensor-core products on its own (wide and tall operands, ragged
+shapes) against fp64 products of the same bf16-rounded intermediates; the
+five-iteration runs and the steps are held to the oracle tolerance:
+relative Frobenius error <= 2e-2 and per-row cosine >= 0.999.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import memory_reduced_muon_gb300 as q
+import workloads
+from oracle import codec, muonbp, ns
+
+from gpu_util import bf16_to_f64, min_row_cos, random_grad, rel_fro, to_oracle_grad
+
+pytestmark = pytest.mark.gpu
+
+COEFFS = workloads.COEFFS
+
+
+def _bf16_round(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+def _one_iteration_reference(M, coeffs, inv):
+    a, b, c = coeffs
+    X = M * inv
+    tall = X.shape[0] > X.shape[1]
+    if tall:
+        X = X.T
+    A = _bf16_round(X @ X.T)
+    B = _bf16_round(b * A + c * (A @ A))
+    out = a * X + B @ X
+    return out.T if tall else out
+
+
+def _run_ns(mats, iters, coeffs, invs=None):
+    probs = []
+    for i, Mt in enumerate(mats):
+        r, c = Mt.shape
+        probs.append(q.ns_problem(Mt, r, c, inv_norm=None if invs is None else invs[i]))
+    ws = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device="cuda")
+    q.qmuon_newton_schulz_batched(probs, iters, coeffs, ws)
+    q.qmuon_sync_status(ws)
+
+
+SHAPES = [(128, 256), (256, 128), (8, 16), (24, 40), (40, 24), (300, 520), (520, 304), (512, 512), (1000, 136),
+          (64, 1024)]
+
+
+@pytest.mark.parametrize("coeffs", [(1.0, 0.0, 0.0), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0), COEFFS])
+def test_single_iteration_products(coeffs):
+    rng = np.random.default_rng(1)
+    mats, ref = [], []
+    for r, c in SHAPES:
+        M = rng.standard_normal((r, c)).astype(np.float32)
+        Mt = torch.from_numpy(M).to(torch.bfloat16).cuda()
+        Mb = Mt.float().cpu().numpy().astype(np.float64)
+        inv = 1.0 / np.linalg.norm(Mb)
+        mats.append(Mt)
+        ref.append(_one_iteration_reference(Mb, coeffs, inv))
+    invs = [torch.tensor([1.0 / np.linalg.norm(bf16_to_f64(m))], dtype=torch.float32, device="cuda") for m in mats]
+    _run_ns(mats, 1, coeffs, invs)
+    for (r, c), Mt, R in zip(SHAPES, mats, ref):
+        got = bf16_to_f64(Mt)
+        err = rel_fro(got, R)
+        assert err <= 6e-3, ((r, c), coeffs, err)
+
+
+@pytest.mark.parametrize("shape", SHAPES + [(2048, 1024), (1024, 3072)])
+def test_five_iterations_vs_oracle(shape):
+    r, c = shape
+    g = random_grad(r * c, "bf16", 77).reshape(r, c)
+    M = bf16_to_f64(g)
+    inv_h = 1.0 / (np.linalg.norm(M) + 1e-7)
+    inv = torch.tensor([inv_h], dtype=torch.float32, device="cuda")
+    ref = ns.newton_schulz(M, inv_norm=float(inv.item()))
+    _run_ns([g], 5, COEFFS, [inv])
+    got = bf16_to_f64(g)
+    assert rel_fro(got, ref) <= 2e-2
+    assert min_row_cos(got, ref) >= 0.999
+
+
+def test_batch_of_mixed_problems_and_strided_view():
+    # one launch sequence over problems of different shapes, one of them a
+    # column block of a wider matrix (row stride larger than its width)
+    base = random_grad(384 * 1024, "bf16", 5).reshape(384, 1024)
+    view_ref = bf16_to_f64(base[:, 256:512])
+    others = [random_grad(r * c, "bf16", 6 + i).reshape(r, c) for i, (r, c) in enumerate([(96, 200), (700, 256)])]
+    refs = [ns.newton_schulz(view_ref)] + [ns.newton_schulz(bf16_to_f64(t)) for t in others]
+    untouched = base[:, :256].clone()
+    probs = [q.ns_problem(base.data_ptr() + 256 * 2, 384, 256, ld=1024)] + \
+            [q.ns_problem(t, t.shape[0], t.shape[1]) for t in others]
+    ws = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device="cuda")
+    q.qmuon_newton_schulz_batched(probs, 5, COEFFS, ws)
+    q.qmuon_sync_status(ws)
+    outs = [bf16_to_f64(base[:, 256:512])] + [bf16_to_f64(t) for t in others]
+    for got, ref in zip(outs, refs):
+        assert rel_fro(got, ref) <= 2e-2 and min_row_cos(got, ref) >= 0.999
+    assert torch.equal(base[:, :256], untouched)
+
+
+def _step_case(shapes, tile, seed):
+    mats = [workloads.Matrix(f"m{i}", r, c) for i, (r, c) in enumerate(shapes)]
+    dev = "cuda"
+    states_d, weights_d, grads_d = [], [], []
+    for i, m in enumerate(mats):
+        qs, a = workloads.random_state(m, seed + i, device=dev)
+        states_d.append((qs, a))
+        weights_d.append((torch.randn(m.rows, m.cols, device=dev) * 0.02).contiguous())
+        grads_d.append(torch.empty(m.rows, m.cols, dtype=torch.bfloat16, device=dev))
+    plan = q.qmuon_plan_create([(s, a, g, m.rows, m.cols) for (s, a), g, m in zip(states_d, grads_d, mats)],
+                               "int8", "bf16", tile=tile)
+    host = [muonbp.MatrixState(m.rows, m.cols, s.cpu().numpy(), a.cpu().numpy(), w.cpu().numpy())
+            for (s, a), w, m in zip(states_d, weights_d, mats)]
+    return mats, plan, states_d, weights_d, grads_d, host
+
+
+@pytest.mark.parametrize("P", [5, 1, 0])
+def test_muonbp_steps_vs_oracle(P):
+    shapes = [(512, 2048), (256, 2048), (1024, 4096), (2048, 2048)]
+    tile = (1, 8)
+    mats, plan, states_d, weights_d, grads_d, host = _step_case(shapes, tile, 40)
+    ws = torch.empty(q.qmuon_workspace_size(plan, q.QMUON_WS_STEP), dtype=torch.uint8, device="cuda")
+    eta_full, eta_block = 0.02, 0.02 / math.sqrt(8)
+    for t in range(1, 6):
+        gh = []
+        for i, (m, g) in enumerate(zip(mats, grads_d)):
+            src = random_grad(m.numel, "bf16", 900 + 10 * t + i).reshape(m.rows, m.cols)
+            g.copy_(src)
+            gh.append(to_oracle_grad(g, "bf16"))
+        full = muonbp.is_full_step(t, P)
+        ngr = q.qmuon_plan_info(plan)["n_full_groups" if full else "n_block_groups"]
+        sums = torch.zeros(ngr, device="cuda")
+        w_before = [w.cpu().numpy().astype(np.float64) for w in weights_d]
+        q.qmuon_step(plan, t, P, 0.95, eta_full, eta_block, weights_d, COEFFS, 5, sums, ws)
+        q.qmuon_sync_status(ws)
+        host, U, info = muonbp.muonbp_step(t, P, host, gh, 0.95, eta_full, eta_block, tile=tile)
+        assert info["full"] == full
+        np.testing.assert_allclose(sums.cpu().numpy(), info["S"], rtol=1e-5)
+        for i, m in enumerate(mats):
+            np.testing.assert_array_equal(states_d[i][0].cpu().numpy(), host[i].q8)
+            np.testing.assert_array_equal(states_d[i][1].cpu().numpy(), host[i].absmax)
+            got = bf16_to_f64(grads_d[i])
+            ref = codec.f32_from_bf16_bits(U[i]).astype(np.float64)
+            if full:
+                assert rel_fro(got, ref) <= 2e-2 and min_row_cos(got, ref) >= 0.999, (t, m)
+            else:
+                th, tw = m.rows // tile[0], m.cols // tile[1]
+                for j in range(tile[1]):
+                    sl = (slice(None), slice(j * tw, (j + 1) * tw))
+                    assert rel_fro(got[sl], ref[sl]) <= 2e-2 and min_row_cos(got[sl], ref[sl]) >= 0.999, (t, m, j)
+            # the weight moved by eta * U (eta_full on full steps, eta_block
+            # otherwise): compare the applied updates
+            dW = weights_d[i].cpu().numpy().astype(np.float64) - w_before[i]
+            dW_ref = host[i].weight.astype(np.float64) - w_before[i]
+            assert rel_fro(dW, dW_ref) <= 2e-2, (t, m)
+        # keep both sides on the same weights so errors do not accumulate
+        for i in range(len(mats)):
+            weights_d[i].copy_(torch.from_numpy(host[i].weight).cuda())
