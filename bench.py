@@ -251,14 +251,20 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    ev[0].record(stream)
+    kinds = []
+    for k in range(args.steps):
         t += 1
         refill(t)
+        ev[2 * k + 1].record(stream)
         step(t)
-    e1.record(stream)
+        ev[2 * k + 2].record(stream)
+        kinds.append("full" if (w.P and t % w.P == 0) else "block")
+    e0, e1 = ev[0], ev[-1]
     torch.cuda.synchronize()
+    per_step = [{"kind": kinds[k], "refill_ms": ev[2 * k].elapsed_time(ev[2 * k + 1]),
+                 "step_ms": ev[2 * k + 1].elapsed_time(ev[2 * k + 2])} for k in range(args.steps)]
     barrier(world)
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
@@ -339,7 +345,7 @@ def run_gpu(args, world, rank, local):
 
     # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
-    return dict(value=value, ms=ms_max, clocks=clocks, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
+    return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
                 ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=4 * ngr, n_full=n_full,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
@@ -403,7 +409,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (NS operands, fp32 accumulate); int8 state, fp32 codec",
             "data": "synthetic (seeded gradients, zero initial state, N(0,0.02^2) weights)", "config": config,
-            "full_steps_timed": r["n_full"],
+            "full_steps_timed": r["n_full"], "per_step": r["per_step"],
             "update_gbs": r["upd_gbs"], "ns_tflops": ns_tflops,
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
             "e2e": {"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],

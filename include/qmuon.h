@@ -208,6 +208,11 @@ QMUON_API qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, 
  * (QMUON_ERR_TIMEOUT when a bounded wait expired), then clear it. */
 QMUON_API qmuon_status qmuon_sync_status(void* ws, void* stream);
 
+/* Detail of the last non-OK status returned on the calling thread (which
+ * call failed and the CUDA error string), or "" if none.  The pointer stays
+ * valid until the next qmuon call on this thread. */
+QMUON_API const char* qmuon_last_error(void);
+
 /* Static description of a status code (never NULL). */
 QMUON_API const char* qmuon_status_string(qmuon_status status);
 

@@ -40,7 +40,12 @@ DTYPES = {"bf16": QMUON_BF16, "f16": QMUON_FP16, "f32": QMUON_FP32}
 class QmuonError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        detail = ""
+        try:
+            detail = lib().qmuon_last_error().decode()
+        except Exception:
+            pass
+        super().__init__(f"{where}: {status_string(status)} (status {status})" + (f" -- {detail}" if detail else ""))
 
 
 class qmuon_tensor(C.Structure):
@@ -87,6 +92,7 @@ def lib() -> C.CDLL:
         "qmuon_sync_status": (i32, [vp, vp]),
         "qmuon_status_string": (C.c_char_p, [i32]),
         "qmuon_version": (C.c_char_p, []),
+        "qmuon_last_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -100,7 +106,7 @@ def exported_symbols() -> list:
     return ["qmuon_plan_create", "qmuon_plan_destroy", "qmuon_plan_info", "qmuon_workspace_size",
             "qmuon_update_multi_normalize_groups", "qmuon_carrier_workspace_size",
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
-            "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version"]
+            "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error"]
 
 
 # --------------------------------------------------------------------------
@@ -145,6 +151,10 @@ qmuon_status_string = status_string
 
 def qmuon_version() -> str:
     return lib().qmuon_version().decode()
+
+
+def qmuon_last_error() -> str:
+    return lib().qmuon_last_error().decode()
 
 
 class Plan:

@@ -4,6 +4,7 @@
 // workspace carving and launches.  Every device computation happens in the
 // kernels of update.cu and ns_gemm.cu.
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <memory>
 #include <new>
@@ -63,8 +64,25 @@ void build_slots(HostLayout& L, int32_t grid, int64_t chunk, int64_t nb) {
   L.grp_ptr[L.n_groups] = (int32_t)L.grp_slots.size();
 }
 
-qmuon_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMUON_OK : QMUON_ERR_CUDA; }
+thread_local char g_last_error[512] = "";
 
+}  // namespace
+
+qmuon_status qm::set_error(const char* where, cudaError_t e, qmuon_status status) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorString(e),
+                cudaGetErrorName(e));
+  return status;
+}
+
+qmuon_status qm::set_error_msg(const char* msg, qmuon_status status) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+  return status;
+}
+
+namespace {
+qmuon_status cuda_status(cudaError_t e, const char* where) {
+  return e == cudaSuccess ? QMUON_OK : set_error(where, e);
+}
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -217,11 +235,12 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
   }
 
   // ---- device properties and geometry ----
-  if (cudaGetDevice(&P->device) != cudaSuccess) return QMUON_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
-    return QMUON_ERR_CUDA;
+  cudaError_t ce = cudaGetDevice(&P->device);
+  if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaGetDevice)", ce);
+  ce = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+  if (ce != cudaSuccess) return set_error("qmuon_plan_create (SM count)", ce);
   const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
-  if (per_sm <= 0) return QMUON_ERR_CUDA;
+  if (per_sm <= 0) return set_error_msg("qmuon_plan_create: occupancy query failed", QMUON_ERR_CUDA);
   update_geometry(nb, P->num_sms, per_sm, &P->grid, &P->chunk);
   for (auto& h : H) build_slots(h, P->grid, P->chunk, nb);
 
@@ -253,10 +272,12 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
     o_l[l][3] = put(H[l].grp_ptr.data(), H[l].grp_ptr.size() * 4);
     o_l[l][4] = put(H[l].grp_slots.data(), H[l].grp_slots.size() * 4);
   }
-  if (cudaMalloc(&P->d_table, blob.size()) != cudaSuccess) return QMUON_ERR_CUDA;
-  if (cudaMemcpy(P->d_table, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+  ce = cudaMalloc(&P->d_table, blob.size());
+  if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaMalloc tables)", ce);
+  ce = cudaMemcpy(P->d_table, blob.data(), blob.size(), cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) {
     cudaFree(P->d_table);
-    return QMUON_ERR_CUDA;
+    return set_error("qmuon_plan_create (upload tables)", ce);
   }
   unsigned char* base = static_cast<unsigned char*>(P->d_table);
   P->d_tensors = reinterpret_cast<UpdTensor*>(base + o_t);
@@ -384,7 +405,7 @@ extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* pl
   cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
   if (e == cudaSuccess && normalize_mode == 1) e = launch_scale_groups(L, plan->dt, inv, s);
-  return cuda_status(e);
+  return cuda_status(e, "qmuon_update_multi_normalize_groups (launch)");
 }
 
 extern "C" size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols) {
@@ -442,7 +463,7 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, q
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, true, s);
-  return cuda_status(e);
+  return cuda_status(e, "qmuon_update_mxfp8_carrier (launch)");
 }
 
 // ---------------------------------------------------------------------------
@@ -466,7 +487,8 @@ extern "C" qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* prob
     return QMUON_ERR_WORKSPACE_TOO_SMALL;
   unsigned char* b = static_cast<unsigned char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(b, 0, kWsHeader, s) != cudaSuccess) return QMUON_ERR_CUDA;
+  const cudaError_t me = cudaMemsetAsync(b, 0, kWsHeader, s);
+  if (me != cudaSuccess) return set_error("qmuon_newton_schulz_batched (memset)", me);
   return ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
                        b + kWsHeader, ws_bytes - kWsHeader, s);
 }
@@ -497,20 +519,24 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
   UpdLaunch L = make_launch(plan, full ? 1 : 2, beta, w, group_sumsq ? group_sumsq : w.sumsq, w.inv);
   cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
-  if (e != cudaSuccess) return QMUON_ERR_CUDA;
+  if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);
   return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
 }
 
 extern "C" qmuon_status qmuon_sync_status(void* ws, void* stream) {
   if (!ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return QMUON_ERR_CUDA;
-  unsigned int err = 0;
-  if (cudaMemcpy(&err, ws, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return QMUON_ERR_CUDA;
-  if (err != 0) {
-    const unsigned int zero = 0;
-    cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-    return (qmuon_status)err;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error("qmuon_sync_status (stream synchronize)", e);
+  unsigned int err[2] = {0u, 0u};
+  e = cudaMemcpy(err, ws, sizeof(err), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error("qmuon_sync_status (read header)", e);
+  if (err[0] != 0) {
+    const unsigned int zero[2] = {0u, 0u};
+    cudaMemcpy(ws, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    char msg[128];
+    std::snprintf(msg, sizeof(msg), "kernel reported status %u at site 0x%x", err[0], err[1]);
+    return set_error_msg(msg, (qmuon_status)err[0]);
   }
   return QMUON_OK;
 }
@@ -529,3 +555,5 @@ extern "C" const char* qmuon_status_string(qmuon_status status) {
 }
 
 extern "C" const char* qmuon_version(void) { return "qmuon 0.1 sm_103a"; }
+
+extern "C" const char* qmuon_last_error(void) { return g_last_error; }

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <vector>
 
@@ -53,6 +54,7 @@ struct alignas(128) NsProb {
   int64_t x_ld[3];
   __nv_bfloat16* a;
   __nv_bfloat16* b;
+  int64_t ab_ld;          // row stride of A and B: m rounded up to 8 (16-byte rows for TMA)
   float* w;               // fp32 weights (stored orientation) or null
   int64_t w_ld;
   const float* inv;       // inverse norm applied on the first iteration, or null
@@ -192,6 +194,10 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) { return
 __device__ __forceinline__ uint32_t make_idesc(bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -349,9 +355,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     // ---- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----
     const int quarter = warp & 3;
     const int r = row0 + quarter * 32 + lane;
-    const bool ok = mbar_wait(done_bar, 0, args.hdr, 0x400u | KIND);
+    // while the tensor cores run, pull this thread's epilogue operands into L2
+    if (r < M_) {
+      const int span = (N_ - col0) < BN ? (N_ - col0) : BN;   // columns of this tile
+      if (KIND == G_POLY) {
+        const char* p = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + col0);
+        for (int o = 0; o < span * 2; o += 128) prefetch_l2(p + o);
+      } else if (KIND == G_UPDATE) {
+        const char* p = reinterpret_cast<const char*>(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + col0);
+        for (int o = 0; o < span * 2; o += 128) prefetch_l2(p + o);
+        if (args.apply_w && P.w) {
+          const char* q = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + col0);
+          for (int o = 0; o < span * 4; o += 128) prefetch_l2(q + o);
+        }
+      }
+    }
+    bool ok = mbar_wait(done_bar, 0, args.hdr, 0x400u | KIND);
     tc_fence_after();
-    if (ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u) {
+    ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
+    // tcgen05.ld is warp-collective: the whole warp reads TMEM or none of it does
+    if (__all_sync(0xffffffffu, ok ? 1 : 0)) {
       float s_first = 1.0f;
       if (args.first && P.inv) {
         const float iv = *P.inv;
@@ -367,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if (KIND == G_GRAM) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(acc[i]);
-          store_row32(P.a + (int64_t)r * P.m + cb, nv, out);
+          store_row32(P.a + (int64_t)r * P.ab_ld + cb, nv, out);
         } else if (KIND == G_POLY) {
           float av[32];
-          load_row32(P.a + (int64_t)r * P.m + cb, nv, av);
+          load_row32(P.a + (int64_t)r * P.ab_ld + cb, nv, av);
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[i] = args.cb * av[i] + args.cc * __uint_as_float(acc[i]);
-          store_row32(P.b + (int64_t)r * P.m + cb, nv, out);
+          store_row32(P.b + (int64_t)r * P.ab_ld + cb, nv, out);
         } else {
           float xv[32];
           load_row32(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + cb, nv, xv);
@@ -381,12 +404,32 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(acc[i]));
           store_row32(P.x[args.dst] + (int64_t)r * P.x_ld[args.dst] + cb, nv, out);
           if (args.apply_w && P.w) {
+            // W <- W - eta * bf16(U): one rounded product, one rounded difference
             float* wp = P.w + (int64_t)r * P.w_ld + cb;
+            if (nv >= 32) {
+              float4 wv[8];
+              const float4* src = reinterpret_cast<const float4*>(wp);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i < nv) {
-                const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
-                wp[i] = __fsub_rn(wp[i], __fmul_rn(args.eta, u));
+              for (int j = 0; j < 8; ++j) wv[j] = __ldcs(src + j);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float* e = reinterpret_cast<float*>(&wv[j]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float u = __bfloat162float(__float2bfloat16_rn(out[4 * j + k]));
+                  e[k] = __fsub_rn(e[k], __fmul_rn(args.eta, u));
+                }
+              }
+              float4* dstw = reinterpret_cast<float4*>(wp);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) __stcs(dstw + j, wv[j]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                if (i < nv) {
+                  const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
+                  wp[i] = __fsub_rn(wp[i], __fmul_rn(args.eta, u));
+                }
               }
             }
           }
@@ -426,10 +469,16 @@ EncodeTiledFn encoder() {
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && p) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+    } else {
+      char msg[160];
+      std::snprintf(msg, sizeof(msg), "driver entry point cuTensorMapEncodeTiled: %s, query result %d",
+                    cudaGetErrorString(e), (int)q);
+      set_error_msg(msg, QMUON_ERR_CUDA);
+    }
   }
   return fn;
 }
@@ -442,9 +491,18 @@ bool encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[256];
+    std::snprintf(msg, sizeof(msg),
+                  "cuTensorMapEncodeTiled returned %d for a %lld x %lld bf16 matrix (row stride %lld) at %p, map at %p",
+                  (int)r, (long long)rows, (long long)cols, (long long)ld, base, (void*)m);
+    set_error_msg(msg, QMUON_ERR_CUDA);
+    return false;
+  }
+  return true;
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -455,7 +513,8 @@ struct Shape {
 };
 size_t scratch_bytes(const Shape& s) {
   const int64_t m = std::min(s.rows, s.cols);
-  return 2 * align_up((size_t)(m * m) * 2, 256) + 2 * align_up((size_t)(s.rows * s.cols) * 2, 256);
+  const int64_t ld = (m + 7) / 8 * 8;
+  return 2 * align_up((size_t)(m * ld) * 2, 256) + 2 * align_up((size_t)(s.rows * s.cols) * 2, 256);
 }
 size_t table_bytes(int32_t n) { return align_up((size_t)n * sizeof(NsProb), 256) + align_up((size_t)3 * (n + 1) * 4, 256); }
 
@@ -469,10 +528,11 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   P.m = (int32_t)std::min(rows, cols);
   P.n = (int32_t)std::max(rows, cols);
   const int64_t m = P.m;
+  P.ab_ld = (m + 7) / 8 * 8;
   P.a = reinterpret_cast<__nv_bfloat16*>(ws);
-  ws += align_up((size_t)(m * m) * 2, 256);
+  ws += align_up((size_t)(m * P.ab_ld) * 2, 256);
   P.b = reinterpret_cast<__nv_bfloat16*>(ws);
-  ws += align_up((size_t)(m * m) * 2, 256);
+  ws += align_up((size_t)(m * P.ab_ld) * 2, 256);
   P.x[0] = static_cast<__nv_bfloat16*>(x0);
   P.x_ld[0] = ld;
   for (int i = 1; i < 3; ++i) {
@@ -485,7 +545,7 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   P.w_ld = w_ld;
   for (int i = 0; i < 3; ++i)
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
-  if (!encode_bf16(&P.map_a, P.a, m, m, m) || !encode_bf16(&P.map_b, P.b, m, m, m)) return false;
+  if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
   const int64_t tm = (m + BM - 1) / BM, tnm = (m + BN - 1) / BN;
   P.tiles_n[G_GRAM] = P.tiles_n[G_POLY] = (int32_t)tnm;
   P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)(tm * tnm);
@@ -511,15 +571,15 @@ void prefix(const std::vector<NsProb>& probs, std::vector<int32_t>& ts, int32_t 
   }
 }
 
-bool configure_kernels() {
-  static bool done = false, ok = false;
-  if (!done) {
-    ok = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
-         cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess &&
-         cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) == cudaSuccess;
-    done = true;
+cudaError_t configure_kernels() {
+  static cudaError_t result = cudaErrorNotReady;
+  if (result == cudaErrorNotReady) {
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    result = e;
   }
-  return ok;
+  return result;
 }
 
 cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
@@ -536,7 +596,8 @@ cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaS
 // iteration writes back into buffer 0 (its source is never 0 when iters >= 2).
 qmuon_status run_iterations(const Launchable& L, int32_t iters, const float coeffs[3], float eta, bool apply_w,
                             WsHeader* hdr, cudaStream_t s, const std::vector<NsProb>& host_probs) {
-  if (!configure_kernels()) return QMUON_ERR_CUDA;
+  const cudaError_t ce = configure_kernels();
+  if (ce != cudaSuccess) return set_error("newton-schulz: cudaFuncSetAttribute(max dynamic shared memory)", ce);
   GemmArgs a{};
   a.probs = L.d_probs;
   a.n_probs = L.n;
@@ -556,14 +617,15 @@ qmuon_status run_iterations(const Launchable& L, int32_t iters, const float coef
     cudaError_t e = launch_gemm(G_GRAM, L, a, s);
     if (e == cudaSuccess) e = launch_gemm(G_POLY, L, a, s);
     if (e == cudaSuccess) e = launch_gemm(G_UPDATE, L, a, s);
-    if (e != cudaSuccess) return QMUON_ERR_CUDA;
+    if (e != cudaSuccess) return set_error("newton-schulz: cudaLaunchKernel(ns_gemm)", e);
     src = dst;
   }
   if (src != 0) {
     for (int32_t p = 0; p < L.n; ++p) {
       copy_back_kernel<<<256, 256, 0, s>>>(L.d_probs, p, src);
     }
-    if (cudaGetLastError() != cudaSuccess) return QMUON_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error("newton-schulz: copy-back launch", e);
   }
   (void)host_probs;
   return QMUON_OK;
@@ -593,14 +655,14 @@ size_t batch_workspace_bytes(const qmuon_ns_problem* probs, int32_t n) {
 
 qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, const float coeffs[3],
                        WsHeader* hdr, unsigned char* ws, size_t ws_bytes, cudaStream_t s) {
-  if (!encoder()) return QMUON_ERR_CUDA;
+  if (!encoder()) return set_error_msg("cuTensorMapEncodeTiled not available from the driver", QMUON_ERR_CUDA);
   std::vector<NsProb> hp(n);
   unsigned char* table = ws;
   unsigned char* scratch = ws + table_bytes(n);
   for (int32_t i = 0; i < n; ++i) {
     if (!fill_problem(hp[i], probs[i].x, probs[i].rows, probs[i].cols, probs[i].ld, probs[i].inv_norm, nullptr, 0,
                       scratch))
-      return QMUON_ERR_CUDA;
+      return QMUON_ERR_CUDA;   // detail recorded by encode_bf16
   }
   if ((size_t)(scratch - ws) > ws_bytes) return QMUON_ERR_WORKSPACE_TOO_SMALL;
   Launchable L;
@@ -609,9 +671,9 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
   L.d_tile_start = reinterpret_cast<int32_t*>(table + align_up((size_t)n * sizeof(NsProb), 256));
   std::vector<int32_t> ts;
   prefix(hp, ts, L.total);
-  if (cudaMemcpyAsync(L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return QMUON_ERR_CUDA;
+  cudaError_t ce = cudaMemcpyAsync(L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return set_error("newton-schulz: upload problem table", ce);
   const qmuon_status st = run_iterations(L, iters, coeffs, 0.0f, false, hdr, s, hp);
   // the pageable host vectors are staged by the copies above before they return
   return st;
@@ -649,7 +711,7 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
   if (T && T->ws == ws && T->ws_bytes == ws_bytes && T->inv == inv && T->tile_r == tile_r && T->tile_c == tile_c &&
       std::equal(T->weights.begin(), T->weights.end(), weights))
     return QMUON_OK;
-  if (!encoder()) return QMUON_ERR_CUDA;
+  if (!encoder()) return set_error_msg("cuTensorMapEncodeTiled not available from the driver", QMUON_ERR_CUDA);
   std::vector<NsProb> hp;
   unsigned char* scratch = ws;
   int32_t g = 0;
@@ -662,7 +724,8 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
         NsProb P;
         const int64_t off = bi * th * C + bj * tw;
         void* x0 = static_cast<__nv_bfloat16*>(t[i].grad) + off;
-        if (!fill_problem(P, x0, th, tw, C, inv + g, weights[i] + off, C, scratch)) return QMUON_ERR_CUDA;
+        if (!fill_problem(P, x0, th, tw, C, inv + g, weights[i] + off, C, scratch))
+          return QMUON_ERR_CUDA;   // detail recorded by encode_bf16
         hp.push_back(P);
       }
   }
@@ -677,7 +740,8 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
     if (T->d_mem) cudaFree(T->d_mem);
     T->d_mem = nullptr;
     T->d_bytes = 0;
-    if (cudaMalloc(&T->d_mem, need) != cudaSuccess) return QMUON_ERR_CUDA;
+    const cudaError_t me = cudaMalloc(&T->d_mem, need);
+    if (me != cudaSuccess) return set_error("qmuon_step: cudaMalloc problem table", me);
     T->d_bytes = need;
   }
   T->L.n = np;
@@ -686,9 +750,9 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
                                                  align_up((size_t)np * sizeof(NsProb), 256));
   std::vector<int32_t> ts;
   prefix(hp, ts, T->L.total);
-  if (cudaMemcpy(T->L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(T->L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
-    return QMUON_ERR_CUDA;
+  cudaError_t ue = cudaMemcpy(T->L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice);
+  if (ue == cudaSuccess) ue = cudaMemcpy(T->L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice);
+  if (ue != cudaSuccess) return set_error("qmuon_step: upload problem table", ue);
   T->host = std::move(hp);
   T->ws = ws;
   T->ws_bytes = ws_bytes;

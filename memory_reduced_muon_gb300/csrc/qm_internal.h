@@ -67,6 +67,11 @@ struct UpdLaunch {
   float* group_inv;           // D or null
 };
 
+// Record the detail of a failure for qmuon_last_error() (api.cu); returns
+// QMUON_ERR_CUDA (or `status`) for convenient `return set_error(...)`.
+qmuon_status set_error(const char* where, cudaError_t e, qmuon_status status = QMUON_ERR_CUDA);
+qmuon_status set_error_msg(const char* msg, qmuon_status status);
+
 // Host-side launchers (update.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, bool carrier,
                           cudaStream_t stream);

@@ -189,10 +189,13 @@ __device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, in
 }
 
 // Steps 1-9 for one lane's 16 elements; returns the block's sum of m*m
-// (identical in all 16 lanes of the half-warp).
+// (identical in all 16 lanes of the half-warp).  The two half-warps of a warp
+// may be on different blocks or one may have none, so every shuffle names
+// only the 16 lanes of its own half.
 template <int QK, int DT, bool CARRIER>
 __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTensor& T, int64_t lb,
                                               int hl, float beta, float omb) {
+  const unsigned hmask = 0xFFFFu << (threadIdx.x & 16u);
   const int64_t e0 = lb * kBlock + hl * 16;
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(&in.q);
   // (1)-(2) dequantise: one division per block, one multiply per element
@@ -214,8 +217,8 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   float amax_l = amax;
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) {
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, o));
+    ss += __shfl_xor_sync(hmask, ss, o);
   }
   // (7) requantise: sc = 127 / amax, q = clamp(rint(m * sc), -127, 127)
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
@@ -263,7 +266,7 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   } else {
     // MXFP8 carrier: a 32-element row block is two neighbouring lanes (the
     // tensor's columns are a multiple of 32, so flat 32-groups are row blocks)
-    const float amax32 = fmaxf(amax_l, __shfl_xor_sync(0xffffffffu, amax_l, 1));
+    const float amax32 = fmaxf(amax_l, __shfl_xor_sync(hmask, amax_l, 1));
     const int byte = e8m0_of_amax(amax32);
     const float mult = pow2_from_e8m0(byte);
     uint32_t pw[4];

@@ -93,10 +93,13 @@ def test_batch_of_mixed_problems_and_strided_view():
     base = random_grad(384 * 1024, "bf16", 5).reshape(384, 1024)
     view_ref = bf16_to_f64(base[:, 256:512])
     others = [random_grad(r * c, "bf16", 6 + i).reshape(r, c) for i, (r, c) in enumerate([(96, 200), (700, 256)])]
-    refs = [ns.newton_schulz(view_ref)] + [ns.newton_schulz(bf16_to_f64(t)) for t in others]
+    inputs = [view_ref] + [bf16_to_f64(t) for t in others]
+    # the inverse norms travel as device scalars (a NULL inverse norm means 1)
+    invs = [torch.tensor([1.0 / (np.linalg.norm(x) + 1e-7)], dtype=torch.float32, device="cuda") for x in inputs]
+    refs = [ns.newton_schulz(x, inv_norm=float(i.item())) for x, i in zip(inputs, invs)]
     untouched = base[:, :256].clone()
-    probs = [q.ns_problem(base.data_ptr() + 256 * 2, 384, 256, ld=1024)] + \
-            [q.ns_problem(t, t.shape[0], t.shape[1]) for t in others]
+    probs = [q.ns_problem(base.data_ptr() + 256 * 2, 384, 256, ld=1024, inv_norm=invs[0])] + \
+            [q.ns_problem(t, t.shape[0], t.shape[1], inv_norm=i) for t, i in zip(others, invs[1:])]
     ws = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device="cuda")
     q.qmuon_newton_schulz_batched(probs, 5, COEFFS, ws)
     q.qmuon_sync_status(ws)
