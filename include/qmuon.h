@@ -204,6 +204,36 @@ QMUON_API qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, 
                         const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Largest tensor (elements) qmuon_update_normalize_noalloc accepts. */
+#define QMUON_NOALLOC_MAX_ELEMS ((int64_t)1 << 31)
+
+/* The momentum update of one tensor with one norm group, for callers that
+ * must not allocate device memory at this point -- for example a C caller
+ * with no device allocator at hand, or code inside a framework whose caching
+ * allocator owns the device's memory, where a side cudaMalloc could fail,
+ * fragment that pool or escape its accounting, and where cudaMalloc/cudaFree
+ * may also synchronise the device.  It needs no plan and no workspace and
+ * calls neither cudaMalloc nor cudaFree: its scratch (the last-CTA ticket and
+ * one partial sum per CTA, about 64 KB) is a static array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The arithmetic and outputs are those of
+ * qmuon_update_multi_normalize_groups on a plan holding this single tensor
+ * with normalize_mode 2.  The pages have no counterpart: this entry exists
+ * for integration only.
+ *   tensor     H  q8/absmax D, updated in place; grad D, IN gradient, OUT m
+ *   sumsq      D  one fp32, sum of m*m over the tensor, or NULL
+ *   inv_norm   D  one fp32, 1/(sqrt(sum)+1e-7), or NULL
+ * Tensors above QMUON_NOALLOC_MAX_ELEMS elements are rejected with
+ * QMUON_ERR_INVALID_ARGUMENT (qmuon_last_error says why).  The first call on
+ * a device looks up the array's device address with that device current;
+ * make that first call before any stream capture begins.  Every call uses the
+ * same array (the call clears what must start at zero), so calls that may
+ * overlap on the GPU -- on different streams or from different threads --
+ * race on it; enqueue them in order on one stream. */
+QMUON_API qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
+                                                      qmuon_dtype grad_dtype, float beta, float* sumsq,
+                                                      float* inv_norm, void* stream);
+
 /* Synchronise `stream` and report a kernel-side error recorded in `ws`
  * (QMUON_ERR_TIMEOUT when a bounded wait expired), then clear it. */
 QMUON_API qmuon_status qmuon_sync_status(void* ws, void* stream);

@@ -93,6 +93,7 @@ def lib() -> C.CDLL:
         "qmuon_status_string": (C.c_char_p, [i32]),
         "qmuon_version": (C.c_char_p, []),
         "qmuon_last_error": (C.c_char_p, []),
+        "qmuon_update_normalize_noalloc": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -106,7 +107,8 @@ def exported_symbols() -> list:
     return ["qmuon_plan_create", "qmuon_plan_destroy", "qmuon_plan_info", "qmuon_workspace_size",
             "qmuon_update_multi_normalize_groups", "qmuon_carrier_workspace_size",
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
-            "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error"]
+            "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
+            "qmuon_update_normalize_noalloc"]
 
 
 # --------------------------------------------------------------------------
@@ -267,6 +269,17 @@ def qmuon_step(plan: Plan, t: int, P: int, beta: float, eta_full: float, eta_blo
                           int(iters), _ptr(group_sumsq), _ptr(ws),
                           _nbytes(ws) if ws_bytes is None else int(ws_bytes), _stream(stream))
     _check(st, "qmuon_step")
+
+
+def qmuon_update_normalize_noalloc(q8, absmax, grad, rows: int, cols: int, q8_kind, grad_dtype, beta: float,
+                                   sumsq=None, inv_norm=None, stream=None):
+    """The single-tensor update whose scratch is a static array in the
+    library (no plan, no workspace, no device allocation)."""
+    t = tensor_desc(q8, absmax, grad, rows, cols)
+    st = lib().qmuon_update_normalize_noalloc(C.byref(t), Q8_KINDS.get(q8_kind, q8_kind),
+                                              DTYPES.get(grad_dtype, grad_dtype), float(beta), _ptr(sumsq),
+                                              _ptr(inv_norm), _stream(stream))
+    _check(st, "qmuon_update_normalize_noalloc")
 
 
 def qmuon_sync_status(ws, stream=None):

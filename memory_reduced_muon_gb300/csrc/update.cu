@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "qm_internal.h"
 
 namespace qm {
@@ -464,3 +466,107 @@ cudaError_t launch_scale_groups(const UpdLaunch& L, qmuon_dtype dt, const float*
 }
 
 }  // namespace qm
+
+// ---------------------------------------------------------------------------
+// Allocation-free single-tensor update (qmuon_update_normalize_noalloc).
+//
+// The same update kernel as above, launched for one tensor and one norm
+// group, with its scratch -- the workspace header holding the last-CTA ticket
+// and one fp64 partial sum per CTA -- in a file-scope device array instead of
+// a caller-provided workspace.  Host code cannot use the array's name as a
+// device address, so the address is looked up once per device with
+// cudaGetSymbolAddress (that device current) and passed to the kernel.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kStaticSlots = 8192;  // partial-sum slots: one per CTA of the launch
+static __device__ __align__(256) unsigned char g_static_scratch[qm::kWsHeader + kStaticSlots * sizeof(double)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device).
+cudaError_t static_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
+                                                       qmuon_dtype grad_dtype, float beta, float* sumsq,
+                                                       float* inv_norm, void* stream) {
+  using namespace qm;
+  // ---- host validation, before any CUDA call ----
+  if (!tensor) return set_error_msg("qmuon_update_normalize_noalloc: null tensor", QMUON_ERR_INVALID_ARGUMENT);
+  if (q8_kind != QMUON_Q8_INT8 && q8_kind != QMUON_Q8_UINT8) return QMUON_ERR_INVALID_ARGUMENT;
+  if (grad_dtype != QMUON_BF16 && grad_dtype != QMUON_FP16 && grad_dtype != QMUON_FP32) return QMUON_ERR_INVALID_ARGUMENT;
+  if (tensor->rows <= 0 || tensor->cols <= 0) return QMUON_ERR_INVALID_ARGUMENT;
+  if (tensor->cols > QMUON_NOALLOC_MAX_ELEMS / tensor->rows)
+    return set_error_msg("qmuon_update_normalize_noalloc: tensor larger than QMUON_NOALLOC_MAX_ELEMS, the capacity "
+                         "of the static scratch array", QMUON_ERR_INVALID_ARGUMENT);
+  const int64_t n = tensor->rows * tensor->cols;
+  if (!tensor->q8 || !tensor->absmax || !tensor->grad) return QMUON_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(tensor->q8) & 15) || (reinterpret_cast<uintptr_t>(tensor->grad) & 15) ||
+      (reinterpret_cast<uintptr_t>(tensor->absmax) & 3))
+    return QMUON_ERR_INVALID_ARGUMENT;
+  if ((sumsq && (reinterpret_cast<uintptr_t>(sumsq) & 3)) || (inv_norm && (reinterpret_cast<uintptr_t>(inv_norm) & 3)))
+    return QMUON_ERR_INVALID_ARGUMENT;
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (cudaGetDevice)", e);
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error_msg("qmuon_update_normalize_noalloc: device ordinal beyond the static table", QMUON_ERR_UNSUPPORTED);
+  void* scratch = nullptr;
+  e = static_scratch(dev, &scratch);
+  if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (cudaGetSymbolAddress)", e);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (SM count)", e);
+  const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
+  if (per_sm <= 0) return set_error_msg("qmuon_update_normalize_noalloc: occupancy query failed", QMUON_ERR_CUDA);
+
+  // launch geometry: whole waves of resident CTAs, <= kMaxChunk blocks each
+  const int64_t nb = (n + kBlock - 1) / kBlock;
+  const int64_t wave = (int64_t)sms * per_sm;
+  int64_t g = (nb <= wave * 16) ? (nb + 15) / 16 : wave * ((nb + wave * kMaxChunk - 1) / (wave * kMaxChunk));
+  if (g < 1) g = 1;
+  const int64_t chunk = (nb + g - 1) / g;
+  g = (nb + chunk - 1) / chunk;
+  if (g > kStaticSlots)
+    return set_error_msg("qmuon_update_normalize_noalloc: launch needs more partial-sum slots than the static "
+                         "scratch array holds", QMUON_ERR_INVALID_ARGUMENT);
+
+  UpdLaunch L{};
+  L.tensors = nullptr;
+  L.single.q8 = tensor->q8;
+  L.single.absmax = tensor->absmax;
+  L.single.grad = tensor->grad;
+  L.single.numel = n;
+  L.single.block_begin = 0;
+  L.n_tensors = 1;
+  L.nb_total = nb;
+  L.chunk = chunk;
+  L.grid = (int32_t)g;
+  L.beta = beta;
+  L.layout.n_groups = (sumsq || inv_norm) ? 1 : 0;  // block_group null: one group, one slot per CTA
+  L.header = static_cast<WsHeader*>(scratch);
+  L.partials = reinterpret_cast<double*>(static_cast<unsigned char*>(scratch) + kWsHeader);
+  L.group_sumsq = sumsq;
+  L.group_inv = inv_norm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the ticket must start at zero
+  e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
+  if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, false, s);
+  if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (launch)", e);
+  return QMUON_OK;
+}
