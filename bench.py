@@ -203,8 +203,8 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = workloads.get(args.workload)
-    if args.scale > 1:
-        w = workloads.scaled(w, args.scale)
+    if args.row_scale > 1:
+        w.matrices = [workloads.Matrix(m.name, max(8, m.rows // args.row_scale), m.cols) for m in w.matrices]
     mats = w.matrices
     n_params = w.numel
     stream = torch.cuda.current_stream()
@@ -357,7 +357,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=4)
-    ap.add_argument("--scale", type=int, default=1, help="divide matrix sizes (profiling captures only)")
+    ap.add_argument("--row-scale", type=int, default=1,
+                    help="divide every matrix's row count, keeping its columns and tiles (profiling captures only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_info()
@@ -370,8 +371,9 @@ def main():
     config = {"workload": wl_name, "description": w.name, "params": w.numel, "matrices": len(w.matrices),
               "P": w.P, "tile": list(w.tile), "ns_iters": w.iters, "beta": w.beta,
               "l2": "inputs larger than L2 (1.75 GB of bf16 gradients per step)", "parallelism": f"replicas x{world}"}
-    if args.scale > 1:
-        config["scale"] = f"1/{args.scale} (profiling only)"
+    if args.row_scale > 1:
+        config["row_scale"] = f"rows / {args.row_scale} (profiling only, not a reported number)"
+        config["params"] = sum(max(8, m.rows // args.row_scale) * m.cols for m in w.matrices)
 
     if args.impl == "reference":
         if rank != 0:

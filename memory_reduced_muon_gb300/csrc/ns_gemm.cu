@@ -40,8 +40,9 @@ constexpr uint32_t kBox = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16 = 8
 constexpr uint32_t kStageA = 2 * kBox;          // 128 rows (or columns) x 64
 constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
 constexpr uint32_t kStageBytes = kStageA + kStageB;
-constexpr uint32_t kTmemCols = 256;
-constexpr size_t kSmemBytes = STAGES * kStageBytes + 1024 + 256;
+constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
+constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // epilogue staging: half an output tile
+constexpr size_t kSmemBytes = STAGES * kStageBytes + kStageOutBytes + 1024 + 256;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2 };
@@ -69,6 +70,7 @@ struct GemmArgs {
   const NsProb* probs;
   const int32_t* tile_start;  // [n_probs + 1] prefix of tiles for this kind
   int32_t n_probs;
+  int32_t total_tiles;
   int32_t src, dst;           // X buffer indices read / written (G_UPDATE); src for G_GRAM
   int32_t first;              // apply inv (first iteration)
   int32_t apply_w;            // W -= eta * U (last iteration of a step)
@@ -238,58 +240,121 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* p, int n, const float
   }
 }
 
+// Output tile (I, J) of problem P for product KIND, from its index in the
+// problem's tile list.  Symmetric products list only the tiles that touch the
+// upper triangle (128 I < 256 J + 256), column block J by column block J.
+__device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local, int& I, int& J) {
+  if (kind == G_UPDATE) {
+    const int tn = P.tiles_n[G_UPDATE];
+    I = local / tn;
+    J = local % tn;
+    return;
+  }
+  const int TM = (P.m + BM - 1) / BM;
+  int j = 0;
+  for (;;) {
+    const int cnt = (2 * j + 2 < TM) ? 2 * j + 2 : TM;
+    if (local < cnt) {
+      I = local;
+      J = j;
+      return;
+    }
+    local -= cnt;
+    ++j;
+  }
+}
+
+struct TileGeom {
+  const NsProb* P;
+  int row0, col0;
+  int M_, N_, K_;
+  bool a_mn, b_mn;
+  const CUtensorMap* mapA;
+  const CUtensorMap* mapB;
+};
+
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                         ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), done_bar = smem_u32(bars + 2 * STAGES);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- which problem and which output tile ----
-  const int tile = blockIdx.x;
+__device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile) {
   int lo = 0, hi = args.n_probs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(args.tile_start + mid) <= tile) lo = mid; else hi = mid - 1;
   }
-  const NsProb& P = args.probs[lo];
-  const int local = tile - __ldg(args.tile_start + lo);
-  const int tn = P.tiles_n[KIND];
-  const int row0 = (local / tn) * BM, col0 = (local % tn) * BN;
-
-  int M_, N_, K_;
-  bool a_mn, b_mn;
-  const CUtensorMap* mapA;
-  const CUtensorMap* mapB;
+  TileGeom g;
+  g.P = args.probs + lo;
+  const NsProb& P = *g.P;
+  int I, J;
+  decode_tile(P, KIND, tile - __ldg(args.tile_start + lo), I, J);
+  g.row0 = I * BM;
+  g.col0 = J * BN;
   if (KIND == G_GRAM) {
-    M_ = P.m; N_ = P.m; K_ = P.n;
-    mapA = mapB = &P.map_x[args.src];
-    a_mn = b_mn = (P.tall != 0);
+    g.M_ = P.m; g.N_ = P.m; g.K_ = P.n;
+    g.mapA = g.mapB = &P.map_x[args.src];
+    g.a_mn = g.b_mn = (P.tall != 0);
   } else if (KIND == G_POLY) {
-    M_ = P.m; N_ = P.m; K_ = P.m;
-    mapA = mapB = &P.map_a;
-    a_mn = b_mn = false;
+    g.M_ = P.m; g.N_ = P.m; g.K_ = P.m;
+    g.mapA = g.mapB = &P.map_a;
+    g.a_mn = g.b_mn = false;
   } else if (!P.tall) {
-    M_ = P.m; N_ = P.n; K_ = P.m;
-    mapA = &P.map_b; a_mn = false;
-    mapB = &P.map_x[args.src]; b_mn = true;
+    g.M_ = P.m; g.N_ = P.n; g.K_ = P.m;
+    g.mapA = &P.map_b; g.a_mn = false;
+    g.mapB = &P.map_x[args.src]; g.b_mn = true;
   } else {
-    M_ = P.n; N_ = P.m; K_ = P.m;
-    mapA = &P.map_x[args.src]; a_mn = false;
-    mapB = &P.map_b; b_mn = false;
+    g.M_ = P.n; g.N_ = P.m; g.K_ = P.m;
+    g.mapA = &P.map_x[args.src]; g.a_mn = false;
+    g.mapB = &P.map_b; g.b_mn = false;
   }
-  const int num_kb = (K_ + BK - 1) / BK;
+  return g;
+}
+
+__device__ __forceinline__ void named_barrier_epilogue() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+// AND of `v` over the 128 epilogue threads (also a barrier among them), so the
+// four epilogue warps always take the same branch around their barriers.
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Persistent kernel: one CTA per SM walks the launch's tile list with stride
+// gridDim.x.  The shared-memory ring and the two TMEM accumulators carry over
+// from tile to tile, so loads for the next tile and the epilogue of the last
+// one overlap the tensor cores.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  uint32_t* stage_out = reinterpret_cast<uint32_t*>(smem + STAGES * kStageBytes);   // 128 x 64 words
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes + kStageOutBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = args.total_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(done_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4);   // one arrival per epilogue warp
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -304,104 +369,123 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer ----
-      fence_tensormap(mapA);
-      if (mapB != mapA) fence_tensormap(mapB);
-      int issued = 0;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % STAGES, round = kb / STAGES;
-        if (round > 0 && !mbar_wait(empty0 + 8 * s, (round - 1) & 1, args.hdr, 0x100u | KIND)) break;
-        const uint32_t bar = full0 + 8 * s;
-        mbar_expect_tx(bar, kStageBytes);
-        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
-        const int k0 = kb * BK;
-        if (!a_mn) {
-          tma_load_2d(sa, mapA, bar, k0, row0);
-          tma_load_2d(sa + kBox, mapA, bar, k0, row0 + 64);
-        } else {
-          tma_load_2d(sa, mapA, bar, row0, k0);
-          tma_load_2d(sa + kBox, mapA, bar, row0 + 64, k0);
-        }
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileGeom g = tile_geom<KIND>(args, tile);
+        fence_tensormap(g.mapA);
+        if (g.mapB != g.mapA) fence_tensormap(g.mapB);
+        const int num_kb = (g.K_ + BK - 1) / BK;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % STAGES, round = it / STAGES;
+          if (round > 0 && !mbar_wait(empty0 + 8 * s, (round - 1) & 1, args.hdr, 0x100u | KIND)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = full0 + 8 * s;
+          mbar_expect_tx(bar, kStageBytes);
+          const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+          const int k0 = kb * BK;
+          if (!g.a_mn) {
+            tma_load_2d(sa, g.mapA, bar, k0, g.row0);
+            tma_load_2d(sa + kBox, g.mapA, bar, k0, g.row0 + 64);
+          } else {
+            tma_load_2d(sa, g.mapA, bar, g.row0, k0);
+            tma_load_2d(sa + kBox, g.mapA, bar, g.row0 + 64, k0);
+          }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (!b_mn) tma_load_2d(sb + j * kBox, mapB, bar, k0, col0 + 64 * j);
-          else       tma_load_2d(sb + j * kBox, mapB, bar, col0 + 64 * j, k0);
+          for (int j = 0; j < 4; ++j) {
+            if (!g.b_mn) tma_load_2d(sb + j * kBox, g.mapB, bar, k0, g.col0 + 64 * j);
+            else         tma_load_2d(sb + j * kBox, g.mapB, bar, g.col0 + 64 * j, k0);
+          }
         }
-        ++issued;
       }
       // every load this thread issued has landed before the CTA may exit
-      for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
-        mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1, args.hdr, 0x200u | KIND);
+      for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
+        mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      const uint32_t idesc = make_idesc(a_mn, b_mn);
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % STAGES, round = kb / STAGES;
-        if (!mbar_wait(full0 + 8 * s, round & 1, args.hdr, 0x300u | KIND)) break;
+      int it = 0, ti = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++ti) {
+        const TileGeom g = tile_geom<KIND>(args, tile);
+        const uint32_t idesc = make_idesc(g.a_mn, g.b_mn);
+        const int acc = ti & 1, use = ti >> 1;
+        if (use > 0 && !mbar_wait(tempty0 + 8 * acc, (use - 1) & 1, args.hdr, 0x500u | KIND)) break;
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        const int num_kb = (g.K_ + BK - 1) / BK;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % STAGES, round = it / STAGES;
+          if (!mbar_wait(full0 + 8 * s, round & 1, args.hdr, 0x300u | KIND)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
-          const uint64_t bd = b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
-          mma_bf16(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = g.a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
+            const uint64_t bd = g.b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
+            mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * s);   // frees the stage once these MMAs are done
         }
-        mma_commit(empty0 + 8 * s);   // frees the stage once these MMAs are done
+        mma_commit(tfull0 + 8 * acc);   // accumulator ready (also on the error path)
       }
-      mma_commit(done_bar);           // accumulator complete (also on the error path)
     }
   } else {
-    // ---- epilogue: warps 2..5, TMEM lane quarter = warp % 4 ----
+    // ---- epilogue: warps 2..5; TMEM lane quarter = warp % 4 ----
     const int quarter = warp & 3;
-    const int r = row0 + quarter * 32 + lane;
-    // while the tensor cores run, pull this thread's epilogue operands into L2
-    if (r < M_) {
-      const int span = (N_ - col0) < BN ? (N_ - col0) : BN;   // columns of this tile
-      if (KIND == G_POLY) {
-        const char* p = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + col0);
-        for (int o = 0; o < span * 2; o += 128) prefetch_l2(p + o);
-      } else if (KIND == G_UPDATE) {
-        const char* p = reinterpret_cast<const char*>(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + col0);
-        for (int o = 0; o < span * 2; o += 128) prefetch_l2(p + o);
-        if (args.apply_w && P.w) {
-          const char* q = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + col0);
-          for (int o = 0; o < span * 4; o += 128) prefetch_l2(q + o);
+    const int ew = warp - 2;   // epilogue warp 0..3
+    int ti = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
+      const TileGeom g = tile_geom<KIND>(args, tile);
+      const NsProb& P = *g.P;
+      const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
+      const int acc = ti & 1, use = ti >> 1;
+      // pull this thread's epilogue operands into L2 while the tensor cores run
+      if (r < g.M_) {
+        const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
+        if (KIND == G_POLY) {
+          const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
+          for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
+        } else if (KIND == G_UPDATE) {
+          const char* px = reinterpret_cast<const char*>(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + g.col0);
+          for (int o = 0; o < span * 2; o += 128) prefetch_l2(px + o);
+          if (args.apply_w && P.w) {
+            const char* pw = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + g.col0);
+            for (int o = 0; o < span * 4; o += 128) prefetch_l2(pw + o);
+          }
         }
       }
-    }
-    bool ok = mbar_wait(done_bar, 0, args.hdr, 0x400u | KIND);
-    tc_fence_after();
-    ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
-    // tcgen05.ld is warp-collective: the whole warp reads TMEM or none of it does
-    if (__all_sync(0xffffffffu, ok ? 1 : 0)) {
+      bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
+      tc_fence_after();
+      ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
+      // tcgen05.ld is warp-collective, and the staging barriers need all four
+      // warps: all 128 epilogue threads continue or stop together
+      if (!epilogue_all(ok)) break;
       float s_first = 1.0f;
       if (args.first && P.inv) {
         const float iv = *P.inv;
         s_first = (KIND == G_GRAM) ? iv * iv : iv;
       }
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t acc[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(c * 32), acc);
-        const int cb = col0 + c * 32;
-        if (r >= M_ || cb >= N_) continue;
-        const int nv = N_ - cb;
-        float out[32];
-        if (KIND == G_GRAM) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(acc[i]);
-          store_row32(P.a + (int64_t)r * P.ab_ld + cb, nv, out);
-        } else if (KIND == G_POLY) {
-          float av[32];
-          load_row32(P.a + (int64_t)r * P.ab_ld + cb, nv, av);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = args.cb * av[i] + args.cc * __uint_as_float(acc[i]);
-          store_row32(P.b + (int64_t)r * P.ab_ld + cb, nv, out);
-        } else {
-          float xv[32];
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+
+      if (KIND == G_UPDATE) {
+        // X <- s3 (a X + B X) [, W -= eta U]: each thread owns one output row
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          const int cb = g.col0 + c * 32;
+          if (r >= g.M_ || cb >= g.N_) continue;
+          const int nv = g.N_ - cb;
+          float xv[32], out[32];
           load_row32(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + cb, nv, xv);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(acc[i]));
+          for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(v[i]));
           store_row32(P.x[args.dst] + (int64_t)r * P.x_ld[args.dst] + cb, nv, out);
           if (args.apply_w && P.w) {
             // W <- W - eta * bf16(U): one rounded product, one rounded difference
@@ -434,11 +518,90 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      } else {
+        // symmetric products: stage 128 x 128 halves in shared memory (4-byte
+        // words XOR-swizzled by row), store rows coalesced and, for tiles
+        // strictly above the diagonal, the transposed tile as well
+        __nv_bfloat16* outp = (KIND == G_GRAM) ? P.a : P.b;
+        const int64_t ld = P.ab_ld;
+        const int m = g.M_;
+        const bool mirror = (g.row0 + BM <= g.col0);
+        const int rl = quarter * 32 + lane;   // staging row of this thread
+        for (int h = 0; h < 2; ++h) {
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + (uint32_t)(h * 128 + c * 32), v);
+            float out[32];
+            if (KIND == G_GRAM) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
+            } else {
+              float av[32];
+              const int cb = g.col0 + h * 128 + c * 32;
+              if (r < m && cb < m) load_row32(P.a + (int64_t)r * ld + cb, m - cb, av);
+              else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) av[i] = 0.0f;
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int w = c * 16 + i;
+              stage_out[rl * 64 + (w ^ (rl & 31))] = pack_bf16(out[2 * i], out[2 * i + 1]);
+            }
+          }
+          if (h == 1) {   // every TMEM read of this accumulator is done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+          }
+          named_barrier_epilogue();
+          const int cbase = g.col0 + h * 128;
+          // rows: warp ew stores rows 32 ew .. 32 ew + 31, two words per lane
+          for (int rr = ew * 32; rr < ew * 32 + 32; ++rr) {
+            const int orow = g.row0 + rr;
+            if (orow >= m) break;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int w = lane + 32 * k;
+              const int col = cbase + 2 * w;
+              const uint32_t val = stage_out[rr * 64 + (w ^ (rr & 31))];
+              __nv_bfloat16* dst = outp + (int64_t)orow * ld + col;
+              if (col + 1 < m) *reinterpret_cast<uint32_t*>(dst) = val;
+              else if (col < m) *dst = __ushort_as_bfloat16((unsigned short)(val & 0xFFFFu));
+            }
+          }
+          if (mirror) {
+            // transposed: word w holds columns 2w, 2w+1 of row rr; they go to
+            // output rows cbase + 2w (+1), column row0 + rr
+            for (int w = ew * 16; w < ew * 16 + 16; ++w) {
+              const int orow = cbase + 2 * w;
+              if (orow >= m) break;
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const int rr = p * 32 + lane;
+                const int ocol = g.row0 + rr;
+                const uint32_t val = stage_out[rr * 64 + (w ^ (rr & 31))];
+                if (ocol < m) {
+                  outp[(int64_t)orow * ld + ocol] = __ushort_as_bfloat16((unsigned short)(val & 0xFFFFu));
+                  if (orow + 1 < m)
+                    outp[(int64_t)(orow + 1) * ld + ocol] = __ushort_as_bfloat16((unsigned short)(val >> 16));
+                }
+              }
+            }
+          }
+          named_barrier_epilogue();   // staging is free for the next half
+        }
       }
     }
   }
 
-  // ---- teardown: the accumulator is idle once done_bar has fired ----
+  // ---- teardown: the accumulators are idle once their last readers are done ----
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -546,9 +709,12 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   for (int i = 0; i < 3; ++i)
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
   if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
+  // symmetric products: only tiles touching the upper triangle (128 I < 256 J + 256)
   const int64_t tm = (m + BM - 1) / BM, tnm = (m + BN - 1) / BN;
+  int64_t sym = 0;
+  for (int64_t j = 0; j < tnm; ++j) sym += std::min<int64_t>(tm, 2 * j + 2);
   P.tiles_n[G_GRAM] = P.tiles_n[G_POLY] = (int32_t)tnm;
-  P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)(tm * tnm);
+  P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)sym;
   const int64_t um = P.tall ? P.n : P.m, un = P.tall ? P.m : P.n;   // G_UPDATE output (stored orientation)
   P.tiles_n[G_UPDATE] = (int32_t)((un + BN - 1) / BN);
   P.tiles[G_UPDATE] = (int32_t)(((um + BM - 1) / BM) * P.tiles_n[G_UPDATE]);
@@ -582,14 +748,27 @@ cudaError_t configure_kernels() {
   return result;
 }
 
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
 cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
   if (L.total[kind] == 0) return cudaSuccess;
   GemmArgs a = a0;
   a.tile_start = L.d_tile_start + kind * (L.n + 1);
+  a.total_tiles = L.total[kind];
   void* args[] = {&a};
   void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM>
            : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY> : (void*)ns_gemm_kernel<G_UPDATE>;
-  return cudaLaunchKernel(fn, dim3(L.total[kind]), dim3(kThreads), args, kSmemBytes, s);
+  const int grid = std::min(L.total[kind], num_sms());   // persistent: one CTA per SM
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, kSmemBytes, s);
 }
 
 // The iteration schedule over X buffers: 0 -> 1 -> 2 -> 1 -> ... and the last

@@ -45,8 +45,9 @@ template <> struct Grad<QMUON_BF16> {
     return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
   __device__ __forceinline__ static uint32_t pack2(float a, float b) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    // one cvt.rn.bf16x2.f32: both halves rounded to nearest even
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
   __device__ __forceinline__ static float load1(const void* p, int64_t i) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
@@ -63,8 +64,8 @@ template <> struct Grad<QMUON_FP16> {
     return __half2float(__ushort_as_half((unsigned short)((i & 1) ? (w >> 16) : (w & 0xFFFFu))));
   }
   __device__ __forceinline__ static uint32_t pack2(float a, float b) {
-    return (uint32_t)__half_as_ushort(__float2half_rn(a)) |
-           ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
   __device__ __forceinline__ static float load1(const void* p, int64_t i) {
     return __half2float(reinterpret_cast<const __half*>(p)[i]);
@@ -87,16 +88,27 @@ template <> struct Grad<QMUON_FP32> {
   }
 };
 
+// Stored codes as offset binary (u = q + 128): uint8 storage already is,
+// int8 storage differs in the top bit of every byte.
 template <int QK>
-__device__ __forceinline__ int decode_q(uint32_t w, int b) {
-  if (QK == QMUON_Q8_INT8) return (int)(int8_t)((w >> (8 * b)) & 0xFFu);
-  return (int)((w >> (8 * b)) & 0xFFu) - 128;
+__device__ __forceinline__ uint32_t to_offset_binary(uint32_t w) {
+  return (QK == QMUON_Q8_INT8) ? (w ^ 0x80808080u) : w;
 }
 
+// float(q) for byte b of an offset-binary word, exactly: prmt builds the
+// fp32 pattern 0x4B0000uu = 2^23 + u, and subtracting 2^23 + 128 (both exact)
+// leaves u - 128 = q.
+__device__ __forceinline__ float code_to_float(uint32_t u, int b) {
+  return __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650u | (uint32_t)b)), 8388736.0f);
+}
+
+// Four codes (their int32 low bytes, two's complement) into one stored word.
 template <int QK>
-__device__ __forceinline__ uint32_t encode_q(int q, int b) {
-  const uint32_t u = (QK == QMUON_Q8_INT8) ? (uint32_t)(q & 0xFF) : (uint32_t)((q + 128) & 0xFF);
-  return u << (8 * b);
+__device__ __forceinline__ uint32_t pack_codes(int q0, int q1, int q2, int q3) {
+  const uint32_t lo = __byte_perm((uint32_t)q0, (uint32_t)q1, 0x0040u);
+  const uint32_t hi = __byte_perm((uint32_t)q2, (uint32_t)q3, 0x0040u);
+  const uint32_t w = __byte_perm(lo, hi, 0x5410u);
+  return (QK == QMUON_Q8_INT8) ? w : (w ^ 0x80808080u);
 }
 
 // E8M0 exponent byte of a 32-element block: 127 + e with e the smallest
@@ -151,12 +163,12 @@ struct LaneIn {
 };
 
 template <int QK, int DT>
-__device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, int64_t lb, int hl) {
+__device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, int64_t lb, int hl, bool full) {
   const int64_t e0 = lb * kBlock + hl * 16;
   in.amax_old = __ldcs(T.absmax + lb);
   const int64_t rem = T.numel - e0;
   in.valid = rem >= 16 ? 16 : (rem > 0 ? (int)rem : 0);
-  if (in.valid == 16) {
+  if (full) {
     in.q = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(T.q8) + e0));
     constexpr int esz = (DT == QMUON_FP32) ? 4 : 2;
     const uint4* gp = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(T.grad) + e0 * esz);
@@ -193,24 +205,29 @@ __device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, in
 // Steps 1-9 for one lane's 16 elements; returns the block's sum of m*m
 // (identical in all 16 lanes of the half-warp).  The two half-warps of a warp
 // may be on different blocks or one may have none, so every shuffle names
-// only the 16 lanes of its own half.
-template <int QK, int DT, bool CARRIER>
+// only the 16 lanes of its own half.  FULL: the whole block lies inside the
+// tensor (every lane has 16 elements); the tail block of a tensor takes the
+// masked path, chosen by the whole half-warp together.
+template <int QK, int DT, bool CARRIER, bool FULL>
 __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTensor& T, int64_t lb,
                                               int hl, float beta, float omb) {
   const unsigned hmask = 0xFFFFu << (threadIdx.x & 16u);
   const int64_t e0 = lb * kBlock + hl * 16;
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(&in.q);
+  uint32_t u[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) u[w] = to_offset_binary<QK>(qw[w]);
   // (1)-(2) dequantise: one division per block, one multiply per element
   const float s_old = __fdiv_rn(in.amax_old, 127.0f);
   float m[16];
   float amax = 0.0f, ss = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float old = __fmul_rn(__int2float_rn(decode_q<QK>(qw[i >> 2], i & 3)), s_old);
+    const float old = __fmul_rn(code_to_float(u[i >> 2], i & 3), s_old);
     const float g = Grad<DT>::get(in.g, i);
     // (4) m = beta * old + (1 - beta) * g: two rounded products, one rounded sum
     float mi = __fadd_rn(__fmul_rn(beta, old), __fmul_rn(omb, g));
-    if (i >= in.valid) mi = 0.0f;
+    if (!FULL && i >= in.valid) mi = 0.0f;
     m[i] = mi;
     amax = fmaxf(amax, fabsf(mi));
     ss = fmaf(mi, mi, ss);
@@ -222,18 +239,17 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
     amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, o));
     ss += __shfl_xor_sync(hmask, ss, o);
   }
-  // (7) requantise: sc = 127 / amax, q = clamp(rint(m * sc), -127, 127)
+  // (7) requantise: sc = 127 / amax, q = rint(m * sc).  No clamp is needed:
+  // |m| <= amax, so |m * sc| <= 127 (1 + 2^-24) and rounds to at most 127;
+  // amax == 0 gives sc = 0 and q = 0; a NaN product converts to 0.
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
-  uint32_t qo[4] = {0u, 0u, 0u, 0u};
+  uint32_t qo[4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    int q = __float2int_rn(__fmul_rn(m[i], sc));
-    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-    if (amax == 0.0f) q = 0;
-    qo[i >> 2] |= encode_q<QK>(q, i & 3);
-  }
+  for (int w = 0; w < 4; ++w)
+    qo[w] = pack_codes<QK>(__float2int_rn(__fmul_rn(m[4 * w], sc)), __float2int_rn(__fmul_rn(m[4 * w + 1], sc)),
+                           __float2int_rn(__fmul_rn(m[4 * w + 2], sc)), __float2int_rn(__fmul_rn(m[4 * w + 3], sc)));
   uint8_t* q8p = static_cast<uint8_t*>(T.q8) + e0;
-  if (in.valid == 16) {
+  if (FULL) {
     __stcs(reinterpret_cast<uint4*>(q8p), make_uint4(qo[0], qo[1], qo[2], qo[3]));
   } else {
 #pragma unroll
@@ -244,7 +260,7 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
 
   if constexpr (!CARRIER) {
     // (5) the momentum overwrites the gradient
-    if (in.valid == 16) {
+    if (FULL) {
       constexpr int esz = (DT == QMUON_FP32) ? 4 : 2;
       uint4* gp = reinterpret_cast<uint4*>(static_cast<uint8_t*>(T.grad) + e0 * esz);
       if constexpr (DT == QMUON_FP32) {
@@ -278,7 +294,7 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
       const uint32_t hi = cvt_e4m3x2(__fmul_rn(m[4 * v + 2], mult), __fmul_rn(m[4 * v + 3], mult));
       pw[v] = lo | (hi << 16);
     }
-    if (in.valid == 16) {
+    if (FULL || in.valid == 16) {
       __stcs(reinterpret_cast<uint4*>(T.payload + e0), make_uint4(pw[0], pw[1], pw[2], pw[3]));
       if ((hl & 1) == 0) T.scale[e0 >> 5] = (uint8_t)byte;
     }
@@ -328,17 +344,22 @@ __global__ void __launch_bounds__(kUpdThreads, 3) update_kernel(UpdLaunch L) {
     const UpdTensor T0 = single ? L.single : L.tensors[t];
     const UpdTensor T1 = single ? L.single : L.tensors[t2];
     LaneIn<DT> in0, in1;
-    load_lane<QK, DT>(in0, T0, k - T0.block_begin, hl);
-    if (has2) load_lane<QK, DT>(in1, T1, k2 - T1.block_begin, hl);
+    const int64_t lb0 = k - T0.block_begin, lb1 = k2 - T1.block_begin;
+    const bool full0 = (lb0 + 1) * kBlock <= T0.numel;   // uniform across the half-warp
+    const bool full1 = (lb1 + 1) * kBlock <= T1.numel;
+    load_lane<QK, DT>(in0, T0, lb0, hl, full0);
+    if (has2) load_lane<QK, DT>(in1, T1, lb1, hl, full1);
     int32_t g0 = 0, g1 = 0;
     if (reduce && hl == 0 && L.layout.block_group) {
       g0 = __ldg(L.layout.block_group + k);
       if (has2) g1 = __ldg(L.layout.block_group + k2);
     }
-    const float ss0 = compute_lane<QK, DT, CARRIER>(in0, T0, k - T0.block_begin, hl, beta, omb);
+    const float ss0 = full0 ? compute_lane<QK, DT, CARRIER, true>(in0, T0, lb0, hl, beta, omb)
+                            : compute_lane<QK, DT, CARRIER, false>(in0, T0, lb0, hl, beta, omb);
     if (reduce && hl == 0) { s_bsum[k - kb] = ss0; s_bgrp[k - kb] = g0; }
     if (has2) {
-      const float ss1 = compute_lane<QK, DT, CARRIER>(in1, T1, k2 - T1.block_begin, hl, beta, omb);
+      const float ss1 = full1 ? compute_lane<QK, DT, CARRIER, true>(in1, T1, lb1, hl, beta, omb)
+                              : compute_lane<QK, DT, CARRIER, false>(in1, T1, lb1, hl, beta, omb);
       if (reduce && hl == 0) { s_bsum[k2 - kb] = ss1; s_bgrp[k2 - kb] = g1; }
     }
     t = t2;
