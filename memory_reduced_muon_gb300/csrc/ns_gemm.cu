@@ -34,15 +34,24 @@ namespace qm {
 namespace ns {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kThreads = 192;
 constexpr uint32_t kBox = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16 = 8 KB
 constexpr uint32_t kStageA = 2 * kBox;          // 128 rows (or columns) x 64
 constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
-constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // epilogue staging: half an output tile
-constexpr size_t kSmemBytes = STAGES * kStageBytes + kStageOutBytes + 1024 + 256;
+constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // symmetric epilogue staging: half an output tile
+constexpr uint32_t kXTileBytes = 8 * kBox;           // G_UPDATE: the 128 x 256 X tile of the a X term
+
+// Shared memory per product kind: the symmetric products keep 4 operand
+// stages and a staging buffer for coalesced (and mirrored) stores; the
+// update product keeps 3 stages and a TMA-loaded copy of its X output tile.
+__host__ __device__ constexpr int stages_of(int kind) { return kind == 2 ? 3 : 4; }
+__host__ __device__ constexpr uint32_t side_bytes_of(int kind) { return kind == 2 ? kXTileBytes : kStageOutBytes; }
+__host__ __device__ constexpr size_t smem_bytes_of(int kind) {
+  return (size_t)stages_of(kind) * kStageBytes + side_bytes_of(kind) + 1024 + 256;
+}
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2 };
@@ -335,13 +344,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  constexpr int STAGES = stages_of(KIND);
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  uint32_t* stage_out = reinterpret_cast<uint32_t*>(smem + STAGES * kStageBytes);   // 128 x 64 words
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kStageBytes + kStageOutBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  unsigned char* side = smem + STAGES * kStageBytes;          // staging (symmetric) or X tile (update)
+  uint32_t* stage_out = reinterpret_cast<uint32_t*>(side);    // 128 x 64 words
+  uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 6);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t xfull = smem_u32(bars + 2 * STAGES + 4), xempty = smem_u32(bars + 2 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = args.total_tiles;
@@ -355,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       mbar_init(tfull0 + 8 * b, 1);
       mbar_init(tempty0 + 8 * b, 4);   // one arrival per epilogue warp
     }
+    mbar_init(xfull, 1);
+    mbar_init(xempty, 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer ----
-      int it = 0;
+      int it = 0, xt = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileGeom g = tile_geom<KIND>(args, tile);
@@ -399,10 +413,29 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             else         tma_load_2d(sb + j * kBox, g.mapB, bar, g.col0 + 64 * j, k0);
           }
         }
+        if (KIND == G_UPDATE && ok) {
+          // the X tile of the a X term (output orientation), once the previous
+          // tile's epilogue has finished reading the buffer
+          if (xt > 0 && !mbar_wait(xempty, (xt - 1) & 1, args.hdr, 0x600u | KIND)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* mx = &g.P->map_x[args.src];
+          if (mx != g.mapA && mx != g.mapB) fence_tensormap(mx);
+          mbar_expect_tx(xfull, kXTileBytes);
+          const uint32_t xs = smem_u32(side);
+#pragma unroll
+          for (int bi = 0; bi < 2; ++bi)
+#pragma unroll
+            for (int bj = 0; bj < 4; ++bj)
+              tma_load_2d(xs + (bi * 4 + bj) * kBox, mx, xfull, g.col0 + 64 * bj, g.row0 + 64 * bi);
+          ++xt;
+        }
       }
       // every load this thread issued has landed before the CTA may exit
       for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
         mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
+      if (KIND == G_UPDATE && xt > 0) mbar_wait(xfull, (xt - 1) & 1, args.hdr, 0x700u | KIND);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -453,8 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
           for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
         } else if (KIND == G_UPDATE) {
-          const char* px = reinterpret_cast<const char*>(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + g.col0);
-          for (int o = 0; o < span * 2; o += 128) prefetch_l2(px + o);
           if (args.apply_w && P.w) {
             const char* pw = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + g.col0);
             for (int o = 0; o < span * 4; o += 128) prefetch_l2(pw + o);
@@ -475,15 +506,31 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 
       if (KIND == G_UPDATE) {
-        // X <- s3 (a X + B X) [, W -= eta U]: each thread owns one output row
+        // X <- s3 (a X + B X) [, W -= eta U]: each thread owns one output row;
+        // its X row comes from the TMA copy in shared memory (128-byte swizzle:
+        // box (row/64, col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
+        const bool xok = mbar_wait(xfull, ti & 1, args.hdr, 0x800u | KIND);
+        const int rl = quarter * 32 + lane;
+        const unsigned char* xrow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
           const int cb = g.col0 + c * 32;
-          if (r >= g.M_ || cb >= g.N_) continue;
+          if (!xok || r >= g.M_ || cb >= g.N_) continue;
           const int nv = g.N_ - cb;
           float xv[32], out[32];
-          load_row32(P.x[args.src] + (int64_t)r * P.x_ld[args.src] + cb, nv, xv);
+          {
+            const unsigned char* bx = xrow + (c >> 1) * kBox;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int q = (c & 1) * 4 + t;
+              const uint4 u4 = *reinterpret_cast<const uint4*>(bx + ((q ^ (rl & 7)) << 4));
+              xv[8 * t + 0] = bf16_lo(u4.x); xv[8 * t + 1] = bf16_hi(u4.x);
+              xv[8 * t + 2] = bf16_lo(u4.y); xv[8 * t + 3] = bf16_hi(u4.y);
+              xv[8 * t + 4] = bf16_lo(u4.z); xv[8 * t + 5] = bf16_hi(u4.z);
+              xv[8 * t + 6] = bf16_lo(u4.w); xv[8 * t + 7] = bf16_hi(u4.w);
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(v[i]));
           store_row32(P.x[args.dst] + (int64_t)r * P.x_ld[args.dst] + cb, nv, out);
@@ -520,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        if (lane == 0) {
+          mbar_arrive(tempty0 + 8 * acc);
+          mbar_arrive(xempty);   // the X buffer may be refilled
+        }
       } else {
         // symmetric products: stage 128 x 128 halves in shared memory (4-byte
         // words XOR-swizzled by row), store rows coalesced and, for tiles
@@ -740,9 +790,9 @@ void prefix(const std::vector<NsProb>& probs, std::vector<int32_t>& ts, int32_t 
 cudaError_t configure_kernels() {
   static cudaError_t result = cudaErrorNotReady;
   if (result == cudaErrorNotReady) {
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_GRAM));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_POLY));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_UPDATE));
     result = e;
   }
   return result;
@@ -768,7 +818,7 @@ cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaS
   void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM>
            : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY> : (void*)ns_gemm_kernel<G_UPDATE>;
   const int grid = std::min(L.total[kind], num_sms());   // persistent: one CTA per SM
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, kSmemBytes, s);
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem_bytes_of(kind), s);
 }
 
 // The iteration schedule over X buffers: 0 -> 1 -> 2 -> 1 -> ... and the last
