@@ -157,8 +157,11 @@ typedef enum { QMUON_NS_BF16 = 0, QMUON_NS_MXFP8 = 1 } qmuon_ns_input;
  *                 (MXFP8 input: OUT only)
  *   inv_norm   D  fp32 scalar applied to the input, or NULL for 1
  *   input      QMUON_NS_BF16, or QMUON_NS_MXFP8 with payload/scale_inv:
- *   payload    D  rows x cols E4M3 codes (row stride cols), cols % 32 == 0
- *   scale_inv  D  rows x (cols/32) E8M0 bytes */
+ *   payload    D  rows x cols E4M3 codes (row stride cols), cols % 32 == 0,
+ *                 16-byte aligned -- the carrier of qmuon_update_mxfp8_carrier
+ *   scale_inv  D  rows x (cols/32) E8M0 bytes
+ * An MXFP8 problem is expanded exactly (E4M3 times a power of two fits in
+ * bf16) into x, which then receives the result; inv_norm is the carrier's. */
 typedef struct {
   void* x;
   int64_t rows;

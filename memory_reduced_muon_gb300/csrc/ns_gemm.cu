@@ -22,6 +22,7 @@
 // winds down instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -660,6 +661,42 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   }
 }
 
+// MXFP8 carrier -> bf16 Newton-Schulz input: x[r][c] = E4M3(payload[r][c]) *
+// 2^(scale[r][c/32] - 127).  An E4M3 value has at most 4 significant bits, so
+// the product with a power of two is exact in bf16 (within bf16's exponent
+// range); the carrier is consumed as it is, the inverse norm is applied later
+// by the first iteration.  One thread per 16 payload bytes.
+__global__ void decode_carrier_kernel(const uint8_t* __restrict__ payload, const uint8_t* __restrict__ scale,
+                                      __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ld) {
+  const int64_t per_row = cols / 16;
+  const int64_t total = rows * per_row;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / per_row, c0 = (v % per_row) * 16;
+    const uint4 p = *reinterpret_cast<const uint4*>(payload + r * cols + c0);
+    const int e = (int)scale[r * (cols / 32) + c0 / 32] - 127;
+    // 2^e as fp32 (e in [-127, 127]; 2^-127 is the subnormal 0x00400000)
+    const float mult = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // two E4M3 codes -> two halves (exact), then fp32, scale, bf16
+        const unsigned short pair = (unsigned short)((w[k] >> (16 * h)) & 0xFFFFu);
+        uint32_t hh;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pair));
+        const __half2 hv = *reinterpret_cast<const __half2*>(&hh);
+        const float lo = __fmul_rn(__low2float(hv), mult), hi = __fmul_rn(__high2float(hv), mult);
+        o[2 * k + h] = pack_bf16(lo, hi);
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(x + r * ld + c0);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // Copy the workspace result back to the caller's matrix (single-iteration runs).
 __global__ void copy_back_kernel(const NsProb* probs, int32_t p, int32_t from) {
   const NsProb& P = probs[p];
@@ -872,7 +909,10 @@ qmuon_status validate_problem(const qmuon_ns_problem& p) {
   if (p.ld < p.cols) return QMUON_ERR_INVALID_ARGUMENT;
   if (p.ld % 8 || p.cols % 8) return QMUON_ERR_UNSUPPORTED;
   if (p.inv_norm && (reinterpret_cast<uintptr_t>(p.inv_norm) & 3)) return QMUON_ERR_INVALID_ARGUMENT;
-  if (p.input == QMUON_NS_MXFP8) return QMUON_ERR_UNSUPPORTED;
+  if (p.input == QMUON_NS_MXFP8) {
+    if (!p.payload || !p.scale_inv || (reinterpret_cast<uintptr_t>(p.payload) & 15)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (p.cols % 32) return QMUON_ERR_UNSUPPORTED;
+  }
   return QMUON_OK;
 }
 
@@ -903,6 +943,17 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
   cudaError_t ce = cudaMemcpyAsync(L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice, s);
   if (ce == cudaSuccess) ce = cudaMemcpyAsync(L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s);
   if (ce != cudaSuccess) return set_error("newton-schulz: upload problem table", ce);
+  // MXFP8 inputs: expand the carrier into the problem's bf16 matrix first
+  for (int32_t i = 0; i < n; ++i) {
+    if (probs[i].input != QMUON_NS_MXFP8) continue;
+    const int64_t vecs = probs[i].rows * (probs[i].cols / 16);
+    const int grid = (int)std::min<int64_t>((vecs + 255) / 256, (int64_t)num_sms() * 8);
+    decode_carrier_kernel<<<grid, 256, 0, s>>>(probs[i].payload, probs[i].scale_inv,
+                                               static_cast<__nv_bfloat16*>(probs[i].x), probs[i].rows, probs[i].cols,
+                                               probs[i].ld);
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess) return set_error("newton-schulz: carrier decode launch", ce);
+  }
   const qmuon_status st = run_iterations(L, iters, coeffs, 0.0f, false, hdr, s, hp);
   // the pageable host vectors are staged by the copies above before they return
   return st;
