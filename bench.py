@@ -133,12 +133,19 @@ def dist_info():
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (replicas: the job ends when the last one does)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(n_params: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job Mparams/s: every rank runs its own replica of the workload."""
+    return world * n_params * steps / (ms_max / 1e3) / 1e6
 
 
 def barrier(world):
@@ -197,6 +204,88 @@ def oracle_sample(w, budget_s=15.0):
 # the GPU leg
 # --------------------------------------------------------------------------
 
+def run_gpu_carrier(args, world, rank, local, w):
+    """Workload 5: per-matrix MXFP8 carrier update (E4M3 payload + E8M0 scales
+    + inverse norm; the gradient is only read) followed by full Newton-Schulz
+    on every matrix, fed by the carrier.  The orthogonalised update lands in
+    the gradient buffer; no weight update is part of this workload."""
+    import memory_reduced_muon_gb300 as q
+
+    dev = torch.device("cuda", local)
+    mats = w.matrices
+    stream = torch.cuda.current_stream()
+    states = [workloads.zero_state(m, w.q8_kind, device=dev) for m in mats]
+    grads = [torch.empty(m.rows, m.cols, dtype=torch.bfloat16, device=dev) for m in mats]
+    pool = [[workloads.make_grad(w, i, s + 1, device=dev) for i in range(len(mats))] for s in range(2)]
+    payload = [torch.empty(m.numel, dtype=torch.uint8, device=dev) for m in mats]
+    scale = [torch.empty(m.rows * (m.cols // 32), dtype=torch.uint8, device=dev) for m in mats]
+    inv = torch.zeros(len(mats), dtype=torch.float32, device=dev)
+    ws_c = torch.empty(max(q.qmuon_carrier_workspace_size(m.rows, m.cols) for m in mats), dtype=torch.uint8,
+                       device=dev)
+    probs = [q.ns_problem(g, m.rows, m.cols, inv_norm=inv.data_ptr() + 4 * i, input_kind=q.QMUON_NS_MXFP8,
+                          payload=payload[i], scale_inv=scale[i]) for i, (g, m) in enumerate(zip(grads, mats))]
+    ws_n = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device=dev)
+
+    def refill(t):
+        for g, s in zip(grads, pool[t % 2]):
+            g.copy_(s, non_blocking=True)
+
+    def carrier_all():
+        for i, m in enumerate(mats):
+            q.qmuon_update_mxfp8_carrier(states[i][0], states[i][1], grads[i], m.rows, m.cols, w.q8_kind, "bf16",
+                                         w.beta, payload[i], scale[i], inv.data_ptr() + 4 * i, ws_c, stream=stream)
+
+    def step(t):
+        carrier_all()
+        q.qmuon_newton_schulz_batched(probs, w.iters, w.coeffs, ws_n, stream=stream)
+
+    t = 0
+    for _ in range(max(args.warmup, 1)):
+        t += 1
+        refill(t)
+        step(t)
+    q.qmuon_sync_status(ws_n, stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        refill(t)
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    q.qmuon_sync_status(ws_n, stream)
+    # the carrier update alone and the Newton-Schulz alone
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(3):
+        carrier_all()
+    u1.record(stream)
+    torch.cuda.synchronize()
+    upd_ms = u0.elapsed_time(u1) / 3
+    n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0.record(stream)
+    for _ in range(3):
+        q.qmuon_newton_schulz_batched(probs, w.iters, w.coeffs, ws_n, stream=stream)
+    n1.record(stream)
+    torch.cuda.synchronize()
+    ns_ms = n0.elapsed_time(n1) / 3
+    n_params = w.numel
+    upd_bytes = (1 + 2 + 1 + 1 + 1.0 / 32 + 8.0 / 256) * n_params
+    flop = step_ns_flops(w, True)
+    return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks,
+                per_step=[], upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes,
+                ns_ms={"full": ns_ms}, ns_flop={"full": flop}, e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
+                launches=(len(mats) + 1 + 3 * w.iters) * args.steps, n_params=n_params, w=w)
+
+
 def run_gpu(args, world, rank, local):
     import memory_reduced_muon_gb300 as q
 
@@ -205,6 +294,8 @@ def run_gpu(args, world, rank, local):
     w = workloads.get(args.workload)
     if args.row_scale > 1:
         w.matrices = [workloads.Matrix(m.name, max(8, m.rows // args.row_scale), m.cols) for m in w.matrices]
+    if w.carrier:
+        return run_gpu_carrier(args, world, rank, local, w)
     mats = w.matrices
     n_params = w.numel
     stream = torch.cuda.current_stream()
@@ -270,7 +361,7 @@ def run_gpu(args, world, rank, local):
     ms = e0.elapsed_time(e1)
     q.qmuon_sync_status(ws, stream)
     ms_max = max_over_ranks(ms, world)
-    value = world * n_params * args.steps / (ms_max / 1e3) / 1e6
+    value = job_throughput(n_params, args.steps, world, ms_max)
 
     # ---- per-kernel timing: the update alone and the Newton-Schulz engine alone ----
     plan_u = q.qmuon_plan_create([(s[0], s[1], g, m.rows, m.cols) for s, g, m in zip(states, grads, mats)],
@@ -414,8 +505,8 @@ def main():
             "full_steps_timed": r["n_full"], "per_step": r["per_step"],
             "update_gbs": r["upd_gbs"], "ns_tflops": ns_tflops,
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
-            "e2e": {"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"]},
+            "e2e": ({"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
+                     "d2h_bytes_per_step": r["d2h"]} if r["e2e_value"] is not None else None),
             "gpu_launches": r["launches"]}
     if not args.no_cpu_baseline:
         v, sample, cores, dt = oracle_sample(w, budget_s=15.0)

@@ -1,0 +1,73 @@
+"""The multi-process path of bench.py on CPU (gloo, world size 2).
+
+The quantized Muon step does not shard across GPUs here ("replicas only"):
+every rank runs its own copy of the workload and the job's time is the
+slowest rank's.  These tests run the bench's rank helpers in two gloo
+processes and the CPU-oracle leg on a small sample.
+"""
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, local = bench.dist_info()
+        assert (ws, r, local) == (world, rank, rank)
+        bench.barrier(world)
+        t = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+        v = bench.job_throughput(1_000_000, 4, world, t)
+        out.put((rank, t, v))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_and_throughput():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # every rank sees the slowest rank's 15 ms; 2 replicas x 1M params x 4 steps in 15 ms
+    assert [r[1] for r in res] == [15.0, 15.0]
+    assert all(abs(r[2] - 2 * 1e6 * 4 / 0.015 / 1e6) < 1e-6 for r in res)
+
+
+def test_single_rank_helpers():
+    assert bench.max_over_ranks(3.0, 1) == 3.0
+    assert bench.job_throughput(872_415_232, 10, 1, 1000.0) == pytest.approx(8724.15232)
+
+
+def test_oracle_sample_leg():
+    v, sample, cores, dt = bench.oracle_sample(workloads.get(1), budget_s=5.0)
+    assert v > 0 and cores >= 1 and "512x512" in sample
+
+
+def test_step_flop_count_matches_page_formula():
+    w = workloads.get(4)
+    full = bench.step_ns_flops(w, True)
+    block = bench.step_ns_flops(w, False)
+    assert abs(full - 8.324e13) / 8.324e13 < 1e-3      # 2(2nm^2+m^3) x 5 over the 28 matrices
+    assert abs(block - 1.705e13) / 1.705e13 < 1e-3     # the same over 224 tiles of 1x8 columns
