@@ -45,17 +45,27 @@ constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulato
 constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // symmetric epilogue staging: half an output tile
 constexpr uint32_t kXTileBytes = 8 * kBox;           // G_UPDATE: the 128 x 256 X tile of the a X term
 
-// Shared memory per product kind: the symmetric products keep 4 operand
-// stages and a staging buffer for coalesced (and mirrored) stores; the
-// update product keeps 3 stages and a TMA-loaded copy of its X output tile.
-__host__ __device__ constexpr int stages_of(int kind) { return kind == 2 ? 3 : 4; }
-__host__ __device__ constexpr uint32_t side_bytes_of(int kind) { return kind == 2 ? kXTileBytes : kStageOutBytes; }
-__host__ __device__ constexpr size_t smem_bytes_of(int kind) {
-  return (size_t)stages_of(kind) * kStageBytes + side_bytes_of(kind) + 1024 + 256;
+// Shared memory per product kind and CTA group.  One CTA (CG = 1) owns a
+// 128 x 256 output tile and loads all of A (128 rows) and B (256 rows) per
+// stage (48 KB); a CTA pair (CG = 2) owns 256 x 256, each CTA loading its
+// 128 rows of A and half of B (32 KB per stage per CTA).  The symmetric
+// products keep a staging buffer for coalesced (and mirrored) stores; the
+// update product keeps a TMA-loaded copy of its X output tile.
+__host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ? 4 * kBox : kStageBytes; }
+__host__ __device__ constexpr int stages_of(int kind, int cg) {
+  return cg == 2 ? (kind == 2 ? 4 : 6) : (kind == 2 ? 3 : 4);
 }
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+__host__ __device__ constexpr uint32_t side_bytes_of(int kind) { return kind == 2 ? kXTileBytes : kStageOutBytes; }
+__host__ __device__ constexpr size_t smem_bytes_of(int kind, int cg) {
+  return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind) + 1024 + 256;
+}
+
+constexpr long long kWaitCycles = 4000000000LL;  // bounded waits: ~2 s at 2 GHz
 
 enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2 };
+
+// CTA group of the Newton-Schulz GEMMs: 2 = CTA pairs (cta_group::2).
+constexpr int kCG = 2;
 
 struct alignas(128) NsProb {
   CUtensorMap map_x[3];   // X buffers: 0 = caller's matrix, 1/2 = workspace ping-pong
@@ -144,31 +154,85 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void fence_tensormap(const CUtensorMap* map) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
+// ---- CTA-pair (cta_group::2) forms: every tcgen05 instruction of a kernel
+// uses the same CTA group, so each wrapper is templated on it ----
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t dst_smem, uint32_t ncols) {
+  if (CG == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
 }
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {
+  if (CG == 2) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {
+  if (CG == 2) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+template <int CG>
+__device__ __forceinline__ void mma_bf16_cg(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  if (CG == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on barrier `bar` (same offset) in every CTA of the group once all
+// prior tcgen05 operations of this thread have completed.
+template <int CG>
+__device__ __forceinline__ void mma_commit_cg(uint32_t bar) {
+  if (CG == 2)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"((unsigned short)0x3)
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// The address of the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on the
+// barrier of the pair's leader CTA (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -203,9 +267,9 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) { return
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B
 // major-ness, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t make_idesc(bool a_mn, bool b_mn) {
+__device__ __forceinline__ uint32_t make_idesc(bool a_mn, bool b_mn, int M = BM) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -251,8 +315,11 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* p, int n, const float
 }
 
 // Output tile (I, J) of problem P for product KIND, from its index in the
-// problem's tile list.  Symmetric products list only the tiles that touch the
-// upper triangle (128 I < 256 J + 256), column block J by column block J.
+// problem's tile list.  Tiles are (128 CG) x 256.  The symmetric products list
+// only tiles touching the upper triangle, column block J by column block J:
+// for CG = 1 the 128 x 256 tiles with 128 I < 256 J + 256, for CG = 2 the
+// square tiles with I <= J.
+template <int CG>
 __device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local, int& I, int& J) {
   if (kind == G_UPDATE) {
     const int tn = P.tiles_n[G_UPDATE];
@@ -260,10 +327,11 @@ __device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local
     J = local % tn;
     return;
   }
-  const int TM = (P.m + BM - 1) / BM;
+  const int TM = (P.m + 128 * CG - 1) / (128 * CG);
   int j = 0;
   for (;;) {
-    const int cnt = (2 * j + 2 < TM) ? 2 * j + 2 : TM;
+    const int want = (CG == 2) ? j + 1 : 2 * j + 2;
+    const int cnt = want < TM ? want : TM;
     if (local < cnt) {
       I = local;
       J = j;
@@ -276,15 +344,17 @@ __device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local
 
 struct TileGeom {
   const NsProb* P;
-  int row0, col0;
+  int row0, col0;    // this CTA's first output row / the tile's first column
+  int bcol0;         // first B row (output column) this CTA loads
   int M_, N_, K_;
   bool a_mn, b_mn;
+  bool mirror;       // symmetric product, tile strictly above the diagonal
   const CUtensorMap* mapA;
   const CUtensorMap* mapB;
 };
 
-template <int KIND>
-__device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile) {
+template <int KIND, int CG>
+__device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile, int rank) {
   int lo = 0, hi = args.n_probs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -294,9 +364,11 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile) {
   g.P = args.probs + lo;
   const NsProb& P = *g.P;
   int I, J;
-  decode_tile(P, KIND, tile - __ldg(args.tile_start + lo), I, J);
-  g.row0 = I * BM;
+  decode_tile<CG>(P, KIND, tile - __ldg(args.tile_start + lo), I, J);
+  g.row0 = I * (128 * CG) + 128 * rank;
   g.col0 = J * BN;
+  g.bcol0 = g.col0 + (CG == 2 ? 128 * rank : 0);
+  g.mirror = (CG == 2) ? (I < J) : (g.row0 + BM <= g.col0);
   if (KIND == G_GRAM) {
     g.M_ = P.m; g.N_ = P.m; g.K_ = P.n;
     g.mapA = g.mapB = &P.map_x[args.src];
@@ -314,6 +386,7 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile) {
     g.mapA = &P.map_x[args.src]; g.a_mn = false;
     g.mapB = &P.map_b; g.b_mn = false;
   }
+  if (KIND == G_UPDATE) g.mirror = false;   // only the symmetric products mirror
   return g;
 }
 
@@ -338,17 +411,23 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Persistent kernel: one CTA per SM walks the launch's tile list with stride
-// gridDim.x.  The shared-memory ring and the two TMEM accumulators carry over
-// from tile to tile, so loads for the next tile and the epilogue of the last
-// one overlap the tensor cores.
-template <int KIND>
+// Persistent kernel: one CTA (CG = 1) or one CTA pair (CG = 2) per SM (pair)
+// walks the launch's tile list with a stride of the number of groups.  The
+// shared-memory ring and the two TMEM accumulators carry over from tile to
+// tile, so the loads of the next tile and the epilogue of the last one
+// overlap the tensor cores.  In a pair, the leader CTA (rank 0) issues the
+// M = 256 MMAs for both; every CTA's loads complete on the leader's "full"
+// barriers, and the leader's commits arrive on both CTAs' barriers.
+template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs args) {
+  constexpr int STAGES = stages_of(KIND, CG);
+  constexpr uint32_t SB = stage_bytes_of(CG);          // bytes per stage per CTA
+  constexpr uint32_t SA = 2 * kBox;                    // A part: 128 rows (or columns) x 64
+  constexpr int NB = (CG == 2) ? 2 : 4;                // B boxes per stage per CTA
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  constexpr int STAGES = stages_of(KIND);
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  unsigned char* side = smem + STAGES * kStageBytes;          // staging (symmetric) or X tile (update)
+  unsigned char* side = smem + STAGES * SB;                   // staging (symmetric) or X tile (update)
   uint32_t* stage_out = reinterpret_cast<uint32_t*>(side);    // 128 x 64 words
   uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 6);
@@ -358,6 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = args.total_tiles;
+  const int rank = (CG == 2) ? (int)cluster_rank() : 0;
+  const bool leader = (rank == 0);
+  const int group = blockIdx.x / CG, ngroups = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -366,28 +448,31 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4);   // one arrival per epilogue warp
+      mbar_init(tempty0 + 8 * b, 4 * CG);   // one arrival per epilogue warp of the group
     }
     mbar_init(xfull, 1);
     mbar_init(xempty, 4);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_cg<CG>(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();   // the cluster barrier is warp-aligned: reconverge first
+  if (CG == 2) cluster_sync_all();   // the peer's barriers exist before anyone signals them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer ----
+      // ---- TMA producer (every CTA loads its own operand halves) ----
+      const uint32_t full_l = (CG == 2) ? cluster_map(full0, 0) : full0;   // the leader's barriers
       int it = 0, xt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileGeom g = tile_geom<KIND>(args, tile);
+      for (int tile = group; tile < total && ok; tile += ngroups) {
+        const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
         fence_tensormap(g.mapA);
         if (g.mapB != g.mapA) fence_tensormap(g.mapB);
         const int num_kb = (g.K_ + BK - 1) / BK;
@@ -397,26 +482,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             ok = false;
             break;
           }
-          const uint32_t bar = full0 + 8 * s;
-          mbar_expect_tx(bar, kStageBytes);
-          const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+          if (leader) mbar_expect_tx(full0 + 8 * s, SB * CG);
+          const uint32_t bar = full_l + 8 * s;
+          const uint32_t sa = smem_u32(smem + s * SB), sb = sa + SA;
           const int k0 = kb * BK;
-          if (!g.a_mn) {
-            tma_load_2d(sa, g.mapA, bar, k0, g.row0);
-            tma_load_2d(sa + kBox, g.mapA, bar, k0, g.row0 + 64);
-          } else {
-            tma_load_2d(sa, g.mapA, bar, g.row0, k0);
-            tma_load_2d(sa + kBox, g.mapA, bar, g.row0 + 64, k0);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int x = g.a_mn ? g.row0 + 64 * i : k0, y = g.a_mn ? k0 : g.row0 + 64 * i;
+            if (CG == 2) tma_load_2d_pair(sa + i * kBox, g.mapA, bar, x, y);
+            else tma_load_2d(sa + i * kBox, g.mapA, bar, x, y);
           }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (!g.b_mn) tma_load_2d(sb + j * kBox, g.mapB, bar, k0, g.col0 + 64 * j);
-            else         tma_load_2d(sb + j * kBox, g.mapB, bar, g.col0 + 64 * j, k0);
+          for (int j = 0; j < NB; ++j) {
+            const int x = g.b_mn ? g.bcol0 + 64 * j : k0, y = g.b_mn ? k0 : g.bcol0 + 64 * j;
+            if (CG == 2) tma_load_2d_pair(sb + j * kBox, g.mapB, bar, x, y);
+            else tma_load_2d(sb + j * kBox, g.mapB, bar, x, y);
           }
         }
         if (KIND == G_UPDATE && ok) {
-          // the X tile of the a X term (output orientation), once the previous
-          // tile's epilogue has finished reading the buffer
+          // this CTA's X rows of the a X term (output orientation), once the
+          // previous tile's epilogue has finished reading the buffer
           if (xt > 0 && !mbar_wait(xempty, (xt - 1) & 1, args.hdr, 0x600u | KIND)) {
             ok = false;
             break;
@@ -433,19 +518,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           ++xt;
         }
       }
-      // every load this thread issued has landed before the CTA may exit
-      for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
-        mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
+      // every load issued has landed before the CTA may exit (the leader's
+      // full barriers also count the peer's loads)
+      if (leader)
+        for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
+          mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
       if (KIND == G_UPDATE && xt > 0) mbar_wait(xfull, (xt - 1) & 1, args.hdr, 0x700u | KIND);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer ----
+    if (lane == 0 && leader) {
+      // ---- MMA issuer (the leader CTA of the group) ----
       int it = 0, ti = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++ti) {
-        const TileGeom g = tile_geom<KIND>(args, tile);
-        const uint32_t idesc = make_idesc(g.a_mn, g.b_mn);
+      for (int tile = group; tile < total && ok; tile += ngroups, ++ti) {
+        const TileGeom g = tile_geom<KIND, CG>(args, tile, 0);
+        const uint32_t idesc = make_idesc(g.a_mn, g.b_mn, 128 * CG);
         const int acc = ti & 1, use = ti >> 1;
         if (use > 0 && !mbar_wait(tempty0 + 8 * acc, (use - 1) & 1, args.hdr, 0x500u | KIND)) break;
         tc_fence_after();
@@ -458,36 +545,37 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kStageA;
+          const uint32_t sa = smem_u32(smem + s * SB), sb = sa + SA;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = g.a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
             const uint64_t bd = g.b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
-            mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_cg<CG>(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(empty0 + 8 * s);   // frees the stage once these MMAs are done
+          mma_commit_cg<CG>(empty0 + 8 * s);   // frees the stage (in every CTA of the group)
         }
-        mma_commit(tfull0 + 8 * acc);   // accumulator ready (also on the error path)
+        mma_commit_cg<CG>(tfull0 + 8 * acc);   // accumulator ready (also on the error path)
       }
     }
   } else {
     // ---- epilogue: warps 2..5; TMEM lane quarter = warp % 4 ----
     const int quarter = warp & 3;
     const int ew = warp - 2;   // epilogue warp 0..3
+    const uint32_t tempty_l = (CG == 2) ? cluster_map(tempty0, 0) : tempty0;
     int ti = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ti) {
-      const TileGeom g = tile_geom<KIND>(args, tile);
+    for (int tile = group; tile < total; tile += ngroups, ++ti) {
+      const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
       const NsProb& P = *g.P;
       const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
       const int acc = ti & 1, use = ti >> 1;
-      // pull this thread's epilogue operands into L2 while the tensor cores run
-      if (r < g.M_) {
-        const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
-        if (KIND == G_POLY) {
-          const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
-          for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
-        } else if (KIND == G_UPDATE) {
-          if (args.apply_w && P.w) {
+      if (KIND == G_POLY || KIND == G_UPDATE) {
+        // pull this thread's global epilogue operands into L2 while the tensor cores run
+        if (r < g.M_) {
+          const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
+          if (KIND == G_POLY) {
+            const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
+            for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
+          } else if (args.apply_w && P.w) {
             const char* pw = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + g.col0);
             for (int o = 0; o < span * 4; o += 128) prefetch_l2(pw + o);
           }
@@ -569,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(tempty0 + 8 * acc);
+          if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
+          else mbar_arrive(tempty0 + 8 * acc);
           mbar_arrive(xempty);   // the X buffer may be refilled
         }
       } else {
@@ -579,7 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         __nv_bfloat16* outp = (KIND == G_GRAM) ? P.a : P.b;
         const int64_t ld = P.ab_ld;
         const int m = g.M_;
-        const bool mirror = (g.row0 + BM <= g.col0);
         const int rl = quarter * 32 + lane;   // staging row of this thread
         for (int h = 0; h < 2; ++h) {
           for (int c = 0; c < 4; ++c) {
@@ -609,7 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (h == 1) {   // every TMEM read of this accumulator is done
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (lane == 0) {
+              if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
+              else mbar_arrive(tempty0 + 8 * acc);
+            }
           }
           named_barrier_epilogue();
           const int cbase = g.col0 + h * 128;
@@ -627,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
               else if (col < m) *dst = __ushort_as_bfloat16((unsigned short)(val & 0xFFFFu));
             }
           }
-          if (mirror) {
+          if (g.mirror) {
             // transposed: word w holds columns 2w, 2w+1 of row rr; they go to
             // output rows cbase + 2w (+1), column row0 + rr
             for (int w = ew * 16; w < ew * 16 + 16; ++w) {
@@ -652,12 +743,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
   }
 
-  // ---- teardown: the accumulators are idle once their last readers are done ----
+  // ---- teardown: every accumulator read is done and, in a pair, the peer
+  // no longer touches this CTA's barriers or shared memory ----
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();   // lanes that skipped the single-thread roles rejoin before the aligned barrier
+  if (CG == 2) cluster_sync_all();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_cg<CG>(tmem, kTmemCols);
   }
 }
 
@@ -796,15 +890,17 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   for (int i = 0; i < 3; ++i)
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
   if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
-  // symmetric products: only tiles touching the upper triangle (128 I < 256 J + 256)
-  const int64_t tm = (m + BM - 1) / BM, tnm = (m + BN - 1) / BN;
+  // tiles are (128 kCG) x 256; symmetric products list only tiles touching the
+  // upper triangle (kCG = 1: 128 I < 256 J + 256; kCG = 2: I <= J)
+  const int64_t tile_m = 128 * kCG;
+  const int64_t tm = (m + tile_m - 1) / tile_m, tnm = (m + BN - 1) / BN;
   int64_t sym = 0;
-  for (int64_t j = 0; j < tnm; ++j) sym += std::min<int64_t>(tm, 2 * j + 2);
+  for (int64_t j = 0; j < tnm; ++j) sym += std::min<int64_t>(tm, kCG == 2 ? j + 1 : 2 * j + 2);
   P.tiles_n[G_GRAM] = P.tiles_n[G_POLY] = (int32_t)tnm;
   P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)sym;
   const int64_t um = P.tall ? P.n : P.m, un = P.tall ? P.m : P.n;   // G_UPDATE output (stored orientation)
   P.tiles_n[G_UPDATE] = (int32_t)((un + BN - 1) / BN);
-  P.tiles[G_UPDATE] = (int32_t)(((um + BM - 1) / BM) * P.tiles_n[G_UPDATE]);
+  P.tiles[G_UPDATE] = (int32_t)(((um + tile_m - 1) / tile_m) * P.tiles_n[G_UPDATE]);
   return true;
 }
 
@@ -827,9 +923,10 @@ void prefix(const std::vector<NsProb>& probs, std::vector<int32_t>& ts, int32_t 
 cudaError_t configure_kernels() {
   static cudaError_t result = cudaErrorNotReady;
   if (result == cudaErrorNotReady) {
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_GRAM));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_POLY));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_of(G_UPDATE));
+    const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM, kCG>, attr, (int)smem_bytes_of(G_GRAM, kCG));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY, kCG>, attr, (int)smem_bytes_of(G_POLY, kCG));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE, kCG>, attr, (int)smem_bytes_of(G_UPDATE, kCG));
     result = e;
   }
   return result;
@@ -852,10 +949,23 @@ cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaS
   a.tile_start = L.d_tile_start + kind * (L.n + 1);
   a.total_tiles = L.total[kind];
   void* args[] = {&a};
-  void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM>
-           : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY> : (void*)ns_gemm_kernel<G_UPDATE>;
-  const int grid = std::min(L.total[kind], num_sms());   // persistent: one CTA per SM
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem_bytes_of(kind), s);
+  void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM, kCG>
+           : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY, kCG> : (void*)ns_gemm_kernel<G_UPDATE, kCG>;
+  // persistent: one CTA group per SM group, never more groups than tiles
+  const int groups = std::min(L.total[kind], num_sms() / kCG);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * kCG);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes_of(kind, kCG);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // The iteration schedule over X buffers: 0 -> 1 -> 2 -> 1 -> ... and the last
