@@ -205,6 +205,21 @@ __device__ __forceinline__ void mma_commit_cg(uint32_t bar) {
   else
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// TMA store of one box from this CTA's shared memory (bulk async group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(map), "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA) before a barrier hands the data to the storing thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // The address of the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
   uint32_t r;
@@ -298,19 +313,6 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* p, int n, float 
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = (i < n) ? __bfloat162float(p[i]) : 0.0f;
-  }
-}
-__device__ __forceinline__ void store_row32(__nv_bfloat16* p, int n, const float (&v)[32]) {
-  if (n >= 32) {
-    uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      q[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                        pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < n) p[i] = __float2bfloat16_rn(v[i]);
   }
 }
 
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       mbar_init(tempty0 + 8 * b, 4 * CG);   // one arrival per epilogue warp of the group
     }
     mbar_init(xfull, 1);
-    mbar_init(xempty, 4);
+    mbar_init(xempty, 1);   // the storing thread, once its TMA store has read the buffer
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -600,31 +602,36 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // box (row/64, col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
         const bool xok = mbar_wait(xfull, ti & 1, args.hdr, 0x800u | KIND);
         const int rl = quarter * 32 + lane;
-        const unsigned char* xrow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
+        unsigned char* xrow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
-          const int cb = g.col0 + c * 32;
-          if (!xok || r >= g.M_ || cb >= g.N_) continue;
-          const int nv = g.N_ - cb;
+          if (!xok) continue;
+          // this thread's 32 X values of chunk c, read and then overwritten in
+          // place with the result (only this thread touches these 64 bytes)
+          unsigned char* bx = xrow + (c >> 1) * kBox;
+          uint4* q4[4];
           float xv[32], out[32];
-          {
-            const unsigned char* bx = xrow + (c >> 1) * kBox;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int q = (c & 1) * 4 + t;
-              const uint4 u4 = *reinterpret_cast<const uint4*>(bx + ((q ^ (rl & 7)) << 4));
-              xv[8 * t + 0] = bf16_lo(u4.x); xv[8 * t + 1] = bf16_hi(u4.x);
-              xv[8 * t + 2] = bf16_lo(u4.y); xv[8 * t + 3] = bf16_hi(u4.y);
-              xv[8 * t + 4] = bf16_lo(u4.z); xv[8 * t + 5] = bf16_hi(u4.z);
-              xv[8 * t + 6] = bf16_lo(u4.w); xv[8 * t + 7] = bf16_hi(u4.w);
-            }
+          for (int t = 0; t < 4; ++t) {
+            const int q = (c & 1) * 4 + t;
+            q4[t] = reinterpret_cast<uint4*>(bx + ((q ^ (rl & 7)) << 4));
+            const uint4 u4 = *q4[t];
+            xv[8 * t + 0] = bf16_lo(u4.x); xv[8 * t + 1] = bf16_hi(u4.x);
+            xv[8 * t + 2] = bf16_lo(u4.y); xv[8 * t + 3] = bf16_hi(u4.y);
+            xv[8 * t + 4] = bf16_lo(u4.z); xv[8 * t + 5] = bf16_hi(u4.z);
+            xv[8 * t + 6] = bf16_lo(u4.w); xv[8 * t + 7] = bf16_hi(u4.w);
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(v[i]));
-          store_row32(P.x[args.dst] + (int64_t)r * P.x_ld[args.dst] + cb, nv, out);
-          if (args.apply_w && P.w) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *q4[t] = make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
+                                pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
+          const int cb = g.col0 + c * 32;
+          if (args.apply_w && P.w && r < g.M_ && cb < g.N_) {
             // W <- W - eta * bf16(U): one rounded product, one rounded difference
+            const int nv = g.N_ - cb;
             float* wp = P.w + (int64_t)r * P.w_ld + cb;
             if (nv >= 32) {
               float4 wv[8];
@@ -659,7 +666,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if (lane == 0) {
           if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
           else mbar_arrive(tempty0 + 8 * acc);
-          mbar_arrive(xempty);   // the X buffer may be refilled
+        }
+        // the finished tile leaves by TMA (boxes outside the matrix are skipped,
+        // partial ones are clipped by the tensor map); the X buffer is handed
+        // back to the producer once the stores have read it
+        fence_proxy_async_smem();
+        named_barrier_epilogue();
+        if (ew == 0 && lane == 0) {
+          if (xok) {
+            const CUtensorMap* md = &P.map_x[args.dst];
+            const uint32_t xs = smem_u32(side);
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi)
+#pragma unroll
+              for (int bj = 0; bj < 4; ++bj)
+                if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * bj < g.N_)
+                  tma_store_2d(md, xs + (bi * 4 + bj) * kBox, g.col0 + 64 * bj, g.row0 + 64 * bi);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(xempty);
         }
       } else {
         // symmetric products: stage 128 x 128 halves in shared memory (4-byte
@@ -743,8 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
   }
 
-  // ---- teardown: every accumulator read is done and, in a pair, the peer
-  // no longer touches this CTA's barriers or shared memory ----
+  // ---- teardown: every accumulator read is done, every TMA store has
+  // completed and, in a pair, the peer no longer touches this CTA's barriers
+  // or shared memory ----
+  if (KIND == G_UPDATE && warp == 2 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncwarp();   // lanes that skipped the single-thread roles rejoin before the aligned barrier
   if (CG == 2) cluster_sync_all();
