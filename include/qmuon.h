@@ -237,6 +237,15 @@ QMUON_API qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor
                                                       qmuon_dtype grad_dtype, float beta, float* sumsq,
                                                       float* inv_norm, void* stream);
 
+/* Build, ahead of time, the Newton-Schulz problem tables qmuon_step needs for
+ * both step kinds with these weights and this workspace (tensor maps and
+ * tile lists; one synchronous upload each).  Optional: qmuon_step builds them
+ * on first use and rebuilds them when the weights or workspace change;
+ * preparing keeps that host work and its synchronising copy out of the
+ * steps that follow.  Arguments as for qmuon_step. */
+QMUON_API qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,
+                                          size_t ws_bytes);
+
 /* Synchronise `stream` and report a kernel-side error recorded in `ws`
  * (QMUON_ERR_TIMEOUT when a bounded wait expired), then clear it. */
 QMUON_API qmuon_status qmuon_sync_status(void* ws, void* stream);

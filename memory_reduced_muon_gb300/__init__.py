@@ -94,6 +94,7 @@ def lib() -> C.CDLL:
         "qmuon_version": (C.c_char_p, []),
         "qmuon_last_error": (C.c_char_p, []),
         "qmuon_update_normalize_noalloc": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp]),
+        "qmuon_step_prepare": (i32, [vp, C.POINTER(vp), vp, sz]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -108,7 +109,7 @@ def exported_symbols() -> list:
             "qmuon_update_multi_normalize_groups", "qmuon_carrier_workspace_size",
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
-            "qmuon_update_normalize_noalloc"]
+            "qmuon_update_normalize_noalloc", "qmuon_step_prepare"]
 
 
 # --------------------------------------------------------------------------
@@ -280,6 +281,12 @@ def qmuon_update_normalize_noalloc(q8, absmax, grad, rows: int, cols: int, q8_ki
                                               DTYPES.get(grad_dtype, grad_dtype), float(beta), _ptr(sumsq),
                                               _ptr(inv_norm), _stream(stream))
     _check(st, "qmuon_update_normalize_noalloc")
+
+
+def qmuon_step_prepare(plan: Plan, weights, ws, ws_bytes: Optional[int] = None):
+    wp = (C.c_void_p * max(1, len(weights)))(*[_ptr(w) for w in weights])
+    _check(lib().qmuon_step_prepare(plan.handle, wp, _ptr(ws), _nbytes(ws) if ws_bytes is None else int(ws_bytes)),
+           "qmuon_step_prepare")
 
 
 def qmuon_sync_status(ws, stream=None):

@@ -523,6 +523,27 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
   return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
 }
 
+extern "C" qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,
+                                           size_t ws_bytes) {
+  if (!plan || !weights || !ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
+  const int32_t n = (int32_t)plan->tensors.size();
+  for (int32_t i = 0; i < n; ++i) {
+    const qmuon_tensor& T = plan->tensors[i];
+    if (T.rows * T.cols == 0) continue;
+    if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
+  }
+  if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  const UpdWs w = carve(plan, ws, ws_bytes);
+  qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
+  qmuon_status st = ns::ensure_step_tables(&mp->ns_full, plan->tensors.data(), n, 1, 1, weights, w.inv, w.ns,
+                                           w.ns_bytes);
+  if (st != QMUON_OK) return st;
+  return ns::ensure_step_tables(&mp->ns_block, plan->tensors.data(), n, plan->tile_r, plan->tile_c, weights, w.inv,
+                                w.ns, w.ns_bytes);
+}
+
 extern "C" qmuon_status qmuon_sync_status(void* ws, void* stream) {
   if (!ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
