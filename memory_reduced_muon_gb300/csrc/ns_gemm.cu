@@ -36,7 +36,9 @@ namespace ns {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                      // epilogue warps: two per TMEM lane quarter
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;        // warp 0 TMA, warp 1 MMA, warps 2.. epilogue
 constexpr uint32_t kBox = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16 = 8 KB
 constexpr uint32_t kStageA = 2 * kBox;          // 128 rows (or columns) x 64
 constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
@@ -55,9 +57,13 @@ __host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ?
 __host__ __device__ constexpr int stages_of(int kind, int cg) {
   return cg == 2 ? (kind == 2 ? 4 : 6) : (kind == 2 ? 3 : 4);
 }
-__host__ __device__ constexpr uint32_t side_bytes_of(int kind) { return kind == 2 ? kXTileBytes : kStageOutBytes; }
+// X tile buffers of the update product (one: a second would cost an operand stage).
+__host__ __device__ constexpr int x_bufs_of(int cg) { return cg > 0 ? 1 : 1; }
+__host__ __device__ constexpr uint32_t side_bytes_of(int kind, int cg) {
+  return kind == 2 ? x_bufs_of(cg) * kXTileBytes : kStageOutBytes;
+}
 __host__ __device__ constexpr size_t smem_bytes_of(int kind, int cg) {
-  return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind) + 1024 + 256;
+  return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind, cg) + 1024 + 256;
 }
 
 constexpr long long kWaitCycles = 4000000000LL;  // bounded waits: ~2 s at 2 GHz
@@ -393,7 +399,7 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile, in
 }
 
 __device__ __forceinline__ void named_barrier_epilogue() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 // AND of `v` over the 128 epilogue threads (also a barrier among them), so the
 // four epilogue warps always take the same branch around their barriers.
@@ -402,10 +408,10 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(v ? 1u : 0u)
+      : "r"(v ? 1u : 0u), "n"(kEpiThreads)
       : "memory");
   return r != 0;
 }
@@ -431,11 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                                                          ~static_cast<uintptr_t>(1023));
   unsigned char* side = smem + STAGES * SB;                   // staging (symmetric) or X tile (update)
   uint32_t* stage_out = reinterpret_cast<uint32_t*>(side);    // 128 x 64 words
-  uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 6);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND, CG));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  const uint32_t xfull = smem_u32(bars + 2 * STAGES + 4), xempty = smem_u32(bars + 2 * STAGES + 5);
+  constexpr int XB = x_bufs_of(CG);
+  const uint32_t xfull0 = smem_u32(bars + 2 * STAGES + 4), xempty0 = smem_u32(bars + 2 * STAGES + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = args.total_tiles;
@@ -450,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4 * CG);   // one arrival per epilogue warp of the group
+      mbar_init(tempty0 + 8 * b, kEpiWarps * CG);   // one arrival per epilogue warp of the group
     }
-    mbar_init(xfull, 1);
-    mbar_init(xempty, 1);   // the storing thread, once its TMA store has read the buffer
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(xfull0 + 8 * b, 1);
+      mbar_init(xempty0 + 8 * b, 1);   // the storing thread, once its TMA store has read the buffer
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -473,10 +482,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const uint32_t full_l = (CG == 2) ? cluster_map(full0, 0) : full0;   // the leader's barriers
       int it = 0, xt = 0;
       bool ok = true;
+      const CUtensorMap* fenced[3] = {nullptr, nullptr, nullptr};   // maps fenced for the last tile
+      auto fence_once = [&](const CUtensorMap* mp) {
+        if (mp != fenced[0] && mp != fenced[1] && mp != fenced[2]) fence_tensormap(mp);
+      };
       for (int tile = group; tile < total && ok; tile += ngroups) {
         const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
-        fence_tensormap(g.mapA);
-        if (g.mapB != g.mapA) fence_tensormap(g.mapB);
+        // a tensor map written by the host is fenced once per run of tiles using it
+        fence_once(g.mapA);
+        if (g.mapB != g.mapA) fence_once(g.mapB);
+        const CUtensorMap* mx_t = (KIND == G_UPDATE) ? &g.P->map_x[args.src] : nullptr;
+        if (mx_t && mx_t != g.mapA && mx_t != g.mapB) fence_once(mx_t);
+        fenced[0] = g.mapA;
+        fenced[1] = g.mapB;
+        fenced[2] = mx_t;
         const int num_kb = (g.K_ + BK - 1) / BK;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES, round = it / STAGES;
@@ -504,14 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if (KIND == G_UPDATE && ok) {
           // this CTA's X rows of the a X term (output orientation), once the
           // previous tile's epilogue has finished reading the buffer
-          if (xt > 0 && !mbar_wait(xempty, (xt - 1) & 1, args.hdr, 0x600u | KIND)) {
+          const int xb = xt % XB, xuse = xt / XB;
+          if (xuse > 0 && !mbar_wait(xempty0 + 8 * xb, (xuse - 1) & 1, args.hdr, 0x600u | KIND)) {
             ok = false;
             break;
           }
           const CUtensorMap* mx = &g.P->map_x[args.src];
-          if (mx != g.mapA && mx != g.mapB) fence_tensormap(mx);
+          const uint32_t xfull = xfull0 + 8 * xb;
           mbar_expect_tx(xfull, kXTileBytes);
-          const uint32_t xs = smem_u32(side);
+          const uint32_t xs = smem_u32(side + xb * kXTileBytes);
 #pragma unroll
           for (int bi = 0; bi < 2; ++bi)
 #pragma unroll
@@ -525,7 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if (leader)
         for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
           mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
-      if (KIND == G_UPDATE && xt > 0) mbar_wait(xfull, (xt - 1) & 1, args.hdr, 0x700u | KIND);
+      if (KIND == G_UPDATE)
+        for (int k = (xt > XB ? xt - XB : 0); k < xt; ++k)
+          mbar_wait(xfull0 + 8 * (k % XB), (k / XB) & 1, args.hdr, 0x700u | KIND);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -562,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   } else {
     // ---- epilogue: warps 2..5; TMEM lane quarter = warp % 4 ----
     const int quarter = warp & 3;
-    const int ew = warp - 2;   // epilogue warp 0..3
+    const int ew = warp - 2;          // epilogue warp 0..7
+    const int ch = ew >> 2;           // column half of the tile (TMEM lanes are shared per quarter)
     const uint32_t tempty_l = (CG == 2) ? cluster_map(tempty0, 0) : tempty0;
     int ti = 0;
     for (int tile = group; tile < total; tile += ngroups, ++ti) {
@@ -600,10 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // X <- s3 (a X + B X) [, W -= eta U]: each thread owns one output row;
         // its X row comes from the TMA copy in shared memory (128-byte swizzle:
         // box (row/64, col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
-        const bool xok = mbar_wait(xfull, ti & 1, args.hdr, 0x800u | KIND);
+        const int xb = ti % XB;
+        const bool xok = mbar_wait(xfull0 + 8 * xb, (ti / XB) & 1, args.hdr, 0x800u | KIND);
         const int rl = quarter * 32 + lane;
-        unsigned char* xrow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
-        for (int c = 0; c < BN / 32; ++c) {
+        unsigned char* xbase = side + xb * kXTileBytes;
+        unsigned char* xrow = xbase + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
+        for (int c = 4 * ch; c < 4 * ch + 4; ++c) {   // this warp's 128 columns
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
           if (!xok) continue;
@@ -675,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if (ew == 0 && lane == 0) {
           if (xok) {
             const CUtensorMap* md = &P.map_x[args.dst];
-            const uint32_t xs = smem_u32(side);
+            const uint32_t xs = smem_u32(xbase);
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi)
 #pragma unroll
@@ -685,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             bulk_commit();
             bulk_wait_read_all();
           }
-          mbar_arrive(xempty);
+          mbar_arrive(xempty0 + 8 * xb);
         }
       } else {
         // symmetric products: stage 128 x 128 halves in shared memory (4-byte
@@ -696,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         const int m = g.M_;
         const int rl = quarter * 32 + lane;   // staging row of this thread
         for (int h = 0; h < 2; ++h) {
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 2 * ch; c < 2 * ch + 2; ++c) {   // this warp's 64 columns of the half
             uint32_t v[32];
             tmem_ld32(tbase + (uint32_t)(h * 128 + c * 32), v);
             float out[32];
@@ -730,8 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
           named_barrier_epilogue();
           const int cbase = g.col0 + h * 128;
-          // rows: warp ew stores rows 32 ew .. 32 ew + 31, two words per lane
-          for (int rr = ew * 32; rr < ew * 32 + 32; ++rr) {
+          // rows: warp ew stores rows 16 ew .. 16 ew + 15, two words per lane
+          for (int rr = ew * 16; rr < ew * 16 + 16; ++rr) {
             const int orow = g.row0 + rr;
             if (orow >= m) break;
 #pragma unroll
@@ -747,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (g.mirror) {
             // transposed: word w holds columns 2w, 2w+1 of row rr; they go to
             // output rows cbase + 2w (+1), column row0 + rr
-            for (int w = ew * 16; w < ew * 16 + 16; ++w) {
+            for (int w = ew * 8; w < ew * 8 + 8; ++w) {
               const int orow = cbase + 2 * w;
               if (orow >= m) break;
 #pragma unroll
