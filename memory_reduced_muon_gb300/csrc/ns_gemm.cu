@@ -628,9 +628,28 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         const int rl = quarter * 32 + lane;
         unsigned char* xbase = side + xb * kXTileBytes;
         unsigned char* xrow = xbase + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
+        // W <- W - eta * bf16(U) on the last iteration of a step: the fp32 row
+        // segment of the next chunk is loaded while this chunk is processed
+        const bool do_w = args.apply_w && P.w && r < g.M_;
+        float* wrow = do_w ? P.w + (int64_t)r * P.w_ld : nullptr;
+        float4 wnext[8];
+        auto w_full = [&](int cc) { return do_w && g.col0 + cc * 32 + 32 <= g.N_; };
+        if (w_full(4 * ch)) {
+          const float4* src = reinterpret_cast<const float4*>(wrow + g.col0 + 4 * ch * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wnext[j] = __ldcs(src + j);
+        }
         for (int c = 4 * ch; c < 4 * ch + 4; ++c) {   // this warp's 128 columns
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          float4 wv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wv[j] = wnext[j];
+          if (c + 1 < 4 * ch + 4 && w_full(c + 1)) {
+            const float4* src = reinterpret_cast<const float4*>(wrow + g.col0 + (c + 1) * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) wnext[j] = __ldcs(src + j);
+          }
           if (!xok) continue;
           // this thread's 32 X values of chunk c, read and then overwritten in
           // place with the result (only this thread touches these 64 bytes)
@@ -654,34 +673,27 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             *q4[t] = make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
                                 pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
           const int cb = g.col0 + c * 32;
-          if (args.apply_w && P.w && r < g.M_ && cb < g.N_) {
-            // W <- W - eta * bf16(U): one rounded product, one rounded difference
-            const int nv = g.N_ - cb;
-            float* wp = P.w + (int64_t)r * P.w_ld + cb;
-            if (nv >= 32) {
-              float4 wv[8];
-              const float4* src = reinterpret_cast<const float4*>(wp);
+          if (w_full(c)) {
+            // one rounded product, one rounded difference per element
 #pragma unroll
-              for (int j = 0; j < 8; ++j) wv[j] = __ldcs(src + j);
+            for (int j = 0; j < 8; ++j) {
+              float* e = reinterpret_cast<float*>(&wv[j]);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float* e = reinterpret_cast<float*>(&wv[j]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float u = __bfloat162float(__float2bfloat16_rn(out[4 * j + k]));
-                  e[k] = __fsub_rn(e[k], __fmul_rn(args.eta, u));
-                }
+              for (int k = 0; k < 4; ++k) {
+                const float u = __bfloat162float(__float2bfloat16_rn(out[4 * j + k]));
+                e[k] = __fsub_rn(e[k], __fmul_rn(args.eta, u));
               }
-              float4* dstw = reinterpret_cast<float4*>(wp);
+            }
+            float4* dstw = reinterpret_cast<float4*>(wrow + cb);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) __stcs(dstw + j, wv[j]);
-            } else {
+            for (int j = 0; j < 8; ++j) __stcs(dstw + j, wv[j]);
+          } else if (do_w && cb < g.N_) {
+            const int nv = g.N_ - cb;   // ragged last chunk: element by element
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                if (i < nv) {
-                  const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
-                  wp[i] = __fsub_rn(wp[i], __fmul_rn(args.eta, u));
-                }
+            for (int i = 0; i < 32; ++i) {
+              if (i < nv) {
+                const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
+                wrow[cb + i] = __fsub_rn(wrow[cb + i], __fmul_rn(args.eta, u));
               }
             }
           }
