@@ -52,13 +52,18 @@ def load_peaks():
 
 
 def load_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from a committed ncu capture."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """Per-launch (or per-call) DRAM bytes from the committed ncu summary
+    (``key = bytes`` lines in profiles/dram_traffic_llama8b_x4_muonbp.md)."""
+    out = {}
     try:
-        with open(p) as f:
-            return json.load(f)
+        with open(os.path.join(ROOT, "profiles", "dram_traffic_llama8b_x4_muonbp.md")) as f:
+            for line in f:
+                parts = line.split("=")
+                if len(parts) == 2 and parts[0].strip().endswith(("_per_launch", "_per_call")):
+                    out[parts[0].strip()] = float(parts[1])
     except Exception:
-        return {}
+        pass
+    return out
 
 
 def ns_flops_of(rows, cols, iters):
@@ -489,12 +494,12 @@ def main():
     roof = {"bound": "tensor", "kernel": f"ns_gemm ({key} step, 15 launches per call)",
             "achieved": ns_tflops[key], "peak": peak_t, "unit": "TFLOP/s", "frac": ns_tflops[key] / peak_t,
             "peak_source": f"bf16_tflops_sustained of {peak_src}",
-            "traffic": traffic.get(f"ns_{key}_bytes_per_call"),
+            "traffic": traffic.get(f"ns_{key}_bytes_per_call") if args.row_scale == 1 and args.workload == 4 else None,
             "flops_per_call": r["ns_flop"][key], "ms_per_call": r["ns_ms"][key]}
     upd_roof = {"bound": "hbm", "achieved": r["upd_gbs"], "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": r["upd_gbs"] / float(peaks["hbm_gbs"]), "frac_of_8000": r["upd_gbs"] / 8000.0,
                 "bytes_per_launch": r["upd_bytes"], "ms_per_launch": r["upd_ms"],
-                "traffic": traffic.get("update_bytes_per_launch")}
+                "traffic": traffic.get("update_bytes_per_launch") if args.row_scale == 1 and args.workload == 4 else None}
     line = {"metric": METRIC, "value": r["value"], "unit": "Mparams/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (NS operands, fp32 accumulate); int8 state, fp32 codec",
