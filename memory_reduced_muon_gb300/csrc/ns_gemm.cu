@@ -3,23 +3,27 @@
 // One iteration is three matrix products ("NVIDIA impulsa optimizadores
 // avanzados ... con Megatron", section "Newton-Schulz distribuido"):
 //   G_GRAM   A = s1 * X X^T            (s1 = inv^2 on the first iteration)
-//   G_POLY   B = b A + c A A
-//   G_UPDATE X <- s3 * (a X + B X)     (s3 = inv on the first iteration;
+//   G_POLY   B = a I + b A + c A A
+//   G_UPDATE X <- s3 * (B X)           (s3 = inv on the first iteration;
 //                                       the last one may also apply W -= eta U)
-// A matrix stored with more rows than columns (S, n x m) is orthogonalised as
-// its transpose without moving data: A = S^T S and S <- a S + S B, since
-// (B X)^T = X^T B for the symmetric B.  Operands are bf16, accumulation fp32
-// in tensor memory.
+// The a X term of the quintic rides in B's diagonal: a X + (b A + c A A) X =
+// (a I + b A + c A A) X, so the update is one plain product and never reads X
+// outside its operand pipeline.  A matrix stored with more rows than columns
+// (S, n x m) is orthogonalised as its transpose without moving data: A = S^T S
+// and S <- S B, since (B X)^T = X^T B for the symmetric B.  Operands are bf16,
+// accumulation fp32 in tensor memory.
 //
-// Kernel: one CTA per 128 x 256 output tile of one problem of a batch.
-// 6 warps: warp 0 issues TMA loads (64 x 64 bf16 boxes, 128-byte swizzle)
-// into a 4-stage shared-memory ring, warp 1 allocates 256 TMEM columns and
-// issues tcgen05.mma (M=128, N=256, K=16) from one thread, warps 2-5 read the
-// accumulator back with tcgen05.ld and run the fused epilogue.  K-major and
-// MN-major operands are both read straight from the row-major buffers; the
-// instruction descriptor says which.  Every mbarrier wait is bounded: on
-// expiry it records QMUON_ERR_TIMEOUT in the workspace header and the CTA
-// winds down instead of hanging.
+// Kernel: a persistent CTA pair (cta_group::2, one cluster) per two SMs runs
+// the 256 x 256 output tiles the host scheduled for it, over every problem of
+// the batch.  10 warps per CTA: warp 0 issues TMA loads (64 x 64 bf16 boxes,
+// 128-byte swizzle) into a shared-memory ring, warp 1 allocates 512 TMEM
+// columns (two accumulators) and, in the leader CTA, issues tcgen05.mma
+// (M=256, N=256, K=16) from one thread; warps 2-9 read the accumulator back
+// with tcgen05.ld and run the fused epilogue.  K-major and MN-major operands
+// are both read straight from the row-major buffers; the instruction
+// descriptor says which.  Every mbarrier wait is bounded: on expiry it records
+// QMUON_ERR_TIMEOUT in the workspace header and the CTA winds down instead of
+// hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -27,6 +31,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "qm_ns.h"
@@ -45,22 +50,20 @@ constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // symmetric epilogue staging: half an output tile
-constexpr uint32_t kXTileBytes = 8 * kBox;           // G_UPDATE: the 128 x 256 X tile of the a X term
+constexpr uint32_t kOutTileBytes = 8 * kBox;         // G_UPDATE: a CTA's 128 x 256 output tile (TMA boxes)
 
 // Shared memory per product kind and CTA group.  One CTA (CG = 1) owns a
 // 128 x 256 output tile and loads all of A (128 rows) and B (256 rows) per
 // stage (48 KB); a CTA pair (CG = 2) owns 256 x 256, each CTA loading its
 // 128 rows of A and half of B (32 KB per stage per CTA).  The symmetric
 // products keep a staging buffer for coalesced (and mirrored) stores; the
-// update product keeps a TMA-loaded copy of its X output tile.
+// update product stages its whole output tile in TMA box layout.
 __host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ? 4 * kBox : kStageBytes; }
 __host__ __device__ constexpr int stages_of(int kind, int cg) {
   return cg == 2 ? (kind == 2 ? 4 : 6) : (kind == 2 ? 3 : 4);
 }
-// X tile buffers of the update product (one: a second would cost an operand stage).
-__host__ __device__ constexpr int x_bufs_of(int cg) { return cg > 0 ? 1 : 1; }
 __host__ __device__ constexpr uint32_t side_bytes_of(int kind, int cg) {
-  return kind == 2 ? x_bufs_of(cg) * kXTileBytes : kStageOutBytes;
+  return kind == 2 ? kOutTileBytes : kStageOutBytes;
 }
 __host__ __device__ constexpr size_t smem_bytes_of(int kind, int cg) {
   return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind, cg) + 1024 + 256;
@@ -92,11 +95,15 @@ struct alignas(128) NsProb {
   int32_t tiles[3];       // output tiles per product kind
 };
 
+// One entry of a launch's tile schedule: output tile `local` of problem `prob`.
+struct TileRef {
+  int32_t prob, local;
+};
+
 struct GemmArgs {
   const NsProb* probs;
-  const int32_t* tile_start;  // [n_probs + 1] prefix of tiles for this kind
-  int32_t n_probs;
-  int32_t total_tiles;
+  const int32_t* sched_start;  // [groups + 1]: CTA group g runs sched[sched_start[g] .. sched_start[g + 1])
+  const TileRef* sched;
   int32_t src, dst;           // X buffer indices read / written (G_UPDATE); src for G_GRAM
   int32_t first;              // apply inv (first iteration)
   int32_t apply_w;            // W -= eta * U (last iteration of a step)
@@ -362,17 +369,13 @@ struct TileGeom {
 };
 
 template <int KIND, int CG>
-__device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int tile, int rank) {
-  int lo = 0, hi = args.n_probs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(args.tile_start + mid) <= tile) lo = mid; else hi = mid - 1;
-  }
+__device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int k, int rank) {
+  const int2 e = __ldg(reinterpret_cast<const int2*>(args.sched) + k);
   TileGeom g;
-  g.P = args.probs + lo;
+  g.P = args.probs + e.x;
   const NsProb& P = *g.P;
   int I, J;
-  decode_tile<CG>(P, KIND, tile - __ldg(args.tile_start + lo), I, J);
+  decode_tile<CG>(P, KIND, e.y, I, J);
   g.row0 = I * (128 * CG) + 128 * rank;
   g.col0 = J * BN;
   g.bcol0 = g.col0 + (CG == 2 ? 128 * rank : 0);
@@ -420,7 +423,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Persistent kernel: one CTA (CG = 1) or one CTA pair (CG = 2) per SM (pair)
-// walks the launch's tile list with a stride of the number of groups.  The
+// runs its own list of tiles, which the host balanced by their cost.  The
 // shared-memory ring and the two TMEM accumulators carry over from tile to
 // tile, so the loads of the next tile and the epilogue of the last one
 // overlap the tensor cores.  In a pair, the leader CTA (rank 0) issues the
@@ -435,20 +438,19 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-  unsigned char* side = smem + STAGES * SB;                   // staging (symmetric) or X tile (update)
+  unsigned char* side = smem + STAGES * SB;                   // staging: half tile (symmetric) or tile (update)
   uint32_t* stage_out = reinterpret_cast<uint32_t*>(side);    // 128 x 64 words
   uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND, CG));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  constexpr int XB = x_bufs_of(CG);
-  const uint32_t xfull0 = smem_u32(bars + 2 * STAGES + 4), xempty0 = smem_u32(bars + 2 * STAGES + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = args.total_tiles;
   const int rank = (CG == 2) ? (int)cluster_rank() : 0;
   const bool leader = (rank == 0);
-  const int group = blockIdx.x / CG, ngroups = gridDim.x / CG;
+  // this CTA group's tiles, in the order the host's schedule lists them
+  const int group = blockIdx.x / CG;
+  const int k_begin = __ldg(args.sched_start + group), k_end = __ldg(args.sched_start + group + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -458,10 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
       mbar_init(tempty0 + 8 * b, kEpiWarps * CG);   // one arrival per epilogue warp of the group
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(xfull0 + 8 * b, 1);
-      mbar_init(xempty0 + 8 * b, 1);   // the storing thread, once its TMA store has read the buffer
     }
     fence_mbar_init();
   }
@@ -480,22 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     if (lane == 0) {
       // ---- TMA producer (every CTA loads its own operand halves) ----
       const uint32_t full_l = (CG == 2) ? cluster_map(full0, 0) : full0;   // the leader's barriers
-      int it = 0, xt = 0;
+      int it = 0;
       bool ok = true;
-      const CUtensorMap* fenced[3] = {nullptr, nullptr, nullptr};   // maps fenced for the last tile
+      const CUtensorMap* fenced[2] = {nullptr, nullptr};   // maps fenced for the last tile
       auto fence_once = [&](const CUtensorMap* mp) {
-        if (mp != fenced[0] && mp != fenced[1] && mp != fenced[2]) fence_tensormap(mp);
+        if (mp != fenced[0] && mp != fenced[1]) fence_tensormap(mp);
       };
-      for (int tile = group; tile < total && ok; tile += ngroups) {
+      for (int tile = k_begin; tile < k_end && ok; ++tile) {
         const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
         // a tensor map written by the host is fenced once per run of tiles using it
         fence_once(g.mapA);
         if (g.mapB != g.mapA) fence_once(g.mapB);
-        const CUtensorMap* mx_t = (KIND == G_UPDATE) ? &g.P->map_x[args.src] : nullptr;
-        if (mx_t && mx_t != g.mapA && mx_t != g.mapB) fence_once(mx_t);
         fenced[0] = g.mapA;
         fenced[1] = g.mapB;
-        fenced[2] = mx_t;
         const int num_kb = (g.K_ + BK - 1) / BK;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES, round = it / STAGES;
@@ -520,41 +515,19 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             else tma_load_2d(sb + j * kBox, g.mapB, bar, x, y);
           }
         }
-        if (KIND == G_UPDATE && ok) {
-          // this CTA's X rows of the a X term (output orientation), once the
-          // previous tile's epilogue has finished reading the buffer
-          const int xb = xt % XB, xuse = xt / XB;
-          if (xuse > 0 && !mbar_wait(xempty0 + 8 * xb, (xuse - 1) & 1, args.hdr, 0x600u | KIND)) {
-            ok = false;
-            break;
-          }
-          const CUtensorMap* mx = &g.P->map_x[args.src];
-          const uint32_t xfull = xfull0 + 8 * xb;
-          mbar_expect_tx(xfull, kXTileBytes);
-          const uint32_t xs = smem_u32(side + xb * kXTileBytes);
-#pragma unroll
-          for (int bi = 0; bi < 2; ++bi)
-#pragma unroll
-            for (int bj = 0; bj < 4; ++bj)
-              tma_load_2d(xs + (bi * 4 + bj) * kBox, mx, xfull, g.col0 + 64 * bj, g.row0 + 64 * bi);
-          ++xt;
-        }
       }
       // every load issued has landed before the CTA may exit (the leader's
       // full barriers also count the peer's loads)
       if (leader)
         for (int k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
           mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1, args.hdr, 0x200u | KIND);
-      if (KIND == G_UPDATE)
-        for (int k = (xt > XB ? xt - XB : 0); k < xt; ++k)
-          mbar_wait(xfull0 + 8 * (k % XB), (k / XB) & 1, args.hdr, 0x700u | KIND);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---- MMA issuer (the leader CTA of the group) ----
       int it = 0, ti = 0;
       bool ok = true;
-      for (int tile = group; tile < total && ok; tile += ngroups, ++ti) {
+      for (int tile = k_begin; tile < k_end && ok; ++tile, ++ti) {
         const TileGeom g = tile_geom<KIND, CG>(args, tile, 0);
         const uint32_t idesc = make_idesc(g.a_mn, g.b_mn, 128 * CG);
         const int acc = ti & 1, use = ti >> 1;
@@ -588,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     const int ch = ew >> 2;           // column half of the tile (TMEM lanes are shared per quarter)
     const uint32_t tempty_l = (CG == 2) ? cluster_map(tempty0, 0) : tempty0;
     int ti = 0;
-    for (int tile = group; tile < total; tile += ngroups, ++ti) {
+    for (int tile = k_begin; tile < k_end; ++tile, ++ti) {
       const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
       const NsProb& P = *g.P;
       const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
@@ -609,8 +582,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
       tc_fence_after();
       ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
-      // tcgen05.ld is warp-collective, and the staging barriers need all four
-      // warps: all 128 epilogue threads continue or stop together
+      // the update's staging tile is free again once the previous tile's TMA
+      // store has read it; the vote below is the barrier that publishes this
+      if (KIND == G_UPDATE && ew == 0 && lane == 0 && ti > 0) bulk_wait_read_all();
+      // tcgen05.ld is warp-collective, and the staging barriers need all
+      // epilogue warps: they continue or stop together
       if (!epilogue_all(ok)) break;
       float s_first = 1.0f;
       if (args.first && P.inv) {
@@ -620,14 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 
       if (KIND == G_UPDATE) {
-        // X <- s3 (a X + B X) [, W -= eta U]: each thread owns one output row;
-        // its X row comes from the TMA copy in shared memory (128-byte swizzle:
+        // X <- s3 (B X) [, W -= eta U]: each thread owns one output row and
+        // writes it into the staging tile in TMA box layout (128-byte swizzle:
         // box (row/64, col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
-        const int xb = ti % XB;
-        const bool xok = mbar_wait(xfull0 + 8 * xb, (ti / XB) & 1, args.hdr, 0x800u | KIND);
         const int rl = quarter * 32 + lane;
-        unsigned char* xbase = side + xb * kXTileBytes;
-        unsigned char* xrow = xbase + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
+        unsigned char* orow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
         // W <- W - eta * bf16(U) on the last iteration of a step: the fp32 row
         // segment of the next chunk is loaded while this chunk is processed
         const bool do_w = args.apply_w && P.w && r < g.M_;
@@ -650,28 +623,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 #pragma unroll
             for (int j = 0; j < 8; ++j) wnext[j] = __ldcs(src + j);
           }
-          if (!xok) continue;
-          // this thread's 32 X values of chunk c, read and then overwritten in
-          // place with the result (only this thread touches these 64 bytes)
-          unsigned char* bx = xrow + (c >> 1) * kBox;
-          uint4* q4[4];
-          float xv[32], out[32];
+          float out[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
+          unsigned char* bx = orow + (c >> 1) * kBox;
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int q = (c & 1) * 4 + t;
-            q4[t] = reinterpret_cast<uint4*>(bx + ((q ^ (rl & 7)) << 4));
-            const uint4 u4 = *q4[t];
-            xv[8 * t + 0] = bf16_lo(u4.x); xv[8 * t + 1] = bf16_hi(u4.x);
-            xv[8 * t + 2] = bf16_lo(u4.y); xv[8 * t + 3] = bf16_hi(u4.y);
-            xv[8 * t + 4] = bf16_lo(u4.z); xv[8 * t + 5] = bf16_hi(u4.z);
-            xv[8 * t + 6] = bf16_lo(u4.w); xv[8 * t + 7] = bf16_hi(u4.w);
+            *reinterpret_cast<uint4*>(bx + ((q ^ (rl & 7)) << 4)) =
+                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
+                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
           }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = s_first * (args.ca * xv[i] + __uint_as_float(v[i]));
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            *q4[t] = make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
-                                pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
           const int cb = g.col0 + c * 32;
           if (w_full(c)) {
             // one rounded product, one rounded difference per element
@@ -704,25 +666,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
           else mbar_arrive(tempty0 + 8 * acc);
         }
-        // the finished tile leaves by TMA (boxes outside the matrix are skipped,
-        // partial ones are clipped by the tensor map); the X buffer is handed
-        // back to the producer once the stores have read it
+        // the finished tile leaves by TMA (boxes outside the matrix are
+        // skipped, partial ones are clipped by the tensor map); the storing
+        // thread waits for the read before the next tile's vote
         fence_proxy_async_smem();
         named_barrier_epilogue();
         if (ew == 0 && lane == 0) {
-          if (xok) {
-            const CUtensorMap* md = &P.map_x[args.dst];
-            const uint32_t xs = smem_u32(xbase);
+          const CUtensorMap* md = &P.map_x[args.dst];
+          const uint32_t xs = smem_u32(side);
 #pragma unroll
-            for (int bi = 0; bi < 2; ++bi)
+          for (int bi = 0; bi < 2; ++bi)
 #pragma unroll
-              for (int bj = 0; bj < 4; ++bj)
-                if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * bj < g.N_)
-                  tma_store_2d(md, xs + (bi * 4 + bj) * kBox, g.col0 + 64 * bj, g.row0 + 64 * bi);
-            bulk_commit();
-            bulk_wait_read_all();
-          }
-          mbar_arrive(xempty0 + 8 * xb);
+            for (int bj = 0; bj < 4; ++bj)
+              if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * bj < g.N_)
+                tma_store_2d(md, xs + (bi * 4 + bj) * kBox, g.col0 + 64 * bj, g.row0 + 64 * bi);
+          bulk_commit();
         }
       } else {
         // symmetric products: stage 128 x 128 halves in shared memory (4-byte
@@ -748,8 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 #pragma unroll
                 for (int i = 0; i < 32; ++i) av[i] = 0.0f;
               }
+              // a on the diagonal (row r, column cb + i): the a X term of the update
 #pragma unroll
-              for (int i = 0; i < 32; ++i) out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]);
+              for (int i = 0; i < 32; ++i)
+                out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]) + (cb + i == r ? args.ca : 0.0f);
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -925,7 +885,32 @@ size_t scratch_bytes(const Shape& s) {
   const int64_t ld = (m + 7) / 8 * 8;
   return 2 * align_up((size_t)(m * ld) * 2, 256) + 2 * align_up((size_t)(s.rows * s.cols) * 2, 256);
 }
-size_t table_bytes(int32_t n) { return align_up((size_t)n * sizeof(NsProb), 256) + align_up((size_t)3 * (n + 1) * 4, 256); }
+
+// Output tiles of a rows x cols problem per product kind.  Tiles are
+// (128 kCG) x 256; the symmetric products list only tiles touching the upper
+// triangle (kCG = 1: 128 I < 256 J + 256; kCG = 2: I <= J).
+void count_tiles(int64_t rows, int64_t cols, int32_t tiles_n[3], int32_t tiles[3]) {
+  const int64_t m = std::min(rows, cols), n = std::max(rows, cols);
+  const int64_t tile_m = 128 * kCG;
+  const int64_t tm = (m + tile_m - 1) / tile_m, tnm = (m + BN - 1) / BN;
+  int64_t sym = 0;
+  for (int64_t j = 0; j < tnm; ++j) sym += std::min<int64_t>(tm, kCG == 2 ? j + 1 : 2 * j + 2);
+  tiles_n[G_GRAM] = tiles_n[G_POLY] = (int32_t)tnm;
+  tiles[G_GRAM] = tiles[G_POLY] = (int32_t)sym;
+  const bool tall = rows > cols;
+  const int64_t um = tall ? n : m, un = tall ? m : n;   // G_UPDATE output (stored orientation)
+  tiles_n[G_UPDATE] = (int32_t)((un + BN - 1) / BN);
+  tiles[G_UPDATE] = (int32_t)(((um + tile_m - 1) / tile_m) * tiles_n[G_UPDATE]);
+}
+
+constexpr int kMaxGroups = 512;   // schedule capacity: CTA groups per launch
+
+// Device table of a problem set: the problems, then per product kind the
+// group starts [kMaxGroups + 1] and the schedule entries.
+size_t table_bytes(int32_t n, const int64_t total_tiles) {
+  return align_up((size_t)n * sizeof(NsProb), 256) + 3 * align_up((size_t)(kMaxGroups + 1) * 4, 256) +
+         align_up((size_t)total_tiles * 8, 256);
+}
 
 // Fill one problem: x0 is the caller's matrix (row stride ld), scratch is carved from `ws`.
 bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, const float* inv, float* w,
@@ -955,34 +940,122 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   for (int i = 0; i < 3; ++i)
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
   if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
-  // tiles are (128 kCG) x 256; symmetric products list only tiles touching the
-  // upper triangle (kCG = 1: 128 I < 256 J + 256; kCG = 2: I <= J)
-  const int64_t tile_m = 128 * kCG;
-  const int64_t tm = (m + tile_m - 1) / tile_m, tnm = (m + BN - 1) / BN;
-  int64_t sym = 0;
-  for (int64_t j = 0; j < tnm; ++j) sym += std::min<int64_t>(tm, kCG == 2 ? j + 1 : 2 * j + 2);
-  P.tiles_n[G_GRAM] = P.tiles_n[G_POLY] = (int32_t)tnm;
-  P.tiles[G_GRAM] = P.tiles[G_POLY] = (int32_t)sym;
-  const int64_t um = P.tall ? P.n : P.m, un = P.tall ? P.m : P.n;   // G_UPDATE output (stored orientation)
-  P.tiles_n[G_UPDATE] = (int32_t)((un + BN - 1) / BN);
-  P.tiles[G_UPDATE] = (int32_t)(((um + tile_m - 1) / tile_m) * P.tiles_n[G_UPDATE]);
+  count_tiles(rows, cols, P.tiles_n, P.tiles);
   return true;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
 }
 
 struct Launchable {
   NsProb* d_probs = nullptr;
-  int32_t* d_tile_start = nullptr;  // [3][n+1]
+  int32_t* d_sched_start[3] = {nullptr, nullptr, nullptr};   // [groups + 1] per kind
+  TileRef* d_sched[3] = {nullptr, nullptr, nullptr};
   int32_t n = 0;
   int32_t total[3] = {0, 0, 0};
+  int32_t groups[3] = {0, 0, 0};
 };
 
-void prefix(const std::vector<NsProb>& probs, std::vector<int32_t>& ts, int32_t total[3]) {
-  const int32_t n = (int32_t)probs.size();
-  ts.assign(3 * (n + 1), 0);
-  for (int k = 0; k < 3; ++k) {
-    for (int32_t i = 0; i < n; ++i) ts[k * (n + 1) + i + 1] = ts[k * (n + 1) + i] + probs[i].tiles[k];
-    total[k] = ts[k * (n + 1) + n];
+// Relative cost of one output tile: its K loop in 64-wide steps plus the
+// epilogue, which overlaps the next tile's loop only in part.
+int64_t tile_cost(const NsProb& P, int kind) {
+  const int64_t K = (kind == G_GRAM) ? P.n : P.m;
+  return (K + BK - 1) / BK + 4;
+}
+
+// Host-side schedule of each product kind: tiles are dealt, costliest first,
+// to the least-loaded CTA group (longest processing time first); each group
+// then runs its tiles in that order.  The schedule and the problem table go
+// to `table` (device memory) with one copy each.
+struct Schedule {
+  std::vector<int32_t> start[3];
+  std::vector<TileRef> entries[3];
+};
+
+void build_schedule(const std::vector<NsProb>& probs, int groups_cap, Launchable& L, Schedule& S) {
+  for (int kind = 0; kind < 3; ++kind) {
+    std::vector<std::pair<int64_t, TileRef>> tiles;
+    for (int32_t p = 0; p < (int32_t)probs.size(); ++p) {
+      const int64_t c = tile_cost(probs[p], kind);
+      for (int32_t t = 0; t < probs[p].tiles[kind]; ++t) tiles.push_back({c, TileRef{p, t}});
+    }
+    const int32_t total = (int32_t)tiles.size();
+    const int groups = std::max(1, std::min<int>(total, groups_cap));
+    std::stable_sort(tiles.begin(), tiles.end(),
+                     [](const std::pair<int64_t, TileRef>& a, const std::pair<int64_t, TileRef>& b) {
+                       return a.first > b.first;
+                     });
+    // least-loaded group first, the lower index among equals
+    std::vector<std::pair<int64_t, int>> heap;
+    for (int g = 0; g < groups; ++g) heap.push_back({0, g});
+    auto later = [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) {
+      return a.first != b.first ? a.first > b.first : a.second > b.second;
+    };
+    std::make_heap(heap.begin(), heap.end(), later);
+    std::vector<std::vector<TileRef>> lists(groups);
+    for (const auto& t : tiles) {
+      std::pop_heap(heap.begin(), heap.end(), later);
+      auto& h = heap.back();
+      lists[h.second].push_back(t.second);
+      h.first += t.first;
+      std::push_heap(heap.begin(), heap.end(), later);
+    }
+    S.start[kind].assign(1, 0);
+    S.entries[kind].clear();
+    for (int g = 0; g < groups; ++g) {
+      S.entries[kind].insert(S.entries[kind].end(), lists[g].begin(), lists[g].end());
+      S.start[kind].push_back((int32_t)S.entries[kind].size());
+    }
+    L.total[kind] = total;
+    L.groups[kind] = total ? groups : 0;
   }
+}
+
+// Carve the schedule arrays out of a table laid out as `table_bytes` says.
+void carve_table(unsigned char* table, int32_t n, Launchable& L) {
+  L.n = n;
+  L.d_probs = reinterpret_cast<NsProb*>(table);
+  unsigned char* p = table + align_up((size_t)n * sizeof(NsProb), 256);
+  for (int k = 0; k < 3; ++k) {
+    L.d_sched_start[k] = reinterpret_cast<int32_t*>(p);
+    p += align_up((size_t)(kMaxGroups + 1) * 4, 256);
+  }
+  TileRef* e = reinterpret_cast<TileRef*>(p);
+  for (int k = 0; k < 3; ++k) {
+    L.d_sched[k] = e;
+    e += L.total[k];
+  }
+}
+
+// The copies of the problem table and the schedule (stream-ordered when `s`
+// is given, else synchronous).
+cudaError_t upload_table(const Launchable& L, const std::vector<NsProb>& hp, const Schedule& S, cudaStream_t s,
+                         bool async) {
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    if (bytes == 0) return cudaSuccess;
+    return async ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s)
+                 : cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice);
+  };
+  cudaError_t e = copy(L.d_probs, hp.data(), hp.size() * sizeof(NsProb));
+  for (int k = 0; k < 3 && e == cudaSuccess; ++k) {
+    e = copy(L.d_sched_start[k], S.start[k].data(), S.start[k].size() * 4);
+    if (e == cudaSuccess) e = copy(L.d_sched[k], S.entries[k].data(), S.entries[k].size() * sizeof(TileRef));
+  }
+  return e;
+}
+
+int64_t all_tiles(int64_t rows, int64_t cols) {
+  int32_t tn[3], t[3];
+  count_tiles(rows, cols, tn, t);
+  return (int64_t)t[0] + t[1] + t[2];
 }
 
 cudaError_t configure_kernels() {
@@ -997,27 +1070,16 @@ cudaError_t configure_kernels() {
   return result;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
   if (L.total[kind] == 0) return cudaSuccess;
   GemmArgs a = a0;
-  a.tile_start = L.d_tile_start + kind * (L.n + 1);
-  a.total_tiles = L.total[kind];
+  a.sched_start = L.d_sched_start[kind];
+  a.sched = L.d_sched[kind];
   void* args[] = {&a};
   void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM, kCG>
            : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY, kCG> : (void*)ns_gemm_kernel<G_UPDATE, kCG>;
   // persistent: one CTA group per SM group, never more groups than tiles
-  const int groups = std::min(L.total[kind], num_sms() / kCG);
+  const int groups = L.groups[kind];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * kCG);
   cfg.blockDim = dim3(kThreads);
@@ -1041,7 +1103,6 @@ qmuon_status run_iterations(const Launchable& L, int32_t iters, const float coef
   if (ce != cudaSuccess) return set_error("newton-schulz: cudaFuncSetAttribute(max dynamic shared memory)", ce);
   GemmArgs a{};
   a.probs = L.d_probs;
-  a.n_probs = L.n;
   a.ca = coeffs[0];
   a.cb = coeffs[1];
   a.cc = coeffs[2];
@@ -1091,8 +1152,14 @@ qmuon_status validate_problem(const qmuon_ns_problem& p) {
   return QMUON_OK;
 }
 
+size_t batch_table_bytes(const qmuon_ns_problem* probs, int32_t n) {
+  int64_t tiles = 0;
+  for (int32_t i = 0; i < n; ++i) tiles += all_tiles(probs[i].rows, probs[i].cols);
+  return table_bytes(n, tiles);
+}
+
 size_t batch_workspace_bytes(const qmuon_ns_problem* probs, int32_t n) {
-  size_t b = table_bytes(n);
+  size_t b = batch_table_bytes(probs, n);
   for (int32_t i = 0; i < n; ++i) b += scratch_bytes({probs[i].rows, probs[i].cols});
   return b;
 }
@@ -1102,7 +1169,7 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
   if (!encoder()) return set_error_msg("cuTensorMapEncodeTiled not available from the driver", QMUON_ERR_CUDA);
   std::vector<NsProb> hp(n);
   unsigned char* table = ws;
-  unsigned char* scratch = ws + table_bytes(n);
+  unsigned char* scratch = ws + batch_table_bytes(probs, n);
   for (int32_t i = 0; i < n; ++i) {
     if (!fill_problem(hp[i], probs[i].x, probs[i].rows, probs[i].cols, probs[i].ld, probs[i].inv_norm, nullptr, 0,
                       scratch))
@@ -1110,13 +1177,10 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
   }
   if ((size_t)(scratch - ws) > ws_bytes) return QMUON_ERR_WORKSPACE_TOO_SMALL;
   Launchable L;
-  L.n = n;
-  L.d_probs = reinterpret_cast<NsProb*>(table);
-  L.d_tile_start = reinterpret_cast<int32_t*>(table + align_up((size_t)n * sizeof(NsProb), 256));
-  std::vector<int32_t> ts;
-  prefix(hp, ts, L.total);
-  cudaError_t ce = cudaMemcpyAsync(L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaMemcpyAsync(L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s);
+  Schedule S;
+  build_schedule(hp, std::min(num_sms() / kCG, kMaxGroups), L, S);
+  carve_table(table, n, L);
+  cudaError_t ce = upload_table(L, hp, S, s, true);
   if (ce != cudaSuccess) return set_error("newton-schulz: upload problem table", ce);
   // MXFP8 inputs: expand the carrier into the problem's bf16 matrix first
   for (int32_t i = 0; i < n; ++i) {
@@ -1190,7 +1254,9 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
     *tabs = T;
   }
   const int32_t np = (int32_t)hp.size();
-  const size_t need = table_bytes(np);
+  int64_t tiles = 0;
+  for (const NsProb& P : hp) tiles += (int64_t)P.tiles[0] + P.tiles[1] + P.tiles[2];
+  const size_t need = table_bytes(np, tiles);
   if (T->d_bytes < need) {
     if (T->d_mem) cudaFree(T->d_mem);
     T->d_mem = nullptr;
@@ -1199,14 +1265,10 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
     if (me != cudaSuccess) return set_error("qmuon_step: cudaMalloc problem table", me);
     T->d_bytes = need;
   }
-  T->L.n = np;
-  T->L.d_probs = static_cast<NsProb*>(T->d_mem);
-  T->L.d_tile_start = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(T->d_mem) +
-                                                 align_up((size_t)np * sizeof(NsProb), 256));
-  std::vector<int32_t> ts;
-  prefix(hp, ts, T->L.total);
-  cudaError_t ue = cudaMemcpy(T->L.d_probs, hp.data(), hp.size() * sizeof(NsProb), cudaMemcpyHostToDevice);
-  if (ue == cudaSuccess) ue = cudaMemcpy(T->L.d_tile_start, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice);
+  Schedule S;
+  build_schedule(hp, std::min(num_sms() / kCG, kMaxGroups), T->L, S);
+  carve_table(static_cast<unsigned char*>(T->d_mem), np, T->L);
+  const cudaError_t ue = upload_table(T->L, hp, S, nullptr, false);
   if (ue != cudaSuccess) return set_error("qmuon_step: upload problem table", ue);
   T->host = std::move(hp);
   T->ws = ws;

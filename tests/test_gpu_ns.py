@@ -1,8 +1,9 @@
 """GPU parity of the Newton-Schulz engine (tcgen05) and of the MuonBP step.
 
 Single-iteration runs with one coefficient switched on at a time check each
-of the three tensor-core products on its own (wide and tall operands, ragged
-shapes) against fp64 products of the same bf16-rounded intermediates; the
+term of the three tensor-core products on its own (wide and tall operands,
+ragged shapes) against fp64 products of the same bf16-rounded intermediates
+(the a X term travels on the diagonal of the bf16 polynomial B); the
 five-iteration runs and the steps are held to the oracle tolerance:
 relative Frobenius error <= 2e-2 and per-row cosine >= 0.999.
 """
@@ -29,14 +30,17 @@ def _bf16_round(x: np.ndarray) -> np.ndarray:
 
 
 def _one_iteration_reference(M, coeffs, inv):
+    # the engine's rounding points: A and the polynomial B = a I + b A + c A A
+    # (the a X term folded into B's diagonal) are stored in bf16, the update
+    # is the single product B X; everything else here is fp64
     a, b, c = coeffs
     X = M * inv
     tall = X.shape[0] > X.shape[1]
     if tall:
         X = X.T
     A = _bf16_round(X @ X.T)
-    B = _bf16_round(b * A + c * (A @ A))
-    out = a * X + B @ X
+    B = _bf16_round(a * np.eye(A.shape[0]) + b * A + c * (A @ A))
+    out = B @ X
     return out.T if tall else out
 
 
