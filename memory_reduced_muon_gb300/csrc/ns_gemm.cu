@@ -51,27 +51,42 @@ constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // symmetric epilogue staging: half an output tile
 constexpr uint32_t kOutTileBytes = 8 * kBox;         // G_UPDATE: a CTA's 128 x 256 output tile (TMA boxes)
+constexpr uint32_t kUSlotBytes = 2 * kBox;           // G_UPDATE_W: 128 x 64 output columns of one step
+constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 32 fp32 weights (one TMA box)
 
 // Shared memory per product kind and CTA group.  One CTA (CG = 1) owns a
 // 128 x 256 output tile and loads all of A (128 rows) and B (256 rows) per
 // stage (48 KB); a CTA pair (CG = 2) owns 256 x 256, each CTA loading its
 // 128 rows of A and half of B (32 KB per stage per CTA).  The symmetric
 // products keep a staging buffer for coalesced (and mirrored) stores; the
-// update product stages its whole output tile in TMA box layout.
+// update product stages its whole output tile in TMA box layout; the updates
+// that also move the weights keep two output slots of one step each and a
+// ring of weight chunks, two per step (one per column half), two steps deep
+// (kind 3, for short K loops where the weights bound the tile) or one step
+// deep with a fifth operand stage (kind 4, for long K loops).
 __host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ? 4 * kBox : kStageBytes; }
+__host__ __device__ constexpr int w_depth_of(int kind) { return kind == 3 ? 2 : 1; }
 __host__ __device__ constexpr int stages_of(int kind, int cg) {
-  return cg == 2 ? (kind == 2 ? 4 : 6) : (kind == 2 ? 3 : 4);
+  return cg == 2 ? (kind == 3 ? 4 : kind == 2 || kind == 4 ? 5 : 6) : (kind >= 3 ? 2 : kind == 2 ? 3 : 4);
 }
 __host__ __device__ constexpr uint32_t side_bytes_of(int kind, int cg) {
-  return kind == 2 ? kOutTileBytes : kStageOutBytes;
+  return kind >= 3 ? 2 * kUSlotBytes + 2 * w_depth_of(kind) * kWChunkBytes
+                   : kind == 2 ? kOutTileBytes : kStageOutBytes;
 }
 __host__ __device__ constexpr size_t smem_bytes_of(int kind, int cg) {
   return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind, cg) + 1024 + 256;
 }
 
+static_assert(smem_bytes_of(0, 2) <= 232448 && smem_bytes_of(1, 2) <= 232448 && smem_bytes_of(2, 2) <= 232448 &&
+                  smem_bytes_of(3, 2) <= 232448 && smem_bytes_of(4, 2) <= 232448,
+              "dynamic shared memory above the 227 KB a CTA may use");
+
 constexpr long long kWaitCycles = 4000000000LL;  // bounded waits: ~2 s at 2 GHz
 
-enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2 };
+// G_UPDATE_W and G_UPDATE_W1 are G_UPDATE on the last iteration of a step:
+// they also apply W <- W - eta * bf16(U) to the fp32 weights (weight ring two
+// steps or one step deep).
+enum { G_GRAM = 0, G_POLY = 1, G_UPDATE = 2, G_UPDATE_W = 3, G_UPDATE_W1 = 4 };
 
 // CTA group of the Newton-Schulz GEMMs: 2 = CTA pairs (cta_group::2).
 constexpr int kCG = 2;
@@ -80,6 +95,7 @@ struct alignas(128) NsProb {
   CUtensorMap map_x[3];   // X buffers: 0 = caller's matrix, 1/2 = workspace ping-pong
   CUtensorMap map_a;      // m x m Gram
   CUtensorMap map_b;      // m x m polynomial
+  CUtensorMap map_w;      // fp32 weights (stored orientation, 32 x 128 boxes), when w is set
   __nv_bfloat16* x[3];
   int64_t x_ld[3];
   __nv_bfloat16* a;
@@ -106,7 +122,6 @@ struct GemmArgs {
   const TileRef* sched;
   int32_t src, dst;           // X buffer indices read / written (G_UPDATE); src for G_GRAM
   int32_t first;              // apply inv (first iteration)
-  int32_t apply_w;            // W -= eta * U (last iteration of a step)
   float ca, cb, cc, eta;
   WsHeader* hdr;
 };
@@ -161,6 +176,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+// The same with an L2 cache policy (streams read once: evict first).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 // Make tensor maps written through the generic proxy (host copies into global
 // memory) visible to the tensor-map proxy before the first TMA that uses them.
@@ -222,6 +251,12 @@ __device__ __forceinline__ void mma_commit_cg(uint32_t bar) {
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
                ::"l"(map), "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int x, int y,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+               ::"l"(map), "r"(src), "r"(x), "r"(y), "l"(policy)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -336,7 +371,7 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* p, int n, float 
 // square tiles with I <= J.
 template <int CG>
 __device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local, int& I, int& J) {
-  if (kind == G_UPDATE) {
+  if (kind >= G_UPDATE) {
     const int tn = P.tiles_n[G_UPDATE];
     I = local / tn;
     J = local % tn;
@@ -397,7 +432,7 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int k, int r
     g.mapA = &P.map_x[args.src]; g.a_mn = false;
     g.mapB = &P.map_b; g.b_mn = false;
   }
-  if (KIND == G_UPDATE) g.mirror = false;   // only the symmetric products mirror
+  if (KIND >= G_UPDATE) g.mirror = false;   // only the symmetric products mirror
   return g;
 }
 
@@ -444,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t wfull0 = smem_u32(bars + 2 * STAGES + 4);   // weight passes: chunk slots 0..3
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (CG == 2) ? (int)cluster_rank() : 0;
@@ -461,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       mbar_init(tfull0 + 8 * b, 1);
       mbar_init(tempty0 + 8 * b, kEpiWarps * CG);   // one arrival per epilogue warp of the group
     }
+    for (int b = 0; b < 4; ++b) mbar_init(wfull0 + 8 * b, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -555,29 +592,49 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       }
     }
   } else {
-    // ---- epilogue: warps 2..5; TMEM lane quarter = warp % 4 ----
+    // ---- epilogue: warps 2..9; TMEM lane quarter = warp % 4 ----
     const int quarter = warp & 3;
     const int ew = warp - 2;          // epilogue warp 0..7
     const int ch = ew >> 2;           // column half of the tile (TMEM lanes are shared per quarter)
     const uint32_t tempty_l = (CG == 2) ? cluster_map(tempty0, 0) : tempty0;
+    // Weight passes: the weight ring.  Step w (four per tile) of half h uses
+    // slot 2 (w % WD) + h; one thread per half loads and stores that half's
+    // chunks, loading each WD steps before it is used.
+    constexpr bool WPASS = KIND >= G_UPDATE_W;
+    constexpr int WD = w_depth_of(KIND);
+    unsigned char* wring = side + 2 * kUSlotBytes;
+    const bool wthread = WPASS && (ew & 3) == 1 && lane == 0;
+    const int w_steps = 4 * (k_end - k_begin);
+    int wstep = 0, w_issued = 0;
+    const CUtensorMap* w_fenced = nullptr;
+    // weights and the final output are touched once: keep the operands in L2 instead
+    const uint64_t stream_policy = WPASS ? policy_evict_first() : 0ull;
+    auto issue_w = [&](int w) {
+      const TileGeom gw = tile_geom<KIND, CG>(args, k_begin + (w >> 2), rank);
+      const CUtensorMap* mw = &gw.P->map_w;
+      if (mw != w_fenced) {
+        fence_tensormap(mw);
+        w_fenced = mw;
+      }
+      const int slot = 2 * (w % WD) + ch;
+      const uint32_t bar = wfull0 + 8 * slot;
+      mbar_expect_tx(bar, kWChunkBytes);
+      tma_load_2d_hint(smem_u32(wring + slot * kWChunkBytes), mw, bar, gw.col0 + 32 * (2 * (w & 3) + ch), gw.row0,
+                       stream_policy);
+    };
+    if (wthread)
+      while (w_issued < WD && w_issued < w_steps) issue_w(w_issued++);
     int ti = 0;
     for (int tile = k_begin; tile < k_end; ++tile, ++ti) {
       const TileGeom g = tile_geom<KIND, CG>(args, tile, rank);
       const NsProb& P = *g.P;
       const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
       const int acc = ti & 1, use = ti >> 1;
-      if (KIND == G_POLY || KIND == G_UPDATE) {
-        // pull this thread's global epilogue operands into L2 while the tensor cores run
-        if (r < g.M_) {
-          const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
-          if (KIND == G_POLY) {
-            const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
-            for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
-          } else if (args.apply_w && P.w) {
-            const char* pw = reinterpret_cast<const char*>(P.w + (int64_t)r * P.w_ld + g.col0);
-            for (int o = 0; o < span * 4; o += 128) prefetch_l2(pw + o);
-          }
-        }
+      if (KIND == G_POLY && r < g.M_) {
+        // pull this thread's row of A (the b A term) into L2 while the tensor cores run
+        const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
+        const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
+        for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
       }
       bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
       tc_fence_after();
@@ -596,33 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 
       if (KIND == G_UPDATE) {
-        // X <- s3 (B X) [, W -= eta U]: each thread owns one output row and
-        // writes it into the staging tile in TMA box layout (128-byte swizzle:
-        // box (row/64, col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
+        // X <- s3 (B X): each thread owns one output row and writes it into
+        // the staging tile in TMA box layout (128-byte swizzle: box (row/64,
+        // col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
         const int rl = quarter * 32 + lane;
         unsigned char* orow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
-        // W <- W - eta * bf16(U) on the last iteration of a step: the fp32 row
-        // segment of the next chunk is loaded while this chunk is processed
-        const bool do_w = args.apply_w && P.w && r < g.M_;
-        float* wrow = do_w ? P.w + (int64_t)r * P.w_ld : nullptr;
-        float4 wnext[8];
-        auto w_full = [&](int cc) { return do_w && g.col0 + cc * 32 + 32 <= g.N_; };
-        if (w_full(4 * ch)) {
-          const float4* src = reinterpret_cast<const float4*>(wrow + g.col0 + 4 * ch * 32);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) wnext[j] = __ldcs(src + j);
-        }
         for (int c = 4 * ch; c < 4 * ch + 4; ++c) {   // this warp's 128 columns
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(c * 32), v);
-          float4 wv[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) wv[j] = wnext[j];
-          if (c + 1 < 4 * ch + 4 && w_full(c + 1)) {
-            const float4* src = reinterpret_cast<const float4*>(wrow + g.col0 + (c + 1) * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) wnext[j] = __ldcs(src + j);
-          }
           float out[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
@@ -633,31 +671,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             *reinterpret_cast<uint4*>(bx + ((q ^ (rl & 7)) << 4)) =
                 make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
                            pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
-          }
-          const int cb = g.col0 + c * 32;
-          if (w_full(c)) {
-            // one rounded product, one rounded difference per element
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float* e = reinterpret_cast<float*>(&wv[j]);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float u = __bfloat162float(__float2bfloat16_rn(out[4 * j + k]));
-                e[k] = __fsub_rn(e[k], __fmul_rn(args.eta, u));
-              }
-            }
-            float4* dstw = reinterpret_cast<float4*>(wrow + cb);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) __stcs(dstw + j, wv[j]);
-          } else if (do_w && cb < g.N_) {
-            const int nv = g.N_ - cb;   // ragged last chunk: element by element
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i < nv) {
-                const float u = __bfloat162float(__float2bfloat16_rn(out[i]));
-                wrow[cb + i] = __fsub_rn(wrow[cb + i], __fmul_rn(args.eta, u));
-              }
-            }
           }
         }
         tc_fence_before();
@@ -681,6 +694,81 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
               if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * bj < g.N_)
                 tma_store_2d(md, xs + (bi * 4 + bj) * kBox, g.col0 + 64 * bj, g.row0 + 64 * bi);
           bulk_commit();
+        }
+      } else if (WPASS) {
+        // X <- s3 (B X) and W <- W - eta * bf16(X), in four steps of 64
+        // columns: at step s, half h of the epilogue warps takes column chunk
+        // c = 2 s + h.  The step's output columns go to an output slot (two
+        // 64 x 64 boxes) and leave by TMA; the chunk's weights arrive by TMA
+        // in a ring slot, are updated in place and leave by TMA.
+        const int rl = quarter * 32 + lane;
+        for (int st = 0; st < 4; ++st, ++wstep) {
+          const int c = 2 * st + ch;
+          const int slot = 2 * (wstep % WD) + ch;
+          const bool wok = mbar_wait(wfull0 + 8 * slot, (wstep / WD) & 1, args.hdr, 0x900u | KIND);
+          __syncwarp();   // tcgen05.ld is warp-collective: the lane back from its single-thread role rejoins
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          if (st == 3) {   // every TMEM read of this accumulator is done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
+              else mbar_arrive(tempty0 + 8 * acc);
+            }
+          }
+          float out[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
+          unsigned char* ub = side + (wstep & 1) * kUSlotBytes + (rl >> 6) * kBox + (rl & 63) * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = ch * 4 + t;
+            *reinterpret_cast<uint4*>(ub + ((q ^ (rl & 7)) << 4)) =
+                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
+                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
+          }
+          if (wok) {
+            // this thread's 32 weights: one rounded product and one rounded
+            // difference per element (128-byte swizzle, like the boxes above)
+            unsigned char* wb = wring + slot * kWChunkBytes + rl * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4* pw = reinterpret_cast<float4*>(wb + ((j ^ (rl & 7)) << 4));
+              float4 w4 = *pw;
+              float* e = reinterpret_cast<float*>(&w4);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float u = __bfloat162float(__float2bfloat16_rn(out[4 * j + k]));
+                e[k] = __fsub_rn(e[k], __fmul_rn(args.eta, u));
+              }
+              *pw = w4;
+            }
+          }
+          fence_proxy_async_smem();
+          // the output slot written now was last stored two steps ago: its
+          // store has read it once the storing thread passes this point
+          if (ew == 0 && lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          named_barrier_epilogue();
+          if (ew == 0 && lane == 0) {
+            const CUtensorMap* md = &P.map_x[args.dst];
+            const uint32_t us = smem_u32(side + (wstep & 1) * kUSlotBytes);
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi)
+              if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * st < g.N_)
+                tma_store_2d_hint(md, us + bi * kBox, g.col0 + 64 * st, g.row0 + 64 * bi, stream_policy);
+            bulk_commit();
+          }
+          if (wthread) {
+            const bool clean = *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
+            if (wok && clean && g.row0 < g.M_ && g.col0 + 32 * c < g.N_)
+              tma_store_2d_hint(&P.map_w, smem_u32(wring + slot * kWChunkBytes), g.col0 + 32 * c, g.row0,
+                                stream_policy);
+            bulk_commit();
+            bulk_wait_read_all();   // the slot is free for the chunk WD steps ahead
+            if (clean && w_issued < w_steps) issue_w(w_issued++);
+          }
         }
       } else {
         // symmetric products: stage 128 x 128 halves in shared memory (4-byte
@@ -764,12 +852,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
       }
     }
+    // weight chunks loaded but never used (the run stopped early) land before exit
+    if (wthread)
+      for (int w = wstep; w < w_issued; ++w)
+        mbar_wait(wfull0 + 8 * (2 * (w % WD) + ch), (w / WD) & 1, args.hdr, 0xA00u | KIND);
   }
 
   // ---- teardown: every accumulator read is done, every TMA store has
   // completed and, in a pair, the peer no longer touches this CTA's barriers
   // or shared memory ----
-  if (KIND == G_UPDATE && warp == 2 && lane == 0) bulk_wait_all();
+  if (KIND >= G_UPDATE && warp >= 2 && ((warp - 2) & 3) <= 1 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncwarp();   // lanes that skipped the single-thread roles rejoin before the aligned barrier
   if (CG == 2) cluster_sync_all();
@@ -874,6 +966,29 @@ bool encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
   return true;
 }
 
+// 2-D fp32 map of the weights (rows x cols, row stride ld elements), boxes of
+// 32 columns x 128 rows (128-byte rows, 128-byte swizzle).
+bool encode_w(CUtensorMap* m, const float* base, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[256];
+    std::snprintf(msg, sizeof(msg),
+                  "cuTensorMapEncodeTiled returned %d for a %lld x %lld fp32 weight matrix (row stride %lld) at %p",
+                  (int)r, (long long)rows, (long long)cols, (long long)ld, (const void*)base);
+    set_error_msg(msg, QMUON_ERR_CUDA);
+    return false;
+  }
+  return true;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Shape of one problem's scratch: A and B (m x m) and two X buffers (rows x cols, compact).
@@ -940,6 +1055,7 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   for (int i = 0; i < 3; ++i)
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
   if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
+  if (w && !encode_w(&P.map_w, w, rows, cols, w_ld)) return false;
   count_tiles(rows, cols, P.tiles_n, P.tiles);
   return true;
 }
@@ -962,6 +1078,9 @@ struct Launchable {
   int32_t n = 0;
   int32_t total[3] = {0, 0, 0};
   int32_t groups[3] = {0, 0, 0};
+  // the update tiles' K loops are long on average (>= 2048): the weight pass
+  // then hides behind the tensor cores and runs with more operand stages
+  bool long_k = false;
 };
 
 // Relative cost of one output tile: its K loop in 64-wide steps plus the
@@ -1016,6 +1135,11 @@ void build_schedule(const std::vector<NsProb>& probs, int groups_cap, Launchable
     }
     L.total[kind] = total;
     L.groups[kind] = total ? groups : 0;
+    if (kind == G_UPDATE) {
+      double sum_k = 0.0;
+      for (const auto& t : tiles) sum_k += probs[t.second.prob].m;
+      L.long_k = total > 0 && sum_k >= 2048.0 * total;
+    }
   }
 }
 
@@ -1065,21 +1189,28 @@ cudaError_t configure_kernels() {
     cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM, kCG>, attr, (int)smem_bytes_of(G_GRAM, kCG));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY, kCG>, attr, (int)smem_bytes_of(G_POLY, kCG));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE, kCG>, attr, (int)smem_bytes_of(G_UPDATE, kCG));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE_W, kCG>, attr, (int)smem_bytes_of(G_UPDATE_W, kCG));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE_W1, kCG>, attr, (int)smem_bytes_of(G_UPDATE_W1, kCG));
     result = e;
   }
   return result;
 }
 
 cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
-  if (L.total[kind] == 0) return cudaSuccess;
+  const int sk = kind >= G_UPDATE_W ? G_UPDATE : kind;   // the weight passes run the update's tiles
+  if (L.total[sk] == 0) return cudaSuccess;
   GemmArgs a = a0;
-  a.sched_start = L.d_sched_start[kind];
-  a.sched = L.d_sched[kind];
+  a.sched_start = L.d_sched_start[sk];
+  a.sched = L.d_sched[sk];
   void* args[] = {&a};
   void* fn = kind == G_GRAM ? (void*)ns_gemm_kernel<G_GRAM, kCG>
-           : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY, kCG> : (void*)ns_gemm_kernel<G_UPDATE, kCG>;
+           : kind == G_POLY ? (void*)ns_gemm_kernel<G_POLY, kCG>
+           : kind == G_UPDATE ? (void*)ns_gemm_kernel<G_UPDATE, kCG>
+           : kind == G_UPDATE_W ? (void*)ns_gemm_kernel<G_UPDATE_W, kCG> : (void*)ns_gemm_kernel<G_UPDATE_W1, kCG>;
   // persistent: one CTA group per SM group, never more groups than tiles
-  const int groups = L.groups[kind];
+  const int groups = L.groups[sk];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * kCG);
   cfg.blockDim = dim3(kThreads);
@@ -1115,10 +1246,9 @@ qmuon_status run_iterations(const Launchable& L, int32_t iters, const float coef
     a.src = src;
     a.dst = dst;
     a.first = (it == 0);
-    a.apply_w = (last && apply_w) ? 1 : 0;
     cudaError_t e = launch_gemm(G_GRAM, L, a, s);
     if (e == cudaSuccess) e = launch_gemm(G_POLY, L, a, s);
-    if (e == cudaSuccess) e = launch_gemm(G_UPDATE, L, a, s);
+    if (e == cudaSuccess) e = launch_gemm((last && apply_w) ? (L.long_k ? G_UPDATE_W1 : G_UPDATE_W) : G_UPDATE, L, a, s);
     if (e != cudaSuccess) return set_error("newton-schulz: cudaLaunchKernel(ns_gemm)", e);
     src = dst;
   }

@@ -129,14 +129,11 @@ def _step_case(shapes, tile, seed):
     return mats, plan, states_d, weights_d, grads_d, host
 
 
-@pytest.mark.parametrize("P", [5, 1, 0])
-def test_muonbp_steps_vs_oracle(P):
-    shapes = [(512, 2048), (256, 2048), (1024, 4096), (2048, 2048)]
-    tile = (1, 8)
-    mats, plan, states_d, weights_d, grads_d, host = _step_case(shapes, tile, 40)
+def _run_steps(shapes, tile, P, steps, seed):
+    mats, plan, states_d, weights_d, grads_d, host = _step_case(shapes, tile, seed)
     ws = torch.empty(q.qmuon_workspace_size(plan, q.QMUON_WS_STEP), dtype=torch.uint8, device="cuda")
-    eta_full, eta_block = 0.02, 0.02 / math.sqrt(8)
-    for t in range(1, 6):
+    eta_full, eta_block = 0.02, 0.02 / math.sqrt(tile[0] * tile[1])
+    for t in range(1, steps + 1):
         gh = []
         for i, (m, g) in enumerate(zip(mats, grads_d)):
             src = random_grad(m.numel, "bf16", 900 + 10 * t + i).reshape(m.rows, m.cols)
@@ -156,18 +153,44 @@ def test_muonbp_steps_vs_oracle(P):
             np.testing.assert_array_equal(states_d[i][1].cpu().numpy(), host[i].absmax)
             got = bf16_to_f64(grads_d[i])
             ref = codec.f32_from_bf16_bits(U[i]).astype(np.float64)
-            if full:
-                assert rel_fro(got, ref) <= 2e-2 and min_row_cos(got, ref) >= 0.999, (t, m)
-            else:
-                th, tw = m.rows // tile[0], m.cols // tile[1]
-                for j in range(tile[1]):
-                    sl = (slice(None), slice(j * tw, (j + 1) * tw))
-                    assert rel_fro(got[sl], ref[sl]) <= 2e-2 and min_row_cos(got[sl], ref[sl]) >= 0.999, (t, m, j)
+            th, tw = (m.rows, m.cols) if full else (m.rows // tile[0], m.cols // tile[1])
+            for bi in range(m.rows // th):
+                for bj in range(m.cols // tw):
+                    sl = (slice(bi * th, (bi + 1) * th), slice(bj * tw, (bj + 1) * tw))
+                    assert rel_fro(got[sl], ref[sl]) <= 2e-2 and min_row_cos(got[sl], ref[sl]) >= 0.999, (t, m, bi, bj)
             # the weight moved by eta * U (eta_full on full steps, eta_block
-            # otherwise): compare the applied updates
-            dW = weights_d[i].cpu().numpy().astype(np.float64) - w_before[i]
+            # otherwise): compare the applied updates, and check that every
+            # weight moved by exactly fl(eta * bf16(U)) of the U left in place
+            w_after = weights_d[i].cpu().numpy()
+            dW = w_after.astype(np.float64) - w_before[i]
             dW_ref = host[i].weight.astype(np.float64) - w_before[i]
             assert rel_fro(dW, dW_ref) <= 2e-2, (t, m)
+            eta = np.float32(eta_full if full else eta_block)
+            u32 = grads_d[i].float().cpu().numpy()
+            expect = (w_before[i].astype(np.float32) - (eta * u32).astype(np.float32)).astype(np.float32)
+            np.testing.assert_array_equal(w_after, expect)
         # keep both sides on the same weights so errors do not accumulate
         for i in range(len(mats)):
             weights_d[i].copy_(torch.from_numpy(host[i].weight).cuda())
+
+
+@pytest.mark.parametrize("P", [5, 1, 0])
+def test_muonbp_steps_vs_oracle(P):
+    _run_steps([(512, 2048), (256, 2048), (1024, 4096), (2048, 2048)], (1, 8), P, 5, 40)
+
+
+def test_steps_ragged_shapes():
+    # full steps on shapes that are not multiples of the 256 x 256 tile (wide,
+    # tall, tiny): partial weight and output boxes at every edge
+    _run_steps([(300, 520), (520, 136), (8, 16), (1000, 264), (130, 136)], (1, 1), 1, 2, 70)
+
+
+def test_steps_row_tiles():
+    # block steps on a 2 x 1 row tiling: problems that start mid-matrix
+    _run_steps([(512, 136), (1024, 256)], (2, 1), 0, 2, 90)
+
+
+def test_steps_long_k():
+    # full steps whose update tiles have K >= 2048 on average: the weight pass
+    # with the one-step weight ring and five operand stages (a ragged shape too)
+    _run_steps([(2048, 2304), (2100, 2056)], (1, 1), 1, 2, 110)
