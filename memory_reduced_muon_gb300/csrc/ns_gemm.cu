@@ -335,9 +335,6 @@ __device__ __forceinline__ uint32_t make_idesc(bool a_mn, bool b_mn, int M = BM)
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -474,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
   unsigned char* side = smem + STAGES * SB;                   // staging: half tile (symmetric) or tile (update)
-  uint32_t* stage_out = reinterpret_cast<uint32_t*>(side);    // 128 x 64 words
   uint64_t* bars = reinterpret_cast<uint64_t*>(side + side_bytes_of(KIND, CG));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 8);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
@@ -630,11 +626,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const NsProb& P = *g.P;
       const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
       const int acc = ti & 1, use = ti >> 1;
-      if (KIND == G_POLY && r < g.M_) {
-        // pull this thread's row of A (the b A term) into L2 while the tensor cores run
-        const int span = (g.N_ - g.col0) < BN ? (g.N_ - g.col0) : BN;
-        const char* pa = reinterpret_cast<const char*>(P.a + (int64_t)r * P.ab_ld + g.col0);
-        for (int o = 0; o < span * 2; o += 128) prefetch_l2(pa + o);
+      // G_POLY: this thread's A values for the b A term (its row, the four
+      // 32-column chunks c = 2 st + h it will finish) are loaded before the
+      // accumulator is ready, so their latency overlaps the tensor cores; a
+      // chunk that crosses the matrix edge is read element by element when used
+      uint4 apre[4][4];
+      if (KIND == G_POLY) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int cb = g.col0 + (2 * j + ch) * 32;
+          if (r < g.M_ && cb + 32 <= g.M_) {
+            const uint4* q = reinterpret_cast<const uint4*>(P.a + (int64_t)r * P.ab_ld + cb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) apre[j][i] = __ldg(q + i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) apre[j][i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
       }
       bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
       tc_fence_after();
@@ -771,41 +780,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
         }
       } else {
-        // symmetric products: stage 128 x 128 halves in shared memory (4-byte
-        // words XOR-swizzled by row), store rows coalesced and, for tiles
-        // strictly above the diagonal, the transposed tile as well
-        __nv_bfloat16* outp = (KIND == G_GRAM) ? P.a : P.b;
-        const int64_t ld = P.ab_ld;
+        // symmetric products, in four steps of 64 columns: at step st, half h
+        // of the epilogue warps takes column chunk c = 2 st + h.  The step's
+        // 128 x 64 block is staged in TMA box layout (two 64 x 64 boxes,
+        // 128-byte swizzle) and, for tiles strictly above the diagonal, its
+        // 64 x 128 transpose as well; one thread TMA-stores both and, before
+        // the next step's writes, waits until the stores have read them.
+        const CUtensorMap* mo = (KIND == G_GRAM) ? &P.map_a : &P.map_b;
         const int m = g.M_;
-        const int rl = quarter * 32 + lane;   // staging row of this thread
-        for (int h = 0; h < 2; ++h) {
-          for (int c = 2 * ch; c < 2 * ch + 2; ++c) {   // this warp's 64 columns of the half
-            uint32_t v[32];
-            tmem_ld32(tbase + (uint32_t)(h * 128 + c * 32), v);
-            float out[32];
-            if (KIND == G_GRAM) {
+        const int rl = quarter * 32 + lane;   // this thread's row of the tile
+        unsigned char* sd = side;             // direct: boxes of rows 0-63 and 64-127
+        unsigned char* stp = side + 2 * kBox;  // transposed: boxes of columns row0.. and row0 + 64..
+        const int jj = rl & 63;               // this thread's column within a transposed box
 #pragma unroll
-              for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
-            } else {
-              float av[32];
-              const int cb = g.col0 + h * 128 + c * 32;
-              if (r < m && cb < m) load_row32(P.a + (int64_t)r * ld + cb, m - cb, av);
-              else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) av[i] = 0.0f;
-              }
-              // a on the diagonal (row r, column cb + i): the a X term of the update
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]) + (cb + i == r ? args.ca : 0.0f);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int w = c * 16 + i;
-              stage_out[rl * 64 + (w ^ (rl & 31))] = pack_bf16(out[2 * i], out[2 * i + 1]);
-            }
-          }
-          if (h == 1) {   // every TMEM read of this accumulator is done
+        for (int st = 0; st < 4; ++st) {
+          const int c = 2 * st + ch;
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          if (st == 3) {   // every TMEM read of this accumulator is done
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -813,42 +805,68 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
               else mbar_arrive(tempty0 + 8 * acc);
             }
           }
-          named_barrier_epilogue();
-          const int cbase = g.col0 + h * 128;
-          // rows: warp ew stores rows 16 ew .. 16 ew + 15, two words per lane
-          for (int rr = ew * 16; rr < ew * 16 + 16; ++rr) {
-            const int orow = g.row0 + rr;
-            if (orow >= m) break;
+          float out[32];
+          if (KIND == G_GRAM) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int w = lane + 32 * k;
-              const int col = cbase + 2 * w;
-              const uint32_t val = stage_out[rr * 64 + (w ^ (rr & 31))];
-              __nv_bfloat16* dst = outp + (int64_t)orow * ld + col;
-              if (col + 1 < m) *reinterpret_cast<uint32_t*>(dst) = val;
-              else if (col < m) *dst = __ushort_as_bfloat16((unsigned short)(val & 0xFFFFu));
+            for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
+          } else {
+            float av[32];
+            const int cb = g.col0 + c * 32;
+            if (r < m && cb < m && cb + 32 > m) {
+              load_row32(P.a + (int64_t)r * P.ab_ld + cb, m - cb, av);   // the matrix edge
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 u = apre[st][i];
+                av[8 * i + 0] = bf16_lo(u.x); av[8 * i + 1] = bf16_hi(u.x);
+                av[8 * i + 2] = bf16_lo(u.y); av[8 * i + 3] = bf16_hi(u.y);
+                av[8 * i + 4] = bf16_lo(u.z); av[8 * i + 5] = bf16_hi(u.z);
+                av[8 * i + 6] = bf16_lo(u.w); av[8 * i + 7] = bf16_hi(u.w);
+              }
             }
+            // a on the diagonal (row r, column cb + i): the a X term of the update
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]) + (cb + i == r ? args.ca : 0.0f);
+          }
+          // the staging is free once the previous step's stores have read it
+          if (ew == 0 && lane == 0 && (st > 0 || ti > 0)) bulk_wait_read_all();
+          __syncwarp();
+          named_barrier_epilogue();
+          unsigned char* drow = sd + (rl >> 6) * kBox + (rl & 63) * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = ch * 4 + t;
+            *reinterpret_cast<uint4*>(drow + ((q ^ (rl & 7)) << 4)) =
+                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
+                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
           }
           if (g.mirror) {
-            // transposed: word w holds columns 2w, 2w+1 of row rr; they go to
-            // output rows cbase + 2w (+1), column row0 + rr
-            for (int w = ew * 8; w < ew * 8 + 8; ++w) {
-              const int orow = cbase + 2 * w;
-              if (orow >= m) break;
+            // element (row rl, column 32 ch + e) of the block is element
+            // (32 ch + e, rl) of the transpose
+            unsigned char* tb = stp + (rl >> 6) * kBox + ((jj & 7) << 1);
 #pragma unroll
-              for (int p = 0; p < 4; ++p) {
-                const int rr = p * 32 + lane;
-                const int ocol = g.row0 + rr;
-                const uint32_t val = stage_out[rr * 64 + (w ^ (rr & 31))];
-                if (ocol < m) {
-                  outp[(int64_t)orow * ld + ocol] = __ushort_as_bfloat16((unsigned short)(val & 0xFFFFu));
-                  if (orow + 1 < m)
-                    outp[(int64_t)(orow + 1) * ld + ocol] = __ushort_as_bfloat16((unsigned short)(val >> 16));
+            for (int e = 0; e < 32; ++e) {
+              const int i = 32 * ch + e;
+              *reinterpret_cast<__nv_bfloat16*>(tb + i * 128 + ((((jj >> 3) ^ (i & 7))) << 4)) =
+                  __float2bfloat16_rn(out[e]);
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier_epilogue();
+          if (ew == 0 && lane == 0) {
+            const int cs = g.col0 + 64 * st;
+            if (cs < m) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                if (g.row0 + 64 * b < m) {
+                  tma_store_2d(mo, smem_u32(sd + b * kBox), cs, g.row0 + 64 * b);
+                  if (g.mirror) tma_store_2d(mo, smem_u32(stp + b * kBox), g.row0 + 64 * b, cs);
                 }
               }
             }
+            bulk_commit();
           }
-          named_barrier_epilogue();   // staging is free for the next half
         }
       }
     }
@@ -861,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   // ---- teardown: every accumulator read is done, every TMA store has
   // completed and, in a pair, the peer no longer touches this CTA's barriers
   // or shared memory ----
-  if (KIND >= G_UPDATE && warp >= 2 && ((warp - 2) & 3) <= 1 && lane == 0) bulk_wait_all();
+  if (warp >= 2 && ((warp - 2) & 3) <= 1 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncwarp();   // lanes that skipped the single-thread roles rejoin before the aligned barrier
   if (CG == 2) cluster_sync_all();
