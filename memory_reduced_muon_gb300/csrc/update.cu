@@ -6,16 +6,20 @@
 // "Grouped QKV And Sharding"), and the MXFP8 carrier of section "Wave18B
 // MXFP8 Carrier Probe".
 //
-// Layout on the GPU: a CTA of 256 threads owns a contiguous chunk of
-// quantization blocks (the grid is a whole number of waves of resident CTAs).
-// A half-warp (16 lanes) handles one 256-element block; a lane owns 16
-// consecutive elements, so one 16-byte load brings its q8 codes and two
-// (bf16/fp16) or four (fp32) 16-byte loads its gradient.  Each half-warp
-// keeps two blocks in flight.  absmax and the block sum of squares are
-// shuffle reductions inside the half-warp.  The codec arithmetic uses the
-// round-to-nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn,
-// __float2int_rn), which the compiler never contracts into FMAs, in exactly
-// the order of the page's steps.
+// Layout on the GPU: a CTA owns a contiguous chunk of quantization blocks
+// (the grid is a whole number of waves of resident CTAs).  Its producer warp
+// streams the chunk through a ring of four shared-memory stages of 16 blocks:
+// one bulk asynchronous copy per tensor segment for the codes and one for the
+// gradient, and a 4-byte asynchronous copy per block for the old absmax, all
+// counted on the stage's mbarrier.  Its eight compute warps take one block
+// per half-warp and stage: a lane reads its 16 consecutive elements (16 bytes
+// of codes, 32 or 64 bytes of gradient) from shared memory, hands the stage
+// back, and computes; results leave by coalesced 16-byte stores.  absmax and
+// the block sum of squares are shuffle reductions inside the half-warp.  The
+// codec arithmetic uses the round-to-nearest intrinsics (__fmul_rn, __fadd_rn,
+// __fdiv_rn), which the compiler never contracts into FMAs, in exactly the
+// order of the page's steps.  Every wait on a stage is bounded: on expiry it
+// records QMUON_ERR_TIMEOUT in the workspace header and the CTA winds down.
 //
 // Group sums without a second pass over HBM: every CTA writes its block sums
 // into shared memory, folds them per norm group into one partial per
@@ -241,13 +245,16 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   }
   // (7) requantise: sc = 127 / amax, q = rint(m * sc).  No clamp is needed:
   // |m| <= amax, so |m * sc| <= 127 (1 + 2^-24) and rounds to at most 127;
-  // amax == 0 gives sc = 0 and q = 0; a NaN product converts to 0.
+  // amax == 0 gives sc = 0 and q = 0.  The rounding to an integer (ties to
+  // even) is one fp32 addition of 1.5 * 2^23: the sum lies in [2^23, 2^24),
+  // where the spacing is 1, and its low byte is q in two's complement; a NaN
+  // product gives a zero low byte, i.e. q = 0.
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
+  auto code = [sc](float x) { return (int)__float_as_uint(__fadd_rn(__fmul_rn(x, sc), 12582912.0f)); };
   uint32_t qo[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w)
-    qo[w] = pack_codes<QK>(__float2int_rn(__fmul_rn(m[4 * w], sc)), __float2int_rn(__fmul_rn(m[4 * w + 1], sc)),
-                           __float2int_rn(__fmul_rn(m[4 * w + 2], sc)), __float2int_rn(__fmul_rn(m[4 * w + 3], sc)));
+    qo[w] = pack_codes<QK>(code(m[4 * w]), code(m[4 * w + 1]), code(m[4 * w + 2]), code(m[4 * w + 3]));
   uint8_t* q8p = static_cast<uint8_t*>(T.q8) + e0;
   if (FULL) {
     __stcs(reinterpret_cast<uint4*>(q8p), make_uint4(qo[0], qo[1], qo[2], qo[3]));
@@ -303,66 +310,263 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   return ss;
 }
 
+// ---------------------------------------------------------------------------
+// The input stream: a producer warp copies each CTA's blocks into a ring of
+// shared-memory stages (16 blocks per stage, one per half-warp) with bulk
+// asynchronous copies, four stages ahead of the compute warps.
+// ---------------------------------------------------------------------------
+constexpr int kStageBlocks = 16;                 // one block per half-warp of the compute warps
+constexpr int kUpdStages = 4;
+constexpr int kUpdWarps = kUpdThreads / 32;      // compute warps
+constexpr int kUpdThreadsAll = kUpdThreads + 32; // plus the producer warp
+constexpr long long kUpdWaitCycles = 4000000000LL;   // bounded waits: ~2 s at 2 GHz
+
+template <int DT>
+struct UpdStage {
+  static constexpr int kEsz = (DT == QMUON_FP32) ? 4 : 2;
+  static constexpr uint32_t kQBytes = kStageBlocks * kBlock;          // codes
+  static constexpr uint32_t kGBytes = kStageBlocks * kBlock * kEsz;   // gradient
+  static constexpr uint32_t kABytes = kStageBlocks * 4;               // old absmax
+  static constexpr uint32_t kBytes = kQBytes + kGBytes + kABytes;
+};
+
+template <int DT>
+constexpr size_t upd_smem_bytes() {
+  return (size_t)kUpdStages * UpdStage<DT>::kBytes + (size_t)kMaxChunk * (sizeof(float) + sizeof(int32_t)) +
+         2 * kUpdStages * sizeof(uint64_t);
+}
+
+__device__ __forceinline__ uint32_t upd_smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool upd_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false once the phase has not completed in ~2 s (or another
+// CTA already gave up), after recording QMUON_ERR_TIMEOUT in the header.
+__device__ __noinline__ bool upd_wait(uint32_t bar, uint32_t parity, WsHeader* h, unsigned where) {
+  if (upd_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (upd_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile unsigned*>(&h->error) != 0u) return false;
+    if (clock64() - t0 > kUpdWaitCycles) {
+      if (atomicCAS(&h->error, 0u, (unsigned)QMUON_ERR_TIMEOUT) == 0u) h->error_info = where;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void upd_bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void upd_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void upd_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// global -> shared bulk copy (16-byte aligned ends, size a multiple of 16)
+// counted on `bar` as transaction bytes
+__device__ __forceinline__ void upd_bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// 4-byte asynchronous copy, and an arrival on `bar` once this thread's
+// earlier asynchronous copies have landed (the barrier's count includes it)
+__device__ __forceinline__ void upd_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void upd_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 template <int QK, int DT, bool CARRIER>
-__global__ void __launch_bounds__(kUpdThreads, 3) update_kernel(UpdLaunch L) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* s_bsum = reinterpret_cast<float*>(smem_raw);
-  int32_t* s_bgrp = reinterpret_cast<int32_t*>(smem_raw + kMaxChunk * sizeof(float));
+__global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) {
+  using ST = UpdStage<DT>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* stage0 = smem_raw;   // kUpdStages x (codes | gradient | old absmax)
+  float* s_bsum = reinterpret_cast<float*>(smem_raw + kUpdStages * ST::kBytes);
+  int32_t* s_bgrp = reinterpret_cast<int32_t*>(s_bsum + kMaxChunk);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_bgrp + kMaxChunk);
+  const uint32_t full0 = upd_smem_u32(bars), empty0 = upd_smem_u32(bars + kUpdStages);
   __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int hw = tid >> 4, hl = tid & 15;
   const int64_t kb = (int64_t)blockIdx.x * L.chunk;
   const int64_t ke = (kb + L.chunk < L.nb_total) ? kb + L.chunk : L.nb_total;
+  const int n_stages = (int)((ke - kb + kStageBlocks - 1) / kStageBlocks);
   const bool reduce = L.layout.n_groups > 0;
-  const float beta = L.beta;
-  const float omb = __fsub_rn(1.0f, beta);
-
   const bool single = (L.tensors == nullptr);
-  // tensor holding this half-warp's first block (tensor_begin is ascending)
-  int t = 0;
-  if (!single) {
-    const int64_t k0 = kb + hw;
-    int lo = 0, hi = L.n_tensors - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(L.tensor_begin + mid) <= k0) lo = mid; else hi = mid - 1;
-    }
-    t = lo;
-  }
 
-  for (int64_t k = kb + hw; k < ke; k += 32) {
-    const int64_t k2 = k + 16;
-    const bool has2 = k2 < ke;
-    int t2 = t;
+  if (tid == 0) {
+    for (int s = 0; s < kUpdStages; ++s) {
+      upd_bar_init(full0 + 8 * s, 1 + kStageBlocks);   // the copying lane + one async-copy arrival per block lane
+      upd_bar_init(empty0 + 8 * s, kUpdWarps);          // every compute warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kUpdWarps) {
+    // ---- producer: stage i holds blocks kb + 16 i .. kb + 16 i + 15.  The
+    // tensor of the stage's first block is cached with its fields (block
+    // indices only grow) ----
+    int t = 0;
     if (!single) {
-      while (k >= __ldg(L.tensor_begin + t + 1)) ++t;
-      t2 = t;
-      if (has2) while (k2 >= __ldg(L.tensor_begin + t2 + 1)) ++t2;
+      int lo = 0, hi = L.n_tensors - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(L.tensor_begin + mid) <= kb) lo = mid; else hi = mid - 1;
+      }
+      t = lo;
     }
-    const UpdTensor T0 = single ? L.single : L.tensors[t];
-    const UpdTensor T1 = single ? L.single : L.tensors[t2];
-    LaneIn<DT> in0, in1;
-    const int64_t lb0 = k - T0.block_begin, lb1 = k2 - T1.block_begin;
-    const bool full0 = (lb0 + 1) * kBlock <= T0.numel;   // uniform across the half-warp
-    const bool full1 = (lb1 + 1) * kBlock <= T1.numel;
-    load_lane<QK, DT>(in0, T0, lb0, hl, full0);
-    if (has2) load_lane<QK, DT>(in1, T1, lb1, hl, full1);
-    int32_t g0 = 0, g1 = 0;
-    if (reduce && hl == 0 && L.layout.block_group) {
-      g0 = __ldg(L.layout.block_group + k);
-      if (has2) g1 = __ldg(L.layout.block_group + k2);
+    UpdTensor T = single ? L.single : L.tensors[t];
+    int64_t tend = single ? L.nb_total : __ldg(L.tensor_begin + t + 1);
+    bool ok = true;
+    int i = 0;
+    for (; i < n_stages; ++i) {
+      const int slot = i % kUpdStages;
+      // lane 0 waits for the slot, the warp follows its verdict
+      if (lane == 0 && i >= kUpdStages) ok = upd_wait(empty0 + 8 * slot, ((i / kUpdStages) - 1) & 1, L.header, 0x1100u);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      unsigned char* st = stage0 + slot * ST::kBytes;
+      const uint32_t fb = full0 + 8 * slot;
+      const int64_t k0 = kb + (int64_t)i * kStageBlocks;
+      const int64_t k1 = (k0 + kStageBlocks < ke) ? k0 + kStageBlocks : ke;
+      while (k0 >= tend) {   // never for a single tensor
+        ++t;
+        T = L.tensors[t];
+        tend = __ldg(L.tensor_begin + t + 1);
+      }
+      // lane j < 16: the old absmax of block k0 + j (4-byte asynchronous copy)
+      if (lane < kStageBlocks) {
+        const int64_t k = k0 + lane;
+        if (k < k1) {
+          const float* src;
+          if (k < tend) {
+            src = T.absmax + (k - T.block_begin);
+          } else {   // the stage crosses into a later tensor
+            int tt = t + 1;
+            while (k >= __ldg(L.tensor_begin + tt + 1)) ++tt;
+            src = L.tensors[tt].absmax + (k - __ldg(L.tensor_begin + tt));
+          }
+          upd_async4(upd_smem_u32(st + ST::kQBytes + ST::kGBytes + 4 * lane), src);
+        }
+        upd_async_arrive(fb);
+      }
+      // lane 0: codes and gradient of the whole blocks, one bulk copy each per
+      // tensor segment (a tensor's partial last block is read by its compute
+      // lanes directly); the byte count is armed before the copies start
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int pass = 0; pass < 2; ++pass) {
+          if (pass == 1) upd_arrive_expect_tx(fb, bytes);
+          int tt = t;
+          UpdTensor TT = T;
+          int64_t te = tend;
+          for (int64_t a = k0; a < k1;) {
+            if (a >= te) {
+              ++tt;
+              TT = L.tensors[tt];
+              te = __ldg(L.tensor_begin + tt + 1);
+              continue;
+            }
+            const int64_t b = (te < k1) ? te : k1;
+            const int64_t lb = a - TT.block_begin;
+            int64_t nfull = b - a;
+            if ((lb + nfull) * kBlock > TT.numel) nfull = TT.numel / kBlock - lb;   // drop a partial last block
+            if (nfull > 0) {
+              if (pass == 0) {
+                bytes += (uint32_t)(nfull * kBlock * (1 + ST::kEsz));
+              } else {
+                const int j = (int)(a - k0);
+                upd_bulk_load(upd_smem_u32(st + j * kBlock), static_cast<const uint8_t*>(TT.q8) + lb * kBlock,
+                              (uint32_t)(nfull * kBlock), fb);
+                upd_bulk_load(upd_smem_u32(st + ST::kQBytes + j * kBlock * ST::kEsz),
+                              static_cast<const uint8_t*>(TT.grad) + lb * kBlock * ST::kEsz,
+                              (uint32_t)(nfull * kBlock * ST::kEsz), fb);
+              }
+            }
+            a = b;
+          }
+        }
+      }
+      __syncwarp();
     }
-    const float ss0 = full0 ? compute_lane<QK, DT, CARRIER, true>(in0, T0, lb0, hl, beta, omb)
-                            : compute_lane<QK, DT, CARRIER, false>(in0, T0, lb0, hl, beta, omb);
-    if (reduce && hl == 0) { s_bsum[k - kb] = ss0; s_bgrp[k - kb] = g0; }
-    if (has2) {
-      const float ss1 = full1 ? compute_lane<QK, DT, CARRIER, true>(in1, T1, lb1, hl, beta, omb)
-                              : compute_lane<QK, DT, CARRIER, false>(in1, T1, lb1, hl, beta, omb);
-      if (reduce && hl == 0) { s_bsum[k2 - kb] = ss1; s_bgrp[k2 - kb] = g1; }
+    // every copy issued lands before the CTA moves on
+    if (lane == 0)
+      for (int k = (i > kUpdStages ? i - kUpdStages : 0); k < i; ++k)
+        upd_wait(full0 + 8 * (k % kUpdStages), (k / kUpdStages) & 1, L.header, 0x1200u);
+    __syncwarp();
+  } else {
+    // ---- compute warps: half-warp hw takes block kb + 16 i + hw of stage i ----
+    const int hw = tid >> 4, hl = tid & 15;
+    const float beta = L.beta;
+    const float omb = __fsub_rn(1.0f, beta);
+    int t = 0;
+    if (!single) {
+      const int64_t k0 = kb + hw;
+      int lo = 0, hi = L.n_tensors - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(L.tensor_begin + mid) <= k0) lo = mid; else hi = mid - 1;
+      }
+      t = lo;
     }
-    t = t2;
+    // this half-warp's current tensor, cached with its fields
+    UpdTensor T = single ? L.single : L.tensors[t];
+    int64_t tend = single ? L.nb_total : __ldg(L.tensor_begin + t + 1);
+    for (int i = 0; i < n_stages; ++i) {
+      const int slot = i % kUpdStages;
+      const int64_t k = kb + (int64_t)i * kStageBlocks + hw;
+      const bool has = k < ke;
+      // the whole warp goes on or stops together (half-warp shuffles follow)
+      const bool ok = __all_sync(0xffffffffu, upd_wait(full0 + 8 * slot, (i / kUpdStages) & 1, L.header, 0x1300u));
+      const unsigned char* st = stage0 + slot * ST::kBytes;
+      LaneIn<DT> in;
+      int64_t lb = 0;
+      bool full = true;
+      if (has && ok) {
+        while (k >= tend) {
+          ++t;
+          T = L.tensors[t];
+          tend = __ldg(L.tensor_begin + t + 1);
+        }
+        lb = k - T.block_begin;
+        full = (lb + 1) * kBlock <= T.numel;   // uniform across the half-warp
+        if (full) {
+          in.q = *reinterpret_cast<const uint4*>(st + hw * kBlock + hl * 16);
+          const uint4* gs = reinterpret_cast<const uint4*>(st + ST::kQBytes + hw * kBlock * ST::kEsz + hl * 16 * ST::kEsz);
+#pragma unroll
+          for (int v = 0; v < Grad<DT>::kVecs; ++v) in.g[v] = gs[v];
+          in.amax_old = *reinterpret_cast<const float*>(st + ST::kQBytes + ST::kGBytes + 4 * hw);
+          in.valid = 16;
+        } else {
+          load_lane<QK, DT>(in, T, lb, hl, false);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) upd_arrive(empty0 + 8 * slot);   // this warp is done reading the stage
+      if (!ok) break;
+      if (has) {
+        int32_t g = 0;
+        if (reduce && hl == 0 && L.layout.block_group) g = __ldg(L.layout.block_group + k);
+        const float ss = full ? compute_lane<QK, DT, CARRIER, true>(in, T, lb, hl, beta, omb)
+                              : compute_lane<QK, DT, CARRIER, false>(in, T, lb, hl, beta, omb);
+        if (reduce && hl == 0) { s_bsum[k - kb] = ss; s_bgrp[k - kb] = g; }
+      }
+    }
   }
   if (!reduce) return;
 
@@ -372,7 +576,7 @@ __global__ void __launch_bounds__(kUpdThreads, 3) update_kernel(UpdLaunch L) {
   const bool one_group = (L.layout.block_group == nullptr);
   const int s0 = one_group ? (int)blockIdx.x : __ldg(L.layout.cta_slot_begin + blockIdx.x);
   const int s1 = one_group ? (int)blockIdx.x + 1 : __ldg(L.layout.cta_slot_begin + blockIdx.x + 1);
-  for (int s = s0 + warp; s < s1; s += kUpdThreads / 32) {
+  for (int s = s0 + warp; s < s1 && warp < kUpdWarps; s += kUpdWarps) {
     const int g = one_group ? 0 : __ldg(L.layout.slot_group + s);
     float sum = 0.0f, comp = 0.0f;   // compensated fp32 sum per lane
     for (int i = lane; i < nloc; i += 32) {
@@ -394,7 +598,7 @@ __global__ void __launch_bounds__(kUpdThreads, 3) update_kernel(UpdLaunch L) {
 
   // ---- the last CTA: per-group totals in slot order ----
   __threadfence();
-  for (int g = warp; g < L.layout.n_groups; g += kUpdThreads / 32) {
+  for (int g = warp; g < L.layout.n_groups && warp < kUpdWarps; g += kUpdWarps) {
     const int j0 = one_group ? 0 : __ldg(L.layout.grp_ptr + g);
     const int j1 = one_group ? (int)gridDim.x : __ldg(L.layout.grp_ptr + g + 1);
     double acc = 0.0;
@@ -449,15 +653,20 @@ void* pick_kernel(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
   return nullptr;
 }
 
-constexpr size_t kUpdSmem = kMaxChunk * (sizeof(float) + sizeof(int32_t));
+size_t upd_smem(qmuon_dtype dt) { return dt == QMUON_FP32 ? upd_smem_bytes<QMUON_FP32>() : upd_smem_bytes<QMUON_BF16>(); }
+
+// Dynamic shared memory above the 48 KB default needs an opt-in per kernel.
+cudaError_t prepare_kernel(void* k, qmuon_dtype dt) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem(dt));
+}
 
 }  // namespace
 
 int update_blocks_per_sm(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
   void* k = pick_kernel(q8, dt, carrier);
-  if (!k) return 0;
+  if (!k || prepare_kernel(k, dt) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kUpdThreads, kUpdSmem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kUpdThreadsAll, upd_smem(dt)) != cudaSuccess) return 0;
   return n;
 }
 
@@ -465,9 +674,11 @@ cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, 
                           cudaStream_t stream) {
   void* k = pick_kernel(q8, dt, carrier);
   if (!k) return cudaErrorInvalidValue;
+  const cudaError_t e = prepare_kernel(k, dt);
+  if (e != cudaSuccess) return e;
   UpdLaunch arg = L;
   void* args[] = {&arg};
-  return cudaLaunchKernel(k, dim3(L.grid), dim3(kUpdThreads), args, kUpdSmem, stream);
+  return cudaLaunchKernel(k, dim3(L.grid), dim3(kUpdThreadsAll), args, upd_smem(dt), stream);
 }
 
 cudaError_t launch_scale_groups(const UpdLaunch& L, qmuon_dtype dt, const float* inv,
