@@ -26,6 +26,15 @@ silent:
 * the per-block sum of squares is taken over the fp32 ``m`` (step 9) and
   accumulated in fp64; a group's inverse norm is ``1 / (sqrt(S) + 1e-7)``
   evaluated in fp64 and rounded once to fp32.
+
+Stochastic requantisation (optional; the page's section "Open Issues" says
+only that it is not implemented yet): with ``x = m * sc`` as above and a
+uniform ``u`` in [0, 1) per element (``oracle.rng``: Philox4x32-10 keyed by
+the seed, counter from the element, tensor and step), ``q = clamp(floor(x +
+u), -127, 127)``, a NaN product giving 0.  ``x + u`` is evaluated in fp64,
+where it is exact enough for the floor: the exact sum lies on the grid of
+min(ulp(x), 2^-24) and never falls within fp64's rounding error of an
+integer it does not reach.
 """
 
 from __future__ import annotations
@@ -34,6 +43,8 @@ from dataclasses import dataclass
 from typing import Optional, Sequence
 
 import numpy as np
+
+from . import rng
 
 QBLOCK = 256
 EPS = 1e-7
@@ -146,8 +157,18 @@ def dequantize(q8: np.ndarray, absmax: np.ndarray, q8_kind: str = "int8") -> np.
     return old.reshape(-1)[:numel]
 
 
+@dataclass(frozen=True)
+class StochasticRounding:
+    """Stochastic requantisation of one tensor: the generator's key and the
+    step and tensor words of its counter."""
+    seed: int
+    step: int
+    tensor_index: int = 0
+
+
 def momentum_update(q8: np.ndarray, absmax: np.ndarray, grad: np.ndarray, beta: float,
-                    *, grad_dtype: str = "bf16", q8_kind: str = "int8") -> UpdateResult:
+                    *, grad_dtype: str = "bf16", q8_kind: str = "int8",
+                    rounding: Optional[StochasticRounding] = None) -> UpdateResult:
     """One quantized momentum update of a flat tensor.
 
     Follows "Quantized Muon Momentum", section "Algorithm": load the codes and
@@ -156,6 +177,7 @@ def momentum_update(q8: np.ndarray, absmax: np.ndarray, grad: np.ndarray, beta: 
     gradient (5), take the new block absmax (6), requantise (7), store codes
     and absmax (8), and the block sum of squares (9).  The last block of a
     tensor whose size is not a multiple of 256 holds only its real elements.
+    With ``rounding`` set, step 7 rounds stochastically (module docstring).
     """
     q8 = np.asarray(q8).reshape(-1)
     numel = q8.size
@@ -187,7 +209,12 @@ def momentum_update(q8: np.ndarray, absmax: np.ndarray, grad: np.ndarray, beta: 
     with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
         sc = np.where(amax == 0, F32(0.0), F32(127.0) / np.where(amax == 0, F32(1.0), amax)).astype(F32)
         x = (m * sc[:, None]).astype(F32)
-        r = np.rint(x)
+        if rounding is None:
+            r = np.rint(x)
+        else:
+            u = _pad_blocks(rng.rounding_uniforms(numel, rounding.seed, rounding.step, rounding.tensor_index),
+                            numel)
+            r = np.floor(x.astype(np.float64) + u)
         r = np.where(np.isnan(r), 0.0, r)
         qn = np.clip(r, -127, 127).astype(np.int32)
     qn = np.where(amax[:, None] == 0, 0, qn)
@@ -298,15 +325,18 @@ def normalize_inplace(grad: np.ndarray, groups: np.ndarray, inv: np.ndarray,
 
 
 def multi_update(q8s, absmaxes, grads, beta, *, grad_dtype="bf16", q8_kind="int8",
-                 segments=None, n_groups=None):
+                 segments=None, n_groups=None, sr_seed: Optional[int] = None, sr_step: int = 0):
     """Update a list of tensors and reduce their norm groups.
 
     The multi-tensor form of "What Exists" (one call over many tensors, each
     gradient overwritten with the new momentum) with the grouped reduction of
-    "Grouped QKV And Sharding".  Returns ``(results, S, inv, groups)``.
+    "Grouped QKV And Sharding".  With ``sr_seed`` set, requantisation is
+    stochastic, tensor i drawing with tensor word i.  Returns
+    ``(results, S, inv, groups)``.
     """
-    results = [momentum_update(q, a, g, beta, grad_dtype=grad_dtype, q8_kind=q8_kind)
-               for q, a, g in zip(q8s, absmaxes, grads)]
+    results = [momentum_update(q, a, g, beta, grad_dtype=grad_dtype, q8_kind=q8_kind,
+                               rounding=None if sr_seed is None else StochasticRounding(sr_seed, sr_step, i))
+               for i, (q, a, g) in enumerate(zip(q8s, absmaxes, grads))]
     numels = [np.asarray(q).size for q in q8s]
     if n_groups is None:
         n_groups = len(numels) if segments is None else 1 + max(s.group_id for s in segments)
