@@ -395,6 +395,15 @@ def run_gpu(args, world, rank, local):
     upd_ms = u0.elapsed_time(u1) / reps
     upd_bytes = UPDATE_BYTES_PER_ELEM * n_params
     upd_gbs = upd_bytes / (upd_ms / 1e3) / 1e9
+    # the same update with stochastic requantisation (Philox4x32-10 per element)
+    q.qmuon_update_multi_normalize_groups_sr(plan_u, w.beta, 2, 1234, 1, None, inv_u, ws_u, stream=stream)
+    torch.cuda.synchronize()
+    u0.record(stream)
+    for k in range(reps):
+        q.qmuon_update_multi_normalize_groups_sr(plan_u, w.beta, 2, 1234, 2 + k, None, inv_u, ws_u, stream=stream)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    upd_sr_ms = u0.elapsed_time(u1) / reps
 
     def ns_problems(full):
         tr, tc = (1, 1) if full else w.tile
@@ -451,6 +460,7 @@ def run_gpu(args, world, rank, local):
     # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
     return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
+                upd_sr_ms=upd_sr_ms,
                 ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=4 * ngr, n_full=n_full,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
@@ -518,6 +528,10 @@ def main():
             "data": "synthetic (seeded gradients, zero initial state, N(0,0.02^2) weights)", "config": config,
             "full_steps_timed": r["n_full"], "per_step": r["per_step"],
             "update_gbs": r["upd_gbs"], "ns_tflops": ns_tflops,
+            "update_stochastic_rounding": ({"gbs": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9,
+                                            "ms_per_launch": r["upd_sr_ms"],
+                                            "frac": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9 / float(peaks["hbm_gbs"])}
+                                           if r.get("upd_sr_ms") else None),
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
             "e2e": ({"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
                      "d2h_bytes_per_step": r["d2h"]} if r["e2e_value"] is not None else None),

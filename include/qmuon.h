@@ -132,6 +132,28 @@ QMUON_API qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* pla
                                                  float* group_inv_norm, void* ws,
                                                  size_t ws_bytes, void* stream);
 
+/* qmuon_update_multi_normalize_groups with stochastic requantisation (the
+ * page, section "Known Limitations", lists stochastic rounding as not yet
+ * implemented; this is the reading taken): with x = fl(m * (127/absmax)),
+ *   q = clamp(floor(x + u), -127, 127)   (a NaN product gives 0)
+ * where u = (w >> 8) * 2^-24 and w is word (e mod 4) of Philox4x32-10
+ * (Salmon et al., SC'11; 10 rounds) with
+ *   key     = (seed mod 2^32, seed >> 32)
+ *   counter = (e/4 mod 2^32, e/2^34, tensor index in the plan, step mod 2^32)
+ * for element e (flat index) of the tensor.  E[q] = x up to 2^-24, so the
+ * dequantised state is unbiased.  Everything else, arguments and errors
+ * included, is as in qmuon_update_multi_normalize_groups. */
+QMUON_API qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan* plan, float beta,
+                                                    int32_t normalize_mode, uint64_t seed, int64_t step,
+                                                    float* group_sumsq, float* group_inv_norm, void* ws,
+                                                    size_t ws_bytes, void* stream);
+
+/* Make qmuon_step requantise stochastically (enable = 1; 0 restores nearest
+ * rounding), as qmuon_update_multi_normalize_groups_sr does with this seed
+ * and step = the step's t.  Host-only: changes no device state.
+ * QMUON_ERR_INVALID_ARGUMENT on a NULL plan or enable not 0/1. */
+QMUON_API qmuon_status qmuon_plan_set_stochastic_rounding(qmuon_plan* plan, int32_t enable, uint64_t seed);
+
 /* Workspace bytes of qmuon_update_mxfp8_carrier for a rows x cols tensor. */
 QMUON_API size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols);
 

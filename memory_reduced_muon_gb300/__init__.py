@@ -84,6 +84,8 @@ def lib() -> C.CDLL:
         "qmuon_plan_info": (i32, [vp, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]),
         "qmuon_workspace_size": (sz, [vp, i32]),
         "qmuon_update_multi_normalize_groups": (i32, [vp, f32, i32, vp, vp, vp, sz, vp]),
+        "qmuon_update_multi_normalize_groups_sr": (i32, [vp, f32, i32, C.c_uint64, i64, vp, vp, vp, sz, vp]),
+        "qmuon_plan_set_stochastic_rounding": (i32, [vp, i32, C.c_uint64]),
         "qmuon_carrier_workspace_size": (sz, [i64, i64]),
         "qmuon_update_mxfp8_carrier": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp, vp, sz, vp]),
         "qmuon_ns_workspace_size": (sz, [C.POINTER(qmuon_ns_problem), i32]),
@@ -109,7 +111,8 @@ def exported_symbols() -> list:
             "qmuon_update_multi_normalize_groups", "qmuon_carrier_workspace_size",
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
-            "qmuon_update_normalize_noalloc", "qmuon_step_prepare"]
+            "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
+            "qmuon_plan_set_stochastic_rounding"]
 
 
 # --------------------------------------------------------------------------
@@ -222,6 +225,22 @@ def qmuon_update_multi_normalize_groups(plan: Plan, beta: float, normalize_mode:
         plan.handle, float(beta), int(normalize_mode), _ptr(group_sumsq), _ptr(group_inv_norm), _ptr(ws),
         _nbytes(ws) if ws_bytes is None else int(ws_bytes), _stream(stream))
     _check(st, "qmuon_update_multi_normalize_groups")
+
+
+def qmuon_update_multi_normalize_groups_sr(plan: Plan, beta: float, normalize_mode: int, seed: int, step: int,
+                                           group_sumsq, group_inv_norm, ws, ws_bytes: Optional[int] = None,
+                                           stream=None):
+    st = lib().qmuon_update_multi_normalize_groups_sr(
+        plan.handle, float(beta), int(normalize_mode), int(seed) & 0xFFFFFFFFFFFFFFFF, int(step),
+        _ptr(group_sumsq), _ptr(group_inv_norm), _ptr(ws), _nbytes(ws) if ws_bytes is None else int(ws_bytes),
+        _stream(stream))
+    _check(st, "qmuon_update_multi_normalize_groups_sr")
+
+
+def qmuon_plan_set_stochastic_rounding(plan: Plan, enable: bool, seed: int = 0):
+    _check(lib().qmuon_plan_set_stochastic_rounding(plan.handle, 1 if enable else 0,
+                                                    int(seed) & 0xFFFFFFFFFFFFFFFF),
+           "qmuon_plan_set_stochastic_rounding")
 
 
 def qmuon_carrier_workspace_size(rows: int, cols: int) -> int:

@@ -108,6 +108,8 @@ struct qmuon_plan {
   int64_t* d_tensor_begin = nullptr;
   ns::StepTables* ns_full = nullptr;  // Newton-Schulz problem sets of qmuon_step
   ns::StepTables* ns_block = nullptr;
+  bool sr = false;                    // qmuon_step requantises stochastically (counter step = t)
+  uint64_t sr_seed = 0;
 };
 
 namespace {
@@ -254,6 +256,7 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
     ut[i].scale = nullptr;
     ut[i].numel = tensors[i].rows * tensors[i].cols;
     ut[i].block_begin = begin[i];
+    ut[i].index = i;
   }
   std::vector<unsigned char> blob;
   auto put = [&blob](const void* src, size_t bytes) {
@@ -384,10 +387,18 @@ extern "C" size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind whi
   return b;
 }
 
-extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* plan, float beta,
-                                                            int32_t normalize_mode,
-                                                            float* group_sumsq, float* group_inv_norm,
-                                                            void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+void set_sr(UpdLaunch& L, bool on, uint64_t seed, int64_t step) {
+  L.sr = on ? 1 : 0;
+  L.sr_key0 = (uint32_t)seed;
+  L.sr_key1 = (uint32_t)(seed >> 32);
+  L.sr_step = (uint32_t)step;
+}
+
+qmuon_status update_groups(const qmuon_plan* plan, float beta, int32_t normalize_mode, float* group_sumsq,
+                           float* group_inv_norm, void* ws, size_t ws_bytes, void* stream, bool sr,
+                           uint64_t seed, int64_t step) {
   if (!plan || !ws) return QMUON_ERR_INVALID_ARGUMENT;
   if (normalize_mode < 0 || normalize_mode > 2) return QMUON_ERR_INVALID_ARGUMENT;
   if (normalize_mode == 2 && !group_inv_norm) return QMUON_ERR_INVALID_ARGUMENT;
@@ -402,10 +413,35 @@ extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* pl
   const bool reduce = group_sumsq || inv;
   UpdLaunch L = make_launch(plan, 0, beta, w, group_sumsq, inv);
   if (!reduce) L.layout.n_groups = 0;
+  set_sr(L, sr, seed, step);
   cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
   if (e == cudaSuccess && normalize_mode == 1) e = launch_scale_groups(L, plan->dt, inv, s);
   return cuda_status(e, "qmuon_update_multi_normalize_groups (launch)");
+}
+
+}  // namespace
+
+extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* plan, float beta,
+                                                            int32_t normalize_mode,
+                                                            float* group_sumsq, float* group_inv_norm,
+                                                            void* ws, size_t ws_bytes, void* stream) {
+  return update_groups(plan, beta, normalize_mode, group_sumsq, group_inv_norm, ws, ws_bytes, stream, false, 0, 0);
+}
+
+extern "C" qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan* plan, float beta,
+                                                               int32_t normalize_mode, uint64_t seed, int64_t step,
+                                                               float* group_sumsq, float* group_inv_norm,
+                                                               void* ws, size_t ws_bytes, void* stream) {
+  return update_groups(plan, beta, normalize_mode, group_sumsq, group_inv_norm, ws, ws_bytes, stream, true, seed,
+                       step);
+}
+
+extern "C" qmuon_status qmuon_plan_set_stochastic_rounding(qmuon_plan* plan, int32_t enable, uint64_t seed) {
+  if (!plan || (enable != 0 && enable != 1)) return QMUON_ERR_INVALID_ARGUMENT;
+  plan->sr = enable != 0;
+  plan->sr_seed = seed;
+  return QMUON_OK;
 }
 
 extern "C" size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols) {
@@ -517,6 +553,7 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
                                                  full ? 1 : plan->tile_c, weights, w.inv, w.ns, w.ns_bytes);
   if (ts != QMUON_OK) return ts;
   UpdLaunch L = make_launch(plan, full ? 1 : 2, beta, w, group_sumsq ? group_sumsq : w.sumsq, w.inv);
+  set_sr(L, plan->sr, plan->sr_seed, t);
   cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
   if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);

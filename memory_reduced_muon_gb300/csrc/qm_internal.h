@@ -35,6 +35,7 @@ struct UpdTensor {
   uint8_t* scale;       // carrier only
   int64_t numel;
   int64_t block_begin;  // global index of the tensor's first quantization block
+  int32_t index;        // the tensor's index in its plan (stochastic rounding's counter)
 };
 
 // Group layout of one launch: which norm group every block feeds, how the
@@ -65,6 +66,9 @@ struct UpdLaunch {
   WsHeader* header;           // workspace header
   float* group_sumsq;         // D or null
   float* group_inv;           // D or null
+  // stochastic requantisation: Philox4x32-10 key (seed) and the step word of its counter
+  int32_t sr;
+  uint32_t sr_key0, sr_key1, sr_step;
 };
 
 // Record the detail of a failure for qmuon_last_error() (api.cu); returns

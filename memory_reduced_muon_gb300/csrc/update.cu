@@ -145,6 +145,23 @@ __device__ __forceinline__ float pow2_from_e8m0(int byte) {
   return __uint_as_float(0x00400000u);  // 2^-127 (subnormal, exact)
 }
 
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): ten rounds of the 4 x 32-bit bijection; a round
+// multiplies c0 and c2 by M0 = 0xD2511F53 and M1 = 0xCD9E8D57 and mixes the
+// halves of the products with c1, c3 and the key, which is bumped by the Weyl
+// constants 0x9E3779B9, 0xBB67AE85 between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   unsigned short r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -212,9 +229,9 @@ __device__ __forceinline__ void load_lane(LaneIn<DT>& in, const UpdTensor& T, in
 // only the 16 lanes of its own half.  FULL: the whole block lies inside the
 // tensor (every lane has 16 elements); the tail block of a tensor takes the
 // masked path, chosen by the whole half-warp together.
-template <int QK, int DT, bool CARRIER, bool FULL>
+template <int QK, int DT, bool CARRIER, bool FULL, bool SR>
 __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTensor& T, int64_t lb,
-                                              int hl, float beta, float omb) {
+                                              int hl, float beta, float omb, const UpdLaunch& L) {
   const unsigned hmask = 0xFFFFu << (threadIdx.x & 16u);
   const int64_t e0 = lb * kBlock + hl * 16;
   const uint32_t* qw = reinterpret_cast<const uint32_t*>(&in.q);
@@ -250,11 +267,34 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   // where the spacing is 1, and its low byte is q in two's complement; a NaN
   // product gives a zero low byte, i.e. q = 0.
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
-  auto code = [sc](float x) { return (int)__float_as_uint(__fadd_rn(__fmul_rn(x, sc), 12582912.0f)); };
   uint32_t qo[4];
+  if constexpr (!SR) {
+    auto code = [sc](float x) { return (int)__float_as_uint(__fadd_rn(__fmul_rn(x, sc), 12582912.0f)); };
 #pragma unroll
-  for (int w = 0; w < 4; ++w)
-    qo[w] = pack_codes<QK>(code(m[4 * w]), code(m[4 * w + 1]), code(m[4 * w + 2]), code(m[4 * w + 3]));
+    for (int w = 0; w < 4; ++w)
+      qo[w] = pack_codes<QK>(code(m[4 * w]), code(m[4 * w + 1]), code(m[4 * w + 2]), code(m[4 * w + 3]));
+  } else {
+    // stochastic: q = clamp(floor(x + u), -127, 127) with x = m * sc and u the
+    // top 24 bits of the element's Philox word over 2^24.  x + u rounded
+    // toward -inf has the floor of the exact sum (integers are representable
+    // there), and cvt.rmi maps NaN to 0.  Element e of the tensor takes word
+    // e & 3 of the generator at counter (e / 4, high word, tensor, step).
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint64_t j = (uint64_t)(e0 >> 2) + (uint64_t)w;
+      const uint4 r = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), (uint32_t)T.index, L.sr_step),
+                                    L.sr_key0, L.sr_key1);
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+      int qi[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float u = __fmul_rn(__uint2float_rn(rw[b] >> 8), 5.9604644775390625e-8f);   // exact: k * 2^-24
+        int qv = __float2int_rd(__fadd_rd(__fmul_rn(m[4 * w + b], sc), u));
+        qi[b] = qv < -127 ? -127 : (qv > 127 ? 127 : qv);
+      }
+      qo[w] = pack_codes<QK>(qi[0], qi[1], qi[2], qi[3]);
+    }
+  }
   uint8_t* q8p = static_cast<uint8_t*>(T.q8) + e0;
   if (FULL) {
     __stcs(reinterpret_cast<uint4*>(q8p), make_uint4(qo[0], qo[1], qo[2], qo[3]));
@@ -389,7 +429,7 @@ __device__ __forceinline__ void upd_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-template <int QK, int DT, bool CARRIER>
+template <int QK, int DT, bool CARRIER, bool SR>
 __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) {
   using ST = UpdStage<DT>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -562,8 +602,8 @@ __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) 
       if (has) {
         int32_t g = 0;
         if (reduce && hl == 0 && L.layout.block_group) g = __ldg(L.layout.block_group + k);
-        const float ss = full ? compute_lane<QK, DT, CARRIER, true>(in, T, lb, hl, beta, omb)
-                              : compute_lane<QK, DT, CARRIER, false>(in, T, lb, hl, beta, omb);
+        const float ss = full ? compute_lane<QK, DT, CARRIER, true, SR>(in, T, lb, hl, beta, omb, L)
+                              : compute_lane<QK, DT, CARRIER, false, SR>(in, T, lb, hl, beta, omb, L);
         if (reduce && hl == 0) { s_bsum[k - kb] = ss; s_bgrp[k - kb] = g; }
       }
     }
@@ -633,23 +673,26 @@ __global__ void __launch_bounds__(kUpdThreads) scale_groups_kernel(UpdLaunch L, 
   }
 }
 
-template <int QK, int DT, bool C>
-void* kernel_ptr() { return reinterpret_cast<void*>(&update_kernel<QK, DT, C>); }
+template <int QK, int DT, bool C, bool SR>
+void* kernel_ptr() { return reinterpret_cast<void*>(&update_kernel<QK, DT, C, SR>); }
 
-void* pick_kernel(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
-#define QM_PICK(QK, DT)                                                        \
-  if (q8 == QK && dt == DT) return carrier ? kernel_ptr<QK, DT, true>() : kernel_ptr<QK, DT, false>();
-  QM_PICK(QMUON_Q8_INT8, QMUON_BF16)
-  QM_PICK(QMUON_Q8_INT8, QMUON_FP16)
-  QM_PICK(QMUON_Q8_UINT8, QMUON_BF16)
-  QM_PICK(QMUON_Q8_UINT8, QMUON_FP16)
-#undef QM_PICK
-  if (dt == QMUON_FP32 && !carrier)
-    return q8 == QMUON_Q8_INT8 ? kernel_ptr<QMUON_Q8_INT8, QMUON_FP32, false>()
-                               : kernel_ptr<QMUON_Q8_UINT8, QMUON_FP32, false>();
-  if (dt == QMUON_FP32 && carrier)
-    return q8 == QMUON_Q8_INT8 ? kernel_ptr<QMUON_Q8_INT8, QMUON_FP32, true>()
-                               : kernel_ptr<QMUON_Q8_UINT8, QMUON_FP32, true>();
+template <int QK, int DT>
+void* pick_variant(bool carrier, bool sr) {
+  if (carrier) return sr ? nullptr : kernel_ptr<QK, DT, true, false>();   // the carrier rounds to nearest only
+  return sr ? kernel_ptr<QK, DT, false, true>() : kernel_ptr<QK, DT, false, false>();
+}
+
+void* pick_kernel(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier, bool sr = false) {
+  const bool i8 = (q8 == QMUON_Q8_INT8);
+  if (q8 != QMUON_Q8_INT8 && q8 != QMUON_Q8_UINT8) return nullptr;
+  switch (dt) {
+    case QMUON_BF16: return i8 ? pick_variant<QMUON_Q8_INT8, QMUON_BF16>(carrier, sr)
+                               : pick_variant<QMUON_Q8_UINT8, QMUON_BF16>(carrier, sr);
+    case QMUON_FP16: return i8 ? pick_variant<QMUON_Q8_INT8, QMUON_FP16>(carrier, sr)
+                               : pick_variant<QMUON_Q8_UINT8, QMUON_FP16>(carrier, sr);
+    case QMUON_FP32: return i8 ? pick_variant<QMUON_Q8_INT8, QMUON_FP32>(carrier, sr)
+                               : pick_variant<QMUON_Q8_UINT8, QMUON_FP32>(carrier, sr);
+  }
   return nullptr;
 }
 
@@ -672,7 +715,7 @@ int update_blocks_per_sm(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier) {
 
 cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, bool carrier,
                           cudaStream_t stream) {
-  void* k = pick_kernel(q8, dt, carrier);
+  void* k = pick_kernel(q8, dt, carrier, L.sr != 0);
   if (!k) return cudaErrorInvalidValue;
   const cudaError_t e = prepare_kernel(k, dt);
   if (e != cudaSuccess) return e;

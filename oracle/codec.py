@@ -27,7 +27,7 @@ silent:
   accumulated in fp64; a group's inverse norm is ``1 / (sqrt(S) + 1e-7)``
   evaluated in fp64 and rounded once to fp32.
 
-Stochastic requantisation (optional; the page's section "Open Issues" says
+Stochastic requantisation (optional; the page's section "Known Limitations" says
 only that it is not implemented yet): with ``x = m * sc`` as above and a
 uniform ``u`` in [0, 1) per element (``oracle.rng``: Philox4x32-10 keyed by
 the seed, counter from the element, tensor and step), ``q = clamp(floor(x +
