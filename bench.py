@@ -239,16 +239,17 @@ def run_gpu_carrier(args, world, rank, local, w):
     payload = [torch.empty(m.numel, dtype=torch.uint8, device=dev) for m in mats]
     scale = [torch.empty(m.rows * (m.cols // 32), dtype=torch.uint8, device=dev) for m in mats]
     inv = torch.zeros(len(mats), dtype=torch.float32, device=dev)
-    ws_c = torch.empty(max(q.qmuon_carrier_workspace_size(m.rows, m.cols) for m in mats), dtype=torch.uint8,
-                       device=dev)
     probs = [q.ns_problem(o, m.rows, m.cols, inv_norm=inv.data_ptr() + 4 * i, input_kind=q.QMUON_NS_MXFP8,
                           payload=payload[i], scale_inv=scale[i]) for i, (o, m) in enumerate(zip(outs, mats))]
     ws_n = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device=dev)
 
+    # one launch over every matrix (one norm group per matrix)
+    plan_c = q.qmuon_plan_create([(s[0], s[1], g, m.rows, m.cols) for s, g, m in zip(states, grads, mats)],
+                                 w.q8_kind, "bf16")
+    ws_c = torch.empty(q.qmuon_workspace_size(plan_c), dtype=torch.uint8, device=dev)
+
     def carrier_all():
-        for i, m in enumerate(mats):
-            q.qmuon_update_mxfp8_carrier(states[i][0], states[i][1], grads[i], m.rows, m.cols, w.q8_kind, "bf16",
-                                         w.beta, payload[i], scale[i], inv.data_ptr() + 4 * i, ws_c, stream=stream)
+        q.qmuon_update_mxfp8_carrier_multi(plan_c, w.beta, payload, scale, inv, ws_c, stream=stream)
 
     def step(t):
         carrier_all()
@@ -296,7 +297,7 @@ def run_gpu_carrier(args, world, rank, local, w):
     return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks,
                 per_step=[], upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes,
                 ns_ms={"full": ns_ms}, ns_flop={"full": flop}, e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
-                launches=(len(mats) + 1 + 3 * w.iters) * args.steps, n_params=n_params, w=w)
+                launches=(1 + len(mats) + 3 * w.iters) * args.steps, n_params=n_params, w=w)
 
 
 def run_gpu(args, world, rank, local):

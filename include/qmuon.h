@@ -170,6 +170,24 @@ QMUON_API qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, qm
                                         uint8_t* scale_inv, float* inv_norm, void* ws,
                                         size_t ws_bytes, void* stream);
 
+/* The carrier of every tensor of a plan in one launch (one norm group per
+ * tensor, as in qmuon_step's full steps):
+ *   payloads    H  n_tensors device pointers (D): tensor i's rows x cols E4M3
+ *                  codes (16-byte aligned)
+ *   scale_invs  H  n_tensors device pointers (D): tensor i's rows x (cols/32)
+ *                  E8M0 exponents
+ *   inv_norms   D  n_tensors fp32: 1/(sqrt(sum m*m)+1e-7) per tensor
+ *   group_sumsq D  n_tensors fp32 sums of m*m, or NULL
+ *   ws, ws_bytes D workspace of qmuon_workspace_size(plan, QMUON_WS_UPDATE);
+ *                  the call copies its tensor table into it (no allocation)
+ * Every non-empty tensor needs cols % 32 == 0 (else QMUON_ERR_UNSUPPORTED).
+ * Gradients are read only; codes, scales, q8 and absmax equal those of
+ * qmuon_update_mxfp8_carrier on each tensor alone. */
+QMUON_API qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan, float beta,
+                                              uint8_t* const* payloads, uint8_t* const* scale_invs,
+                                              float* inv_norms, float* group_sumsq, void* ws,
+                                              size_t ws_bytes, void* stream);
+
 /* Input of one Newton-Schulz problem. */
 typedef enum { QMUON_NS_BF16 = 0, QMUON_NS_MXFP8 = 1 } qmuon_ns_input;
 

@@ -88,6 +88,7 @@ def lib() -> C.CDLL:
         "qmuon_plan_set_stochastic_rounding": (i32, [vp, i32, C.c_uint64]),
         "qmuon_carrier_workspace_size": (sz, [i64, i64]),
         "qmuon_update_mxfp8_carrier": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp, vp, sz, vp]),
+        "qmuon_update_mxfp8_carrier_multi": (i32, [vp, f32, C.POINTER(vp), C.POINTER(vp), vp, vp, vp, sz, vp]),
         "qmuon_ns_workspace_size": (sz, [C.POINTER(qmuon_ns_problem), i32]),
         "qmuon_newton_schulz_batched": (i32, [C.POINTER(qmuon_ns_problem), i32, i32, C.POINTER(f32), vp, sz, vp]),
         "qmuon_step": (i32, [vp, i64, i32, f32, f32, f32, C.POINTER(vp), C.POINTER(f32), i32, vp, vp, sz, vp]),
@@ -112,7 +113,7 @@ def exported_symbols() -> list:
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
-            "qmuon_plan_set_stochastic_rounding"]
+            "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi"]
 
 
 # --------------------------------------------------------------------------
@@ -255,6 +256,17 @@ def qmuon_update_mxfp8_carrier(q8, absmax, grad, rows: int, cols: int, q8_kind, 
         _ptr(payload), _ptr(scale_inv), _ptr(inv_norm), _ptr(ws),
         _nbytes(ws) if ws_bytes is None else int(ws_bytes), _stream(stream))
     _check(st, "qmuon_update_mxfp8_carrier")
+
+
+def qmuon_update_mxfp8_carrier_multi(plan: Plan, beta: float, payloads: Sequence, scale_invs: Sequence, inv_norms,
+                                     ws, group_sumsq=None, ws_bytes: Optional[int] = None, stream=None):
+    n = len(payloads)
+    pp = (C.c_void_p * max(1, n))(*[_ptr(x) for x in payloads])
+    sp = (C.c_void_p * max(1, n))(*[_ptr(x) for x in scale_invs])
+    st = lib().qmuon_update_mxfp8_carrier_multi(plan.handle, float(beta), pp, sp, _ptr(inv_norms), _ptr(group_sumsq),
+                                                _ptr(ws), _nbytes(ws) if ws_bytes is None else int(ws_bytes),
+                                                _stream(stream))
+    _check(st, "qmuon_update_mxfp8_carrier_multi")
 
 
 def ns_problem(x, rows: int, cols: int, ld: Optional[int] = None, inv_norm=None, input_kind=QMUON_NS_BF16,

@@ -326,15 +326,18 @@ struct UpdWs {
   double* partials;
   float* sumsq;
   float* inv;
+  UpdTensor* table;         // per-call tensor table (multi-tensor carrier)
   unsigned char* ns;
   size_t ns_bytes;
 };
+
+size_t table_bytes(const qmuon_plan* p) { return align_up(std::max<size_t>(p->tensors.size(), 1) * sizeof(UpdTensor), 256); }
 
 size_t update_ws_bytes(const qmuon_plan* p) {
   int32_t gmax = 0;
   for (const auto& l : p->layout) gmax = std::max(gmax, l.n_groups);
   return kWsHeader + align_up((size_t)std::max(p->n_slots_max, 1) * 8, 256) +
-         2 * align_up((size_t)std::max(gmax, 1) * 4, 256);
+         2 * align_up((size_t)std::max(gmax, 1) * 4, 256) + table_bytes(p);
 }
 
 UpdWs carve(const qmuon_plan* p, void* ws, size_t ws_bytes) {
@@ -350,6 +353,8 @@ UpdWs carve(const qmuon_plan* p, void* ws, size_t ws_bytes) {
   off += align_up((size_t)std::max(gmax, 1) * 4, 256);
   w.inv = reinterpret_cast<float*>(b + off);
   off += align_up((size_t)std::max(gmax, 1) * 4, 256);
+  w.table = reinterpret_cast<UpdTensor*>(b + off);
+  off += table_bytes(p);
   w.ns = b + off;
   w.ns_bytes = ws_bytes > off ? ws_bytes - off : 0;
   return w;
@@ -500,6 +505,44 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, q
   cudaError_t e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, true, s);
   return cuda_status(e, "qmuon_update_mxfp8_carrier (launch)");
+}
+
+extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan, float beta, uint8_t* const* payloads,
+                                                         uint8_t* const* scale_invs, float* inv_norms,
+                                                         float* group_sumsq, void* ws, size_t ws_bytes,
+                                                         void* stream) {
+  if (!plan || !payloads || !scale_invs || !inv_norms || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, 256) || !aligned(inv_norms, 4) || (group_sumsq && !aligned(group_sumsq, 4)))
+    return QMUON_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < update_ws_bytes(plan)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  const int32_t n = (int32_t)plan->tensors.size();
+  std::vector<UpdTensor> ut(n);
+  for (int32_t i = 0; i < n; ++i) {
+    const qmuon_tensor& T = plan->tensors[i];
+    const int64_t numel = T.rows * T.cols;
+    if (numel > 0) {
+      if (T.cols % QMUON_SCALE_BLOCK) return QMUON_ERR_UNSUPPORTED;
+      if (!payloads[i] || !scale_invs[i] || !aligned(payloads[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+    }
+    ut[i].q8 = T.q8;
+    ut[i].absmax = T.absmax;
+    ut[i].grad = T.grad;
+    ut[i].payload = payloads[i];
+    ut[i].scale = scale_invs[i];
+    ut[i].numel = numel;
+    ut[i].block_begin = plan->tensor_begin[i];
+    ut[i].index = i;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const UpdWs w = carve(plan, ws, ws_bytes);
+  // one group per tensor (the plan's full-step layout): inverse norm i is tensor i's
+  UpdLaunch L = make_launch(plan, 1, beta, w, group_sumsq, inv_norms);
+  L.tensors = w.table;
+  cudaError_t e = cudaMemcpyAsync(w.table, ut.data(), n * sizeof(UpdTensor), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
+  if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, true, s);
+  // the pageable host table is staged by the copy before it returns
+  return cuda_status(e, "qmuon_update_mxfp8_carrier_multi (launch)");
 }
 
 // ---------------------------------------------------------------------------

@@ -189,3 +189,48 @@ def test_carrier_parity(q8_kind, shape):
     np.testing.assert_array_equal(payload.cpu().numpy().reshape(rows, cols), r.payload)
     np.testing.assert_allclose(inv.item(), r.inv_norm, rtol=1e-5)
     assert torch.equal(g, g_before)   # the gradient is read only
+
+
+@pytest.mark.parametrize("q8_kind", ["int8", "uint8"])
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+def test_carrier_multi_matches_oracle(q8_kind, grad_dtype):
+    # one launch over tensors of several shapes (ragged rows, blocks that span
+    # tensors): every tensor as the oracle's single-tensor carrier
+    shapes = [(64, 4096), (37, 96), (1, 32), (300, 1024), (5, 224)]
+    states = [workloads.random_state(workloads.Matrix("t", r, c), 90 + i, q8_kind, device="cuda")
+              for i, (r, c) in enumerate(shapes)]
+    grads = [random_grad(r * c, grad_dtype, 20 + i) for i, (r, c) in enumerate(shapes)]
+    host = [(s.cpu().numpy().copy(), a.cpu().numpy().copy(), to_oracle_grad(g, grad_dtype))
+            for (s, a), g in zip(states, grads)]
+    before = [g.clone() for g in grads]
+    plan = q.qmuon_plan_create([(s, a, g, r, c) for (s, a), g, (r, c) in zip(states, grads, shapes)],
+                               q8_kind, grad_dtype)
+    payloads = [torch.empty(r * c, dtype=torch.uint8, device="cuda") for r, c in shapes]
+    scales = [torch.empty(r * (c // 32), dtype=torch.uint8, device="cuda") for r, c in shapes]
+    inv = torch.zeros(len(shapes), device="cuda")
+    sums = torch.zeros(len(shapes), device="cuda")
+    ws = torch.empty(q.qmuon_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    q.qmuon_update_mxfp8_carrier_multi(plan, 0.95, payloads, scales, inv, ws, group_sumsq=sums)
+    q.qmuon_sync_status(ws)
+    for i, ((r, c), (s, a), h) in enumerate(zip(shapes, states, host)):
+        ref = carrier.carrier_update(h[0], h[1], h[2], 0.95, r, c, q8_kind=q8_kind, grad_dtype=grad_dtype)
+        np.testing.assert_array_equal(s.cpu().numpy(), ref.q8)
+        np.testing.assert_array_equal(a.cpu().numpy(), ref.absmax)
+        np.testing.assert_array_equal(scales[i].cpu().numpy().reshape(r, c // 32), ref.scale_inv)
+        np.testing.assert_array_equal(payloads[i].cpu().numpy().reshape(r, c), ref.payload)
+        np.testing.assert_allclose(inv[i].item(), ref.inv_norm, rtol=1e-5)
+        assert torch.equal(grads[i], before[i])   # gradients are read only
+
+
+def test_carrier_multi_rejects_unaligned_columns():
+    m = workloads.Matrix("t", 4, 40)
+    s, a = workloads.random_state(m, 1, device="cuda")
+    g = random_grad(m.numel, "bf16", 2)
+    plan = q.qmuon_plan_create([(s, a, g, 4, 40)])
+    pay = torch.empty(160, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(8, dtype=torch.uint8, device="cuda")
+    inv = torch.zeros(1, device="cuda")
+    ws = torch.empty(q.qmuon_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    with pytest.raises(q.QmuonError) as e:
+        q.qmuon_update_mxfp8_carrier_multi(plan, 0.9, [pay], [sc], inv, ws)
+    assert e.value.status == q.QMUON_ERR_UNSUPPORTED
