@@ -222,6 +222,41 @@ def oracle_sample(w, budget_s=15.0, min_s=12.0):
 # the GPU leg
 # --------------------------------------------------------------------------
 
+GRASP_BYTES_PER_PARAM = 0.625 + 2 + 2 + 2 + 2 + 0.625   # state r/w, g, M_t w + 2 reads
+
+
+def time_grasp(q, mats, grads, stream, reps, dev):
+    """The 4-bit GRASP momentum step (qmuon_grasp_step) over the same matrices,
+    one call for all of them, from a zero residual and a seeded factor."""
+    descs, keep = [], []
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    for m, grad in zip(mats, grads):
+        rows, cols = m.rows, m.cols
+        nbr, nbc = (rows + 63) // 64, cols // 64
+        t = dict(res=torch.full((rows, cols // 2), 0x88, dtype=torch.uint8, device=dev),
+                 res_rmax=torch.zeros(nbc, rows, device=dev), res_cmax=torch.zeros(nbr, cols, device=dev),
+                 p=torch.zeros(rows, 8, dtype=torch.int8, device=dev), p_rmax=torch.zeros(rows, device=dev),
+                 p_cmax=torch.zeros(nbr, 8, device=dev),
+                 r=torch.randint(-127, 128, (cols, 8), generator=g, device=dev, dtype=torch.int32).to(torch.int8),
+                 r_rmax=torch.ones(cols, device=dev), r_cmax=torch.ones((cols + 63) // 64, 8, device=dev))
+        keep.append(t)
+        descs.append(q.grasp_matrix(rows, cols, t["res"], t["res_rmax"], t["res_cmax"], t["p"], t["p_rmax"],
+                                    t["p_cmax"], t["r"], t["r_rmax"], t["r_cmax"], grad))
+    ws = torch.empty(q.qmuon_grasp_workspace_size(descs), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        q.qmuon_grasp_step(descs, 0.95, ws, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        q.qmuon_grasp_step(descs, 0.95, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    q.qmuon_sync_status(ws, stream)
+    return e0.elapsed_time(e1) / reps
+
+
 def run_gpu_carrier(args, world, rank, local, w):
     """Workload 5: per-matrix MXFP8 carrier update (E4M3 payload + E8M0 scales
     + inverse norm; the gradient is only read) followed by full Newton-Schulz
@@ -405,6 +440,7 @@ def run_gpu(args, world, rank, local):
     u1.record(stream)
     torch.cuda.synchronize()
     upd_sr_ms = u0.elapsed_time(u1) / reps
+    grasp_ms = time_grasp(q, mats, grads, stream, reps, dev)
 
     def ns_problems(full):
         tr, tc = (1, 1) if full else w.tile
@@ -461,7 +497,7 @@ def run_gpu(args, world, rank, local):
     # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
     return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
-                upd_sr_ms=upd_sr_ms,
+                upd_sr_ms=upd_sr_ms, grasp_ms=grasp_ms,
                 ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=4 * ngr, n_full=n_full,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
@@ -529,6 +565,11 @@ def main():
             "data": "synthetic (seeded gradients, zero initial state, N(0,0.02^2) weights)", "config": config,
             "full_steps_timed": r["n_full"], "per_step": r["per_step"],
             "update_gbs": r["upd_gbs"], "ns_tflops": ns_tflops,
+            "grasp_step": ({"ms_per_call": r["grasp_ms"], "mparams_per_s": r["n_params"] / (r["grasp_ms"] / 1e3) / 1e6,
+                            "bytes_per_param": GRASP_BYTES_PER_PARAM,
+                            "gbs": GRASP_BYTES_PER_PARAM * r["n_params"] / (r["grasp_ms"] / 1e3) / 1e9,
+                            "frac": GRASP_BYTES_PER_PARAM * r["n_params"] / (r["grasp_ms"] / 1e3) / 1e9
+                            / float(peaks["hbm_gbs"])} if r.get("grasp_ms") else None),
             "update_stochastic_rounding": ({"gbs": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9,
                                             "ms_per_launch": r["upd_sr_ms"],
                                             "frac": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9 / float(peaks["hbm_gbs"])}

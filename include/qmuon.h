@@ -188,6 +188,52 @@ QMUON_API qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan, 
                                               float* inv_norms, float* group_sumsq, void* ws,
                                               size_t ws_bytes, void* stream);
 
+/* ---- 4-bit GRASP momentum state ("4-bit-Muon-GRASP", the update
+ * equations and the grid quantisation on that page) ----
+ * The momentum of a rows x cols matrix is a rank-8 factor P R^T plus a
+ * residual, every piece grid-quantised: in each block an entry x is coded as
+ * q = clamp(rint(x * L / min(r, c)), -L, L) with r, c the block's maxima of
+ * |x| over the entry's row and column (stored in fp32) and L = 7 (residual,
+ * 64 x 64 blocks) or 127 (P, R: blocks of 64 rows by all 8 columns).  Layouts
+ * (row-major, all device memory, in/out):
+ *   res       rows x cols/2 bytes: 4-bit codes q + 8, column 2c in the low nibble
+ *   res_rmax  [cols/64][rows]     res_cmax [ceil(rows/64)][cols]
+ *   p         rows x 8 int8       p_rmax [rows]   p_cmax [ceil(rows/64)][8]
+ *   r         cols x 8 int8       r_rmax [cols]   r_cmax [ceil(cols/64)][8]
+ *   grad      rows x cols bf16: g_t in, M_t out (round to nearest even)
+ * A first step starts from a zero residual and P and a seeded R (the power
+ * iteration's warm start). */
+#define QMUON_GRASP_RANK 8
+#define QMUON_GRASP_BLOCK 64
+typedef struct {
+  int64_t rows, cols;            /* cols % 64 == 0 (else QMUON_ERR_UNSUPPORTED) */
+  uint8_t* res;
+  float* res_rmax;
+  float* res_cmax;
+  int8_t* p;
+  float* p_rmax;
+  float* p_cmax;
+  int8_t* r;
+  float* r_rmax;
+  float* r_cmax;
+  void* grad;
+} qmuon_grasp_matrix;
+
+/* Workspace bytes of qmuon_grasp_step for these matrices (0 on bad input). */
+QMUON_API size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices, int32_t n);
+
+/* One GRASP momentum step of n matrices (H array of descriptors):
+ *   M_{t-1} = res + P R^T, M_t = mu M_{t-1} + g_t (fp32, one rounding per
+ *   operation, the rank sum left to right), stored in bf16 over g_t;
+ *   Q = ColNorm(R_{t-1}), P_t = orth(M_t Q) (thin QR, positive diagonal),
+ *   R_t = M_t^T P_t, res_t = M_t - P_t R_t^T, all from the stored M_t;
+ *   res_t, P_t, R_t are grid-quantised into the state.
+ * Asynchronous on `stream`; M_t Q of rank below 8 records
+ * QMUON_ERR_INVALID_ARGUMENT in the workspace header (qmuon_sync_status)
+ * and leaves R and the residual unchanged. */
+QMUON_API qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int32_t n, float mu, void* ws,
+                                        size_t ws_bytes, void* stream);
+
 /* Input of one Newton-Schulz problem. */
 typedef enum { QMUON_NS_BF16 = 0, QMUON_NS_MXFP8 = 1 } qmuon_ns_input;
 

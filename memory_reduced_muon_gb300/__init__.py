@@ -64,6 +64,14 @@ class qmuon_ns_problem(C.Structure):
                 ("payload", C.c_void_p), ("scale_inv", C.c_void_p)]
 
 
+class qmuon_grasp_matrix(C.Structure):
+    _fields_ = [("rows", C.c_int64), ("cols", C.c_int64), ("res", C.c_void_p), ("res_rmax", C.c_void_p),
+                ("res_cmax", C.c_void_p), ("p", C.c_void_p), ("p_rmax", C.c_void_p), ("p_cmax", C.c_void_p),
+                ("r", C.c_void_p), ("r_rmax", C.c_void_p), ("r_cmax", C.c_void_p), ("grad", C.c_void_p)]
+
+
+GRASP_RANK, GRASP_BLOCK = 8, 64
+
 _lib_handle = None
 
 
@@ -86,6 +94,8 @@ def lib() -> C.CDLL:
         "qmuon_update_multi_normalize_groups": (i32, [vp, f32, i32, vp, vp, vp, sz, vp]),
         "qmuon_update_multi_normalize_groups_sr": (i32, [vp, f32, i32, C.c_uint64, i64, vp, vp, vp, sz, vp]),
         "qmuon_plan_set_stochastic_rounding": (i32, [vp, i32, C.c_uint64]),
+        "qmuon_grasp_workspace_size": (sz, [C.POINTER(qmuon_grasp_matrix), i32]),
+        "qmuon_grasp_step": (i32, [C.POINTER(qmuon_grasp_matrix), i32, f32, vp, sz, vp]),
         "qmuon_carrier_workspace_size": (sz, [i64, i64]),
         "qmuon_update_mxfp8_carrier": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp, vp, sz, vp]),
         "qmuon_update_mxfp8_carrier_multi": (i32, [vp, f32, C.POINTER(vp), C.POINTER(vp), vp, vp, vp, sz, vp]),
@@ -113,7 +123,8 @@ def exported_symbols() -> list:
             "qmuon_update_mxfp8_carrier", "qmuon_ns_workspace_size", "qmuon_newton_schulz_batched",
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
-            "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi"]
+            "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
+            "qmuon_grasp_workspace_size", "qmuon_grasp_step"]
 
 
 # --------------------------------------------------------------------------
@@ -322,3 +333,29 @@ def qmuon_step_prepare(plan: Plan, weights, ws, ws_bytes: Optional[int] = None):
 
 def qmuon_sync_status(ws, stream=None):
     _check(lib().qmuon_sync_status(_ptr(ws), _stream(stream)), "qmuon_sync_status")
+
+
+# --------------------------------------------------------------------------
+# 4-bit GRASP momentum state
+# --------------------------------------------------------------------------
+
+def grasp_matrix(rows: int, cols: int, res, res_rmax, res_cmax, p, p_rmax, p_cmax, r, r_rmax, r_cmax,
+                 grad) -> qmuon_grasp_matrix:
+    return qmuon_grasp_matrix(int(rows), int(cols), _ptr(res), _ptr(res_rmax), _ptr(res_cmax), _ptr(p), _ptr(p_rmax),
+                              _ptr(p_cmax), _ptr(r), _ptr(r_rmax), _ptr(r_cmax), _ptr(grad))
+
+
+def _grasp_array(matrices: Sequence):
+    arr = (qmuon_grasp_matrix * max(1, len(matrices)))(*matrices)
+    return arr, len(matrices)
+
+
+def qmuon_grasp_workspace_size(matrices: Sequence) -> int:
+    arr, n = _grasp_array(matrices)
+    return int(lib().qmuon_grasp_workspace_size(arr, n))
+
+
+def qmuon_grasp_step(matrices: Sequence, mu: float, ws, ws_bytes: Optional[int] = None, stream=None):
+    arr, n = _grasp_array(matrices)
+    _check(lib().qmuon_grasp_step(arr, n, float(mu), _ptr(ws), _nbytes(ws) if ws_bytes is None else int(ws_bytes),
+                                  _stream(stream)), "qmuon_grasp_step")

@@ -1,0 +1,660 @@
+// 4-bit GRASP momentum state for sm_103a (qmuon_grasp_step).
+//
+// Implements the update of "4-bit-Muon-GRASP" (the page's equations): the
+// momentum of every matrix is held as a rank-8 factor P R^T (8-bit) plus a
+// residual (4-bit), each grid-quantised in 64 x 64 blocks (an entry is scaled
+// by the smaller of its row and column maxima inside its block).  One step:
+//   M_{t-1} = res + P R^T,  M_t = mu M_{t-1} + g_t  (stored in bf16 over g_t)
+//   Q = ColNorm(R_{t-1}),  P_t = orth(M_t Q),  R_t = M_t^T P_t
+//   res_t = M_t - P_t R_t^T,  then res_t, P_t, R_t are grid-quantised.
+// The reconstruction and the momentum are computed in fp32 with one rounding
+// per operation in a fixed order (the sum over the rank runs left to right);
+// the power iteration accumulates in fp32, and orth is CholeskyQR2 in fp64
+// (the orthonormal factor whose triangular factor has a positive diagonal).
+// All matrices of a call share each launch:
+//   grasp_colnorm   per matrix:     Q = ColNorm(dequantised R)
+//   grasp_pass1     per row strip:  reconstruct, momentum, store M_t, Y = M_t Q
+//   grasp_orth      per matrix:     P = CholeskyQR2(Y), quantise P
+//   grasp_pass2     per col strip:  R = M_t^T P
+//   grasp_rfinal    per matrix:     quantise R
+//   grasp_pass3     per tile:       residual, its 4-bit grid codes and maxima
+// A strip (64 rows or 64 columns of one matrix) is one CTA's whole sum, so
+// there are no partial sums and no atomics on results: they are deterministic.
+// Grid steps use fl(min(r, c) / L) = min(fl(r / L), fl(c / L)) (division is
+// monotonic), so divisions run per row and per column, not per entry.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "qm_internal.h"
+
+namespace qm {
+namespace {
+
+constexpr int kRank = QMUON_GRASP_RANK;   // 8
+constexpr int kS = QMUON_GRASP_BLOCK;     // 64
+constexpr int kThreads = 256;
+
+// Device copy of one matrix's description plus its workspace slices.
+struct GraspProb {
+  qmuon_grasp_matrix m;
+  int64_t nbr, nbc;          // row / column blocks
+  float* q;                  // [cols][8]   ColNorm(R_{t-1})
+  float* rdeq;               // [cols][8]   R_{t-1} dequantised
+  float* y;                  // [rows][8]   M_t Q
+  float* p;                  // [rows][8]   P_t
+  float* r;                  // [cols][8]   R_t
+};
+
+struct GraspArgs {
+  const GraspProb* probs;
+  const int64_t* tile_start;  // [n + 1] prefix of pass 3's chunks (64 rows x 4 column blocks)
+  const int64_t* rstrip_start;  // [n + 1] prefix of 64-row strips
+  const int64_t* cstrip_start;  // [n + 1] prefix of 64-column strips
+  int32_t n;
+  float mu;
+};
+
+__device__ __forceinline__ int find_prob(const int64_t* start, int n, int64_t idx) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(start + mid) <= idx) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Grid dequantisation step of an entry: fl(min(rmax, cmax) / L).
+__device__ __forceinline__ float grid_step(float rmax, float cmax, float L) {
+  return __fdiv_rn(fminf(rmax, cmax), L);
+}
+// Grid quantisation factor fl(L / min(r, c)) = max(fl(L / r), fl(L / c)) for
+// positive maxima (division is monotonic); 0 where a maximum is 0.
+__device__ __forceinline__ float grid_factor(float inv_r, float inv_c) { return fmaxf(inv_r, inv_c); }
+__device__ __forceinline__ float inv_level(float mx, float L) { return mx == 0.0f ? 0.0f : __fdiv_rn(L, mx); }
+__device__ __forceinline__ int grid_code(float x, float sc, int L) {
+  if (sc == 0.0f) return 0;
+  const int q = __float2int_rn(__fmul_rn(x, sc));   // NaN converts to 0
+  return q < -L ? -L : (q > L ? L : q);
+}
+
+// Compensated (Neumaier) addition of a block's sum into a running total:
+// the strips add up to 224 blocks, and orth magnifies the error of Y when its
+// columns are nearly parallel.
+__device__ __forceinline__ void comp_add(float& sum, float& c, float v) {
+  const float t = sum + v;
+  c += (fabsf(sum) >= fabsf(v)) ? ((sum - t) + v) : ((v - t) + sum);
+  sum = t;
+}
+
+// Sum over the CTA of 8 fp64 values per thread, in a fixed order.
+__device__ __forceinline__ void block_sum8(double (&v)[kRank], double* red /* [8 warps][8] */) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < kRank; ++c)
+    for (int o = 16; o > 0; o >>= 1) v[c] += __shfl_xor_sync(0xffffffffu, v[c], o);
+  __syncthreads();
+  if (l == 0)
+#pragma unroll
+    for (int c = 0; c < kRank; ++c) red[w * kRank + c] = v[c];
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kRank; ++c) {
+    double s = 0.0;
+    for (int i = 0; i < kThreads / 32; ++i) s += red[i * kRank + c];
+    v[c] = s;
+  }
+}
+
+// Dequantised 8-bit factor row (P or R): codes q[row][8], per-row max, per
+// (row block, column) max.
+__device__ __forceinline__ void factor_row(const int8_t* q, const float* rmax, const float* cmax, int64_t row,
+                                           float (&out)[kRank]) {
+  const float rm = __ldg(rmax + row);
+  const float* cm = cmax + (row / kS) * kRank;
+  const int2 raw = __ldg(reinterpret_cast<const int2*>(q + row * kRank));
+  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+#pragma unroll
+  for (int l = 0; l < kRank; ++l) out[l] = __fmul_rn((float)b[l], grid_step(rm, __ldg(cm + l), 127.0f));
+}
+
+// ---------------------------------------------------------------------------
+// Q = ColNorm(R_{t-1}), one CTA per matrix
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
+  __shared__ double red[kThreads / 32 * kRank];
+  const GraspProb& P = a.probs[blockIdx.x];
+  const int64_t cols = P.m.cols;
+  double ss[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
+    float r[kRank];
+    factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) ss[l] += (double)r[l] * (double)r[l];
+  }
+  block_sum8(ss, red);
+  double inv[kRank];
+#pragma unroll
+  for (int l = 0; l < kRank; ++l) inv[l] = ss[l] > 0.0 ? 1.0 / sqrt(ss[l]) : 0.0;
+  for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
+    float r[kRank];
+    factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) {
+      P.q[j * kRank + l] = (float)((double)r[l] * inv[l]);
+      P.rdeq[j * kRank + l] = r[l];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// pass 1: one CTA per 64-row strip of a matrix, walking its column blocks in
+// chunks of four (256 columns: R, Q and the residual's column steps for the
+// chunk are staged in shared memory by all threads between two barriers).
+// Thread t owns row t/4 of the strip and 16 consecutive columns (t % 4) * 16
+// of each block, and loads its four blocks' codes and gradient up front; Y
+// for the strip's rows is complete when the walk ends.
+// ---------------------------------------------------------------------------
+constexpr int kChunk = 4;   // column blocks per chunk
+
+// Shared rows of 8 floats for the chunk's 256 columns.  The four 16-column
+// groups a warp reads at once sit 16 * 8 = 128 floats apart, one bank apart
+// modulo 32: each group of 16 columns is shifted by 4 more floats so that
+// their float4 reads fall in different banks.
+constexpr int kPadStride = kChunk * kS * kRank + (kChunk * kS / 16) * 4;
+__device__ __forceinline__ int sidx(int col, int l) { return col * kRank + (col >> 4) * 4 + l; }
+
+__global__ void __launch_bounds__(kThreads) grasp_pass1(GraspArgs a) {
+  __shared__ __align__(16) float sR[kPadStride];
+  __shared__ __align__(16) float sQ[kPadStride];
+  __shared__ float sStepC[kChunk * kS];   // fl(cmax_j / 7) of the residual
+  const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[pi];
+  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
+  const int64_t rows = P.m.rows, cols = P.m.cols;
+  const int t = threadIdx.x;
+  const int ti = t >> 2, tj = (t & 3) * 16;
+  const int64_t i = bi * kS + ti;
+  const bool live = i < rows;
+  float p[kRank];
+  if (live) factor_row(P.m.p, P.m.p_rmax, P.m.p_cmax, i, p);
+  float y[kRank] = {0, 0, 0, 0, 0, 0, 0, 0}, yc[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int64_t b0 = 0; b0 < P.nbc; b0 += kChunk) {
+    const int nb = (P.nbc - b0) < kChunk ? (int)(P.nbc - b0) : kChunk;
+    // this thread's inputs for the chunk, in flight while the chunk is staged
+    uint2 codes[kChunk];
+    uint4 g0[kChunk], g1[kChunk];
+    float rmax[kChunk];
+    if (live) {
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        if (c >= nb) break;
+        const int64_t bj = b0 + c;
+        codes[c] = __ldg(reinterpret_cast<const uint2*>(P.m.res + i * (cols / 2) + (bj * kS + tj) / 2));
+        const __nv_bfloat16* grow = static_cast<const __nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
+        g0[c] = *reinterpret_cast<const uint4*>(grow);
+        g1[c] = *reinterpret_cast<const uint4*>(grow + 8);
+        rmax[c] = __ldg(P.m.res_rmax + bj * rows + i);
+      }
+    }
+    __syncthreads();   // the previous chunk's shared data is no longer read
+    {
+      const int64_t j0 = b0 * kS;
+      const int ncol = nb * kS;
+      // half a row of R and of Q (a float4 each) per thread per pass
+      for (int e = t; e < ncol * kRank / 4; e += kThreads) {
+        const int col = e >> 1, h = (e & 1) * 4;
+        *reinterpret_cast<float4*>(&sR[sidx(col, h)]) = __ldg(reinterpret_cast<const float4*>(P.rdeq + j0 * kRank) + e);
+        *reinterpret_cast<float4*>(&sQ[sidx(col, h)]) = __ldg(reinterpret_cast<const float4*>(P.q + j0 * kRank) + e);
+      }
+      if (t < ncol) sStepC[t] = __fdiv_rn(__ldg(P.m.res_cmax + bi * cols + j0 + t), 7.0f);
+    }
+    __syncthreads();
+    if (!live) continue;
+#pragma unroll
+    for (int c = 0; c < kChunk; ++c) {
+      if (c >= nb) break;
+      const int64_t bj = b0 + c;
+      const float step_r = __fdiv_rn(rmax[c], 7.0f);
+      const uint32_t gw[8] = {g0[c].x, g0[c].y, g0[c].z, g0[c].w, g1[c].x, g1[c].y, g1[c].z, g1[c].w};
+      const uint32_t cw[2] = {codes[c].x, codes[c].y};
+      const int cb = c * kS + tj;   // column of the chunk
+      uint32_t out[8];
+      float yb[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
+        const float res = __fmul_rn((float)nib, fminf(step_r, sStepC[cb + e]));
+        float acc = 0.0f;
+#pragma unroll
+        for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], sR[sidx(cb + e, l)]));
+        const float mprev = __fadd_rn(res, acc);
+        const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
+        const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
+        const __nv_bfloat16 mb = __float2bfloat16_rn(m);
+        const float mv = __bfloat162float(mb);
+        if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
+        else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
+#pragma unroll
+        for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, sQ[sidx(cb + e, l)], yb[l]);
+      }
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
+      __nv_bfloat16* grow = static_cast<__nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
+      *reinterpret_cast<uint4*>(grow) = make_uint4(out[0], out[1], out[2], out[3]);
+      *reinterpret_cast<uint4*>(grow + 8) = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+  }
+#pragma unroll
+  for (int l = 0; l < kRank; ++l) y[l] += yc[l];
+  // the 4 threads of a row add their sums (fixed order), one stores the row of Y
+#pragma unroll
+  for (int l = 0; l < kRank; ++l) {
+    y[l] += __shfl_xor_sync(0xffffffffu, y[l], 1);
+    y[l] += __shfl_xor_sync(0xffffffffu, y[l], 2);
+  }
+  if ((t & 3) == 0 && live) {
+    float4* dst = reinterpret_cast<float4*>(P.y + i * kRank);
+    dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+    dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+  }
+}
+
+// Grid quantisation of an 8-column factor (rows x 8, blocks of 64 rows):
+// codes, per-row maxima and per (row block, column) maxima.  One CTA.
+__device__ void quantize_factor(const float* x, int64_t rows, int8_t* q, float* rmax, float* cmax) {
+  const int64_t nbr = (rows + kS - 1) / kS;
+  for (int64_t b = 0; b < nbr; ++b) {
+    // column maxima of block b: thread (row, column) pairs, then a reduction
+    const int64_t r0 = b * kS;
+    __shared__ float cm[kRank];
+    if (threadIdx.x < kRank) cm[threadIdx.x] = 0.0f;
+    __syncthreads();
+    for (int e = threadIdx.x; e < kS * kRank; e += kThreads) {
+      const int64_t row = r0 + e / kRank;
+      if (row < rows) atomicMax(reinterpret_cast<int*>(&cm[e % kRank]), __float_as_int(fabsf(x[row * kRank + e % kRank])));
+    }
+    __syncthreads();
+    if (threadIdx.x < kRank) cmax[b * kRank + threadIdx.x] = cm[threadIdx.x];
+    for (int e = threadIdx.x; e < kS; e += kThreads) {
+      const int64_t row = r0 + e;
+      if (row >= rows) continue;
+      float v[kRank], rm = 0.0f;
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) {
+        v[l] = x[row * kRank + l];
+        rm = fmaxf(rm, fabsf(v[l]));
+      }
+      rmax[row] = rm;
+      const float ir = inv_level(rm, 127.0f);
+      int8_t c[kRank];
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) c[l] = (int8_t)grid_code(v[l], grid_factor(ir, inv_level(cm[l], 127.0f)), 127);
+      *reinterpret_cast<int2*>(q + row * kRank) = *reinterpret_cast<const int2*>(c);
+    }
+    __syncthreads();
+  }
+}
+
+// Cholesky of an 8 x 8 SPD matrix (lower factor, in place), one thread.
+__device__ bool chol8(double (&g)[kRank][kRank]) {
+  for (int j = 0; j < kRank; ++j) {
+    double d = g[j][j];
+    for (int k = 0; k < j; ++k) d -= g[j][k] * g[j][k];
+    if (!(d > 0.0)) return false;
+    d = sqrt(d);
+    g[j][j] = d;
+    for (int i = j + 1; i < kRank; ++i) {
+      double s = g[i][j];
+      for (int k = 0; k < j; ++k) s -= g[i][k] * g[j][k];
+      g[i][j] = s / d;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Y = sum of the partials; P = CholeskyQR2(Y); quantise P.  One CTA per matrix.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) grasp_orth(GraspArgs a, WsHeader* hdr) {
+  __shared__ double red[kThreads / 32 * kRank];
+  __shared__ double sL[kRank][kRank];
+  __shared__ int s_ok;
+  const GraspProb& P = a.probs[blockIdx.x];
+  const int64_t rows = P.m.rows;
+  // Y into P's slot, then two Cholesky passes update it in place
+  for (int64_t e = threadIdx.x; e < rows * kRank; e += kThreads) P.p[e] = P.y[e];
+  __syncthreads();
+  for (int pass = 0; pass < 2; ++pass) {
+    // G = P^T P: 36 distinct entries, accumulated by every thread in fp64
+    double gacc[kRank][kRank];
+#pragma unroll
+    for (int u = 0; u < kRank; ++u)
+#pragma unroll
+      for (int v = 0; v < kRank; ++v) gacc[u][v] = 0.0;
+    for (int64_t i = threadIdx.x; i < rows; i += kThreads) {
+      double y[kRank];
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) y[l] = P.p[i * kRank + l];
+#pragma unroll
+      for (int u = 0; u < kRank; ++u)
+#pragma unroll
+        for (int v = 0; v <= u; ++v) gacc[u][v] += y[u] * y[v];
+    }
+    for (int u = 0; u < kRank; ++u) block_sum8(gacc[u], red);
+    if (threadIdx.x == 0) {
+      double g[kRank][kRank];
+      for (int u = 0; u < kRank; ++u)
+        for (int v = 0; v < kRank; ++v) g[u][v] = (v <= u) ? gacc[u][v] : 0.0;
+      s_ok = chol8(g) ? 1 : 0;
+      for (int u = 0; u < kRank; ++u)
+        for (int v = 0; v < kRank; ++v) sL[u][v] = g[u][v];
+    }
+    __syncthreads();
+    if (!s_ok) {
+      if (threadIdx.x == 0 && atomicCAS(&hdr->error, 0u, (unsigned)QMUON_ERR_INVALID_ARGUMENT) == 0u)
+        hdr->error_info = 0x2000u + blockIdx.x;   // rank-deficient M_t Q: no orthonormal factor
+      return;
+    }
+    // P <- P L^{-T}: solve L z = y for each row (forward substitution)
+    for (int64_t i = threadIdx.x; i < rows; i += kThreads) {
+      double z[kRank];
+#pragma unroll
+      for (int u = 0; u < kRank; ++u) {
+        double s = P.p[i * kRank + u];
+#pragma unroll
+        for (int v = 0; v < u; ++v) s -= sL[u][v] * z[v];
+        z[u] = s / sL[u][u];
+      }
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) P.p[i * kRank + l] = (float)z[l];
+    }
+    __syncthreads();
+  }
+  quantize_factor(P.p, rows, P.m.p, P.m.p_rmax, P.m.p_cmax);
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: R = M_t^T P, one CTA per 64-column strip of a matrix, walking its
+// rows in chunks of four blocks (256 rows of P staged in shared memory per
+// pair of barriers).  Thread t owns columns 2 (t % 32), 2 (t % 32) + 1 of the
+// strip (one 4-byte load per row) and rows 32 (t / 32) ... of each chunk;
+// per-chunk sums are added with compensation, the 8 row groups in shared
+// memory at the end.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHeader* hdr) {
+  __shared__ __align__(16) float sP[kChunk * kS][kRank];
+  __shared__ float part[kThreads / 32][kS][kRank];
+  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
+  const int pi = find_prob(a.cstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[pi];
+  const int64_t bj = blockIdx.x - __ldg(a.cstrip_start + pi);
+  const int64_t rows = P.m.rows, cols = P.m.cols;
+  const int t = threadIdx.x;
+  const int cp = t & 31, rg = t >> 5;   // column pair, row group (one per warp: sP reads broadcast)
+  const int64_t j = bj * kS + 2 * cp;
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(P.m.grad);
+  float acc[2][kRank], accc[2][kRank];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) acc[h][l] = accc[h][l] = 0.0f;
+  for (int64_t r0 = 0; r0 < rows; r0 += kChunk * kS) {
+    const int nr = (rows - r0) < kChunk * kS ? (int)(rows - r0) : kChunk * kS;
+    __syncthreads();
+    for (int e = t; e < nr * kRank / 4; e += kThreads)
+      reinterpret_cast<float4*>(&sP[0][0])[e] = __ldg(reinterpret_cast<const float4*>(P.p + r0 * kRank) + e);
+    __syncthreads();
+    float ab[2][kRank];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) ab[h][l] = 0.0f;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+      const int li = rg * 32 + r;
+      if (li >= nr) break;
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(g + (r0 + li) * cols + j));
+      const float m0 = __uint_as_float(w << 16), m1 = __uint_as_float(w & 0xFFFF0000u);
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) {
+        ab[0][l] = fmaf(m0, sP[li][l], ab[0][l]);
+        ab[1][l] = fmaf(m1, sP[li][l], ab[1][l]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) comp_add(acc[h][l], accc[h][l], ab[h][l]);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) part[rg][2 * cp + h][l] = acc[h][l] + accc[h][l];
+  __syncthreads();
+  if (t < kS) {
+    float sum[kRank];
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) {
+      float v = part[0][t][l];
+      for (int w = 1; w < kThreads / 32; ++w) v += part[w][t][l];
+      sum[l] = v;
+    }
+    float4* dst = reinterpret_cast<float4*>(P.r + (bj * kS + t) * kRank);
+    dst[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
+    dst[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
+  }
+}
+
+// Quantise R (final from pass 2).  One CTA per matrix.
+__global__ void __launch_bounds__(kThreads) grasp_rfinal(GraspArgs a, const WsHeader* hdr) {
+  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
+  const GraspProb& P = a.probs[blockIdx.x];
+  quantize_factor(P.r, P.m.cols, P.m.r, P.m.r_rmax, P.m.r_cmax);
+}
+
+// ---------------------------------------------------------------------------
+// pass 3: residual M_t - P_t R_t^T and its 4-bit grid codes, one CTA per
+// 64-row x 256-column chunk (four 64 x 64 blocks; thread mapping as in pass
+// 1).  Per block: the row maxima by shuffles over the row's 4 threads, the
+// column maxima by a shuffle over the 8 rows a warp holds and then the 8
+// warps' values in shared memory.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
+  __shared__ __align__(16) float sR[kPadStride];
+  __shared__ float wmax[kThreads / 32][kS];
+  __shared__ float sInvC[kS];
+  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
+  const int pi = find_prob(a.tile_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[pi];
+  const int64_t nchunk = (P.nbc + kChunk - 1) / kChunk;
+  const int64_t local = blockIdx.x - __ldg(a.tile_start + pi);
+  const int64_t bi = local / nchunk, b0 = (local % nchunk) * kChunk;
+  const int nb = (P.nbc - b0) < kChunk ? (int)(P.nbc - b0) : kChunk;
+  const int64_t rows = P.m.rows, cols = P.m.cols;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int ti = t >> 2, tj = (t & 3) * 16;
+  const int64_t i = bi * kS + ti;
+  const bool live = i < rows;
+  // the chunk's M_t values of this thread, in flight while R is staged
+  uint4 g0[kChunk], g1[kChunk];
+  if (live) {
+#pragma unroll
+    for (int c = 0; c < kChunk; ++c) {
+      if (c >= nb) break;
+      const __nv_bfloat16* grow = static_cast<const __nv_bfloat16*>(P.m.grad) + i * cols + (b0 + c) * kS + tj;
+      g0[c] = *reinterpret_cast<const uint4*>(grow);
+      g1[c] = *reinterpret_cast<const uint4*>(grow + 8);
+    }
+  }
+  for (int e = t; e < nb * kS * kRank / 4; e += kThreads)
+    *reinterpret_cast<float4*>(&sR[sidx(e >> 1, (e & 1) * 4)]) =
+        __ldg(reinterpret_cast<const float4*>(P.r + b0 * kS * kRank) + e);
+  float p[kRank];
+  if (live) {
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) p[l] = P.p[i * kRank + l];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kChunk; ++c) {
+    if (c >= nb) break;
+    const int64_t bj = b0 + c;
+    float res[16];
+    float rm = 0.0f;
+    if (live) {
+      const uint32_t gw[8] = {g0[c].x, g0[c].y, g0[c].z, g0[c].w, g1[c].x, g1[c].y, g1[c].z, g1[c].w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float m = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
+        float acc = 0.0f;
+#pragma unroll
+        for (int l = 0; l < kRank; ++l) acc = fmaf(p[l], sR[sidx(c * kS + tj + e, l)], acc);
+        res[e] = m - acc;
+        rm = fmaxf(rm, fabsf(res[e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) res[e] = 0.0f;
+    }
+    // row maximum over the block's 64 columns (the 4 threads of the row)
+    rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, 1));
+    rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, 2));
+    // column maxima: lanes l, l ^ 4, l ^ 8, l ^ 16 hold the same columns of the warp's 8 rows
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float v = fabsf(res[e]);
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      if (lane < 4) wmax[warp][tj + e] = v;
+    }
+    __syncthreads();
+    if (t < kS) {
+      float cm = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) cm = fmaxf(cm, wmax[w][t]);
+      P.m.res_cmax[bi * cols + bj * kS + t] = cm;
+      sInvC[t] = inv_level(cm, 7.0f);
+    }
+    __syncthreads();
+    if (live) {
+      if ((t & 3) == 0) P.m.res_rmax[bj * rows + i] = rm;
+      const float ir = inv_level(rm, 7.0f);
+      uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int q = grid_code(res[e], grid_factor(ir, sInvC[tj + e]), 7);
+        cw[e >> 3] |= (uint32_t)(q + 8) << (4 * (e & 7));
+      }
+      *reinterpret_cast<uint2*>(P.m.res + i * (cols / 2) + (bj * kS + tj) / 2) = make_uint2(cw[0], cw[1]);
+    }
+    __syncthreads();   // wmax and sInvC are rewritten by the next block
+  }
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
+  return 3 * align_up((size_t)m.cols * kRank * 4, 256) + 2 * align_up((size_t)m.rows * kRank * 4, 256);
+}
+
+size_t table_bytes(int32_t n) {
+  return align_up((size_t)n * sizeof(GraspProb), 256) + 3 * align_up((size_t)(n + 1) * 8, 256);
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmuon_status validate(const qmuon_grasp_matrix& m) {
+  if (m.rows <= 0 || m.cols <= 0 || m.rows > (1 << 28) || m.cols > (1 << 28)) return QMUON_ERR_INVALID_ARGUMENT;
+  if (m.cols % kS) return QMUON_ERR_UNSUPPORTED;
+  if (!m.res || !m.res_rmax || !m.res_cmax || !m.p || !m.p_rmax || !m.p_cmax || !m.r || !m.r_rmax || !m.r_cmax ||
+      !m.grad)
+    return QMUON_ERR_INVALID_ARGUMENT;
+  if (!aligned_to(m.res, 8) || !aligned_to(m.p, 8) || !aligned_to(m.r, 8) || !aligned_to(m.grad, 16) ||
+      !aligned_to(m.res_rmax, 4) || !aligned_to(m.res_cmax, 4) || !aligned_to(m.p_rmax, 4) ||
+      !aligned_to(m.p_cmax, 4) || !aligned_to(m.r_rmax, 4) || !aligned_to(m.r_cmax, 4))
+    return QMUON_ERR_INVALID_ARGUMENT;
+  return QMUON_OK;
+}
+
+}  // namespace
+}  // namespace qm
+
+extern "C" size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices, int32_t n) {
+  using namespace qm;
+  if (!matrices || n <= 0) return 0;
+  size_t b = kWsHeader + table_bytes(n);
+  for (int32_t i = 0; i < n; ++i) b += prob_scratch_bytes(matrices[i]);
+  return b;
+}
+
+extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int32_t n, float mu, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  using namespace qm;
+  if (!matrices || n <= 0 || !ws || !aligned_to(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+  for (int32_t i = 0; i < n; ++i) {
+    const qmuon_status s = validate(matrices[i]);
+    if (s != QMUON_OK) return s;
+  }
+  if (ws_bytes < qmuon_grasp_workspace_size(matrices, n)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+  unsigned char* b = static_cast<unsigned char*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(b);
+  unsigned char* table = b + kWsHeader;
+  unsigned char* scratch = table + table_bytes(n);
+  std::vector<GraspProb> hp(n);
+  std::vector<int64_t> ts(n + 1, 0), rs(n + 1, 0), cs(n + 1, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    GraspProb& P = hp[i];
+    std::memset(&P, 0, sizeof(P));
+    P.m = matrices[i];
+    P.nbr = (P.m.rows + kS - 1) / kS;
+    P.nbc = P.m.cols / kS;
+    auto carve = [&](size_t bytes) {
+      float* p = reinterpret_cast<float*>(scratch);
+      scratch += align_up(bytes, 256);
+      return p;
+    };
+    P.q = carve((size_t)P.m.cols * kRank * 4);
+    P.rdeq = carve((size_t)P.m.cols * kRank * 4);
+    P.y = carve((size_t)P.m.rows * kRank * 4);
+    P.p = carve((size_t)P.m.rows * kRank * 4);
+    P.r = carve((size_t)P.m.cols * kRank * 4);
+    ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks
+    rs[i + 1] = rs[i] + P.nbr;
+    cs[i + 1] = cs[i] + P.nbc;
+  }
+  GraspArgs a{};
+  a.probs = reinterpret_cast<const GraspProb*>(table);
+  unsigned char* pre = table + align_up((size_t)n * sizeof(GraspProb), 256);
+  a.tile_start = reinterpret_cast<const int64_t*>(pre);
+  a.rstrip_start = reinterpret_cast<const int64_t*>(pre + align_up((size_t)(n + 1) * 8, 256));
+  a.cstrip_start = reinterpret_cast<const int64_t*>(pre + 2 * align_up((size_t)(n + 1) * 8, 256));
+  a.n = n;
+  a.mu = mu;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(hdr, 0, kWsHeader, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(table, hp.data(), (size_t)n * sizeof(GraspProb), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(a.tile_start), ts.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(a.rstrip_start), rs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(a.cstrip_start), cs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return set_error("qmuon_grasp_step (upload)", e);
+  const int64_t tiles = ts[n];
+  if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
+  grasp_colnorm<<<n, kThreads, 0, s>>>(a);
+  grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
+  grasp_orth<<<n, kThreads, 0, s>>>(a, hdr);
+  grasp_pass2<<<(unsigned)cs[n], kThreads, 0, s>>>(a, hdr);
+  grasp_rfinal<<<n, kThreads, 0, s>>>(a, hdr);
+  grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
+  e = cudaGetLastError();
+  // the pageable host tables are staged by the copies above before they return
+  if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
+  return QMUON_OK;
+}

@@ -1,0 +1,119 @@
+"""GPU parity of the GRASP momentum step (qmuon_grasp_step) against the oracle.
+
+M_t, stored in bf16 over the gradient, is bit-exact: the reconstruction and
+the momentum follow the oracle's operations and order.  The power iteration
+and the residual come from different floating-point paths (fp32 tiles and a
+CholeskyQR2 here, an fp64 QR in the oracle), so the new codes are held to:
+at least 99% identical, none off by more than one level, and a
+reconstruction of M_t as close as the oracle's own.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import memory_reduced_muon_gb300 as q
+from oracle import codec, grasp
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 192), (200, 320), (64, 64), (1000, 128), (1024, 2048)]
+
+
+def _to_dev(st, grad_bits, rows, cols):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    d = dict(res=t(st.res), res_rmax=t(st.res_rmax), res_cmax=t(st.res_cmax), p=t(st.p), p_rmax=t(st.p_rmax),
+             p_cmax=t(st.p_cmax), r=t(st.r), r_rmax=t(st.r_rmax), r_cmax=t(st.r_cmax),
+             grad=torch.from_numpy(grad_bits.astype(np.int16).reshape(rows, cols)).cuda().view(torch.bfloat16))
+    return d
+
+
+def _desc(d, rows, cols):
+    return q.grasp_matrix(rows, cols, d["res"], d["res_rmax"], d["res_cmax"], d["p"], d["p_rmax"], d["p_cmax"],
+                          d["r"], d["r_rmax"], d["r_cmax"], d["grad"])
+
+
+def _from_dev(d):
+    n = lambda k: d[k].cpu().numpy()
+    return grasp.GraspState(res=n("res"), res_rmax=n("res_rmax"), res_cmax=n("res_cmax"), p=n("p"),
+                            p_rmax=n("p_rmax"), p_cmax=n("p_cmax"), r=n("r"), r_rmax=n("r_rmax"),
+                            r_cmax=n("r_cmax"))
+
+
+def _grad(rows, cols, seed):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((rows, cols)).astype(np.float32)
+    x += 3.0 * np.outer(r.standard_normal(rows), r.standard_normal(cols)).astype(np.float32)   # a dominant direction
+    return codec.bf16_bits_from_f32(x.reshape(-1)).reshape(rows, cols)
+
+
+def _codes_close(a, b):
+    a, b = a.astype(np.int32), b.astype(np.int32)
+    assert np.abs(a - b).max() <= 1
+    assert np.mean(a == b) >= 0.99
+
+
+def _run_step(states, grads, mu):
+    devs = [_to_dev(st, g, *g.shape) for st, g in zip(states, grads)]
+    descs = [_desc(d, *g.shape) for d, g in zip(devs, grads)]
+    ws = torch.empty(q.qmuon_grasp_workspace_size(descs), dtype=torch.uint8, device="cuda")
+    q.qmuon_grasp_step(descs, mu, ws)
+    q.qmuon_sync_status(ws)
+    return devs
+
+
+@pytest.mark.parametrize("warm", [False, True])
+def test_grasp_step_matches_oracle(warm):
+    states, grads = [], []
+    for i, (rows, cols) in enumerate(SHAPES):
+        st = grasp.initial_state(rows, cols, np.random.default_rng(50 + i).standard_normal((cols, 8)).astype(np.float32))
+        if warm:   # a state with a non-zero residual and factor: one oracle step first
+            st = grasp.grasp_step(st, _grad(rows, cols, 70 + i), 0.9).state
+        states.append(st)
+        grads.append(_grad(rows, cols, 90 + i))
+    devs = _run_step(states, grads, 0.9)
+    for (rows, cols), st, g, d in zip(SHAPES, states, grads, devs):
+        ref = grasp.grasp_step(st, g, 0.9)
+        got_m = d["grad"].view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(got_m, ref.m_bits)
+        gst = _from_dev(d)
+        _codes_close(gst.p, ref.state.p)
+        _codes_close(gst.r, ref.state.r)
+        _codes_close(grasp.unpack4(gst.res), grasp.unpack4(ref.state.res))
+        # the factors' maxima: Y = M_t Q is fp32 here and fp64 in the oracle, and
+        # the orthogonalisation scales its relative error by the condition
+        # number of M_t Q (large when one direction dominates, as here): 1e-3,
+        # an eighth of one 8-bit level
+        np.testing.assert_allclose(gst.p_rmax, ref.state.p_rmax, rtol=1e-3)
+        np.testing.assert_allclose(gst.r_rmax, ref.state.r_rmax, rtol=1e-3, atol=1e-6 * np.abs(ref.state.r_rmax).max())
+        # the stored state reconstructs M_t as well as the oracle's does
+        mt = codec.f32_from_bf16_bits(ref.m_bits).astype(np.float64)
+        def err(s):
+            res, p, r = grasp.dequantize_parts(s)
+            return np.linalg.norm(res.astype(np.float64) + p.astype(np.float64) @ r.astype(np.float64).T - mt)
+        assert err(gst) <= 1.05 * err(ref.state) + 1e-9 * np.linalg.norm(mt)
+
+
+def test_grasp_three_steps_track_the_oracle():
+    rows, cols = 512, 768
+    st_host = grasp.initial_state(rows, cols, np.random.default_rng(1).standard_normal((cols, 8)).astype(np.float32))
+    st_dev = st_host
+    for t in range(3):
+        g = _grad(rows, cols, 200 + t)
+        d = _run_step([st_dev], [g], 0.95)[0]
+        st_dev = _from_dev(d)
+        ref = grasp.grasp_step(st_host, g, 0.95)
+        st_host = ref.state
+        got = codec.f32_from_bf16_bits(d["grad"].view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+        want = codec.f32_from_bf16_bits(ref.m_bits).astype(np.float64)
+        assert np.linalg.norm(got - want) <= 1e-2 * np.linalg.norm(want), t
+
+
+def test_grasp_rejects_bad_shapes():
+    rows, cols = 64, 100   # cols not a multiple of 64
+    st = grasp.initial_state(rows, cols, np.ones((cols, 8), np.float32))
+    d = _to_dev(st, np.zeros((rows, cols), np.uint16), rows, cols)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(q.QmuonError) as e:
+        q.qmuon_grasp_step([_desc(d, rows, cols)], 0.9, ws)
+    assert e.value.status == q.QMUON_ERR_UNSUPPORTED
