@@ -475,30 +475,41 @@ def run_gpu(args, world, rank, local):
         ns_flop[key] = step_ns_flops(w, full)
         del ws_n
 
-    # e2e: host gradients in pinned memory, copied into the gradient buffers of
-    # one plan every step; the group sums (the step's metric) read back every step
+    # e2e through the host-fed entry: every step copies its gradients in from
+    # page-locked host memory and reads its group sums (the step's metric)
+    # back to host memory.  Two plans over the same state and weights
+    # alternate, so step k+1's copies (on a copy stream) overlap step k's
+    # kernels; the clock stops once the last read-back has landed.
     torch.cuda.synchronize()
-    e2e_steps = max(2, min(args.steps, 5))
+    e2e_steps = max(2, args.steps)
     h2d = sum(g.numel() * g.element_size() for g in grads)
-    ngr = info["n_block_groups"] if w.P != 1 else info["n_full_groups"]
+    ngr = max(info["n_block_groups"], info["n_full_groups"])
+    copy_stream = torch.cuda.Stream(device=dev)
+    sums_host = [torch.zeros(ngr).pin_memory() for _ in range(e2e_steps)]
+    d2h = 0
+    barrier(world)
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         t += 1
-        for g, hsrc in zip(batches[0], host_pool[k % 2]):
-            g.copy_(hsrc, non_blocking=True)
-        q.qmuon_step(plans[0], t, w.P, w.beta, w.eta_full, w.eta_block, weights, w.coeffs, w.iters, sums, ws,
-                     stream=stream)
-        _ = sums.cpu()
+        b = k % 2
+        q.qmuon_step_from_host(plans[b % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights, w.coeffs,
+                               w.iters, host_pool[b], sums_host[k], sums, ws, stream=stream, copy_stream=copy_stream)
+        full_k = w.P != 0 and t % w.P == 0
+        d2h += 4 * (info["n_full_groups"] if full_k else info["n_block_groups"])
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
+    q.qmuon_sync_status(ws, stream)
+    if not all(bool(torch.isfinite(x).all()) for x in sums_host):
+        raise RuntimeError("end-to-end leg: non-finite group sums read back")
     e2e_s = max_over_ranks(e2e_s, world)
     e2e_value = world * n_params * e2e_steps / e2e_s / 1e6
+    d2h //= e2e_steps
 
     # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
     return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
                 upd_sr_ms=upd_sr_ms, grasp_ms=grasp_ms,
-                ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=4 * ngr, n_full=n_full,
+                ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=d2h, n_full=n_full,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
 

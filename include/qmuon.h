@@ -323,6 +323,35 @@ QMUON_API qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor
                                                       qmuon_dtype grad_dtype, float beta, float* sumsq,
                                                       float* inv_norm, void* stream);
 
+/* qmuon_step fed from host memory: the step's gradients are copied in, the
+ * step runs, and its group sums are copied out, all enqueued without
+ * blocking the caller.  The copies into the plan's gradient buffers go on
+ * copy_stream and start once this plan's previous qmuon_step_from_host has
+ * finished with those buffers; the step runs on `stream` once the copies
+ * have landed.  A caller that alternates two plans over the same q8 state
+ * (the same q8/absmax pointers, different gradient buffers) therefore
+ * overlaps step t+1's host->device copies with step t's kernels.  The
+ * arithmetic and device outputs are those of qmuon_step.
+ *   host_grads        H  n_tensors host pointers, each rows x cols bf16 in
+ *                        row-major order (page-locked memory lets the copy
+ *                        run asynchronously; pageable memory makes
+ *                        cudaMemcpyAsync stage it before returning)
+ *   host_group_sumsq  H  [n groups of this step kind] fp32, written when the
+ *                        step completes on `stream`; NULL skips the read-back
+ *   group_sumsq       D  as for qmuon_step (NULL: workspace scratch)
+ *   copy_stream       stream of the host->device copies; NULL = `stream`
+ *                     (no overlap)
+ * Anything else that reads or writes the plan's gradient buffers must be
+ * ordered against these calls by the caller.  Returns
+ * QMUON_ERR_INVALID_ARGUMENT for a NULL host_grads or a NULL entry in it
+ * (for a non-empty tensor). */
+QMUON_API qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
+                                            float eta_full, float eta_block, float* const* weights,
+                                            const float coeffs[3], int32_t iters,
+                                            const void* const* host_grads, float* host_group_sumsq,
+                                            float* group_sumsq, void* ws, size_t ws_bytes, void* stream,
+                                            void* copy_stream);
+
 /* Build, ahead of time, the Newton-Schulz problem tables qmuon_step needs for
  * both step kinds with these weights and this workspace (tensor maps and
  * tile lists; one synchronous upload each).  Optional: qmuon_step builds them

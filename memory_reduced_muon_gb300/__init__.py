@@ -108,6 +108,8 @@ def lib() -> C.CDLL:
         "qmuon_last_error": (C.c_char_p, []),
         "qmuon_update_normalize_noalloc": (i32, [C.POINTER(qmuon_tensor), i32, i32, f32, vp, vp, vp]),
         "qmuon_step_prepare": (i32, [vp, C.POINTER(vp), vp, sz]),
+        "qmuon_step_from_host": (i32, [vp, i64, i32, f32, f32, f32, C.POINTER(vp), C.POINTER(f32), i32,
+                                       C.POINTER(vp), vp, vp, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -124,7 +126,7 @@ def exported_symbols() -> list:
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
             "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
-            "qmuon_grasp_workspace_size", "qmuon_grasp_step"]
+            "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host"]
 
 
 # --------------------------------------------------------------------------
@@ -312,6 +314,22 @@ def qmuon_step(plan: Plan, t: int, P: int, beta: float, eta_full: float, eta_blo
                           int(iters), _ptr(group_sumsq), _ptr(ws),
                           _nbytes(ws) if ws_bytes is None else int(ws_bytes), _stream(stream))
     _check(st, "qmuon_step")
+
+
+def qmuon_step_from_host(plan: Plan, t: int, P: int, beta: float, eta_full: float, eta_block: float, weights,
+                         coeffs, iters: int, host_grads, host_group_sumsq, group_sumsq, ws,
+                         ws_bytes: Optional[int] = None, stream=None, copy_stream=None):
+    """``host_grads``: host tensors (page-locked for overlap) or raw host
+    addresses, one per plan tensor; ``host_group_sumsq``: a host fp32 tensor
+    or None."""
+    wp = (C.c_void_p * max(1, len(weights)))(*[_ptr(w) for w in weights])
+    hp = (C.c_void_p * max(1, len(host_grads)))(*[_ptr(h) for h in host_grads])
+    cf = (C.c_float * 3)(*[float(c) for c in coeffs])
+    st = lib().qmuon_step_from_host(plan.handle, int(t), int(P), float(beta), float(eta_full), float(eta_block), wp,
+                                    cf, int(iters), hp, _ptr(host_group_sumsq), _ptr(group_sumsq), _ptr(ws),
+                                    _nbytes(ws) if ws_bytes is None else int(ws_bytes), _stream(stream),
+                                    _stream(copy_stream))
+    _check(st, "qmuon_step_from_host")
 
 
 def qmuon_update_normalize_noalloc(q8, absmax, grad, rows: int, cols: int, q8_kind, grad_dtype, beta: float,

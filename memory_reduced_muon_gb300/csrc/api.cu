@@ -110,6 +110,10 @@ struct qmuon_plan {
   ns::StepTables* ns_block = nullptr;
   bool sr = false;                    // qmuon_step requantises stochastically (counter step = t)
   uint64_t sr_seed = 0;
+  // qmuon_step_from_host: gradient buffers free again / host copies landed
+  cudaEvent_t grads_free = nullptr;
+  cudaEvent_t grads_copied = nullptr;
+  bool grads_free_recorded = false;
 };
 
 namespace {
@@ -303,6 +307,8 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
 extern "C" void qmuon_plan_destroy(qmuon_plan* plan) {
   if (!plan) return;
   if (plan->d_table) cudaFree(plan->d_table);
+  if (plan->grads_free) cudaEventDestroy(plan->grads_free);
+  if (plan->grads_copied) cudaEventDestroy(plan->grads_copied);
   ns::destroy_step_tables(plan->ns_full);
   ns::destroy_step_tables(plan->ns_block);
   delete plan;
@@ -601,6 +607,51 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
   if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);
   return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+}
+
+extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
+                                             float eta_full, float eta_block, float* const* weights,
+                                             const float coeffs[3], int32_t iters,
+                                             const void* const* host_grads, float* host_group_sumsq,
+                                             float* group_sumsq, void* ws, size_t ws_bytes, void* stream,
+                                             void* copy_stream) {
+  if (!plan || !host_grads) return QMUON_ERR_INVALID_ARGUMENT;
+  if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
+  const int32_t n = (int32_t)plan->tensors.size();
+  for (int32_t i = 0; i < n; ++i)
+    if (plan->tensors[i].rows * plan->tensors[i].cols != 0 && !host_grads[i]) return QMUON_ERR_INVALID_ARGUMENT;
+  qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = copy_stream ? static_cast<cudaStream_t>(copy_stream) : s;
+  cudaError_t e = cudaSuccess;
+  if (!mp->grads_free) e = cudaEventCreateWithFlags(&mp->grads_free, cudaEventDisableTiming);
+  if (e == cudaSuccess && !mp->grads_copied) e = cudaEventCreateWithFlags(&mp->grads_copied, cudaEventDisableTiming);
+  if (e != cudaSuccess) return set_error("qmuon_step_from_host (event create)", e);
+  // the buffers are free once this plan's previous step has finished with them
+  if (cs != s && mp->grads_free_recorded) e = cudaStreamWaitEvent(cs, mp->grads_free, 0);
+  for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
+    const qmuon_tensor& T = plan->tensors[i];
+    const size_t bytes = (size_t)(T.rows * T.cols) * sizeof(uint16_t);
+    if (bytes) e = cudaMemcpyAsync(T.grad, host_grads[i], bytes, cudaMemcpyHostToDevice, cs);
+  }
+  if (e == cudaSuccess && cs != s) {
+    e = cudaEventRecord(mp->grads_copied, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, mp->grads_copied, 0);
+  }
+  if (e != cudaSuccess) return set_error("qmuon_step_from_host (gradient copies)", e);
+  const qmuon_status st = qmuon_step(plan, t, P, beta, eta_full, eta_block, weights, coeffs, iters, group_sumsq,
+                                     ws, ws_bytes, stream);
+  if (st != QMUON_OK) return st;
+  if (host_group_sumsq) {
+    const bool full = (P != 0) && (t % P == 0);
+    const int32_t ng = plan->layout[full ? 1 : 2].n_groups;
+    const float* src = group_sumsq ? group_sumsq : carve(plan, ws, ws_bytes).sumsq;
+    if (ng > 0) e = cudaMemcpyAsync(host_group_sumsq, src, (size_t)ng * sizeof(float), cudaMemcpyDeviceToHost, s);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(mp->grads_free, s);
+  if (e != cudaSuccess) return set_error("qmuon_step_from_host (read-back)", e);
+  mp->grads_free_recorded = true;
+  return QMUON_OK;
 }
 
 extern "C" qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,

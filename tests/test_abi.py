@@ -100,6 +100,9 @@ def test_entries_reject_null_plan_and_bad_args(lib):
     cf = (C.c_float * 3)(3.4445, -4.775, 2.0315)
     w = (C.c_void_p * 1)(FAKE)
     assert L.qmuon_step(None, 1, 5, 0.9, 0.02, 0.01, w, cf, 5, None, FAKE, 1 << 20, None) == INV
+    h = (C.c_void_p * 1)(FAKE)
+    assert L.qmuon_step_from_host(None, 1, 5, 0.9, 0.02, 0.01, w, cf, 5, h, None, None, FAKE, 1 << 20, None,
+                                  None) == INV
     assert L.qmuon_sync_status(None, None) == INV
     assert L.qmuon_sync_status(FAKE + 16, None) == INV   # not 256-byte aligned
 
