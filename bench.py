@@ -487,6 +487,13 @@ def run_gpu(args, world, rank, local):
     copy_stream = torch.cuda.Stream(device=dev)
     sums_host = [torch.zeros(ngr).pin_memory() for _ in range(e2e_steps)]
     d2h = 0
+    # untimed warm-up of the same leg: each plan's first host-fed steps
+    for k in range(max(3, args.warmup)):
+        t += 1
+        q.qmuon_step_from_host(plans[(k % 2) % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights,
+                               w.coeffs, w.iters, host_pool[k % 2], sums_host[0], sums, ws, stream=stream,
+                               copy_stream=copy_stream)
+    torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     for k in range(e2e_steps):

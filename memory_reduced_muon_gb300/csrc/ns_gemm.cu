@@ -50,7 +50,6 @@ constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
 constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // symmetric epilogue staging: half an output tile
-constexpr uint32_t kOutTileBytes = 8 * kBox;         // G_UPDATE: a CTA's 128 x 256 output tile (TMA boxes)
 constexpr uint32_t kUSlotBytes = 2 * kBox;           // G_UPDATE_W: 128 x 64 output columns of one step
 constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 32 fp32 weights (one TMA box)
 
@@ -67,11 +66,10 @@ constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 3
 __host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ? 4 * kBox : kStageBytes; }
 __host__ __device__ constexpr int w_depth_of(int kind) { return kind == 3 ? 2 : 1; }
 __host__ __device__ constexpr int stages_of(int kind, int cg) {
-  return cg == 2 ? (kind == 3 ? 4 : kind == 2 || kind == 4 ? 5 : 6) : (kind >= 3 ? 2 : kind == 2 ? 3 : 4);
+  return cg == 2 ? (kind == 3 ? 4 : kind == 4 ? 5 : 6) : (kind >= 3 ? 2 : 4);
 }
 __host__ __device__ constexpr uint32_t side_bytes_of(int kind, int cg) {
-  return kind >= 3 ? 2 * kUSlotBytes + 2 * w_depth_of(kind) * kWChunkBytes
-                   : kind == 2 ? kOutTileBytes : kStageOutBytes;
+  return kind >= 3 ? 2 * kUSlotBytes + 2 * w_depth_of(kind) * kWChunkBytes : kStageOutBytes;
 }
 __host__ __device__ constexpr size_t smem_bytes_of(int kind, int cg) {
   return (size_t)stages_of(kind, cg) * stage_bytes_of(cg) + side_bytes_of(kind, cg) + 1024 + 256;
@@ -96,6 +94,7 @@ struct alignas(128) NsProb {
   CUtensorMap map_a;      // m x m Gram
   CUtensorMap map_b;      // m x m polynomial
   CUtensorMap map_w;      // fp32 weights (stored orientation, 32 x 128 boxes), when w is set
+  CUtensorMap map_x32[3]; // the X buffers with 32-row boxes: one epilogue warp's stores
   __nv_bfloat16* x[3];
   int64_t x_ld[3];
   __nv_bfloat16* a;
@@ -308,6 +307,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// tcgen05.ld without the wait: several loads in flight, then tmem_wait_ld and
+// tmem_hold on each destination, so no use of the registers moves above the wait.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_hold(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and
@@ -648,12 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
       tc_fence_after();
       ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
-      // the update's staging tile is free again once the previous tile's TMA
-      // store has read it; the vote below is the barrier that publishes this
-      if (KIND == G_UPDATE && ew == 0 && lane == 0 && ti > 0) bulk_wait_read_all();
-      // tcgen05.ld is warp-collective, and the staging barriers need all
-      // epilogue warps: they continue or stop together
-      if (!epilogue_all(ok)) break;
+      // the update's staging is per warp: it is free again once this warp's
+      // stores of the previous tile have read it.  tcgen05.ld is
+      // warp-collective, so a warp continues or stops as one; the other
+      // products stage through shared barriers, and all their epilogue warps
+      // continue or stop together
+      if (KIND == G_UPDATE && lane == 0 && ti > 0) bulk_wait_read_all();
+      if (KIND == G_UPDATE ? !__all_sync(0xffffffffu, ok) : !epilogue_all(ok)) break;
       float s_first = 1.0f;
       if (args.first && P.inv) {
         const float iv = *P.inv;
@@ -662,47 +686,54 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 
       if (KIND == G_UPDATE) {
-        // X <- s3 (B X): each thread owns one output row and writes it into
-        // the staging tile in TMA box layout (128-byte swizzle: box (row/64,
-        // col/64), 16-byte chunk q of row rr at q ^ (rr & 7))
-        const int rl = quarter * 32 + lane;
-        unsigned char* orow = side + (rl >> 6) * 4 * kBox + (rl & 63) * 128;
-        for (int c = 4 * ch; c < 4 * ch + 4; ++c) {   // this warp's 128 columns
-          uint32_t v[32];
-          tmem_ld32(tbase + (uint32_t)(c * 32), v);
-          float out[32];
+        // X <- s3 (B X), warp by warp: this warp's 32 rows (its TMEM lane
+        // quarter) and 128 columns (its half) leave through its own 4 KB of
+        // staging, one 32 x 64 TMA box at a time (128-byte swizzle: 16-byte
+        // chunk q of row r at q ^ (r & 7)), by its own TMA stores.  The four
+        // TMEM loads are in flight together.
+        uint32_t v[4][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
-          unsigned char* bx = orow + (c >> 1) * kBox;
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32_async(tbase + (uint32_t)((4 * ch + cc) * 32), v[cc]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int q = (c & 1) * 4 + t;
-            *reinterpret_cast<uint4*>(bx + ((q ^ (rl & 7)) << 4)) =
-                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
-                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
-          }
-        }
+        for (int cc = 0; cc < 4; ++cc) tmem_hold(v[cc]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
           else mbar_arrive(tempty0 + 8 * acc);
         }
-        // the finished tile leaves by TMA (boxes outside the matrix are
-        // skipped, partial ones are clipped by the tensor map); the storing
-        // thread waits for the read before the next tile's vote
-        fence_proxy_async_smem();
-        named_barrier_epilogue();
-        if (ew == 0 && lane == 0) {
-          const CUtensorMap* md = &P.map_x[args.dst];
-          const uint32_t xs = smem_u32(side);
+        unsigned char* wst = side + ew * 4096;
+        const int y = g.row0 + 32 * quarter;
 #pragma unroll
-          for (int bi = 0; bi < 2; ++bi)
+        for (int b = 0; b < 2; ++b) {
+          if (b == 1) {   // the first box's store has read the staging
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
 #pragma unroll
-            for (int bj = 0; bj < 4; ++bj)
-              if (g.row0 + 64 * bi < g.M_ && g.col0 + 64 * bj < g.N_)
-                tma_store_2d(md, xs + (bi * 4 + bj) * kBox, g.col0 + 64 * bj, g.row0 + 64 * bi);
-          bulk_commit();
+          for (int h = 0; h < 2; ++h) {
+            const int cc = 2 * b + h;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int q = 4 * h + t;
+              const uint32_t* u = v[cc] + 8 * t;
+              *reinterpret_cast<uint4*>(wst + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16(s_first * __uint_as_float(u[0]), s_first * __uint_as_float(u[1])),
+                             pack_bf16(s_first * __uint_as_float(u[2]), s_first * __uint_as_float(u[3])),
+                             pack_bf16(s_first * __uint_as_float(u[4]), s_first * __uint_as_float(u[5])),
+                             pack_bf16(s_first * __uint_as_float(u[6]), s_first * __uint_as_float(u[7])));
+            }
+          }
+          // a box outside the matrix is skipped, a partial one is clipped by
+          // the tensor map
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = g.col0 + 128 * ch + 64 * b;
+            if (y < g.M_ && x < g.N_) tma_store_2d(&P.map_x32[args.dst], smem_u32(wst), x, y);
+            bulk_commit();
+          }
         }
       } else if (WPASS) {
         // X <- s3 (B X) and W <- W - eta * bf16(X), in four steps of 64
@@ -879,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   // ---- teardown: every accumulator read is done, every TMA store has
   // completed and, in a pair, the peer no longer touches this CTA's barriers
   // or shared memory ----
-  if (warp >= 2 && ((warp - 2) & 3) <= 1 && lane == 0) bulk_wait_all();
+  if (warp >= 2 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncwarp();   // lanes that skipped the single-thread roles rejoin before the aligned barrier
   if (CG == 2) cluster_sync_all();
@@ -962,13 +993,14 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-// 2-D bf16 map (rows x cols, row stride ld elements), 64 x 64 boxes, 128-byte swizzle.
-bool encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+// 2-D bf16 map (rows x cols, row stride ld elements), boxes of 64 columns x
+// box_rows rows, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows = 64) {
   EncodeTiledFn fn = encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1071,7 +1103,9 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   P.w = w;
   P.w_ld = w_ld;
   for (int i = 0; i < 3; ++i)
-    if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i])) return false;
+    if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i]) ||
+        !encode_bf16(&P.map_x32[i], P.x[i], rows, cols, P.x_ld[i], 32))
+      return false;
   if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
   if (w && !encode_w(&P.map_w, w, rows, cols, w_ld)) return false;
   count_tiles(rows, cols, P.tiles_n, P.tiles);
