@@ -520,6 +520,45 @@ def run_gpu(args, world, rank, local):
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
 
+def measure_gemm_peaks(n=8192, seconds=2.0):
+    """Dense library GEMM rates on this GPU for context: torch._scaled_mm with
+    E4M3 operands (per-tensor scales, bf16 out) and torch.mm in bf16, each run
+    back to back for about `seconds` and timed with CUDA events."""
+    dev = torch.device("cuda", 0)
+    a = torch.randn(n, n, device=dev)
+    b = torch.randn(n, n, device=dev)
+    out = {"n": n}
+
+    def rate(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        reps = max(3, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return 2.0 * n ** 3 / (e0.elapsed_time(e1) / reps / 1e3) / 1e12
+
+    a16, b16 = a.to(torch.bfloat16), b.to(torch.bfloat16)
+    out["bf16_tflops"] = rate(lambda: torch.mm(a16, b16))
+    try:
+        a8 = a.to(torch.float8_e4m3fn)
+        b8 = b.to(torch.float8_e4m3fn).t().contiguous().t()   # column-major second operand
+        one = torch.ones((), device=dev)
+        out["fp8_e4m3_tflops"] = rate(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                                               out_dtype=torch.bfloat16))
+    except Exception as e:   # an FP8 GEMM this torch build cannot run here
+        out["fp8_e4m3_tflops"] = None
+        out["fp8_error"] = str(e).splitlines()[0][:200]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,7 +569,12 @@ def main():
     ap.add_argument("--row-scale", type=int, default=1,
                     help="divide every matrix's row count, keeping its columns and tiles (profiling captures only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--measure-peaks", action="store_true",
+                    help="time cuBLASLt FP8 (E4M3) and bf16 GEMMs at 8192^3 and print one JSON line, nothing else")
     args = ap.parse_args()
+    if args.measure_peaks:
+        print(json.dumps(measure_gemm_peaks()))
+        return
     world, rank, local = dist_info()
     if world > 1:
         import torch.distributed as dist
