@@ -13,10 +13,12 @@
 // (the orthonormal factor whose triangular factor has a positive diagonal).
 // All matrices of a call share each launch:
 //   grasp_colnorm   per matrix:     Q = ColNorm(dequantised R)
-//   grasp_pass1     per row strip:  reconstruct, momentum, store M_t, Y = M_t Q
-//   grasp_orth      per matrix:     P = CholeskyQR2(Y), quantise P
-//   grasp_pass2     per col strip:  R = M_t^T P
-//   grasp_rfinal    per matrix:     quantise R
+//   grasp_pass1     per row strip:  reconstruct, momentum, store M_t, Y = M_t Q,
+//                                   the strip's share of Y^T Y
+//   grasp_chol      per matrix:     the Gram from the strips' shares, its Cholesky L
+//   grasp_tsolve    per row strip:  rows times L^{-T}; first pass: P1 and its
+//                                   shares of P1^T P1; second pass: P, quantised
+//   grasp_pass2     per col strip:  R = M_t^T P, quantised
 //   grasp_pass3     per tile:       residual, its 4-bit grid codes and maxima
 // A strip (64 rows or 64 columns of one matrix) is one CTA's whole sum, so
 // there are no partial sums and no atomics on results: they are deterministic.
@@ -46,6 +48,9 @@ struct GraspProb {
   float* y;                  // [rows][8]   M_t Q
   float* p;                  // [rows][8]   P_t
   float* r;                  // [cols][8]   R_t
+  double* p1;                // [rows][8]   first CholeskyQR pass: Y L1^{-T}
+  double* gpart;             // [nbr][36]   each row strip's share of the Gram (lower triangle)
+  double* L;                 // [8][8]      Cholesky factor of the current pass
 };
 
 struct GraspArgs {
@@ -149,6 +154,57 @@ __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
   }
 }
 
+// The CTA's share of Z^T Z in fp64 (36 lower-triangle entries, row-major
+// (u, v <= u)): the rows are held by the lanes with `mine` set, every `stride`
+// lanes apart; butterfly sums inside each warp, then the warps in order.
+// Written to out[0..35].  Every thread of the CTA calls it.
+__device__ __forceinline__ void gram_share(const double (&z)[kRank], bool mine, int stride, double (*red)[36],
+                                           double* out) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  int k = 0;
+#pragma unroll
+  for (int u = 0; u < kRank; ++u)
+#pragma unroll
+    for (int v = 0; v <= u; ++v, ++k) {
+      double g = mine ? z[u] * z[v] : 0.0;
+      for (int o = stride; o < 32; o <<= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+      if (l == 0) red[w][k] = g;
+    }
+  __syncthreads();
+  if (threadIdx.x < 36) {
+    double s = 0.0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i][threadIdx.x];
+    out[threadIdx.x] = s;
+  }
+}
+
+// Grid quantisation of one 64-row block of an 8-column factor held in shared
+// memory (x[row][8], rows r0 .. r0 + nvalid - 1 of the factor): codes, per-row
+// maxima and the block's per-column maxima.  Every thread of the CTA calls it.
+__device__ __forceinline__ void quantize_block8(const float (*x)[kRank], int nvalid, int64_t r0, int8_t* q,
+                                                float* rmax, float* cmax_blk) {
+  __shared__ float cm[kRank];
+  if (threadIdx.x < kRank) {
+    float m = 0.0f;
+    for (int r = 0; r < nvalid; ++r) m = fmaxf(m, fabsf(x[r][threadIdx.x]));
+    cm[threadIdx.x] = m;
+    cmax_blk[threadIdx.x] = m;
+  }
+  __syncthreads();
+  if ((int)threadIdx.x < nvalid) {
+    const int r = threadIdx.x;
+    float rm = 0.0f;
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) rm = fmaxf(rm, fabsf(x[r][l]));
+    rmax[r0 + r] = rm;
+    const float ir = inv_level(rm, 127.0f);
+    int8_t c[kRank];
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) c[l] = (int8_t)grid_code(x[r][l], grid_factor(ir, inv_level(cm[l], 127.0f)), 127);
+    *reinterpret_cast<int2*>(q + (r0 + r) * kRank) = *reinterpret_cast<const int2*>(c);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // pass 1: one CTA per 64-row strip of a matrix, walking its column blocks in
 // chunks of four (256 columns: R, Q and the residual's column steps for the
@@ -166,7 +222,7 @@ constexpr int kChunk = 4;   // column blocks per chunk
 constexpr int kPadStride = kChunk * kS * kRank + (kChunk * kS / 16) * 4;
 __device__ __forceinline__ int sidx(int col, int l) { return col * kRank + (col >> 4) * 4 + l; }
 
-__global__ void __launch_bounds__(kThreads) grasp_pass1(GraspArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   __shared__ __align__(16) float sR[kPadStride];
   __shared__ __align__(16) float sQ[kPadStride];
   __shared__ float sStepC[kChunk * kS];   // fl(cmax_j / 7) of the residual
@@ -260,42 +316,12 @@ __global__ void __launch_bounds__(kThreads) grasp_pass1(GraspArgs a) {
     dst[0] = make_float4(y[0], y[1], y[2], y[3]);
     dst[1] = make_float4(y[4], y[5], y[6], y[7]);
   }
-}
-
-// Grid quantisation of an 8-column factor (rows x 8, blocks of 64 rows):
-// codes, per-row maxima and per (row block, column) maxima.  One CTA.
-__device__ void quantize_factor(const float* x, int64_t rows, int8_t* q, float* rmax, float* cmax) {
-  const int64_t nbr = (rows + kS - 1) / kS;
-  for (int64_t b = 0; b < nbr; ++b) {
-    // column maxima of block b: thread (row, column) pairs, then a reduction
-    const int64_t r0 = b * kS;
-    __shared__ float cm[kRank];
-    if (threadIdx.x < kRank) cm[threadIdx.x] = 0.0f;
-    __syncthreads();
-    for (int e = threadIdx.x; e < kS * kRank; e += kThreads) {
-      const int64_t row = r0 + e / kRank;
-      if (row < rows) atomicMax(reinterpret_cast<int*>(&cm[e % kRank]), __float_as_int(fabsf(x[row * kRank + e % kRank])));
-    }
-    __syncthreads();
-    if (threadIdx.x < kRank) cmax[b * kRank + threadIdx.x] = cm[threadIdx.x];
-    for (int e = threadIdx.x; e < kS; e += kThreads) {
-      const int64_t row = r0 + e;
-      if (row >= rows) continue;
-      float v[kRank], rm = 0.0f;
+  // the strip's share of Y^T Y in fp64 (rows held by lanes 0, 4, ..., 28)
+  __shared__ double red[kThreads / 32][36];
+  double yd[kRank];
 #pragma unroll
-      for (int l = 0; l < kRank; ++l) {
-        v[l] = x[row * kRank + l];
-        rm = fmaxf(rm, fabsf(v[l]));
-      }
-      rmax[row] = rm;
-      const float ir = inv_level(rm, 127.0f);
-      int8_t c[kRank];
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) c[l] = (int8_t)grid_code(v[l], grid_factor(ir, inv_level(cm[l], 127.0f)), 127);
-      *reinterpret_cast<int2*>(q + row * kRank) = *reinterpret_cast<const int2*>(c);
-    }
-    __syncthreads();
-  }
+  for (int l = 0; l < kRank; ++l) yd[l] = live ? (double)y[l] : 0.0;
+  gram_share(yd, (t & 3) == 0, 4, red, P.gpart + bi * 36);
 }
 
 // Cholesky of an 8 x 8 SPD matrix (lower factor, in place), one thread.
@@ -316,64 +342,81 @@ __device__ bool chol8(double (&g)[kRank][kRank]) {
 }
 
 // ---------------------------------------------------------------------------
-// Y = sum of the partials; P = CholeskyQR2(Y); quantise P.  One CTA per matrix.
+// CholeskyQR2, in two passes of (grasp_chol, grasp_tsolve).  grasp_chol: the
+// Gram as the sum of the row strips' shares (in strip order), its Cholesky
+// factor L; one CTA per matrix.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) grasp_orth(GraspArgs a, WsHeader* hdr) {
-  __shared__ double red[kThreads / 32 * kRank];
-  __shared__ double sL[kRank][kRank];
-  __shared__ int s_ok;
+__global__ void __launch_bounds__(64) grasp_chol(GraspArgs a, WsHeader* hdr) {
+  __shared__ double sG[36];
+  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
   const GraspProb& P = a.probs[blockIdx.x];
-  const int64_t rows = P.m.rows;
-  // Y into P's slot, then two Cholesky passes update it in place
-  for (int64_t e = threadIdx.x; e < rows * kRank; e += kThreads) P.p[e] = P.y[e];
+  if (threadIdx.x < 36) {
+    double g = 0.0;
+    for (int64_t b = 0; b < P.nbr; ++b) g += P.gpart[b * 36 + threadIdx.x];
+    sG[threadIdx.x] = g;
+  }
   __syncthreads();
-  for (int pass = 0; pass < 2; ++pass) {
-    // G = P^T P: 36 distinct entries, accumulated by every thread in fp64
-    double gacc[kRank][kRank];
-#pragma unroll
+  if (threadIdx.x == 0) {
+    double g[kRank][kRank];
+    int k = 0;
     for (int u = 0; u < kRank; ++u)
-#pragma unroll
-      for (int v = 0; v < kRank; ++v) gacc[u][v] = 0.0;
-    for (int64_t i = threadIdx.x; i < rows; i += kThreads) {
-      double y[kRank];
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) y[l] = P.p[i * kRank + l];
-#pragma unroll
-      for (int u = 0; u < kRank; ++u)
-#pragma unroll
-        for (int v = 0; v <= u; ++v) gacc[u][v] += y[u] * y[v];
-    }
-    for (int u = 0; u < kRank; ++u) block_sum8(gacc[u], red);
-    if (threadIdx.x == 0) {
-      double g[kRank][kRank];
-      for (int u = 0; u < kRank; ++u)
-        for (int v = 0; v < kRank; ++v) g[u][v] = (v <= u) ? gacc[u][v] : 0.0;
-      s_ok = chol8(g) ? 1 : 0;
-      for (int u = 0; u < kRank; ++u)
-        for (int v = 0; v < kRank; ++v) sL[u][v] = g[u][v];
-    }
-    __syncthreads();
-    if (!s_ok) {
-      if (threadIdx.x == 0 && atomicCAS(&hdr->error, 0u, (unsigned)QMUON_ERR_INVALID_ARGUMENT) == 0u)
-        hdr->error_info = 0x2000u + blockIdx.x;   // rank-deficient M_t Q: no orthonormal factor
+      for (int v = 0; v < kRank; ++v) g[u][v] = (v <= u) ? sG[k++] : 0.0;
+    if (!chol8(g)) {
+      // rank-deficient M_t Q: no orthonormal factor
+      if (atomicCAS(&hdr->error, 0u, (unsigned)QMUON_ERR_INVALID_ARGUMENT) == 0u) hdr->error_info = 0x2000u + blockIdx.x;
       return;
     }
-    // P <- P L^{-T}: solve L z = y for each row (forward substitution)
-    for (int64_t i = threadIdx.x; i < rows; i += kThreads) {
-      double z[kRank];
+    for (int u = 0; u < kRank; ++u)
+      for (int v = 0; v < kRank; ++v) P.L[u * kRank + v] = g[u][v];
+  }
+}
+
+// grasp_tsolve: one CTA per 64-row strip, one thread per row: z = L^{-1} x by
+// forward substitution in fp64 (x the row of Y on the first pass, of P1 on the
+// second).  First pass: z is P1's row, and the strip's share of P1^T P1 goes to
+// the Gram shares.  Second pass: z rounded to fp32 is P's row, and the strip
+// (one 64-row block of P) is grid-quantised.
+template <int PASS>
+__global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* hdr) {
+  __shared__ double sL[kRank][kRank];
+  __shared__ double red[2][36];
+  __shared__ float sx[kS][kRank];
+  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
+  const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[pi];
+  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
+  const int64_t rows = P.m.rows;
+  sL[threadIdx.x >> 3][threadIdx.x & 7] = P.L[threadIdx.x];
+  __syncthreads();
+  const int64_t i = bi * kS + threadIdx.x;
+  const bool live = i < rows;
+  double z[kRank];
 #pragma unroll
-      for (int u = 0; u < kRank; ++u) {
-        double s = P.p[i * kRank + u];
+  for (int u = 0; u < kRank; ++u) {
+    double s = 0.0;
+    if (live) s = (PASS == 0) ? (double)P.y[i * kRank + u] : P.p1[i * kRank + u];
 #pragma unroll
-        for (int v = 0; v < u; ++v) s -= sL[u][v] * z[v];
-        z[u] = s / sL[u][u];
+    for (int v = 0; v < u; ++v) s -= sL[u][v] * z[v];
+    z[u] = live ? s / sL[u][u] : 0.0;
+  }
+  if (PASS == 0) {
+    if (live)
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) P.p1[i * kRank + l] = z[l];
+    gram_share(z, live, 1, red, P.gpart + bi * 36);
+  } else {
+    const int nvalid = (rows - bi * kS) < kS ? (int)(rows - bi * kS) : kS;
+    if (live) {
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) {
+        const float v = (float)z[l];
+        P.p[i * kRank + l] = v;
+        sx[threadIdx.x][l] = v;
       }
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) P.p[i * kRank + l] = (float)z[l];
     }
     __syncthreads();
+    quantize_block8(sx, nvalid, bi * kS, P.m.p, P.m.p_rmax, P.m.p_cmax + bi * kRank);
   }
-  quantize_factor(P.p, rows, P.m.p, P.m.p_rmax, P.m.p_cmax);
 }
 
 // ---------------------------------------------------------------------------
@@ -412,12 +455,18 @@ __global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHea
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int l = 0; l < kRank; ++l) ab[h][l] = 0.0f;
-#pragma unroll 8
+    // this thread's 32 rows of the chunk: every load in flight, then the sums
+    uint32_t wv[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const int li = rg * 32 + r;
+      wv[r] = (li < nr) ? __ldg(reinterpret_cast<const uint32_t*>(g + (r0 + li) * cols + j)) : 0u;
+    }
+#pragma unroll
     for (int r = 0; r < 32; ++r) {
       const int li = rg * 32 + r;
       if (li >= nr) break;
-      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(g + (r0 + li) * cols + j));
-      const float m0 = __uint_as_float(w << 16), m1 = __uint_as_float(w & 0xFFFF0000u);
+      const float m0 = __uint_as_float(wv[r] << 16), m1 = __uint_as_float(wv[r] & 0xFFFF0000u);
 #pragma unroll
       for (int l = 0; l < kRank; ++l) {
         ab[0][l] = fmaf(m0, sP[li][l], ab[0][l]);
@@ -434,6 +483,7 @@ __global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHea
 #pragma unroll
     for (int l = 0; l < kRank; ++l) part[rg][2 * cp + h][l] = acc[h][l] + accc[h][l];
   __syncthreads();
+  __shared__ float sx[kS][kRank];
   if (t < kS) {
     float sum[kRank];
 #pragma unroll
@@ -441,18 +491,15 @@ __global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHea
       float v = part[0][t][l];
       for (int w = 1; w < kThreads / 32; ++w) v += part[w][t][l];
       sum[l] = v;
+      sx[t][l] = v;
     }
     float4* dst = reinterpret_cast<float4*>(P.r + (bj * kS + t) * kRank);
     dst[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
     dst[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
   }
-}
-
-// Quantise R (final from pass 2).  One CTA per matrix.
-__global__ void __launch_bounds__(kThreads) grasp_rfinal(GraspArgs a, const WsHeader* hdr) {
-  if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
-  const GraspProb& P = a.probs[blockIdx.x];
-  quantize_factor(P.r, P.m.cols, P.m.r, P.m.r_rmax, P.m.r_cmax);
+  __syncthreads();
+  // the strip is one 64-row block of R: its grid quantisation
+  quantize_block8(sx, kS, bj * kS, P.m.r, P.m.r_rmax, P.m.r_cmax + bj * kRank);
 }
 
 // ---------------------------------------------------------------------------
@@ -558,7 +605,9 @@ __global__ void __launch_bounds__(kThreads) grasp_pass3(GraspArgs a, const WsHea
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
-  return 3 * align_up((size_t)m.cols * kRank * 4, 256) + 2 * align_up((size_t)m.rows * kRank * 4, 256);
+  const size_t nbr = (size_t)(m.rows + kS - 1) / kS;
+  return 3 * align_up((size_t)m.cols * kRank * 4, 256) + 2 * align_up((size_t)m.rows * kRank * 4, 256) +
+         align_up((size_t)m.rows * kRank * 8, 256) + align_up(nbr * 36 * 8, 256) + align_up(kRank * kRank * 8, 256);
 }
 
 size_t table_bytes(int32_t n) {
@@ -622,6 +671,9 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     P.y = carve((size_t)P.m.rows * kRank * 4);
     P.p = carve((size_t)P.m.rows * kRank * 4);
     P.r = carve((size_t)P.m.cols * kRank * 4);
+    P.p1 = reinterpret_cast<double*>(carve((size_t)P.m.rows * kRank * 8));
+    P.gpart = reinterpret_cast<double*>(carve((size_t)P.nbr * 36 * 8));
+    P.L = reinterpret_cast<double*>(carve(kRank * kRank * 8));
     ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks
     rs[i + 1] = rs[i] + P.nbr;
     cs[i + 1] = cs[i] + P.nbc;
@@ -649,9 +701,11 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
   if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
   grasp_colnorm<<<n, kThreads, 0, s>>>(a);
   grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
-  grasp_orth<<<n, kThreads, 0, s>>>(a, hdr);
+  grasp_chol<<<n, 64, 0, s>>>(a, hdr);
+  grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
+  grasp_chol<<<n, 64, 0, s>>>(a, hdr);
+  grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
   grasp_pass2<<<(unsigned)cs[n], kThreads, 0, s>>>(a, hdr);
-  grasp_rfinal<<<n, kThreads, 0, s>>>(a, hdr);
   grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
   e = cudaGetLastError();
   // the pageable host tables are staged by the copies above before they return
