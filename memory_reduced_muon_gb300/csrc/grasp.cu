@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHea
 // column maxima by a shuffle over the 8 rows a warp holds and then the 8
 // warps' values in shared memory.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
+__global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
   __shared__ __align__(16) float sR[kPadStride];
   __shared__ float wmax[kThreads / 32][kS];
   __shared__ float sInvC[kS];
