@@ -12,8 +12,9 @@
 // the power iteration accumulates in fp32, and orth is CholeskyQR2 in fp64
 // (the orthonormal factor whose triangular factor has a positive diagonal).
 // All matrices of a call share each launch:
-//   grasp_colnorm   per matrix:     Q = ColNorm(dequantised R)
-//   grasp_pass1     per row strip:  reconstruct, momentum, store M_t, Y = M_t Q,
+//   grasp_colnorm   per matrix:     dequantised R and its column norms
+//   grasp_pass1     per row strip:  reconstruct, momentum, store M_t,
+//                                   Y = M_t Q = (M_t R_{t-1}) diag(1 / norms),
 //                                   the strip's share of Y^T Y
 //   grasp_chol      per matrix:     the Gram from the strips' shares, its Cholesky L
 //   grasp_tsolve    per row strip:  rows times L^{-T}; first pass: P1 and its
@@ -43,7 +44,7 @@ constexpr int kThreads = 256;
 struct GraspProb {
   qmuon_grasp_matrix m;
   int64_t nbr, nbc;          // row / column blocks
-  float* q;                  // [cols][8]   ColNorm(R_{t-1})
+  double* qinv;              // [8]         1 / (column norms of R_{t-1}): Q = R_{t-1} diag(qinv)
   float* rdeq;               // [cols][8]   R_{t-1} dequantised
   float* y;                  // [rows][8]   M_t Q
   float* p;                  // [rows][8]   P_t
@@ -126,7 +127,7 @@ __device__ __forceinline__ void factor_row(const int8_t* q, const float* rmax, c
 }
 
 // ---------------------------------------------------------------------------
-// Q = ColNorm(R_{t-1}), one CTA per matrix
+// R_{t-1} dequantised and the inverse norms of its columns, one CTA per matrix
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
   __shared__ double red[kThreads / 32 * kRank];
@@ -140,17 +141,12 @@ __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
     for (int l = 0; l < kRank; ++l) ss[l] += (double)r[l] * (double)r[l];
   }
   block_sum8(ss, red);
-  double inv[kRank];
-#pragma unroll
-  for (int l = 0; l < kRank; ++l) inv[l] = ss[l] > 0.0 ? 1.0 / sqrt(ss[l]) : 0.0;
+  if (threadIdx.x < kRank) P.qinv[threadIdx.x] = ss[threadIdx.x] > 0.0 ? 1.0 / sqrt(ss[threadIdx.x]) : 0.0;
   for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
     float r[kRank];
     factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
 #pragma unroll
-    for (int l = 0; l < kRank; ++l) {
-      P.q[j * kRank + l] = (float)((double)r[l] * inv[l]);
-      P.rdeq[j * kRank + l] = r[l];
-    }
+    for (int l = 0; l < kRank; ++l) P.rdeq[j * kRank + l] = r[l];
   }
 }
 
@@ -207,7 +203,7 @@ __device__ __forceinline__ void quantize_block8(const float (*x)[kRank], int nva
 
 // ---------------------------------------------------------------------------
 // pass 1: one CTA per 64-row strip of a matrix, walking its column blocks in
-// chunks of four (256 columns: R, Q and the residual's column steps for the
+// chunks of four (256 columns: R and the residual's column steps for the
 // chunk are staged in shared memory by all threads between two barriers).
 // Thread t owns row t/4 of the strip and 16 consecutive columns (t % 4) * 16
 // of each block, and loads its four blocks' codes and gradient up front; Y
@@ -224,7 +220,6 @@ __device__ __forceinline__ int sidx(int col, int l) { return col * kRank + (col 
 
 __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   __shared__ __align__(16) float sR[kPadStride];
-  __shared__ __align__(16) float sQ[kPadStride];
   __shared__ float sStepC[kChunk * kS];   // fl(cmax_j / 7) of the residual
   const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
   const GraspProb& P = a.probs[pi];
@@ -259,11 +254,10 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
     {
       const int64_t j0 = b0 * kS;
       const int ncol = nb * kS;
-      // half a row of R and of Q (a float4 each) per thread per pass
+      // half a row of R (a float4) per thread per pass
       for (int e = t; e < ncol * kRank / 4; e += kThreads) {
         const int col = e >> 1, h = (e & 1) * 4;
         *reinterpret_cast<float4*>(&sR[sidx(col, h)]) = __ldg(reinterpret_cast<const float4*>(P.rdeq + j0 * kRank) + e);
-        *reinterpret_cast<float4*>(&sQ[sidx(col, h)]) = __ldg(reinterpret_cast<const float4*>(P.q + j0 * kRank) + e);
       }
       if (t < ncol) sStepC[t] = __fdiv_rn(__ldg(P.m.res_cmax + bi * cols + j0 + t), 7.0f);
     }
@@ -283,9 +277,12 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
       for (int e = 0; e < 16; ++e) {
         const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
         const float res = __fmul_rn((float)nib, fminf(step_r, sStepC[cb + e]));
+        float rr[kRank];
+        *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&sR[sidx(cb + e, 0)]);
+        *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&sR[sidx(cb + e, 4)]);
         float acc = 0.0f;
 #pragma unroll
-        for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], sR[sidx(cb + e, l)]));
+        for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], rr[l]));
         const float mprev = __fadd_rn(res, acc);
         const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
         const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
@@ -294,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
         if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
         else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
 #pragma unroll
-        for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, sQ[sidx(cb + e, l)], yb[l]);
+        for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, rr[l], yb[l]);
       }
 #pragma unroll
       for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
@@ -305,11 +302,13 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   }
 #pragma unroll
   for (int l = 0; l < kRank; ++l) y[l] += yc[l];
-  // the 4 threads of a row add their sums (fixed order), one stores the row of Y
+  // the 4 threads of a row add their sums of M_t R_{t-1} (fixed order); the
+  // column scaling of Q is applied once, in fp64
 #pragma unroll
   for (int l = 0; l < kRank; ++l) {
     y[l] += __shfl_xor_sync(0xffffffffu, y[l], 1);
     y[l] += __shfl_xor_sync(0xffffffffu, y[l], 2);
+    y[l] = (float)((double)y[l] * P.qinv[l]);
   }
   if ((t & 3) == 0 && live) {
     float4* dst = reinterpret_cast<float4*>(P.y + i * kRank);
@@ -504,13 +503,20 @@ __global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHea
 
 // ---------------------------------------------------------------------------
 // pass 3: residual M_t - P_t R_t^T and its 4-bit grid codes, one CTA per
-// 64-row x 256-column chunk (four 64 x 64 blocks; thread mapping as in pass
-// 1).  Per block: the row maxima by shuffles over the row's 4 threads, the
-// column maxima by a shuffle over the 8 rows a warp holds and then the 8
+// 64-row x 256-column chunk (four 64 x 64 blocks).  Thread t owns rows
+// 2 (t / 8), 2 (t / 8) + 1 of the chunk and the 8 consecutive columns 8 (t % 8)
+// of each block, so each column's R row read from shared memory serves two
+// rows.  Per block: the row maxima by shuffles over the row's 8 threads, the
+// column maxima by a shuffle over the 4 row pairs a warp holds and then the 8
 // warps' values in shared memory.
 // ---------------------------------------------------------------------------
+// Shared rows of 8 floats for the chunk's 256 columns, padded so that the
+// eight columns a warp reads at once (8 apart) fall in different banks.
+constexpr int kPadStride8 = kChunk * kS * kRank + (kChunk * kS / 8) * 4;
+__device__ __forceinline__ int sidx8(int col, int l) { return col * kRank + (col >> 3) * 4 + l; }
+
 __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
-  __shared__ __align__(16) float sR[kPadStride];
+  __shared__ __align__(16) float sR[kPadStride8];
   __shared__ float wmax[kThreads / 32][kS];
   __shared__ float sInvC[kS];
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
@@ -522,61 +528,73 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const Ws
   const int nb = (P.nbc - b0) < kChunk ? (int)(P.nbc - b0) : kChunk;
   const int64_t rows = P.m.rows, cols = P.m.cols;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int ti = t >> 2, tj = (t & 3) * 16;
-  const int64_t i = bi * kS + ti;
-  const bool live = i < rows;
+  const int rp = t >> 3, cg = t & 7;
+  const int64_t i0 = bi * kS + 2 * rp;
+  const bool live[2] = {i0 < rows, i0 + 1 < rows};
   // the chunk's M_t values of this thread, in flight while R is staged
-  uint4 g0[kChunk], g1[kChunk];
-  if (live) {
+  uint4 gv[kChunk][2];
 #pragma unroll
-    for (int c = 0; c < kChunk; ++c) {
-      if (c >= nb) break;
-      const __nv_bfloat16* grow = static_cast<const __nv_bfloat16*>(P.m.grad) + i * cols + (b0 + c) * kS + tj;
-      g0[c] = *reinterpret_cast<const uint4*>(grow);
-      g1[c] = *reinterpret_cast<const uint4*>(grow + 8);
-    }
+  for (int c = 0; c < kChunk; ++c) {
+    if (c >= nb) break;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (live[h])
+        gv[c][h] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.m.grad) + (i0 + h) * cols +
+                                                   (b0 + c) * kS + 8 * cg);
   }
   for (int e = t; e < nb * kS * kRank / 4; e += kThreads)
-    *reinterpret_cast<float4*>(&sR[sidx(e >> 1, (e & 1) * 4)]) =
+    *reinterpret_cast<float4*>(&sR[sidx8(e >> 1, (e & 1) * 4)]) =
         __ldg(reinterpret_cast<const float4*>(P.r + b0 * kS * kRank) + e);
-  float p[kRank];
-  if (live) {
+  float p[2][kRank];
 #pragma unroll
-    for (int l = 0; l < kRank; ++l) p[l] = P.p[i * kRank + l];
-  }
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int l = 0; l < kRank; ++l) p[h][l] = live[h] ? P.p[(i0 + h) * kRank + l] : 0.0f;
   __syncthreads();
 #pragma unroll
   for (int c = 0; c < kChunk; ++c) {
     if (c >= nb) break;
     const int64_t bj = b0 + c;
-    float res[16];
-    float rm = 0.0f;
-    if (live) {
-      const uint32_t gw[8] = {g0[c].x, g0[c].y, g0[c].z, g0[c].w, g1[c].x, g1[c].y, g1[c].z, g1[c].w};
+    float res[2][8];
+    float rm[2] = {0.0f, 0.0f};
+    float cmx[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float m = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
-        float acc = 0.0f;
+    for (int k = 0; k < 8; ++k) {
+      const int cb = c * kS + 8 * cg + k;
+      float rr[kRank];
+      *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 0)]);
+      *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 4)]);
+      cmx[k] = 0.0f;
 #pragma unroll
-        for (int l = 0; l < kRank; ++l) acc = fmaf(p[l], sR[sidx(c * kS + tj + e, l)], acc);
-        res[e] = m - acc;
-        rm = fmaxf(rm, fabsf(res[e]));
+      for (int h = 0; h < 2; ++h) {
+        float v = 0.0f;
+        if (live[h]) {
+          const uint32_t w = (k >> 1) == 0 ? gv[c][h].x : (k >> 1) == 1 ? gv[c][h].y : (k >> 1) == 2 ? gv[c][h].z : gv[c][h].w;
+          const float m = __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
+          float acc = 0.0f;
+#pragma unroll
+          for (int l = 0; l < kRank; ++l) acc = fmaf(p[h][l], rr[l], acc);
+          v = m - acc;
+        }
+        res[h][k] = v;
+        rm[h] = fmaxf(rm[h], fabsf(v));
+        cmx[k] = fmaxf(cmx[k], fabsf(v));
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) res[e] = 0.0f;
     }
-    // row maximum over the block's 64 columns (the 4 threads of the row)
-    rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, 1));
-    rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, 2));
-    // column maxima: lanes l, l ^ 4, l ^ 8, l ^ 16 hold the same columns of the warp's 8 rows
+    // row maxima over the block's 64 columns (the 8 threads of a row pair)
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float v = fabsf(res[e]);
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    for (int h = 0; h < 2; ++h) {
+      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 1));
+      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 2));
+      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 4));
+    }
+    // column maxima: lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same columns of the warp's 8 rows
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float v = cmx[k];
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      if (lane < 4) wmax[warp][tj + e] = v;
+      if (lane < 8) wmax[warp][8 * cg + k] = v;
     }
     __syncthreads();
     if (t < kS) {
@@ -587,16 +605,19 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const Ws
       sInvC[t] = inv_level(cm, 7.0f);
     }
     __syncthreads();
-    if (live) {
-      if ((t & 3) == 0) P.m.res_rmax[bj * rows + i] = rm;
-      const float ir = inv_level(rm, 7.0f);
-      uint32_t cw[2] = {0u, 0u};
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int q = grid_code(res[e], grid_factor(ir, sInvC[tj + e]), 7);
-        cw[e >> 3] |= (uint32_t)(q + 8) << (4 * (e & 7));
+    for (int h = 0; h < 2; ++h) {
+      if (!live[h]) continue;
+      const int64_t i = i0 + h;
+      if (cg == 0) P.m.res_rmax[bj * rows + i] = rm[h];
+      const float ir = inv_level(rm[h], 7.0f);
+      uint32_t cw = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int q = grid_code(res[h][k], grid_factor(ir, sInvC[8 * cg + k]), 7);
+        cw |= (uint32_t)(q + 8) << (4 * k);
       }
-      *reinterpret_cast<uint2*>(P.m.res + i * (cols / 2) + (bj * kS + tj) / 2) = make_uint2(cw[0], cw[1]);
+      *reinterpret_cast<uint32_t*>(P.m.res + i * (cols / 2) + (bj * kS + 8 * cg) / 2) = cw;
     }
     __syncthreads();   // wmax and sInvC are rewritten by the next block
   }
@@ -606,7 +627,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
   const size_t nbr = (size_t)(m.rows + kS - 1) / kS;
-  return 3 * align_up((size_t)m.cols * kRank * 4, 256) + 2 * align_up((size_t)m.rows * kRank * 4, 256) +
+  return 2 * align_up((size_t)m.cols * kRank * 4, 256) + align_up(kRank * 8, 256) +
+         2 * align_up((size_t)m.rows * kRank * 4, 256) +
          align_up((size_t)m.rows * kRank * 8, 256) + align_up(nbr * 36 * 8, 256) + align_up(kRank * kRank * 8, 256);
 }
 
@@ -666,7 +688,7 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
       scratch += align_up(bytes, 256);
       return p;
     };
-    P.q = carve((size_t)P.m.cols * kRank * 4);
+    P.qinv = reinterpret_cast<double*>(carve(kRank * 8));
     P.rdeq = carve((size_t)P.m.cols * kRank * 4);
     P.y = carve((size_t)P.m.rows * kRank * 4);
     P.p = carve((size_t)P.m.rows * kRank * 4);
