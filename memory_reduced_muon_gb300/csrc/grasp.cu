@@ -420,63 +420,101 @@ __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* 
 
 // ---------------------------------------------------------------------------
 // pass 2: R = M_t^T P, one CTA per 64-column strip of a matrix, walking its
-// rows in chunks of four blocks (256 rows of P staged in shared memory per
-// pair of barriers).  Thread t owns columns 2 (t % 32), 2 (t % 32) + 1 of the
-// strip (one 4-byte load per row) and rows 32 (t / 32) ... of each chunk;
-// per-chunk sums are added with compensation, the 8 row groups in shared
-// memory at the end.
+// rows in chunks of 128.  Each chunk's M_t values (128 rows x 64 columns) and
+// P rows arrive in shared memory by 16-byte asynchronous copies through a ring
+// of kP2Stages stages, kP2Stages - 1 chunks ahead of the sums.  Thread t owns
+// columns 2 (t % 32), 2 (t % 32) + 1 of the strip and rows 16 (t / 32) ... of
+// each chunk; per-chunk sums are added with compensation, the 8 row groups in
+// shared memory at the end, and the strip (one 64-row block of R) is
+// grid-quantised.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) grasp_pass2(GraspArgs a, const WsHeader* hdr) {
-  __shared__ __align__(16) float sP[kChunk * kS][kRank];
-  __shared__ float part[kThreads / 32][kS][kRank];
+constexpr int kP2Rows = 128;
+constexpr int kP2Stages = 4;
+constexpr int kP2StageBytes = kP2Rows * kS * 2 + kP2Rows * kRank * 4;   // M_t chunk + P rows
+constexpr int kP2Smem = kP2Stages * kP2StageBytes + (kThreads / 32) * kS * kRank * 4;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const WsHeader* hdr) {
+  extern __shared__ __align__(16) unsigned char p2smem[];
+  float (*part)[kS][kRank] = reinterpret_cast<float (*)[kS][kRank]>(p2smem + kP2Stages * kP2StageBytes);
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
   const int pi = find_prob(a.cstrip_start, a.n, blockIdx.x);
   const GraspProb& P = a.probs[pi];
   const int64_t bj = blockIdx.x - __ldg(a.cstrip_start + pi);
   const int64_t rows = P.m.rows, cols = P.m.cols;
   const int t = threadIdx.x;
-  const int cp = t & 31, rg = t >> 5;   // column pair, row group (one per warp: sP reads broadcast)
-  const int64_t j = bj * kS + 2 * cp;
+  const int cp = t & 31, rg = t >> 5;   // column pair, row group (one per warp: P reads broadcast)
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(P.m.grad);
+  const int64_t nch = (rows + kP2Rows - 1) / kP2Rows;
+  // chunk c into stage c % kP2Stages: rows past the matrix are zero-filled
+  auto load = [&](int64_t c) {
+    unsigned char* st = p2smem + (c % kP2Stages) * kP2StageBytes;
+    const int64_t r0 = c * kP2Rows;
+#pragma unroll
+    for (int k = 0; k < kP2Rows * kS * 2 / 16 / kThreads; ++k) {
+      const int e = t + k * kThreads;
+      const int row = e >> 3, seg = e & 7;
+      const bool ok = r0 + row < rows;
+      cp_async16(st + row * (kS * 2) + seg * 16, g + (ok ? (r0 + row) * cols : 0) + bj * kS + seg * 8, ok);
+    }
+    {
+      const int row = t >> 1, half = t & 1;
+      const bool ok = r0 + row < rows;
+      cp_async16(st + kP2Rows * kS * 2 + row * (kRank * 4) + half * 16, P.p + (ok ? (r0 + row) * kRank : 0) + half * 4,
+                 ok);
+    }
+  };
+#pragma unroll
+  for (int c = 0; c < kP2Stages - 1; ++c) {
+    if (c < nch) load(c);
+    cp_async_commit();
+  }
   float acc[2][kRank], accc[2][kRank];
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
     for (int l = 0; l < kRank; ++l) acc[h][l] = accc[h][l] = 0.0f;
-  for (int64_t r0 = 0; r0 < rows; r0 += kChunk * kS) {
-    const int nr = (rows - r0) < kChunk * kS ? (int)(rows - r0) : kChunk * kS;
-    __syncthreads();
-    for (int e = t; e < nr * kRank / 4; e += kThreads)
-      reinterpret_cast<float4*>(&sP[0][0])[e] = __ldg(reinterpret_cast<const float4*>(P.p + r0 * kRank) + e);
-    __syncthreads();
+  for (int64_t c = 0; c < nch; ++c) {
+    if (c + kP2Stages - 1 < nch) load(c + kP2Stages - 1);
+    cp_async_commit();
+    cp_async_wait<kP2Stages - 1>();   // chunk c has landed (this thread's copies)
+    __syncthreads();                  // ... and every thread's
+    const unsigned char* st = p2smem + (c % kP2Stages) * kP2StageBytes;
+    const uint32_t* sm = reinterpret_cast<const uint32_t*>(st);
+    const float (*sp)[kRank] = reinterpret_cast<const float (*)[kRank]>(st + kP2Rows * kS * 2);
     float ab[2][kRank];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int l = 0; l < kRank; ++l) ab[h][l] = 0.0f;
-    // this thread's 32 rows of the chunk: every load in flight, then the sums
-    uint32_t wv[32];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int li = rg * 32 + r;
-      wv[r] = (li < nr) ? __ldg(reinterpret_cast<const uint32_t*>(g + (r0 + li) * cols + j)) : 0u;
-    }
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const int li = rg * 32 + r;
-      if (li >= nr) break;
-      const float m0 = __uint_as_float(wv[r] << 16), m1 = __uint_as_float(wv[r] & 0xFFFF0000u);
+    for (int r = 0; r < kP2Rows / (kThreads / 32); ++r) {
+      const int li = rg * (kP2Rows / (kThreads / 32)) + r;
+      const uint32_t w = sm[li * (kS / 2) + cp];
+      const float m0 = __uint_as_float(w << 16), m1 = __uint_as_float(w & 0xFFFF0000u);
+      float pr[kRank];
+      *reinterpret_cast<float4*>(pr) = *reinterpret_cast<const float4*>(&sp[li][0]);
+      *reinterpret_cast<float4*>(pr + 4) = *reinterpret_cast<const float4*>(&sp[li][4]);
 #pragma unroll
       for (int l = 0; l < kRank; ++l) {
-        ab[0][l] = fmaf(m0, sP[li][l], ab[0][l]);
-        ab[1][l] = fmaf(m1, sP[li][l], ab[1][l]);
+        ab[0][l] = fmaf(m0, pr[l], ab[0][l]);
+        ab[1][l] = fmaf(m1, pr[l], ab[1][l]);
       }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int l = 0; l < kRank; ++l) comp_add(acc[h][l], accc[h][l], ab[h][l]);
+    __syncthreads();   // the stage is refilled by the next iteration's copies
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -721,13 +759,15 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
   if (e != cudaSuccess) return set_error("qmuon_grasp_step (upload)", e);
   const int64_t tiles = ts[n];
   if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
+  static cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
+  if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
   grasp_colnorm<<<n, kThreads, 0, s>>>(a);
   grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
   grasp_chol<<<n, 64, 0, s>>>(a, hdr);
   grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
   grasp_chol<<<n, 64, 0, s>>>(a, hdr);
   grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
-  grasp_pass2<<<(unsigned)cs[n], kThreads, 0, s>>>(a, hdr);
+  grasp_pass2<<<(unsigned)cs[n], kThreads, kP2Smem, s>>>(a, hdr);
   grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
   e = cudaGetLastError();
   // the pageable host tables are staged by the copies above before they return
