@@ -206,7 +206,8 @@ QMUON_API qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan, 
 #define QMUON_GRASP_RANK 8
 #define QMUON_GRASP_BLOCK 64
 typedef struct {
-  int64_t rows, cols;            /* cols % 64 == 0 (else QMUON_ERR_UNSUPPORTED) */
+  int64_t rows, cols;            /* rows >= 8 (else QMUON_ERR_INVALID_ARGUMENT: a rank-8 factor needs 8 rows),
+                                    cols % 64 == 0 (else QMUON_ERR_UNSUPPORTED) */
   uint8_t* res;
   float* res_rmax;
   float* res_cmax;

@@ -677,7 +677,8 @@ size_t table_bytes(int32_t n) {
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 qmuon_status validate(const qmuon_grasp_matrix& m) {
-  if (m.rows <= 0 || m.cols <= 0 || m.rows > (1 << 28) || m.cols > (1 << 28)) return QMUON_ERR_INVALID_ARGUMENT;
+  // a rank-8 orthonormal factor needs at least 8 rows
+  if (m.rows < kRank || m.cols <= 0 || m.rows > (1 << 28) || m.cols > (1 << 28)) return QMUON_ERR_INVALID_ARGUMENT;
   if (m.cols % kS) return QMUON_ERR_UNSUPPORTED;
   if (!m.res || !m.res_rmax || !m.res_cmax || !m.p || !m.p_rmax || !m.p_cmax || !m.r || !m.r_rmax || !m.r_cmax ||
       !m.grad)

@@ -17,8 +17,10 @@ takes what it can compute one by one or whole-but-affordable:
 
 Workloads: the fused-QKV + MLP grouped set (3 row groups of a 12288 x 4096
 tensor + 8 MLP matrices), MuonBP on four Llama-8B layers (1 x 8 column
-tiles, P = 5; a block step and a full step), and the MXFP8 carrier on the
-same layers.
+tiles, P = 5; a block step and a full step), the MXFP8 carrier on the same
+layers, and the 4-bit GRASP state of those 28 matrices in one call (sampled
+64-row strips of M_t bit-exact, one whole 1024 x 4096 matrix against the
+oracle's step).
 """
 
 import numpy as np
@@ -27,7 +29,7 @@ import torch
 
 import memory_reduced_muon_gb300 as q
 import workloads
-from oracle import carrier, codec, muonbp, ns
+from oracle import carrier, codec, grasp, muonbp, ns
 
 from gpu_util import bf16_to_f64, min_row_cos, rel_fro, to_oracle_grad
 
@@ -268,3 +270,76 @@ def test_carrier_llama8b_full_size():
     ref = ns.newton_schulz(carrier.decode_rows(r.payload, r.scale_inv), inv_norm=float(inv[1].item()),
                            iters=w.iters, coeffs=w.coeffs)
     _assert_ns(bf16_to_f64(outs[1]), ref, m.name, fro=5e-2, cos=0.995)
+
+
+# ---------------------------------------------------------------------------
+# the 4-bit GRASP state on the same 28 matrices, all in one call
+# ---------------------------------------------------------------------------
+
+def _random_grasp_state(rows, cols, gen):
+    """A valid, non-trivial state: random codes and positive maxima (seeded)."""
+    nbr, nbc = (rows + 63) // 64, cols // 64
+    u = lambda *sh: torch.rand(*sh, generator=gen, device="cuda") * 0.9 + 0.1
+    return dict(res=torch.randint(0, 256, (rows, cols // 2), generator=gen, device="cuda", dtype=torch.int32).to(torch.uint8),
+                res_rmax=u(nbc, rows) * 0.02, res_cmax=u(nbr, cols) * 0.02,
+                p=torch.randint(-127, 128, (rows, 8), generator=gen, device="cuda", dtype=torch.int32).to(torch.int8),
+                p_rmax=u(rows) * 0.05, p_cmax=u(nbr, 8) * 0.05,
+                r=torch.randint(-127, 128, (cols, 8), generator=gen, device="cuda", dtype=torch.int32).to(torch.int8),
+                r_rmax=u(cols), r_cmax=u((cols + 63) // 64, 8))
+
+
+def _grasp_host(d):
+    """The device state as the oracle holds it (the factors' row maxima as 1 x n)."""
+    n = lambda k: d[k].cpu().numpy()
+    return grasp.GraspState(res=n("res"), res_rmax=n("res_rmax"), res_cmax=n("res_cmax"), p=n("p"),
+                            p_rmax=n("p_rmax").reshape(1, -1), p_cmax=n("p_cmax"), r=n("r"),
+                            r_rmax=n("r_rmax").reshape(1, -1), r_cmax=n("r_cmax"))
+
+
+def _strip_state(st, b):
+    """Rows 64 b .. 64 b + 63 as a state of their own (one block row)."""
+    sl = slice(64 * b, 64 * b + 64)
+    return grasp.GraspState(res=st.res[sl], res_rmax=st.res_rmax[:, sl], res_cmax=st.res_cmax[b:b + 1],
+                            p=st.p[sl], p_rmax=st.p_rmax[:, sl], p_cmax=st.p_cmax[b:b + 1], r=st.r, r_rmax=st.r_rmax,
+                            r_cmax=st.r_cmax)
+
+
+def test_grasp_llama8b_full_size():
+    w = workloads.get(4)
+    mats = w.matrices
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(31)
+    rng = np.random.default_rng(32)
+    grads = [workloads.make_grad(w, i, 1, device="cuda") for i in range(len(mats))]
+    states = [_random_grasp_state(m.rows, m.cols, gen) for m in mats]
+    host_in = {}
+    picks = []
+    for i, m in enumerate(mats):
+        st = _grasp_host(states[i])
+        for b in rng.choice((m.rows + 63) // 64, size=3, replace=False):
+            sl = slice(64 * int(b), 64 * int(b) + 64)
+            picks.append((i, int(b), _strip_state(st, int(b)), to_oracle_grad(grads[i][sl], "bf16").reshape(64, m.cols)))
+        if i == 1:   # layer 0's k: checked whole
+            host_in[i] = (st, to_oracle_grad(grads[i], "bf16").reshape(m.rows, m.cols))
+    descs = [q.grasp_matrix(m.rows, m.cols, d["res"], d["res_rmax"], d["res_cmax"], d["p"], d["p_rmax"], d["p_cmax"],
+                            d["r"], d["r_rmax"], d["r_cmax"], g) for m, d, g in zip(mats, states, grads)]
+    ws = torch.empty(q.qmuon_grasp_workspace_size(descs), dtype=torch.uint8, device="cuda")
+    q.qmuon_grasp_step(descs, 0.95, ws)
+    q.qmuon_sync_status(ws)
+    # M_t of sampled strips, bit-exact: it depends on the strip's state, all of
+    # R and g only, so the oracle's step on the strip alone gives it
+    for i, b, sst, g in picks:
+        ref = grasp.grasp_step(sst, g, 0.95)
+        got = grads[i][64 * b:64 * b + 64].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(got, ref.m_bits, err_msg=str((i, b)))
+    # one whole matrix through the oracle's step
+    st, g = host_in[1]
+    ref = grasp.grasp_step(st, g, 0.95)
+    d = states[1]
+    np.testing.assert_array_equal(grads[1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16), ref.m_bits)
+    gst = _grasp_host(d)
+    for a_, b_ in ((gst.p, ref.state.p), (gst.r, ref.state.r), (grasp.unpack4(gst.res), grasp.unpack4(ref.state.res))):
+        a_, b_ = a_.astype(np.int32), b_.astype(np.int32)
+        assert np.abs(a_ - b_).max() <= 1 and np.mean(a_ == b_) >= 0.99
+    np.testing.assert_allclose(gst.p_rmax, ref.state.p_rmax, rtol=1e-3)
+    np.testing.assert_allclose(gst.r_rmax, ref.state.r_rmax, rtol=1e-3, atol=1e-6 * np.abs(ref.state.r_rmax).max())

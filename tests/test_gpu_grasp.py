@@ -17,7 +17,11 @@ from oracle import codec, grasp
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(128, 192), (200, 320), (64, 64), (1000, 128), (1024, 2048)]
+# ragged strips (200, 1000 and 201 rows; 201 and 9 also leave half a row pair
+# empty), a single block, one row more than the factor's rank (with exactly 8
+# rows the residual is zero up to rounding and its codes quantise noise), and
+# a tall matrix whose last 128-row chunk of R's sums holds 4 rows
+SHAPES = [(128, 192), (200, 320), (64, 64), (1000, 128), (1024, 2048), (201, 192), (9, 64), (4100, 128)]
 
 
 def _to_dev(st, grad_bits, rows, cols):
@@ -117,3 +121,9 @@ def test_grasp_rejects_bad_shapes():
     with pytest.raises(q.QmuonError) as e:
         q.qmuon_grasp_step([_desc(d, rows, cols)], 0.9, ws)
     assert e.value.status == q.QMUON_ERR_UNSUPPORTED
+    rows, cols = 7, 64     # fewer rows than the factor's rank
+    st = grasp.initial_state(rows, cols, np.ones((cols, 8), np.float32))
+    d = _to_dev(st, np.zeros((rows, cols), np.uint16), rows, cols)
+    with pytest.raises(q.QmuonError) as e:
+        q.qmuon_grasp_step([_desc(d, rows, cols)], 0.9, ws)
+    assert e.value.status == q.QMUON_ERR_INVALID_ARGUMENT
