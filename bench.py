@@ -362,7 +362,17 @@ def run_gpu(args, world, rank, local):
     info = q.qmuon_plan_info(plans[0])
     # pinned host copies of two gradient batches for the end-to-end leg, taken
     # before any step overwrites them
-    host_pool = [[g.cpu().pin_memory() for g in batches[b % n_batches]] for b in range(2)]
+    host_pool = []
+    for b in range(2):   # one page-locked buffer per batch, a view per matrix
+        src = batches[b % n_batches]
+        buf = torch.empty(sum(g.numel() for g in src), dtype=torch.bfloat16, pin_memory=True)
+        views, o = [], 0
+        for g in src:
+            v = buf[o:o + g.numel()].view(g.shape)
+            v.copy_(g.cpu())
+            views.append(v)
+            o += g.numel()
+        host_pool.append(views)
     ws = torch.empty(q.qmuon_workspace_size(plans[0], q.QMUON_WS_STEP), dtype=torch.uint8, device=dev)
     for p in plans:   # Newton-Schulz tables of both step kinds, built before any timing
         q.qmuon_step_prepare(p, weights, ws)
@@ -487,20 +497,26 @@ def run_gpu(args, world, rank, local):
     copy_stream = torch.cuda.Stream(device=dev)
     sums_host = [torch.zeros(ngr).pin_memory() for _ in range(e2e_steps)]
     d2h = 0
-    # untimed warm-up of the same leg: each plan's first host-fed steps
-    for k in range(max(3, args.warmup)):
+    # untimed warm-up of the same leg: the first host-fed steps of a process
+    # run slower (about 30 ms instead of 18 in a probe of ten and ten)
+    for k in range(max(10, args.warmup)):
         t += 1
         q.qmuon_step_from_host(plans[(k % 2) % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights,
                                w.coeffs, w.iters, host_pool[k % 2], sums_host[0], sums, ws, stream=stream,
                                copy_stream=copy_stream)
     torch.cuda.synchronize()
+    # the host runs at most two steps ahead of the GPU, as a training loop would
+    done = [torch.cuda.Event() for _ in range(e2e_steps)]
     barrier(world)
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         t += 1
         b = k % 2
+        if k >= 2:
+            done[k - 2].synchronize()
         q.qmuon_step_from_host(plans[b % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights, w.coeffs,
                                w.iters, host_pool[b], sums_host[k], sums, ws, stream=stream, copy_stream=copy_stream)
+        done[k].record(stream)
         full_k = w.P != 0 and t % w.P == 0
         d2h += 4 * (info["n_full_groups"] if full_k else info["n_block_groups"])
     torch.cuda.synchronize()
