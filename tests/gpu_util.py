@@ -47,3 +47,25 @@ def random_grad(n: int, dtype: str, seed: int, device="cuda") -> torch.Tensor:
     x = torch.randn(n, generator=g, device=device) * scale
     x[torch.rand(n, generator=g, device=device) < 0.02] = 0.0
     return x.to(TORCH_DT[dtype]).contiguous()
+
+
+GUARD = 4096          # guard bytes on each side of a buffer (keeps 256-byte alignment)
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A device tensor of ``shape``/``dtype`` inside a larger byte buffer whose
+    GUARD bytes before and after hold a fixed pattern; ``check()`` asserts the
+    pattern is intact (a write outside the tensor shows up there)."""
+
+    def __init__(self, shape, dtype):
+        n = 1
+        for s in shape:
+            n *= int(s)
+        self.nbytes = n * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((self.nbytes + 2 * GUARD,), GUARD_BYTE, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[GUARD:GUARD + self.nbytes].view(dtype).view(*shape)
+
+    def check(self, what=""):
+        lo, hi = self.raw[:GUARD], self.raw[GUARD + self.nbytes:]
+        assert bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all()), f"guard bytes overwritten {what}"
