@@ -155,6 +155,7 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
                                           const qmuon_norm_segment* segments, int32_t n_segments,
                                           int32_t n_groups, int32_t tile_r, int32_t tile_c,
                                           qmuon_plan** out) {
+  qm::NvtxRange nvtx_range("qmuon_plan_create");
   // ---- host validation: nothing below touches CUDA until it all passes ----
   if (!out) return QMUON_ERR_INVALID_ARGUMENT;
   *out = nullptr;
@@ -437,6 +438,7 @@ extern "C" qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* pl
                                                             int32_t normalize_mode,
                                                             float* group_sumsq, float* group_inv_norm,
                                                             void* ws, size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_update_multi_normalize_groups");
   return update_groups(plan, beta, normalize_mode, group_sumsq, group_inv_norm, ws, ws_bytes, stream, false, 0, 0);
 }
 
@@ -444,6 +446,7 @@ extern "C" qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan*
                                                                int32_t normalize_mode, uint64_t seed, int64_t step,
                                                                float* group_sumsq, float* group_inv_norm,
                                                                void* ws, size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_update_multi_normalize_groups_sr");
   return update_groups(plan, beta, normalize_mode, group_sumsq, group_inv_norm, ws, ws_bytes, stream, true, seed,
                        step);
 }
@@ -470,6 +473,7 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, q
                                                    qmuon_dtype grad_dtype, float beta, uint8_t* payload,
                                                    uint8_t* scale_inv, float* inv_norm, void* ws,
                                                    size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_update_mxfp8_carrier");
   if (!tensor || !payload || !scale_inv || !inv_norm || !ws) return QMUON_ERR_INVALID_ARGUMENT;
   if (!valid_q8(q8_kind) || !valid_dtype(grad_dtype)) return QMUON_ERR_INVALID_ARGUMENT;
   const qmuon_status vs = validate_tensor(*tensor, grad_dtype);
@@ -517,6 +521,7 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan,
                                                          uint8_t* const* scale_invs, float* inv_norms,
                                                          float* group_sumsq, void* ws, size_t ws_bytes,
                                                          void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_update_mxfp8_carrier_multi");
   if (!plan || !payloads || !scale_invs || !inv_norms || !ws) return QMUON_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, 256) || !aligned(inv_norms, 4) || (group_sumsq && !aligned(group_sumsq, 4)))
     return QMUON_ERR_INVALID_ARGUMENT;
@@ -562,6 +567,7 @@ extern "C" size_t qmuon_ns_workspace_size(const qmuon_ns_problem* problems, int3
 extern "C" qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* problems, int32_t n_problems,
                                                     int32_t iters, const float coeffs[3], void* ws,
                                                     size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_newton_schulz_batched");
   if (!problems || n_problems <= 0 || iters < 1 || !coeffs || !ws) return QMUON_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   for (int32_t i = 0; i < n_problems; ++i) {
@@ -582,6 +588,7 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
                                    float eta_full, float eta_block, float* const* weights,
                                    const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,
                                    size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_step");
   if (!plan || !weights || !coeffs || !ws || t < 1 || P < 0 || iters < 1) return QMUON_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
@@ -615,6 +622,7 @@ extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, 
                                              const void* const* host_grads, float* host_group_sumsq,
                                              float* group_sumsq, void* ws, size_t ws_bytes, void* stream,
                                              void* copy_stream) {
+  qm::NvtxRange nvtx_range("qmuon_step_from_host");
   if (!plan || !host_grads) return QMUON_ERR_INVALID_ARGUMENT;
   if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
   const int32_t n = (int32_t)plan->tensors.size();
@@ -656,6 +664,7 @@ extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, 
 
 extern "C" qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,
                                            size_t ws_bytes) {
+  qm::NvtxRange nvtx_range("qmuon_step_prepare");
   if (!plan || !weights || !ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
   const int32_t n = (int32_t)plan->tensors.size();

@@ -703,6 +703,7 @@ extern "C" size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices,
 
 extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int32_t n, float mu, void* ws,
                                          size_t ws_bytes, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_grasp_step");
   using namespace qm;
   if (!matrices || n <= 0 || !ws || !aligned_to(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
   for (int32_t i = 0; i < n; ++i) {

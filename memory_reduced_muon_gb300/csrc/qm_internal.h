@@ -6,10 +6,20 @@
 #include <cstdint>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "qmuon.h"
 
 namespace qm {
+
+// An NVTX range named after a C-ABI entry, open for the entry's host work and
+// launches (visible to nsys/ncu; a no-op call when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kBlock = QMUON_BLOCK;   // elements per quantization block
 constexpr int kUpdThreads = 256;      // 8 warps = 16 half-warps, one block per half-warp

@@ -780,6 +780,7 @@ cudaError_t static_scratch(int dev, void** out) {
 extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
                                                        qmuon_dtype grad_dtype, float beta, float* sumsq,
                                                        float* inv_norm, void* stream) {
+  qm::NvtxRange nvtx_range("qmuon_update_normalize_noalloc");
   using namespace qm;
   // ---- host validation, before any CUDA call ----
   if (!tensor) return set_error_msg("qmuon_update_normalize_noalloc: null tensor", QMUON_ERR_INVALID_ARGUMENT);
