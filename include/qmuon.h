@@ -148,6 +148,18 @@ QMUON_API qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan* 
                                                     float* group_sumsq, float* group_inv_norm, void* ws,
                                                     size_t ws_bytes, void* stream);
 
+/* Count non-finite momenta: every update launch through this plan (the
+ * update entries, the carrier over the plan, qmuon_step and
+ * qmuon_step_from_host) adds to *counter, with an atomic add, the number of
+ * 256-element blocks whose fp32 sum of m*m is not finite (a NaN or an
+ * infinity in m, or squares that overflow fp32).  Such a block's codes and
+ * its stored momentum are not meaningful, and neither is its group's norm.
+ * The caller zeroes and reads the counter.
+ *   counter  D  one uint32, 4-byte aligned, or NULL to stop counting
+ * Host-only: changes no device state.  QMUON_ERR_INVALID_ARGUMENT on a NULL
+ * plan or a misaligned counter. */
+QMUON_API qmuon_status qmuon_plan_set_nonfinite_counter(qmuon_plan* plan, uint32_t* counter);
+
 /* Make qmuon_step requantise stochastically (enable = 1; 0 restores nearest
  * rounding), as qmuon_update_multi_normalize_groups_sr does with this seed
  * and step = the step's t.  Host-only: changes no device state.

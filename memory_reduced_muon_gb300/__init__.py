@@ -110,6 +110,7 @@ def lib() -> C.CDLL:
         "qmuon_step_prepare": (i32, [vp, C.POINTER(vp), vp, sz]),
         "qmuon_step_from_host": (i32, [vp, i64, i32, f32, f32, f32, C.POINTER(vp), C.POINTER(f32), i32,
                                        C.POINTER(vp), vp, vp, vp, sz, vp, vp]),
+        "qmuon_plan_set_nonfinite_counter": (i32, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -126,7 +127,8 @@ def exported_symbols() -> list:
             "qmuon_step", "qmuon_sync_status", "qmuon_status_string", "qmuon_version", "qmuon_last_error",
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
             "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
-            "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host"]
+            "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host",
+            "qmuon_plan_set_nonfinite_counter"]
 
 
 # --------------------------------------------------------------------------
@@ -249,6 +251,11 @@ def qmuon_update_multi_normalize_groups_sr(plan: Plan, beta: float, normalize_mo
         _ptr(group_sumsq), _ptr(group_inv_norm), _ptr(ws), _nbytes(ws) if ws_bytes is None else int(ws_bytes),
         _stream(stream))
     _check(st, "qmuon_update_multi_normalize_groups_sr")
+
+
+def qmuon_plan_set_nonfinite_counter(plan: Plan, counter):
+    """``counter``: a device uint32/int32 tensor of one element, or None."""
+    _check(lib().qmuon_plan_set_nonfinite_counter(plan.handle, _ptr(counter)), "qmuon_plan_set_nonfinite_counter")
 
 
 def qmuon_plan_set_stochastic_rounding(plan: Plan, enable: bool, seed: int = 0):

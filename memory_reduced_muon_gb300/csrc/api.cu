@@ -110,6 +110,7 @@ struct qmuon_plan {
   ns::StepTables* ns_block = nullptr;
   bool sr = false;                    // qmuon_step requantises stochastically (counter step = t)
   uint64_t sr_seed = 0;
+  unsigned int* nonfinite = nullptr;  // device counter of non-finite blocks, or null
   // qmuon_step_from_host: gradient buffers free again / host copies landed
   cudaEvent_t grads_free = nullptr;
   cudaEvent_t grads_copied = nullptr;
@@ -382,6 +383,7 @@ UpdLaunch make_launch(const qmuon_plan* p, int layout, float beta, const UpdWs& 
   L.header = w.header;
   L.group_sumsq = sumsq;
   L.group_inv = inv;
+  L.nonfinite = p->nonfinite;
   return L;
 }
 
@@ -449,6 +451,12 @@ extern "C" qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan*
   qm::NvtxRange nvtx_range("qmuon_update_multi_normalize_groups_sr");
   return update_groups(plan, beta, normalize_mode, group_sumsq, group_inv_norm, ws, ws_bytes, stream, true, seed,
                        step);
+}
+
+extern "C" qmuon_status qmuon_plan_set_nonfinite_counter(qmuon_plan* plan, uint32_t* counter) {
+  if (!plan || (counter && (reinterpret_cast<uintptr_t>(counter) & 3))) return QMUON_ERR_INVALID_ARGUMENT;
+  plan->nonfinite = reinterpret_cast<unsigned int*>(counter);
+  return QMUON_OK;
 }
 
 extern "C" qmuon_status qmuon_plan_set_stochastic_rounding(qmuon_plan* plan, int32_t enable, uint64_t seed) {

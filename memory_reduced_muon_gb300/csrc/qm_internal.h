@@ -79,6 +79,8 @@ struct UpdLaunch {
   // stochastic requantisation: Philox4x32-10 key (seed) and the step word of its counter
   int32_t sr;
   uint32_t sr_key0, sr_key1, sr_step;
+  // D: blocks whose sum of m*m is not finite are counted here, or null
+  unsigned int* nonfinite;
 };
 
 // Record the detail of a failure for qmuon_last_error() (api.cu); returns

@@ -605,6 +605,8 @@ __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) 
         const float ss = full ? compute_lane<QK, DT, CARRIER, true, SR>(in, T, lb, hl, beta, omb, L)
                               : compute_lane<QK, DT, CARRIER, false, SR>(in, T, lb, hl, beta, omb, L);
         if (reduce && hl == 0) { s_bsum[k - kb] = ss; s_bgrp[k - kb] = g; }
+        // a NaN or infinite momentum (or one whose squares overflow) in this block
+        if (L.nonfinite && hl == 0 && !isfinite(ss)) atomicAdd(L.nonfinite, 1u);
       }
     }
   }

@@ -104,6 +104,7 @@ def test_entries_reject_null_plan_and_bad_args(lib):
     assert L.qmuon_step_from_host(None, 1, 5, 0.9, 0.02, 0.01, w, cf, 5, h, None, None, FAKE, 1 << 20, None,
                                   None) == INV
     assert L.qmuon_sync_status(None, None) == INV
+    assert L.qmuon_plan_set_nonfinite_counter(None, None) == INV
     assert L.qmuon_sync_status(FAKE + 16, None) == INV   # not 256-byte aligned
 
 
