@@ -40,7 +40,7 @@ typedef enum {
   QMUON_OK = 0,
   QMUON_ERR_INVALID_ARGUMENT = 1,   /* NULL/misaligned pointer, bad size or enum */
   QMUON_ERR_MISALIGNED_SEGMENT = 2, /* norm segment not on 256-element blocks   */
-  QMUON_ERR_UNSUPPORTED = 3,        /* valid request this build does not serve   */
+  QMUON_ERR_UNSUPPORTED = 3,        /* valid request the library does not serve  */
   QMUON_ERR_WORKSPACE_TOO_SMALL = 4,
   QMUON_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed         */
   QMUON_ERR_TIMEOUT = 6             /* a kernel's bounded wait expired (see qmuon_sync_status) */
