@@ -86,6 +86,17 @@ __device__ __forceinline__ int grid_code(float x, float sc, int L) {
   return q < -L ? -L : (q > L ? L : q);
 }
 
+// Two fp32 fused multiply-adds in one packed instruction, d = a * b + c per
+// component, each rounded once exactly as fmaf rounds it.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 // Compensated (Neumaier) addition of a block's sum into a running total:
 // the strips add up to 224 blocks, and orth magnifies the error of Y when its
 // columns are nearly parallel.
@@ -603,16 +614,17 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const Ws
       *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 0)]);
       *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 4)]);
       cmx[k] = 0.0f;
+      // both rows' dot products P_i . R_j at once, each in the order of fmaf's chain
+      float2 acc2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int l = 0; l < kRank; ++l) acc2 = fma2(make_float2(p[0][l], p[1][l]), make_float2(rr[l], rr[l]), acc2);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v = 0.0f;
         if (live[h]) {
           const uint32_t w = (k >> 1) == 0 ? gv[c][h].x : (k >> 1) == 1 ? gv[c][h].y : (k >> 1) == 2 ? gv[c][h].z : gv[c][h].w;
           const float m = __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
-          float acc = 0.0f;
-#pragma unroll
-          for (int l = 0; l < kRank; ++l) acc = fmaf(p[h][l], rr[l], acc);
-          v = m - acc;
+          v = m - (h == 0 ? acc2.x : acc2.y);
         }
         res[h][k] = v;
         rm[h] = fmaxf(rm[h], fabsf(v));
