@@ -52,17 +52,19 @@ def load_peaks():
 
 
 def load_traffic():
-    """Per-launch (or per-call) DRAM bytes from the committed ncu summary
-    (``key = bytes`` lines in profiles/dram_traffic_llama8b_x4_muonbp.md)."""
+    """Per-launch (or per-call) DRAM bytes from the committed ncu summaries
+    (``key = bytes`` lines in profiles/dram_traffic_llama8b_x4_muonbp.md and
+    profiles/grasp_llama8b_x4.md)."""
     out = {}
-    try:
-        with open(os.path.join(ROOT, "profiles", "dram_traffic_llama8b_x4_muonbp.md")) as f:
-            for line in f:
-                parts = line.split("=")
-                if len(parts) == 2 and parts[0].strip().endswith(("_per_launch", "_per_call")):
-                    out[parts[0].strip()] = float(parts[1])
-    except Exception:
-        pass
+    for name in ("dram_traffic_llama8b_x4_muonbp.md", "grasp_llama8b_x4.md"):
+        try:
+            with open(os.path.join(ROOT, "profiles", name)) as f:
+                for line in f:
+                    parts = line.split("=")
+                    if len(parts) == 2 and parts[0].strip().endswith(("_per_launch", "_per_call")):
+                        out[parts[0].strip()] = float(parts[1])
+        except Exception:
+            pass
     return out
 
 
@@ -647,7 +649,9 @@ def main():
                             "bytes_per_param": GRASP_BYTES_PER_PARAM,
                             "gbs": GRASP_BYTES_PER_PARAM * r["n_params"] / (r["grasp_ms"] / 1e3) / 1e9,
                             "frac": GRASP_BYTES_PER_PARAM * r["n_params"] / (r["grasp_ms"] / 1e3) / 1e9
-                            / float(peaks["hbm_gbs"])} if r.get("grasp_ms") else None),
+                            / float(peaks["hbm_gbs"]),
+                            "traffic": traffic.get("grasp_bytes_per_call")
+                            if args.row_scale == 1 and args.workload == 4 else None} if r.get("grasp_ms") else None),
             "update_stochastic_rounding": ({"gbs": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9,
                                             "ms_per_launch": r["upd_sr_ms"],
                                             "frac": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9 / float(peaks["hbm_gbs"])}
