@@ -334,7 +334,7 @@ def run_gpu_carrier(args, world, rank, local, w):
     return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks,
                 per_step=[], upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes,
                 ns_ms={"full": ns_ms}, ns_flop={"full": flop}, e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
-                launches=(1 + len(mats) + 3 * w.iters) * args.steps, n_params=n_params, w=w)
+                launches=(1 + 1 + 3 * w.iters) * args.steps, n_params=n_params, w=w)
 
 
 def run_gpu(args, world, rank, local):

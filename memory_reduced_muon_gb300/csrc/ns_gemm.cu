@@ -926,34 +926,60 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 // the product with a power of two is exact in bf16 (within bf16's exponent
 // range); the carrier is consumed as it is, the inverse norm is applied later
 // by the first iteration.  One thread per 16 payload bytes.
-__global__ void decode_carrier_kernel(const uint8_t* __restrict__ payload, const uint8_t* __restrict__ scale,
-                                      __nv_bfloat16* __restrict__ x, int64_t rows, int64_t cols, int64_t ld) {
-  const int64_t per_row = cols / 16;
-  const int64_t total = rows * per_row;
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = v / per_row, c0 = (v % per_row) * 16;
-    const uint4 p = *reinterpret_cast<const uint4*>(payload + r * cols + c0);
-    const int e = (int)scale[r * (cols / 32) + c0 / 32] - 127;
-    // 2^e as fp32 (e in [-127, 127]; 2^-127 is the subnormal 0x00400000)
-    const float mult = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-    uint32_t o[8];
+// One carrier to expand: rows x cols E4M3 codes and E8M0 row-block scales into
+// a bf16 matrix with row stride ld; its 16-element vectors are numbered from
+// vec_begin in the launch.
+struct DecodeItem {
+  const uint8_t* payload;
+  const uint8_t* scale;
+  __nv_bfloat16* x;
+  int64_t rows, cols, ld;
+  int64_t vec_begin;
+};
+
+// Vector v (16 payload bytes of one row) of one carrier.
+__device__ __forceinline__ void decode_vec(const DecodeItem& it, int64_t v) {
+  const int64_t per_row = it.cols / 16;
+  const int64_t r = v / per_row, c0 = (v % per_row) * 16;
+  const uint4 p = *reinterpret_cast<const uint4*>(it.payload + r * it.cols + c0);
+  const int e = (int)it.scale[r * (it.cols / 32) + c0 / 32] - 127;
+  // 2^e as fp32 (e in [-127, 127]; 2^-127 is the subnormal 0x00400000)
+  const float mult = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+  uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 4; ++k) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // two E4M3 codes -> two halves (exact), then fp32, scale, bf16
-        const unsigned short pair = (unsigned short)((w[k] >> (16 * h)) & 0xFFFFu);
-        uint32_t hh;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pair));
-        const __half2 hv = *reinterpret_cast<const __half2*>(&hh);
-        const float lo = __fmul_rn(__low2float(hv), mult), hi = __fmul_rn(__high2float(hv), mult);
-        o[2 * k + h] = pack_bf16(lo, hi);
-      }
+    for (int h = 0; h < 2; ++h) {
+      // two E4M3 codes -> two halves (exact), then fp32, scale, bf16
+      const unsigned short pair = (unsigned short)((w[k] >> (16 * h)) & 0xFFFFu);
+      uint32_t hh;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pair));
+      const __half2 hv = *reinterpret_cast<const __half2*>(&hh);
+      const float lo = __fmul_rn(__low2float(hv), mult), hi = __fmul_rn(__high2float(hv), mult);
+      o[2 * k + h] = pack_bf16(lo, hi);
     }
-    uint4* dst = reinterpret_cast<uint4*>(x + r * ld + c0);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(it.x + r * it.ld + c0);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Every carrier of a batch in one launch: thread-strided over all vectors;
+// a thread finds its first carrier by bisection and then only moves forward.
+__global__ void decode_carriers_kernel(const DecodeItem* __restrict__ items, int32_t n, int64_t total) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= total) return;
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (items[mid].vec_begin <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  for (int k = lo; v < total; v += stride) {
+    while (k + 1 < n && items[k + 1].vec_begin <= v) ++k;
+    decode_vec(items[k], v - items[k].vec_begin);
   }
 }
 
@@ -1337,7 +1363,7 @@ qmuon_status validate_problem(const qmuon_ns_problem& p) {
 size_t batch_table_bytes(const qmuon_ns_problem* probs, int32_t n) {
   int64_t tiles = 0;
   for (int32_t i = 0; i < n; ++i) tiles += all_tiles(probs[i].rows, probs[i].cols);
-  return table_bytes(n, tiles);
+  return table_bytes(n, tiles) + align_up((size_t)n * sizeof(DecodeItem), 256);   // + the carriers to expand
 }
 
 size_t batch_workspace_bytes(const qmuon_ns_problem* probs, int32_t n) {
@@ -1364,14 +1390,22 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
   carve_table(table, n, L);
   cudaError_t ce = upload_table(L, hp, S, s, true);
   if (ce != cudaSuccess) return set_error("newton-schulz: upload problem table", ce);
-  // MXFP8 inputs: expand the carrier into the problem's bf16 matrix first
+  // MXFP8 inputs: every carrier expanded into its problem's bf16 matrix first, in one launch
+  std::vector<DecodeItem> items;
+  int64_t vecs = 0;
   for (int32_t i = 0; i < n; ++i) {
     if (probs[i].input != QMUON_NS_MXFP8) continue;
-    const int64_t vecs = probs[i].rows * (probs[i].cols / 16);
+    items.push_back(DecodeItem{probs[i].payload, probs[i].scale_inv, static_cast<__nv_bfloat16*>(probs[i].x),
+                               probs[i].rows, probs[i].cols, probs[i].ld, vecs});
+    vecs += probs[i].rows * (probs[i].cols / 16);
+  }
+  if (!items.empty()) {
+    DecodeItem* d_items = reinterpret_cast<DecodeItem*>(table + batch_table_bytes(probs, n) -
+                                                        align_up((size_t)n * sizeof(DecodeItem), 256));
+    ce = cudaMemcpyAsync(d_items, items.data(), items.size() * sizeof(DecodeItem), cudaMemcpyHostToDevice, s);
+    if (ce != cudaSuccess) return set_error("newton-schulz: upload carrier list", ce);
     const int grid = (int)std::min<int64_t>((vecs + 255) / 256, (int64_t)num_sms() * 8);
-    decode_carrier_kernel<<<grid, 256, 0, s>>>(probs[i].payload, probs[i].scale_inv,
-                                               static_cast<__nv_bfloat16*>(probs[i].x), probs[i].rows, probs[i].cols,
-                                               probs[i].ld);
+    decode_carriers_kernel<<<grid, 256, 0, s>>>(d_items, (int32_t)items.size(), vecs);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return set_error("newton-schulz: carrier decode launch", ce);
   }
