@@ -446,6 +446,7 @@ __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) 
   const int64_t ke = (kb + L.chunk < L.nb_total) ? kb + L.chunk : L.nb_total;
   const int n_stages = (int)((ke - kb + kStageBlocks - 1) / kStageBlocks);
   const bool reduce = L.layout.n_groups > 0;
+  const bool keep = reduce || L.nonfinite != nullptr;   // the block sums are needed after the loop
   const bool single = (L.tensors == nullptr);
 
   if (tid == 0) {
@@ -604,17 +605,27 @@ __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) 
         if (reduce && hl == 0 && L.layout.block_group) g = __ldg(L.layout.block_group + k);
         const float ss = full ? compute_lane<QK, DT, CARRIER, true, SR>(in, T, lb, hl, beta, omb, L)
                               : compute_lane<QK, DT, CARRIER, false, SR>(in, T, lb, hl, beta, omb, L);
-        if (reduce && hl == 0) { s_bsum[k - kb] = ss; s_bgrp[k - kb] = g; }
-        // a NaN or infinite momentum (or one whose squares overflow) in this block
-        if (L.nonfinite && hl == 0 && !isfinite(ss)) atomicAdd(L.nonfinite, 1u);
+        if (keep && hl == 0) {
+          s_bsum[k - kb] = ss;
+          if (reduce) s_bgrp[k - kb] = g;
+        }
       }
     }
+  }
+  if (!keep) return;
+  __syncthreads();
+  const int nloc = (int)(ke - kb);
+  // blocks whose momentum holds a NaN or an infinity (or whose squares overflow)
+  if (L.nonfinite && warp == 0) {
+    unsigned bad = 0;
+    for (int i = lane; i < nloc; i += 32) bad += isfinite(s_bsum[i]) ? 0u : 1u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if (lane == 0 && bad) atomicAdd(L.nonfinite, bad);
   }
   if (!reduce) return;
 
   // ---- per-(CTA, group) partial sums, fixed order ----
-  __syncthreads();
-  const int nloc = (int)(ke - kb);
   const bool one_group = (L.layout.block_group == nullptr);
   const int s0 = one_group ? (int)blockIdx.x : __ldg(L.layout.cta_slot_begin + blockIdx.x);
   const int s1 = one_group ? (int)blockIdx.x + 1 : __ldg(L.layout.cta_slot_begin + blockIdx.x + 1);
