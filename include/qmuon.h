@@ -85,12 +85,20 @@ typedef struct qmuon_plan qmuon_plan;
  *                           equal n_tensors, or be 0 to mean that)
  *   tile_r, tile_c          MuonBP block tiling used by qmuon_step's block
  *                           steps: every tensor is cut into tile_r x tile_c
- *                           tiles of (rows/tile_r) x (cols/tile_c); with
- *                           tile_c > 1 the tile width must be a multiple of
- *                           256, with tile_c == 1 each tile's element count
+ *                           tiles of (rows/tile_r) x (cols/tile_c), so rows
+ *                           and cols must divide (else
+ *                           QMUON_ERR_INVALID_ARGUMENT); tiles must be whole
+ *                           256-element blocks (else
+ *                           QMUON_ERR_MISALIGNED_SEGMENT): with tile_c > 1,
+ *                           cols and the tile width are multiples of 256;
+ *                           with tile_c == 1 and tile_r > 1, each tile's
+ *                           element count is a multiple of 256
  *   out                  H  receives the plan (freed by qmuon_plan_destroy)
- * The plan uploads its tables once (one H2D copy) to the current device and
- * is tied to that device.  Allocates device memory (small tables) only. */
+ * Tensors may be empty (rows or cols 0; their pointers are not used), but the
+ * plan must hold between 1 and 2^31 - 1 quantization blocks in all
+ * (QMUON_ERR_INVALID_ARGUMENT otherwise).  The plan uploads its tables once
+ * (one H2D copy) to the current device and is tied to that device.
+ * Allocates device memory (small tables) only. */
 QMUON_API qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n_tensors,
                                qmuon_q8_kind q8_kind, qmuon_dtype grad_dtype,
                                const qmuon_norm_segment* segments, int32_t n_segments,

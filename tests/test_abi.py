@@ -77,6 +77,7 @@ def test_plan_create_rejects_on_host(lib):
     assert _plan_status([q.qmuon_tensor(FAKE + 8, FAKE, FAKE, 16, 16)]) == INV   # q8 not 16-byte aligned
     assert _plan_status([q.qmuon_tensor(0, FAKE, FAKE, 16, 16)]) == INV          # null pointer
     assert _plan_status([_tensor(-1, 16)]) == INV
+    assert _plan_status([_tensor(0, 16), _tensor(16, 0)]) == INV             # no quantization block at all
     # norm segments ("Grouped QKV And Sharding"): 256-element alignment
     t = [_tensor(8, 512)]
     assert _plan_status(t, segments=[(0, 100, 256, 0)], n_groups=1) == MIS
