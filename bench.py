@@ -654,7 +654,9 @@ def main():
                             if args.row_scale == 1 and args.workload == 4 else None} if r.get("grasp_ms") else None),
             "update_stochastic_rounding": ({"gbs": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9,
                                             "ms_per_launch": r["upd_sr_ms"],
-                                            "frac": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9 / float(peaks["hbm_gbs"])}
+                                            "frac": r["upd_bytes"] / (r["upd_sr_ms"] / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                                            "traffic": traffic.get("update_sr_bytes_per_launch")
+                                            if args.row_scale == 1 and args.workload == 4 else None}
                                            if r.get("upd_sr_ms") else None),
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
             "e2e": ({"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
