@@ -7,7 +7,8 @@
  * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
  * only enqueues work on it and returns; results are ready when the stream
  * reaches that point.  Every entry validates its arguments on the host first
- * and launches nothing when validation fails; no entry aborts or throws.
+ * and launches nothing when validation fails; no entry aborts or throws
+ * (a failed host allocation returns QMUON_ERR_OUT_OF_MEMORY).
  *
  * Layouts: tensors are dense, row-major and contiguous.  q8 codes and
  * gradients must start on a 16-byte boundary; absmax on a 4-byte boundary.
@@ -15,7 +16,10 @@
  * blocks in flat order; the last block may be partial.
  *
  * Concurrency: calls that share a workspace must not overlap on the GPU
- * (enqueue them on one stream).  Distinct plans/workspaces are independent.
+ * (enqueue them on one stream).  The steps of one plan (qmuon_step,
+ * qmuon_step_from_host, qmuon_step_prepare) share the plan's Newton-Schulz
+ * tables: make them from one host thread at a time and enqueue them on one
+ * stream.  Distinct plans/workspaces are independent.
  */
 #ifndef QMUON_H_
 #define QMUON_H_
@@ -43,7 +47,8 @@ typedef enum {
   QMUON_ERR_UNSUPPORTED = 3,        /* valid request the library does not serve  */
   QMUON_ERR_WORKSPACE_TOO_SMALL = 4,
   QMUON_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed         */
-  QMUON_ERR_TIMEOUT = 6             /* a kernel's bounded wait expired (see qmuon_sync_status) */
+  QMUON_ERR_TIMEOUT = 6,            /* a kernel's bounded wait expired (see qmuon_sync_status) */
+  QMUON_ERR_OUT_OF_MEMORY = 7       /* host memory for a plan's or a call's tables could not be allocated */
 } qmuon_status;
 
 typedef enum { QMUON_Q8_INT8 = 0, QMUON_Q8_UINT8 = 1 } qmuon_q8_kind;
@@ -376,9 +381,12 @@ QMUON_API qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, i
 /* Build, ahead of time, the Newton-Schulz problem tables qmuon_step needs for
  * both step kinds with these weights and this workspace (tensor maps and
  * tile lists; one synchronous upload each).  Optional: qmuon_step builds them
- * on first use and rebuilds them when the weights or workspace change;
- * preparing keeps that host work and its synchronising copy out of the
- * steps that follow.  Arguments as for qmuon_step. */
+ * on first use and rebuilds them when the weights or workspace change, with
+ * the upload enqueued on its stream behind the steps already there; preparing
+ * keeps that host work out of the steps that follow, and must precede any
+ * stream capture of them.  When tables already exist and change, this call
+ * first waits for the device to finish every earlier launch, since earlier
+ * steps may still be reading them.  Arguments as for qmuon_step. */
 QMUON_API qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,
                                           size_t ws_bytes);
 

@@ -27,6 +27,7 @@ QMUON_ERR_UNSUPPORTED = 3
 QMUON_ERR_WORKSPACE_TOO_SMALL = 4
 QMUON_ERR_CUDA = 5
 QMUON_ERR_TIMEOUT = 6
+QMUON_ERR_OUT_OF_MEMORY = 7
 
 QMUON_Q8_INT8, QMUON_Q8_UINT8 = 0, 1
 QMUON_BF16, QMUON_FP16, QMUON_FP32 = 0, 1, 2

@@ -79,6 +79,11 @@ qmuon_status qm::set_error_msg(const char* msg, qmuon_status status) {
   return status;
 }
 
+qmuon_status qm::set_error_what(const char* where, const char* what, qmuon_status status) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, what);
+  return status;
+}
+
 namespace {
 qmuon_status cuda_status(cudaError_t e, const char* where) {
   return e == cudaSuccess ? QMUON_OK : set_error(where, e);
@@ -157,153 +162,154 @@ extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n
                                           int32_t n_groups, int32_t tile_r, int32_t tile_c,
                                           qmuon_plan** out) {
   qm::NvtxRange nvtx_range("qmuon_plan_create");
-  // ---- host validation: nothing below touches CUDA until it all passes ----
-  if (!out) return QMUON_ERR_INVALID_ARGUMENT;
-  *out = nullptr;
-  if (!tensors || n_tensors <= 0) return QMUON_ERR_INVALID_ARGUMENT;
-  if (!valid_q8(q8_kind) || !valid_dtype(grad_dtype)) return QMUON_ERR_INVALID_ARGUMENT;
-  if (tile_r < 1 || tile_c < 1) return QMUON_ERR_INVALID_ARGUMENT;
-  if (n_segments < 0 || (n_segments > 0 && !segments)) return QMUON_ERR_INVALID_ARGUMENT;
-  const bool per_tensor = (segments == nullptr || n_segments == 0);
-  if (per_tensor && n_groups != 0 && n_groups != n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
-  if (!per_tensor && n_groups <= 0) return QMUON_ERR_INVALID_ARGUMENT;
-  std::vector<int64_t> begin(n_tensors + 1, 0);
-  for (int32_t i = 0; i < n_tensors; ++i) {
-    const qmuon_status s = validate_tensor(tensors[i], grad_dtype);
-    if (s != QMUON_OK) return s;
-    begin[i + 1] = begin[i] + nblocks(tensors[i].rows * tensors[i].cols);
-  }
-  const int64_t nb = begin[n_tensors];
-  if (nb == 0 || nb > ((int64_t)1 << 31) - 1) return QMUON_ERR_INVALID_ARGUMENT;
-  // tiles of the MuonBP block steps must be whole 256-element runs
-  for (int32_t i = 0; i < n_tensors; ++i) {
-    const int64_t R = tensors[i].rows, C = tensors[i].cols;
-    if (R * C == 0) continue;
-    if (R % tile_r || C % tile_c) return QMUON_ERR_INVALID_ARGUMENT;
-    if (tile_c > 1) {
-      if (C % kBlock || (C / tile_c) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
-    } else if (tile_r > 1) {
-      if (((R / tile_r) * C) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
+  return qm::no_throw("qmuon_plan_create", [&]() -> qmuon_status {
+    // ---- host validation: nothing below touches CUDA until it all passes ----
+    if (!out) return QMUON_ERR_INVALID_ARGUMENT;
+    *out = nullptr;
+    if (!tensors || n_tensors <= 0) return QMUON_ERR_INVALID_ARGUMENT;
+    if (!valid_q8(q8_kind) || !valid_dtype(grad_dtype)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (tile_r < 1 || tile_c < 1) return QMUON_ERR_INVALID_ARGUMENT;
+    if (n_segments < 0 || (n_segments > 0 && !segments)) return QMUON_ERR_INVALID_ARGUMENT;
+    const bool per_tensor = (segments == nullptr || n_segments == 0);
+    if (per_tensor && n_groups != 0 && n_groups != n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
+    if (!per_tensor && n_groups <= 0) return QMUON_ERR_INVALID_ARGUMENT;
+    std::vector<int64_t> begin(n_tensors + 1, 0);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const qmuon_status s = validate_tensor(tensors[i], grad_dtype);
+      if (s != QMUON_OK) return s;
+      begin[i + 1] = begin[i] + nblocks(tensors[i].rows * tensors[i].cols);
     }
-  }
-
-  std::unique_ptr<qmuon_plan> P(new (std::nothrow) qmuon_plan);
-  if (!P) return QMUON_ERR_INVALID_ARGUMENT;
-  P->tensors.assign(tensors, tensors + n_tensors);
-  P->q8 = q8_kind;
-  P->dt = grad_dtype;
-  P->tile_r = tile_r;
-  P->tile_c = tile_c;
-  P->nb_total = nb;
-  P->tensor_begin = begin;
-
-  // ---- group layouts (host) ----
-  HostLayout H[3];
-  H[1].n_groups = n_tensors;
-  H[1].block_group.resize(nb);
-  for (int32_t i = 0; i < n_tensors; ++i)
-    std::fill(H[1].block_group.begin() + begin[i], H[1].block_group.begin() + begin[i + 1], i);
-  if (per_tensor) {
-    H[0].n_groups = n_tensors;
-    H[0].block_group = H[1].block_group;
-  } else {
-    H[0].n_groups = n_groups;
-    H[0].block_group.assign(nb, -1);
-    for (int32_t s = 0; s < n_segments; ++s) {
-      const qmuon_norm_segment& g = segments[s];
-      if (g.tensor_index < 0 || g.tensor_index >= n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
-      if (g.group_id < 0 || g.group_id >= n_groups) return QMUON_ERR_INVALID_ARGUMENT;
-      const int64_t n = tensors[g.tensor_index].rows * tensors[g.tensor_index].cols;
-      if (g.start < 0 || g.length <= 0 || g.start + g.length > n) return QMUON_ERR_INVALID_ARGUMENT;
-      const int64_t end = g.start + g.length;
-      if (g.start % kBlock || (end % kBlock && end != n)) return QMUON_ERR_MISALIGNED_SEGMENT;
-      for (int64_t b = begin[g.tensor_index] + g.start / kBlock,
-                   e = begin[g.tensor_index] + nblocks(end); b < e; ++b) {
-        if (H[0].block_group[b] >= 0) return QMUON_ERR_INVALID_ARGUMENT;  // overlap
-        H[0].block_group[b] = g.group_id;
-      }
-    }
-  }
-  {
-    int32_t gbase = 0;
-    H[2].block_group.assign(nb, -1);
+    const int64_t nb = begin[n_tensors];
+    if (nb == 0 || nb > ((int64_t)1 << 31) - 1) return QMUON_ERR_INVALID_ARGUMENT;
+    // tiles of the MuonBP block steps must be whole 256-element runs
     for (int32_t i = 0; i < n_tensors; ++i) {
       const int64_t R = tensors[i].rows, C = tensors[i].cols;
       if (R * C == 0) continue;
-      const int64_t th = R / tile_r, tw = C / tile_c;
-      for (int64_t r = 0; r < R; ++r)
-        for (int64_t c0 = 0; c0 < C; c0 += tw) {
-          const int32_t g = gbase + (int32_t)((r / th) * tile_c + c0 / tw);
-          const int64_t e0 = r * C + c0, e1 = e0 + tw;
-          for (int64_t b = e0 / kBlock; b < nblocks(e1); ++b) H[2].block_group[begin[i] + b] = g;
-        }
-      gbase += tile_r * tile_c;
+      if (R % tile_r || C % tile_c) return QMUON_ERR_INVALID_ARGUMENT;
+      if (tile_c > 1) {
+        if (C % kBlock || (C / tile_c) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
+      } else if (tile_r > 1) {
+        if (((R / tile_r) * C) % kBlock) return QMUON_ERR_MISALIGNED_SEGMENT;
+      }
     }
-    H[2].n_groups = gbase;
-  }
 
-  // ---- device properties and geometry ----
-  cudaError_t ce = cudaGetDevice(&P->device);
-  if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaGetDevice)", ce);
-  ce = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
-  if (ce != cudaSuccess) return set_error("qmuon_plan_create (SM count)", ce);
-  const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
-  if (per_sm <= 0) return set_error_msg("qmuon_plan_create: occupancy query failed", QMUON_ERR_CUDA);
-  update_geometry(nb, P->num_sms, per_sm, &P->grid, &P->chunk);
-  for (auto& h : H) build_slots(h, P->grid, P->chunk, nb);
+    std::unique_ptr<qmuon_plan> P(new qmuon_plan);
+    P->tensors.assign(tensors, tensors + n_tensors);
+    P->q8 = q8_kind;
+    P->dt = grad_dtype;
+    P->tile_r = tile_r;
+    P->tile_c = tile_c;
+    P->nb_total = nb;
+    P->tensor_begin = begin;
 
-  // ---- one device allocation for every table, one H2D copy ----
-  std::vector<UpdTensor> ut(n_tensors);
-  for (int32_t i = 0; i < n_tensors; ++i) {
-    ut[i].q8 = tensors[i].q8;
-    ut[i].absmax = tensors[i].absmax;
-    ut[i].grad = tensors[i].grad;
-    ut[i].payload = nullptr;
-    ut[i].scale = nullptr;
-    ut[i].numel = tensors[i].rows * tensors[i].cols;
-    ut[i].block_begin = begin[i];
-    ut[i].index = i;
-  }
-  std::vector<unsigned char> blob;
-  auto put = [&blob](const void* src, size_t bytes) {
-    const size_t off = align_up(blob.size(), 256);
-    blob.resize(off + bytes);
-    if (bytes) std::memcpy(blob.data() + off, src, bytes);
-    return off;
-  };
-  const size_t o_t = put(ut.data(), ut.size() * sizeof(UpdTensor));
-  const size_t o_b = put(begin.data(), begin.size() * sizeof(int64_t));
-  size_t o_l[3][5];
-  for (int l = 0; l < 3; ++l) {
-    o_l[l][0] = put(H[l].block_group.data(), H[l].block_group.size() * 4);
-    o_l[l][1] = put(H[l].cta_slot_begin.data(), H[l].cta_slot_begin.size() * 4);
-    o_l[l][2] = put(H[l].slot_group.data(), H[l].slot_group.size() * 4);
-    o_l[l][3] = put(H[l].grp_ptr.data(), H[l].grp_ptr.size() * 4);
-    o_l[l][4] = put(H[l].grp_slots.data(), H[l].grp_slots.size() * 4);
-  }
-  ce = cudaMalloc(&P->d_table, blob.size());
-  if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaMalloc tables)", ce);
-  ce = cudaMemcpy(P->d_table, blob.data(), blob.size(), cudaMemcpyHostToDevice);
-  if (ce != cudaSuccess) {
-    cudaFree(P->d_table);
-    return set_error("qmuon_plan_create (upload tables)", ce);
-  }
-  unsigned char* base = static_cast<unsigned char*>(P->d_table);
-  P->d_tensors = reinterpret_cast<UpdTensor*>(base + o_t);
-  P->d_tensor_begin = reinterpret_cast<int64_t*>(base + o_b);
-  for (int l = 0; l < 3; ++l) {
-    GroupLayout& G = P->layout[l];
-    G.n_groups = H[l].n_groups;
-    G.n_slots = (int32_t)H[l].slot_group.size();
-    G.block_group = reinterpret_cast<const int32_t*>(base + o_l[l][0]);
-    G.cta_slot_begin = reinterpret_cast<const int32_t*>(base + o_l[l][1]);
-    G.slot_group = reinterpret_cast<const int32_t*>(base + o_l[l][2]);
-    G.grp_ptr = reinterpret_cast<const int32_t*>(base + o_l[l][3]);
-    G.grp_slots = reinterpret_cast<const int32_t*>(base + o_l[l][4]);
-    P->n_slots_max = std::max(P->n_slots_max, G.n_slots);
-  }
-  *out = P.release();
-  return QMUON_OK;
+    // ---- group layouts (host) ----
+    HostLayout H[3];
+    H[1].n_groups = n_tensors;
+    H[1].block_group.resize(nb);
+    for (int32_t i = 0; i < n_tensors; ++i)
+      std::fill(H[1].block_group.begin() + begin[i], H[1].block_group.begin() + begin[i + 1], i);
+    if (per_tensor) {
+      H[0].n_groups = n_tensors;
+      H[0].block_group = H[1].block_group;
+    } else {
+      H[0].n_groups = n_groups;
+      H[0].block_group.assign(nb, -1);
+      for (int32_t s = 0; s < n_segments; ++s) {
+        const qmuon_norm_segment& g = segments[s];
+        if (g.tensor_index < 0 || g.tensor_index >= n_tensors) return QMUON_ERR_INVALID_ARGUMENT;
+        if (g.group_id < 0 || g.group_id >= n_groups) return QMUON_ERR_INVALID_ARGUMENT;
+        const int64_t n = tensors[g.tensor_index].rows * tensors[g.tensor_index].cols;
+        if (g.start < 0 || g.length <= 0 || g.start + g.length > n) return QMUON_ERR_INVALID_ARGUMENT;
+        const int64_t end = g.start + g.length;
+        if (g.start % kBlock || (end % kBlock && end != n)) return QMUON_ERR_MISALIGNED_SEGMENT;
+        for (int64_t b = begin[g.tensor_index] + g.start / kBlock,
+                     e = begin[g.tensor_index] + nblocks(end); b < e; ++b) {
+          if (H[0].block_group[b] >= 0) return QMUON_ERR_INVALID_ARGUMENT;  // overlap
+          H[0].block_group[b] = g.group_id;
+        }
+      }
+    }
+    {
+      int32_t gbase = 0;
+      H[2].block_group.assign(nb, -1);
+      for (int32_t i = 0; i < n_tensors; ++i) {
+        const int64_t R = tensors[i].rows, C = tensors[i].cols;
+        if (R * C == 0) continue;
+        const int64_t th = R / tile_r, tw = C / tile_c;
+        for (int64_t r = 0; r < R; ++r)
+          for (int64_t c0 = 0; c0 < C; c0 += tw) {
+            const int32_t g = gbase + (int32_t)((r / th) * tile_c + c0 / tw);
+            const int64_t e0 = r * C + c0, e1 = e0 + tw;
+            for (int64_t b = e0 / kBlock; b < nblocks(e1); ++b) H[2].block_group[begin[i] + b] = g;
+          }
+        gbase += tile_r * tile_c;
+      }
+      H[2].n_groups = gbase;
+    }
+
+    // ---- device properties and geometry ----
+    cudaError_t ce = cudaGetDevice(&P->device);
+    if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaGetDevice)", ce);
+    ce = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+    if (ce != cudaSuccess) return set_error("qmuon_plan_create (SM count)", ce);
+    const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
+    if (per_sm <= 0) return set_error_msg("qmuon_plan_create: occupancy query failed", QMUON_ERR_CUDA);
+    update_geometry(nb, P->num_sms, per_sm, &P->grid, &P->chunk);
+    for (auto& h : H) build_slots(h, P->grid, P->chunk, nb);
+
+    // ---- one device allocation for every table, one H2D copy ----
+    std::vector<UpdTensor> ut(n_tensors);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      ut[i].q8 = tensors[i].q8;
+      ut[i].absmax = tensors[i].absmax;
+      ut[i].grad = tensors[i].grad;
+      ut[i].payload = nullptr;
+      ut[i].scale = nullptr;
+      ut[i].numel = tensors[i].rows * tensors[i].cols;
+      ut[i].block_begin = begin[i];
+      ut[i].index = i;
+    }
+    std::vector<unsigned char> blob;
+    auto put = [&blob](const void* src, size_t bytes) {
+      const size_t off = align_up(blob.size(), 256);
+      blob.resize(off + bytes);
+      if (bytes) std::memcpy(blob.data() + off, src, bytes);
+      return off;
+    };
+    const size_t o_t = put(ut.data(), ut.size() * sizeof(UpdTensor));
+    const size_t o_b = put(begin.data(), begin.size() * sizeof(int64_t));
+    size_t o_l[3][5];
+    for (int l = 0; l < 3; ++l) {
+      o_l[l][0] = put(H[l].block_group.data(), H[l].block_group.size() * 4);
+      o_l[l][1] = put(H[l].cta_slot_begin.data(), H[l].cta_slot_begin.size() * 4);
+      o_l[l][2] = put(H[l].slot_group.data(), H[l].slot_group.size() * 4);
+      o_l[l][3] = put(H[l].grp_ptr.data(), H[l].grp_ptr.size() * 4);
+      o_l[l][4] = put(H[l].grp_slots.data(), H[l].grp_slots.size() * 4);
+    }
+    ce = cudaMalloc(&P->d_table, blob.size());
+    if (ce != cudaSuccess) return set_error("qmuon_plan_create (cudaMalloc tables)", ce);
+    ce = cudaMemcpy(P->d_table, blob.data(), blob.size(), cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) {
+      cudaFree(P->d_table);
+      return set_error("qmuon_plan_create (upload tables)", ce);
+    }
+    unsigned char* base = static_cast<unsigned char*>(P->d_table);
+    P->d_tensors = reinterpret_cast<UpdTensor*>(base + o_t);
+    P->d_tensor_begin = reinterpret_cast<int64_t*>(base + o_b);
+    for (int l = 0; l < 3; ++l) {
+      GroupLayout& G = P->layout[l];
+      G.n_groups = H[l].n_groups;
+      G.n_slots = (int32_t)H[l].slot_group.size();
+      G.block_group = reinterpret_cast<const int32_t*>(base + o_l[l][0]);
+      G.cta_slot_begin = reinterpret_cast<const int32_t*>(base + o_l[l][1]);
+      G.slot_group = reinterpret_cast<const int32_t*>(base + o_l[l][2]);
+      G.grp_ptr = reinterpret_cast<const int32_t*>(base + o_l[l][3]);
+      G.grp_slots = reinterpret_cast<const int32_t*>(base + o_l[l][4]);
+      P->n_slots_max = std::max(P->n_slots_max, G.n_slots);
+    }
+    *out = P.release();
+    return QMUON_OK;
+  });
 }
 
 extern "C" void qmuon_plan_destroy(qmuon_plan* plan) {
@@ -530,38 +536,40 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan,
                                                          float* group_sumsq, void* ws, size_t ws_bytes,
                                                          void* stream) {
   qm::NvtxRange nvtx_range("qmuon_update_mxfp8_carrier_multi");
-  if (!plan || !payloads || !scale_invs || !inv_norms || !ws) return QMUON_ERR_INVALID_ARGUMENT;
-  if (!aligned(ws, 256) || !aligned(inv_norms, 4) || (group_sumsq && !aligned(group_sumsq, 4)))
-    return QMUON_ERR_INVALID_ARGUMENT;
-  if (ws_bytes < update_ws_bytes(plan)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
-  const int32_t n = (int32_t)plan->tensors.size();
-  std::vector<UpdTensor> ut(n);
-  for (int32_t i = 0; i < n; ++i) {
-    const qmuon_tensor& T = plan->tensors[i];
-    const int64_t numel = T.rows * T.cols;
-    if (numel > 0) {
-      if (T.cols % QMUON_SCALE_BLOCK) return QMUON_ERR_UNSUPPORTED;
-      if (!payloads[i] || !scale_invs[i] || !aligned(payloads[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+  return qm::no_throw("qmuon_update_mxfp8_carrier_multi", [&]() -> qmuon_status {
+    if (!plan || !payloads || !scale_invs || !inv_norms || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(ws, 256) || !aligned(inv_norms, 4) || (group_sumsq && !aligned(group_sumsq, 4)))
+      return QMUON_ERR_INVALID_ARGUMENT;
+    if (ws_bytes < update_ws_bytes(plan)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+    const int32_t n = (int32_t)plan->tensors.size();
+    std::vector<UpdTensor> ut(n);
+    for (int32_t i = 0; i < n; ++i) {
+      const qmuon_tensor& T = plan->tensors[i];
+      const int64_t numel = T.rows * T.cols;
+      if (numel > 0) {
+        if (T.cols % QMUON_SCALE_BLOCK) return QMUON_ERR_UNSUPPORTED;
+        if (!payloads[i] || !scale_invs[i] || !aligned(payloads[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+      }
+      ut[i].q8 = T.q8;
+      ut[i].absmax = T.absmax;
+      ut[i].grad = T.grad;
+      ut[i].payload = payloads[i];
+      ut[i].scale = scale_invs[i];
+      ut[i].numel = numel;
+      ut[i].block_begin = plan->tensor_begin[i];
+      ut[i].index = i;
     }
-    ut[i].q8 = T.q8;
-    ut[i].absmax = T.absmax;
-    ut[i].grad = T.grad;
-    ut[i].payload = payloads[i];
-    ut[i].scale = scale_invs[i];
-    ut[i].numel = numel;
-    ut[i].block_begin = plan->tensor_begin[i];
-    ut[i].index = i;
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const UpdWs w = carve(plan, ws, ws_bytes);
-  // one group per tensor (the plan's full-step layout): inverse norm i is tensor i's
-  UpdLaunch L = make_launch(plan, 1, beta, w, group_sumsq, inv_norms);
-  L.tensors = w.table;
-  cudaError_t e = cudaMemcpyAsync(w.table, ut.data(), n * sizeof(UpdTensor), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
-  if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, true, s);
-  // the pageable host table is staged by the copy before it returns
-  return cuda_status(e, "qmuon_update_mxfp8_carrier_multi (launch)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const UpdWs w = carve(plan, ws, ws_bytes);
+    // one group per tensor (the plan's full-step layout): inverse norm i is tensor i's
+    UpdLaunch L = make_launch(plan, 1, beta, w, group_sumsq, inv_norms);
+    L.tensors = w.table;
+    cudaError_t e = cudaMemcpyAsync(w.table, ut.data(), n * sizeof(UpdTensor), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
+    if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, true, s);
+    // the pageable host table is staged by the copy before it returns
+    return cuda_status(e, "qmuon_update_mxfp8_carrier_multi (launch)");
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -576,20 +584,22 @@ extern "C" qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* prob
                                                     int32_t iters, const float coeffs[3], void* ws,
                                                     size_t ws_bytes, void* stream) {
   qm::NvtxRange nvtx_range("qmuon_newton_schulz_batched");
-  if (!problems || n_problems <= 0 || iters < 1 || !coeffs || !ws) return QMUON_ERR_INVALID_ARGUMENT;
-  if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
-  for (int32_t i = 0; i < n_problems; ++i) {
-    const qmuon_status s = ns::validate_problem(problems[i]);
-    if (s != QMUON_OK) return s;
-  }
-  if (ws_bytes < kWsHeader + ns::batch_workspace_bytes(problems, n_problems))
-    return QMUON_ERR_WORKSPACE_TOO_SMALL;
-  unsigned char* b = static_cast<unsigned char*>(ws);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t me = cudaMemsetAsync(b, 0, kWsHeader, s);
-  if (me != cudaSuccess) return set_error("qmuon_newton_schulz_batched (memset)", me);
-  return ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
-                       b + kWsHeader, ws_bytes - kWsHeader, s);
+  return qm::no_throw("qmuon_newton_schulz_batched", [&]() -> qmuon_status {
+    if (!problems || n_problems <= 0 || iters < 1 || !coeffs || !ws) return QMUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+    for (int32_t i = 0; i < n_problems; ++i) {
+      const qmuon_status s = ns::validate_problem(problems[i]);
+      if (s != QMUON_OK) return s;
+    }
+    if (ws_bytes < kWsHeader + ns::batch_workspace_bytes(problems, n_problems))
+      return QMUON_ERR_WORKSPACE_TOO_SMALL;
+    unsigned char* b = static_cast<unsigned char*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t me = cudaMemsetAsync(b, 0, kWsHeader, s);
+    if (me != cudaSuccess) return set_error("qmuon_newton_schulz_batched (memset)", me);
+    return ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
+                         b + kWsHeader, ws_bytes - kWsHeader, s);
+  });
 }
 
 extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
@@ -597,31 +607,34 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
                                    const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,
                                    size_t ws_bytes, void* stream) {
   qm::NvtxRange nvtx_range("qmuon_step");
-  if (!plan || !weights || !coeffs || !ws || t < 1 || P < 0 || iters < 1) return QMUON_ERR_INVALID_ARGUMENT;
-  if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
-  if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
-  const int32_t n = (int32_t)plan->tensors.size();
-  for (int32_t i = 0; i < n; ++i) {
-    const qmuon_tensor& T = plan->tensors[i];
-    if (T.rows * T.cols == 0) continue;
-    if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
-    if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
-  }
-  if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
-  const bool full = (P != 0) && (t % P == 0);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const UpdWs w = carve(plan, ws, ws_bytes);
-  qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
-  ns::StepTables*& tabs = full ? mp->ns_full : mp->ns_block;
-  const qmuon_status ts = ns::ensure_step_tables(&tabs, plan->tensors.data(), n, full ? 1 : plan->tile_r,
-                                                 full ? 1 : plan->tile_c, weights, w.inv, w.ns, w.ns_bytes);
-  if (ts != QMUON_OK) return ts;
-  UpdLaunch L = make_launch(plan, full ? 1 : 2, beta, w, group_sumsq ? group_sumsq : w.sumsq, w.inv);
-  set_sr(L, plan->sr, plan->sr_seed, t);
-  cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
-  if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
-  if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);
-  return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+  return qm::no_throw("qmuon_step", [&]() -> qmuon_status {
+    if (!plan || !weights || !coeffs || !ws || t < 1 || P < 0 || iters < 1) return QMUON_ERR_INVALID_ARGUMENT;
+    if (!aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
+    const int32_t n = (int32_t)plan->tensors.size();
+    for (int32_t i = 0; i < n; ++i) {
+      const qmuon_tensor& T = plan->tensors[i];
+      if (T.rows * T.cols == 0) continue;
+      if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+      if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
+    }
+    if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+    const bool full = (P != 0) && (t % P == 0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const UpdWs w = carve(plan, ws, ws_bytes);
+    qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
+    ns::StepTables*& tabs = full ? mp->ns_full : mp->ns_block;
+    const qmuon_status ts = ns::ensure_step_tables(&tabs, plan->tensors.data(), n, full ? 1 : plan->tile_r,
+                                                   full ? 1 : plan->tile_c, weights, w.inv, w.ns, w.ns_bytes,
+                                                   true, s);
+    if (ts != QMUON_OK) return ts;
+    UpdLaunch L = make_launch(plan, full ? 1 : 2, beta, w, group_sumsq ? group_sumsq : w.sumsq, w.inv);
+    set_sr(L, plan->sr, plan->sr_seed, t);
+    cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
+    if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
+    if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);
+    return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+  });
 }
 
 extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
@@ -673,23 +686,25 @@ extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, 
 extern "C" qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* weights, void* ws,
                                            size_t ws_bytes) {
   qm::NvtxRange nvtx_range("qmuon_step_prepare");
-  if (!plan || !weights || !ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
-  if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
-  const int32_t n = (int32_t)plan->tensors.size();
-  for (int32_t i = 0; i < n; ++i) {
-    const qmuon_tensor& T = plan->tensors[i];
-    if (T.rows * T.cols == 0) continue;
-    if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
-    if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
-  }
-  if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
-  const UpdWs w = carve(plan, ws, ws_bytes);
-  qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
-  qmuon_status st = ns::ensure_step_tables(&mp->ns_full, plan->tensors.data(), n, 1, 1, weights, w.inv, w.ns,
-                                           w.ns_bytes);
-  if (st != QMUON_OK) return st;
-  return ns::ensure_step_tables(&mp->ns_block, plan->tensors.data(), n, plan->tile_r, plan->tile_c, weights, w.inv,
-                                w.ns, w.ns_bytes);
+  return qm::no_throw("qmuon_step_prepare", [&]() -> qmuon_status {
+    if (!plan || !weights || !ws || !aligned(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+    if (plan->dt != QMUON_BF16) return QMUON_ERR_UNSUPPORTED;
+    const int32_t n = (int32_t)plan->tensors.size();
+    for (int32_t i = 0; i < n; ++i) {
+      const qmuon_tensor& T = plan->tensors[i];
+      if (T.rows * T.cols == 0) continue;
+      if (!weights[i] || !aligned(weights[i], 16)) return QMUON_ERR_INVALID_ARGUMENT;
+      if (T.cols % 8) return QMUON_ERR_UNSUPPORTED;
+    }
+    if (ws_bytes < qmuon_workspace_size(plan, QMUON_WS_STEP)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+    const UpdWs w = carve(plan, ws, ws_bytes);
+    qmuon_plan* mp = const_cast<qmuon_plan*>(plan);
+    qmuon_status st = ns::ensure_step_tables(&mp->ns_full, plan->tensors.data(), n, 1, 1, weights, w.inv, w.ns,
+                                             w.ns_bytes, false, nullptr);
+    if (st != QMUON_OK) return st;
+    return ns::ensure_step_tables(&mp->ns_block, plan->tensors.data(), n, plan->tile_r, plan->tile_c, weights, w.inv,
+                                  w.ns, w.ns_bytes, false, nullptr);
+  });
 }
 
 extern "C" qmuon_status qmuon_sync_status(void* ws, void* stream) {
@@ -719,6 +734,7 @@ extern "C" const char* qmuon_status_string(qmuon_status status) {
     case QMUON_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case QMUON_ERR_CUDA: return "CUDA error";
     case QMUON_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+    case QMUON_ERR_OUT_OF_MEMORY: return "host memory allocation failed";
   }
   return "unknown status";
 }

@@ -716,75 +716,78 @@ extern "C" size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices,
 extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int32_t n, float mu, void* ws,
                                          size_t ws_bytes, void* stream) {
   qm::NvtxRange nvtx_range("qmuon_grasp_step");
-  using namespace qm;
-  if (!matrices || n <= 0 || !ws || !aligned_to(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
-  for (int32_t i = 0; i < n; ++i) {
-    const qmuon_status s = validate(matrices[i]);
-    if (s != QMUON_OK) return s;
-  }
-  if (ws_bytes < qmuon_grasp_workspace_size(matrices, n)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
-  unsigned char* b = static_cast<unsigned char*>(ws);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(b);
-  unsigned char* table = b + kWsHeader;
-  unsigned char* scratch = table + table_bytes(n);
-  std::vector<GraspProb> hp(n);
-  std::vector<int64_t> ts(n + 1, 0), rs(n + 1, 0), cs(n + 1, 0);
-  for (int32_t i = 0; i < n; ++i) {
-    GraspProb& P = hp[i];
-    std::memset(&P, 0, sizeof(P));
-    P.m = matrices[i];
-    P.nbr = (P.m.rows + kS - 1) / kS;
-    P.nbc = P.m.cols / kS;
-    auto carve = [&](size_t bytes) {
-      float* p = reinterpret_cast<float*>(scratch);
-      scratch += align_up(bytes, 256);
-      return p;
-    };
-    P.qinv = reinterpret_cast<double*>(carve(kRank * 8));
-    P.rdeq = carve((size_t)P.m.cols * kRank * 4);
-    P.y = carve((size_t)P.m.rows * kRank * 4);
-    P.p = carve((size_t)P.m.rows * kRank * 4);
-    P.r = carve((size_t)P.m.cols * kRank * 4);
-    P.p1 = reinterpret_cast<double*>(carve((size_t)P.m.rows * kRank * 8));
-    P.gpart = reinterpret_cast<double*>(carve((size_t)P.nbr * 36 * 8));
-    P.L = reinterpret_cast<double*>(carve(kRank * kRank * 8));
-    ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks
-    rs[i + 1] = rs[i] + P.nbr;
-    cs[i + 1] = cs[i] + P.nbc;
-  }
-  GraspArgs a{};
-  a.probs = reinterpret_cast<const GraspProb*>(table);
-  unsigned char* pre = table + align_up((size_t)n * sizeof(GraspProb), 256);
-  a.tile_start = reinterpret_cast<const int64_t*>(pre);
-  a.rstrip_start = reinterpret_cast<const int64_t*>(pre + align_up((size_t)(n + 1) * 8, 256));
-  a.cstrip_start = reinterpret_cast<const int64_t*>(pre + 2 * align_up((size_t)(n + 1) * 8, 256));
-  a.n = n;
-  a.mu = mu;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(hdr, 0, kWsHeader, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(table, hp.data(), (size_t)n * sizeof(GraspProb), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<int64_t*>(a.tile_start), ts.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<int64_t*>(a.rstrip_start), rs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<int64_t*>(a.cstrip_start), cs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return set_error("qmuon_grasp_step (upload)", e);
-  const int64_t tiles = ts[n];
-  if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
-  static cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
-  if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
-  grasp_colnorm<<<n, kThreads, 0, s>>>(a);
-  grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
-  grasp_chol<<<n, 64, 0, s>>>(a, hdr);
-  grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
-  grasp_chol<<<n, 64, 0, s>>>(a, hdr);
-  grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
-  grasp_pass2<<<(unsigned)cs[n], kThreads, kP2Smem, s>>>(a, hdr);
-  grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
-  e = cudaGetLastError();
-  // the pageable host tables are staged by the copies above before they return
-  if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
-  return QMUON_OK;
+  return qm::no_throw("qmuon_grasp_step", [&]() -> qmuon_status {
+    using namespace qm;
+    if (!matrices || n <= 0 || !ws || !aligned_to(ws, 256)) return QMUON_ERR_INVALID_ARGUMENT;
+    for (int32_t i = 0; i < n; ++i) {
+      const qmuon_status s = validate(matrices[i]);
+      if (s != QMUON_OK) return s;
+    }
+    if (ws_bytes < qmuon_grasp_workspace_size(matrices, n)) return QMUON_ERR_WORKSPACE_TOO_SMALL;
+    unsigned char* b = static_cast<unsigned char*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(b);
+    unsigned char* table = b + kWsHeader;
+    unsigned char* scratch = table + table_bytes(n);
+    std::vector<GraspProb> hp(n);
+    std::vector<int64_t> ts(n + 1, 0), rs(n + 1, 0), cs(n + 1, 0);
+    for (int32_t i = 0; i < n; ++i) {
+      GraspProb& P = hp[i];
+      std::memset(&P, 0, sizeof(P));
+      P.m = matrices[i];
+      P.nbr = (P.m.rows + kS - 1) / kS;
+      P.nbc = P.m.cols / kS;
+      auto carve = [&](size_t bytes) {
+        float* p = reinterpret_cast<float*>(scratch);
+        scratch += align_up(bytes, 256);
+        return p;
+      };
+      P.qinv = reinterpret_cast<double*>(carve(kRank * 8));
+      P.rdeq = carve((size_t)P.m.cols * kRank * 4);
+      P.y = carve((size_t)P.m.rows * kRank * 4);
+      P.p = carve((size_t)P.m.rows * kRank * 4);
+      P.r = carve((size_t)P.m.cols * kRank * 4);
+      P.p1 = reinterpret_cast<double*>(carve((size_t)P.m.rows * kRank * 8));
+      P.gpart = reinterpret_cast<double*>(carve((size_t)P.nbr * 36 * 8));
+      P.L = reinterpret_cast<double*>(carve(kRank * kRank * 8));
+      ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks
+      rs[i + 1] = rs[i] + P.nbr;
+      cs[i + 1] = cs[i] + P.nbc;
+    }
+    GraspArgs a{};
+    a.probs = reinterpret_cast<const GraspProb*>(table);
+    unsigned char* pre = table + align_up((size_t)n * sizeof(GraspProb), 256);
+    a.tile_start = reinterpret_cast<const int64_t*>(pre);
+    a.rstrip_start = reinterpret_cast<const int64_t*>(pre + align_up((size_t)(n + 1) * 8, 256));
+    a.cstrip_start = reinterpret_cast<const int64_t*>(pre + 2 * align_up((size_t)(n + 1) * 8, 256));
+    a.n = n;
+    a.mu = mu;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(hdr, 0, kWsHeader, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(table, hp.data(), (size_t)n * sizeof(GraspProb), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int64_t*>(a.tile_start), ts.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int64_t*>(a.rstrip_start), rs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int64_t*>(a.cstrip_start), cs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return set_error("qmuon_grasp_step (upload)", e);
+    const int64_t tiles = ts[n];
+    if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
+    // the opt-in belongs to the current device, so it is made on every call
+    const cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
+    if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
+    grasp_colnorm<<<n, kThreads, 0, s>>>(a);
+    grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
+    grasp_chol<<<n, 64, 0, s>>>(a, hdr);
+    grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
+    grasp_chol<<<n, 64, 0, s>>>(a, hdr);
+    grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
+    grasp_pass2<<<(unsigned)cs[n], kThreads, kP2Smem, s>>>(a, hdr);
+    grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
+    e = cudaGetLastError();
+    // the pageable host tables are staged by the copies above before they return
+    if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
+    return QMUON_OK;
+  });
 }

@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <utility>
@@ -1138,13 +1139,22 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
   return true;
 }
 
+// Host facts and setup kept per device, for a process that drives several.
+constexpr int kDeviceSlots = 64;
+
+int current_device() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 int num_sms() {
-  static int n = 0;
+  static std::atomic<int> cached[kDeviceSlots];
+  const int dev = current_device();
+  const bool slot = dev >= 0 && dev < kDeviceSlots;
+  int n = slot ? cached[dev].load(std::memory_order_relaxed) : 0;
   if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+    if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (slot) cached[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }
@@ -1260,9 +1270,13 @@ int64_t all_tiles(int64_t rows, int64_t cols) {
   return (int64_t)t[0] + t[1] + t[2];
 }
 
+// The dynamic shared memory opt-in of every kernel variant, once per device.
 cudaError_t configure_kernels() {
-  static cudaError_t result = cudaErrorNotReady;
-  if (result == cudaErrorNotReady) {
+  static std::atomic<bool> done[kDeviceSlots];
+  const int dev = current_device();
+  const bool slot = dev >= 0 && dev < kDeviceSlots;
+  if (slot && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  {
     const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<G_GRAM, kCG>, attr, (int)smem_bytes_of(G_GRAM, kCG));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ns_gemm_kernel<G_POLY, kCG>, attr, (int)smem_bytes_of(G_POLY, kCG));
@@ -1271,9 +1285,10 @@ cudaError_t configure_kernels() {
       e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE_W, kCG>, attr, (int)smem_bytes_of(G_UPDATE_W, kCG));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(ns_gemm_kernel<G_UPDATE_W1, kCG>, attr, (int)smem_bytes_of(G_UPDATE_W1, kCG));
-    result = e;
+    if (e != cudaSuccess) return e;
   }
-  return result;
+  if (slot) done[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaStream_t s) {
@@ -1441,7 +1456,8 @@ size_t step_workspace_bytes(const qmuon_tensor* t, int32_t n, int32_t tile_r, in
 }
 
 qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_t n, int32_t tile_r, int32_t tile_c,
-                                float* const* weights, const float* inv, unsigned char* ws, size_t ws_bytes) {
+                                float* const* weights, const float* inv, unsigned char* ws, size_t ws_bytes,
+                                bool ordered, cudaStream_t s) {
   StepTables* T = *tabs;
   if (T && T->ws == ws && T->ws_bytes == ws_bytes && T->inv == inv && T->tile_r == tile_r && T->tile_c == tile_c &&
       std::equal(T->weights.begin(), T->weights.end(), weights))
@@ -1468,7 +1484,15 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
   if (!T) {
     T = new StepTables;
     *tabs = T;
+  } else if (!ordered) {
+    // earlier steps, on any stream, may still read the tables rewritten below
+    const cudaError_t se = cudaDeviceSynchronize();
+    if (se != cudaSuccess) return set_error("qmuon_step_prepare: synchronize before rebuilding tables", se);
   }
+  // From here until the rebuild completes the tables match no request, so a
+  // rebuild that fails part-way is redone by the next call instead of reused.
+  T->ws = nullptr;
+  T->weights.clear();
   const int32_t np = (int32_t)hp.size();
   int64_t tiles = 0;
   for (const NsProb& P : hp) tiles += (int64_t)P.tiles[0] + P.tiles[1] + P.tiles[2];
@@ -1484,7 +1508,7 @@ qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_
   Schedule S;
   build_schedule(hp, std::min(num_sms() / kCG, kMaxGroups), T->L, S);
   carve_table(static_cast<unsigned char*>(T->d_mem), np, T->L);
-  const cudaError_t ue = upload_table(T->L, hp, S, nullptr, false);
+  const cudaError_t ue = upload_table(T->L, hp, S, s, ordered);
   if (ue != cudaSuccess) return set_error("qmuon_step: upload problem table", ue);
   T->host = std::move(hp);
   T->ws = ws;

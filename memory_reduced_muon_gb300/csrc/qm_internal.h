@@ -4,6 +4,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <exception>
+#include <new>
 
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
@@ -87,6 +89,24 @@ struct UpdLaunch {
 // QMUON_ERR_CUDA (or `status`) for convenient `return set_error(...)`.
 qmuon_status set_error(const char* where, cudaError_t e, qmuon_status status = QMUON_ERR_CUDA);
 qmuon_status set_error_msg(const char* msg, qmuon_status status);
+qmuon_status set_error_what(const char* where, const char* what, qmuon_status status);
+
+// Runs the body of a C-ABI entry so that no C++ exception leaves the library:
+// a host allocation that fails (std::bad_alloc, e.g. for the tables of a huge
+// plan) returns QMUON_ERR_OUT_OF_MEMORY, any other exception
+// QMUON_ERR_INVALID_ARGUMENT, with the detail kept for qmuon_last_error().
+template <class Body>
+qmuon_status no_throw(const char* where, Body&& body) noexcept {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return set_error_what(where, "host memory allocation failed", QMUON_ERR_OUT_OF_MEMORY);
+  } catch (const std::exception& e) {
+    return set_error_what(where, e.what(), QMUON_ERR_INVALID_ARGUMENT);
+  } catch (...) {
+    return set_error_what(where, "unexpected exception", QMUON_ERR_INVALID_ARGUMENT);
+  }
+}
 
 // Host-side launchers (update.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_update(const UpdLaunch& L, qmuon_q8_kind q8, qmuon_dtype dt, bool carrier,

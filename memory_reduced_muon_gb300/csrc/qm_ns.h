@@ -14,9 +14,13 @@ qmuon_status run_batch(const qmuon_ns_problem* probs, int32_t n, int32_t iters, 
                        WsHeader* hdr, unsigned char* ws, size_t ws_bytes, cudaStream_t s);
 
 size_t step_workspace_bytes(const qmuon_tensor* t, int32_t n, int32_t tile_r, int32_t tile_c);
+// Builds (or keeps) the tables of one step kind.  A rebuild uploads them in
+// the order of `s` when `ordered` (after the steps already enqueued there,
+// which may still read the old tables); otherwise it waits for the device to
+// finish every earlier launch and uploads them synchronously.
 qmuon_status ensure_step_tables(StepTables** tabs, const qmuon_tensor* t, int32_t n, int32_t tile_r,
                                 int32_t tile_c, float* const* weights, const float* inv,
-                                unsigned char* ws, size_t ws_bytes);
+                                unsigned char* ws, size_t ws_bytes, bool ordered, cudaStream_t s);
 qmuon_status run_step(StepTables* tabs, int32_t iters, const float coeffs[3], float eta, WsHeader* hdr,
                       cudaStream_t s);
 void destroy_step_tables(StepTables* t);

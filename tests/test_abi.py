@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     assert q.qmuon_version().startswith("qmuon")
-    for code in range(7):
+    for code in range(8):
         s = q.status_string(code)
         assert s and s != "unknown status"
     assert q.status_string(99) == "unknown status"
@@ -146,3 +146,36 @@ def test_binding_raises_when_library_missing(monkeypatch):
     monkeypatch.setattr(q, "_lib_handle", None)
     with pytest.raises(RuntimeError, match="not built"):
         q.lib()
+
+
+_OOM_CHILD = r"""
+import ctypes as C, resource, sys
+sys.path.insert(0, sys.argv[1])
+import memory_reduced_muon_gb300 as q
+L = q.lib()
+vm_kb = int([l for l in open('/proc/self/status') if l.startswith('VmSize')][0].split()[1])
+lim = vm_kb * 1024 + (2 << 30)
+resource.setrlimit(resource.RLIMIT_AS, (lim, lim))
+FAKE = 0x7F0000000000
+# one row of (2^31 - 1) * 256 elements: the most quantization blocks a plan
+# accepts, whose host group tables (about 26 GB) cannot fit in 2 GB
+t = q.qmuon_tensor(FAKE, FAKE + 0x100000, FAKE + 0x200000, 1, ((1 << 31) - 1) * 256)
+arr = (q.qmuon_tensor * 1)(t)
+out = C.c_void_p()
+st = L.qmuon_plan_create(arr, 1, 0, 0, None, 0, 0, 1, 1, C.byref(out))
+print(st, out.value, L.qmuon_last_error().decode())
+"""
+
+
+@pytest.mark.skipif(not os.path.exists("/proc/self/status"), reason="needs Linux /proc")
+def test_host_allocation_failure_returns_status(lib):
+    # A plan whose host tables cannot be allocated (address space capped in a
+    # child process) must come back as QMUON_ERR_OUT_OF_MEMORY, with no plan
+    # and no exception escaping the C ABI (that would abort the process).
+    import sys
+    r = subprocess.run([sys.executable, "-c", _OOM_CHILD, ROOT], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    status, handle, detail = r.stdout.strip().split(" ", 2)
+    assert int(status) == q.QMUON_ERR_OUT_OF_MEMORY
+    assert handle == "None"
+    assert "host memory allocation failed" in detail
