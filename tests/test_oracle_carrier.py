@@ -50,6 +50,28 @@ def test_e4m3_encode_matches_torch_on_dense_grid():
     np.testing.assert_array_equal(carrier.e4m3_encode(x), _torch_e4m3(x))
 
 
+def test_e4m3_encode_is_nearest_code_by_brute_force():
+    # the encoder against a search over the 127 non-negative finite codes,
+    # independent of torch: the nearest value wins, a tie (exactly halfway
+    # between two adjacent codes) goes to the even code, and the sign is kept
+    table = carrier.e4m3_decode_table()[:0x7F].astype(np.float64)   # codes 0x00..0x7E, ascending
+    rng = np.random.default_rng(11)
+    mags = np.concatenate([
+        np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448.0), 20000)),
+        (table[:-1] + table[1:]) / 2,      # every midpoint (exact in fp32)
+        table,                              # every code's own value
+    ]).astype(F32)
+    mags = mags[mags <= 448.0]
+    dist = np.abs(mags.astype(np.float64)[:, None] - table[None, :])
+    nearest = dist == dist.min(axis=1, keepdims=True)
+    codes = np.arange(0x7F)
+    even = np.where(nearest & (codes % 2 == 0), codes, 0x7F).min(axis=1)
+    pick = np.where(even == 0x7F, np.argmax(nearest, axis=1), even).astype(np.uint8)
+    assert int(nearest.sum(axis=1).max()) == 2   # the midpoints really are ties
+    for sign, bit in ((1.0, 0x00), (-1.0, 0x80)):
+        np.testing.assert_array_equal(carrier.e4m3_encode((sign * mags).astype(F32)), pick | bit)
+
+
 def test_e4m3_ties_to_even_and_saturation():
     # 1.0625 lies halfway between 1.0 (0x38, even) and 1.125 (0x39): -> 0x38
     # 1.1875 lies halfway between 1.125 (0x39) and 1.25 (0x3A, even): -> 0x3A
