@@ -21,6 +21,14 @@ What it computes, and where that is defined:
 * ``oracle.muonbp``  -- the MuonBP block-periodic step with two learning
   rates ("MuonBP: Faster Muon via Block-Periodic Orthogonalization",
   section "整体框架", flowchart, and "关键设计" items 1-3).
+* ``oracle.rng``     -- the Philox4x32-10 counter-based generator (Salmon et
+  al., SC'11) that draws the offsets of the stochastic requantisation in
+  ``oracle.codec`` (a reading: the momentum page lists stochastic rounding
+  as not yet implemented, section "Known Limitations").
+* ``oracle.grasp``   -- the 4-bit GRASP momentum state: a rank-8 factor
+  refreshed by one warm-started power iteration plus a grid-quantised
+  residual ("4-bit-Muon-GRASP", the update equations and the grid
+  quantisation on that page).
 
 Every function names the passage it follows.  Where the pages are silent the
 docstring states the reading taken.  Pins (tests that tie each function to
