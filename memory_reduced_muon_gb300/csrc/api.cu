@@ -497,10 +497,11 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, q
   if (tensor->cols % QMUON_SCALE_BLOCK) return QMUON_ERR_UNSUPPORTED;
   if (!aligned(payload, 16) || !aligned(ws, 256) || !aligned(inv_norm, 4)) return QMUON_ERR_INVALID_ARGUMENT;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QMUON_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMUON_ERR_CUDA;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (de != cudaSuccess) return set_error("qmuon_update_mxfp8_carrier (device query)", de);
   const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, true);
-  if (per_sm <= 0) return QMUON_ERR_CUDA;
+  if (per_sm <= 0) return set_error_msg("qmuon_update_mxfp8_carrier: occupancy query failed", QMUON_ERR_CUDA);
   int32_t grid = 0;
   int64_t chunk = 0;
   update_geometry(nblocks(n), sms, per_sm, &grid, &chunk);

@@ -179,3 +179,18 @@ def test_host_allocation_failure_returns_status(lib):
     assert int(status) == q.QMUON_ERR_OUT_OF_MEMORY
     assert handle == "None"
     assert "host memory allocation failed" in detail
+
+
+def test_cuda_failures_carry_detail(lib):
+    # with no usable device, the first CUDA call of a valid request fails:
+    # the status is QMUON_ERR_CUDA and qmuon_last_error names the entry
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a usable GPU")
+    L = q.lib()
+    assert _plan_status([_tensor(16, 256)]) == q.QMUON_ERR_CUDA
+    assert q.qmuon_last_error().startswith("qmuon_plan_create")
+    t = _tensor(4, 64)
+    r = L.qmuon_update_mxfp8_carrier(C.byref(t), 0, 0, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert r == q.QMUON_ERR_CUDA
+    assert q.qmuon_last_error().startswith("qmuon_update_mxfp8_carrier")
