@@ -15,7 +15,7 @@ takes what it can compute one by one or whole-but-affordable:
   fl(eta * U))`` exactly, with ``U`` the bf16 update left in the gradient
   buffer -- a property that holds at any size.
 
-Workloads: the fused-QKV + MLP grouped set (3 row groups of a 12288 x 4096
+Workloads: the single 512 x 512 matrix (its three steps), the fused-QKV + MLP grouped set (3 row groups of a 12288 x 4096
 tensor + 8 MLP matrices), MuonBP on four Llama-8B layers (1 x 8 column
 tiles, P = 5; a block step and a full step), the MXFP8 carrier on the same
 layers, and the 4-bit GRASP state of those 28 matrices in one call (sampled
@@ -157,6 +157,38 @@ def _oracle_matrix_step(w, t, mats, i, whole, w_before):
     new, U, info = muonbp.muonbp_step(t, w.P, [st], [hg], w.beta, w.eta_full, w.eta_block, tile=w.tile,
                                       iters=w.iters, coeffs=w.coeffs, q8_kind=w.q8_kind)
     return new[0], U[0], info
+
+
+def test_single_512_three_steps_as_benchmarked():
+    # the one-matrix 512 x 512 workload as the benchmark runs it: qmuon_step
+    # with P = 1 from a zero state for its three steps, each step against the
+    # oracle's: codes and absmax bit-exact, the group sum to 1e-5, U within the
+    # Newton-Schulz tolerance, and every weight by the exact update relation
+    w = workloads.get(1)
+    m = w.matrices[0]
+    qs, a = workloads.zero_state(m, w.q8_kind, device="cuda")
+    weight = workloads.make_weight(w, 0, device="cuda")
+    g = torch.empty(m.rows, m.cols, dtype=torch.bfloat16, device="cuda")
+    plan = q.qmuon_plan_create([(qs, a, g, m.rows, m.cols)], w.q8_kind, "bf16", tile=w.tile)
+    ws = torch.empty(q.qmuon_workspace_size(plan, q.QMUON_WS_STEP), dtype=torch.uint8, device="cuda")
+    sums = torch.zeros(1, device="cuda")
+    st = muonbp.MatrixState(m.rows, m.cols, qs.cpu().numpy().copy(), a.cpu().numpy().copy(),
+                            weight.cpu().numpy().copy())
+    for t in range(1, w.steps + 1):
+        g.copy_(workloads.make_grad(w, 0, t, device="cuda").reshape(m.rows, m.cols))
+        hg = to_oracle_grad(g, "bf16")
+        w_before = weight.clone()
+        q.qmuon_step(plan, t, w.P, w.beta, w.eta_full, w.eta_block, [weight], w.coeffs, w.iters, sums, ws)
+        q.qmuon_sync_status(ws)
+        new, U, info = muonbp.muonbp_step(t, w.P, [st], [hg], w.beta, w.eta_full, w.eta_block, tile=w.tile,
+                                          iters=w.iters, coeffs=w.coeffs, q8_kind=w.q8_kind)
+        assert info["full"]
+        np.testing.assert_array_equal(qs.cpu().numpy(), new[0].q8, err_msg=str(t))
+        np.testing.assert_array_equal(a.cpu().numpy(), new[0].absmax, err_msg=str(t))
+        np.testing.assert_allclose(sums.item(), info["S"][0], rtol=1e-5, err_msg=str(t))
+        _assert_ns(bf16_to_f64(g), codec.f32_from_bf16_bits(U[0]).astype(np.float64), ("512x512", t))
+        _check_weight_relation([m], [w_before], [weight], [g], w.eta_full)
+        st = new[0]
 
 
 @pytest.mark.parametrize("t", [1, 5], ids=["block_step", "full_step"])

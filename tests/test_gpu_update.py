@@ -129,6 +129,45 @@ def test_update_three_step_recurrence_c1():
         hq, ha = r.q8, r.absmax
 
 
+@pytest.mark.parametrize("q8_kind", ["int8", "uint8"])
+def test_long_chain_bit_exact_and_drift_bounded(q8_kind):
+    # 40 updates of one plan in a row, each bit-exact against the oracle's
+    # step from the oracle's own previous state (so no error can build up on
+    # either side), and the dequantised state within max(absmax)/254/(1-beta)
+    # of the exact fp64 EMA of the same gradients at every step
+    shapes = [(33, 1000), (1, 17), (64, 256)]
+    beta, steps = 0.95, 40
+    states = [workloads.zero_state(workloads.Matrix("t", r, c), q8_kind, device="cuda") for r, c in shapes]
+    grads = [torch.empty(r * c, dtype=torch.bfloat16, device="cuda") for r, c in shapes]
+    plan = q.qmuon_plan_create([(s, a, g, r, c) for (s, a), g, (r, c) in zip(states, grads, shapes)],
+                               q8_kind, "bf16")
+    ws = torch.empty(q.qmuon_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    sums = torch.zeros(len(shapes), device="cuda")
+    host = [(s.cpu().numpy().copy(), a.cpu().numpy().copy()) for s, a in states]
+    exact = [np.zeros(r * c) for r, c in shapes]
+    amax_seen = [np.zeros((r * c + 255) // 256) for r, c in shapes]
+    bias = [random_grad(r * c, "f32", 77 + i) for i, (r, c) in enumerate(shapes)]
+    for t in range(steps):
+        for i, g in enumerate(grads):
+            g.copy_((bias[i] + random_grad(g.numel(), "f32", 1000 + 10 * t + i)).to(torch.bfloat16))
+        hg = [to_oracle_grad(g, "bf16") for g in grads]
+        q.qmuon_update_multi_normalize_groups(plan, beta, 0, sums, None, ws)
+        q.qmuon_sync_status(ws)
+        res, S, _, _ = codec.multi_update([h[0] for h in host], [h[1] for h in host], hg, beta, q8_kind=q8_kind)
+        np.testing.assert_allclose(sums.cpu().numpy(), S, rtol=1e-5, err_msg=str(t))
+        for i, ((s, a), r) in enumerate(zip(states, res)):
+            np.testing.assert_array_equal(s.cpu().numpy(), r.q8, err_msg=f"step {t} tensor {i}")
+            np.testing.assert_array_equal(a.cpu().numpy(), r.absmax, err_msg=f"step {t} tensor {i}")
+            np.testing.assert_array_equal(to_oracle_grad(grads[i], "bf16"), r.grad, err_msg=f"step {t} tensor {i}")
+            exact[i] = beta * exact[i] + (1.0 - beta) * codec.f32_from_bf16_bits(hg[i]).astype(np.float64)
+            amax_seen[i] = np.maximum(amax_seen[i], r.absmax)
+            drift = codec.dequantize(r.q8, r.absmax, q8_kind).astype(np.float64) - exact[i]
+            bound = np.repeat(amax_seen[i] / 254.0 / (1.0 - beta), 256)[:drift.size] * (1.0 + 1e-5) \
+                + 1e-6 * np.abs(exact[i])
+            assert np.all(np.abs(drift) <= bound), (t, i)
+        host = [(r.q8, r.absmax) for r in res]
+
+
 def test_update_full_size_decoder_sampled():
     # the 24-matrix 2048-hidden workload at full size: every block checked on a
     # sample, group sums of three whole tensors against the oracle

@@ -277,3 +277,38 @@ def test_normalize_inplace():
     np.testing.assert_array_equal(codec.f32_from_bf16_bits(out[:256]), g32[:256] * 0.5)
     np.testing.assert_array_equal(codec.f32_from_bf16_bits(out[256:512]), g32[256:512] * 0.25)
     np.testing.assert_array_equal(out[512:], gb[512:])
+
+
+def test_repeated_update_drift_is_bounded():
+    # Drift of the 8-bit state away from the unquantised momentum over many
+    # steps.  A requantisation moves an element by at most absmax/254 (nearest
+    # rounding, 127 levels a side) and the EMA damps an earlier error by beta
+    # per step, so the dequantised state never strays further than
+    # max(absmax)/254/(1 - beta) from the exact fp64 EMA of the same bf16
+    # gradients (fp32 rounding adds a few ulps on top).  The typical error, a
+    # damped sum of independent roundings, stays near absmax/254/sqrt(3(1-beta^2)).
+    rng = np.random.default_rng(5)
+    n, steps, beta = 16 * 256 + 17, 100, 0.95
+    nb = codec.n_blocks(n)
+    scale = np.repeat(np.exp(rng.uniform(-6.0, 2.0, nb)), 256)[:n]
+    bias = rng.standard_normal(n)           # a persistent direction, so the EMA settles away from 0
+    q8, absmax = np.zeros(n, np.int8), np.zeros(nb, F32)
+    exact = np.zeros(n)
+    amax_seen = np.zeros(nb)
+    rms_rel = []
+    for t in range(steps):
+        g = _bf16(((bias + rng.standard_normal(n)) * scale).astype(F32))
+        exact = beta * exact + (1.0 - beta) * codec.f32_from_bf16_bits(g).astype(np.float64)
+        r = codec.momentum_update(q8, absmax, g, beta)
+        q8, absmax = r.q8, r.absmax
+        amax_seen = np.maximum(amax_seen, absmax)
+        drift = codec.dequantize(q8, absmax).astype(np.float64) - exact
+        bound = np.repeat(amax_seen / 254.0 / (1.0 - beta), 256)[:n] * (1.0 + 1e-5) + 1e-6 * np.abs(exact)
+        assert np.all(np.abs(drift) <= bound), t
+        per_block = np.repeat(absmax.astype(np.float64), 256)[:n]
+        rms_rel.append(np.sqrt(np.mean((drift / np.where(per_block > 0, per_block, 1.0)) ** 2)))
+    typical = 1.0 / 254.0 / np.sqrt(3.0 * (1.0 - beta ** 2))
+    # after a few EMA time constants it sits at the typical level and stops growing
+    late, later = np.mean(rms_rel[60:80]), np.mean(rms_rel[80:])
+    assert 0.7 * typical <= late <= 1.2 * typical and 0.7 * typical <= later <= 1.2 * typical
+    assert abs(later - late) <= 0.1 * late
