@@ -264,12 +264,18 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   // |m| <= amax, so |m * sc| <= 127 (1 + 2^-24) and rounds to at most 127;
   // amax == 0 gives sc = 0 and q = 0.  The rounding to an integer (ties to
   // even) is one fp32 addition of 1.5 * 2^23: the sum lies in [2^23, 2^24),
-  // where the spacing is 1, and its low byte is q in two's complement; a NaN
-  // product gives a zero low byte, i.e. q = 0.
+  // where the spacing is 1, and its low byte is q in two's complement.
+  // A NaN product (a NaN in m, or an infinity times sc = 0) must give q = 0,
+  // but the GPU's NaN has a nonzero low byte; max(product, -inf) turns it
+  // into -inf, whose low byte is 0, and leaves every other product as it is.
+  // (Taking that step only in blocks whose sum of squares is not finite
+  // duplicated the loop and made the kernel spill.)
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
   uint32_t qo[4];
   if constexpr (!SR) {
-    auto code = [sc](float x) { return (int)__float_as_uint(__fadd_rn(__fmul_rn(x, sc), 12582912.0f)); };
+    auto code = [sc](float x) {
+      return (int)__float_as_uint(__fadd_rn(fmaxf(__fmul_rn(x, sc), -INFINITY), 12582912.0f));
+    };
 #pragma unroll
     for (int w = 0; w < 4; ++w)
       qo[w] = pack_codes<QK>(code(m[4 * w]), code(m[4 * w + 1]), code(m[4 * w + 2]), code(m[4 * w + 3]));

@@ -59,3 +59,47 @@ def test_counter_through_the_step_and_finite_inputs():
     q.qmuon_step(plan, 2, 1, 0.9, 0.02, 0.02, weights, COEFFS, 5, sums, ws)
     q.qmuon_sync_status(ws)
     assert int(cnt.item()) == 1
+
+
+@pytest.mark.parametrize("q8_kind", ["int8", "uint8"])
+@pytest.mark.parametrize("sr", [False, True], ids=["nearest", "stochastic"])
+def test_nonfinite_blocks_follow_the_oracle(q8_kind, sr):
+    # Blocks with a NaN or an infinity in the momentum still follow the
+    # oracle's rules bit for bit: NaN lanes are ignored by the absmax, a NaN
+    # product is quantised to 0 and an infinite absmax gives zero codes.  The
+    # stored momentum matches on every element that is not NaN (a NaN is
+    # stored as some NaN).
+    import numpy as np
+    from oracle import codec
+    from gpu_util import to_oracle_grad
+
+    shapes = [(64, 512), (37, 96)]
+    mats = [workloads.Matrix(f"m{i}", r, c) for i, (r, c) in enumerate(shapes)]
+    states = [workloads.random_state(m, 30 + i, q8_kind, device="cuda") for i, m in enumerate(mats)]
+    grads = [random_grad(m.numel, "bf16", 90 + i).reshape(m.rows, m.cols) for i, m in enumerate(mats)]
+    flat = [g.view(-1) for g in grads]
+    flat[0][3 * 256 + 17] = float("nan")      # a NaN among finite values
+    flat[0][5 * 256 + 200] = float("inf")     # an infinity: absmax inf, every code 0
+    flat[0][7 * 256] = float("-inf")
+    flat[0][9 * 256:10 * 256] = float("nan")  # a block of NaN only: absmax 0
+    flat[1][3400] = float("nan")              # the partial last block of the second tensor
+    host = [(s.cpu().numpy().copy(), a.cpu().numpy().copy(), to_oracle_grad(g, "bf16")) for (s, a), g in
+            zip(states, grads)]
+    plan = q.qmuon_plan_create([(s, a, g, m.rows, m.cols) for (s, a), g, m in zip(states, grads, mats)],
+                               q8_kind, "bf16")
+    ws = torch.empty(q.qmuon_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    if sr:
+        q.qmuon_update_multi_normalize_groups_sr(plan, 0.9, 0, 1234, 3, None, None, ws)
+    else:
+        q.qmuon_update_multi_normalize_groups(plan, 0.9, 0, None, None, ws)
+    q.qmuon_sync_status(ws)
+    res, _, _, _ = codec.multi_update([h[0] for h in host], [h[1] for h in host], [h[2] for h in host], 0.9,
+                                      q8_kind=q8_kind, sr_seed=1234 if sr else None, sr_step=3)
+    for i, ((s, a), r) in enumerate(zip(states, res)):
+        np.testing.assert_array_equal(s.cpu().numpy(), r.q8, err_msg=str(i))
+        np.testing.assert_array_equal(a.cpu().numpy(), r.absmax, err_msg=str(i))
+        got = to_oracle_grad(grads[i], "bf16")
+        nan = np.isnan(codec.f32_from_bf16_bits(r.grad))
+        assert np.isnan(codec.f32_from_bf16_bits(got[nan])).all()
+        np.testing.assert_array_equal(got[~nan], r.grad[~nan], err_msg=str(i))
+    assert res[0].absmax[5] == np.inf and res[0].absmax[9] == 0.0   # the cases are really there
