@@ -71,3 +71,25 @@ def test_step_flop_count_matches_page_formula():
     block = bench.step_ns_flops(w, False)
     assert abs(full - 8.324e13) / 8.324e13 < 1e-3      # 2(2nm^2+m^3) x 5 over the 28 matrices
     assert abs(block - 1.705e13) / 1.705e13 < 1e-3     # the same over 224 tiles of 1x8 columns
+
+
+def test_reference_arm_prints_the_contract_line():
+    # `bench.py --impl reference` (the CPU oracle arm) prints one JSON line
+    # with the keys of the benchmark contract, on the CPU, without a GPU
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "1", "--steps", "2",
+                        "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "Mparams/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "single_512"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "Mparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
