@@ -194,3 +194,55 @@ def test_cuda_failures_carry_detail(lib):
     r = L.qmuon_update_mxfp8_carrier(C.byref(t), 0, 0, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None)
     assert r == q.QMUON_ERR_CUDA
     assert q.qmuon_last_error().startswith("qmuon_update_mxfp8_carrier")
+
+
+_C_CALLER = r"""
+/* A plain C99 caller of the library: the header must compile as C, and the
+ * entries must link and answer without a GPU. */
+#include <stdio.h>
+#include <string.h>
+#include "qmuon.h"
+
+int main(void) {
+  qmuon_plan* plan = (qmuon_plan*)0x1;
+  qmuon_tensor t;
+  memset(&t, 0, sizeof(t));
+  if (qmuon_plan_create(&t, 0, QMUON_Q8_INT8, QMUON_BF16, NULL, 0, 0, 1, 1, &plan) != QMUON_ERR_INVALID_ARGUMENT)
+    return 1;
+  if (plan != NULL) return 2;
+  if (qmuon_workspace_size(NULL, QMUON_WS_STEP) != 0) return 3;
+  if (strcmp(qmuon_status_string(QMUON_OK), "ok") != 0) return 4;
+  if (strncmp(qmuon_version(), "qmuon", 5) != 0) return 5;
+  if (sizeof(qmuon_tensor) != 40 || sizeof(qmuon_norm_segment) != 24 || sizeof(qmuon_ns_problem) != 64 ||
+      sizeof(qmuon_grasp_matrix) != 96)
+    return 6;
+  printf("%s\n", qmuon_version());
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    # the boundary is a C ABI: a C99 program built with gcc against the header
+    # and the shared library calls it directly, without Python or torch
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "caller.c"
+    src.write_text(_C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(q.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", libdir, "-lqmuon", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    if r.returncode != 0 and "cannot find -lqmuon" in r.stderr:
+        r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                            str(src), "-o", str(exe), q.LIB_PATH, "-Wl,-rpath," + libdir],
+                           capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.startswith("qmuon")
+    # the binding's structures have the sizes the C compiler gave them
+    assert [C.sizeof(t) for t in (q.qmuon_tensor, q.qmuon_norm_segment, q.qmuon_ns_problem,
+                                  q.qmuon_grasp_matrix)] == [40, 24, 64, 96]
