@@ -312,3 +312,19 @@ def test_repeated_update_drift_is_bounded():
     late, later = np.mean(rms_rel[60:80]), np.mean(rms_rel[80:])
     assert 0.7 * typical <= late <= 1.2 * typical and 0.7 * typical <= later <= 1.2 * typical
     assert abs(later - late) <= 0.1 * late
+
+
+def test_inverse_norm_adds_eps_to_the_norm():
+    # the reading inv = 1/(||m|| + 1e-7), epsilon added to the norm: an empty
+    # (all-zero) group gives 1e7 exactly, and a group of 256 values 2^-10
+    # (sum of squares 2^-12, norm 2^-6) gives 1/(2^-6 + 1e-7) = 64/(1 + 6.4e-6)
+    # = 63.99959040262142...; epsilon under the root would give 3162.3 and 63.987
+    q8, a = np.zeros(512, np.int8), np.zeros(2, F32)
+    g = np.zeros(512, F32)
+    g[256:] = 2.0 ** -10
+    r = codec.momentum_update(q8, a, _bf16(g), 0.0)          # beta = 0: m = g exactly
+    groups = codec.block_groups([512], [codec.NormSegment(0, 0, 256, 0), codec.NormSegment(0, 256, 256, 1)], 2)
+    S, inv = codec.group_sumsq([r.block_sumsq], groups, 2)
+    assert S.tolist() == [0.0, 2.0 ** -12]
+    assert inv[0] == F32(1e7)
+    assert inv[1] == F32(63.99959040262142)

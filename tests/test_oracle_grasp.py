@@ -152,3 +152,22 @@ def test_low_rank_gradient_leaves_small_residual():
         st = out.state
     mt = codec.f32_from_bf16_bits(out.m_bits).astype(np.float64)
     assert np.linalg.norm(out.res) < 0.01 * np.linalg.norm(mt)
+
+
+def test_state_reconstructs_the_momentum():
+    # the stored state (grid-quantised 4-bit residual and 8-bit factors)
+    # dequantises to M_t up to quantisation error, which is small next to the
+    # rank-k part it carries; here a rank-8 signal plus noise over three steps
+    # with mu = 0.9, so the reconstruction of M_{t-1} feeds every later step
+    rng = np.random.default_rng(12)
+    rows, cols, k = 160, 128, 8
+    low = rng.standard_normal((rows, k)) @ rng.standard_normal((k, cols))
+    st = _state(rows, cols, 13, k)
+    for _ in range(3):
+        g = codec.bf16_bits_from_f32((low + 0.3 * rng.standard_normal((rows, cols))).astype(np.float32).reshape(-1))
+        out = grasp.grasp_step(st, g, 0.9)
+        st = out.state
+    mt = codec.f32_from_bf16_bits(out.m_bits).astype(np.float64)
+    rec = grasp.reconstruct(*grasp.dequantize_parts(st)).astype(np.float64)
+    assert np.linalg.norm(rec - mt) < 0.02 * np.linalg.norm(mt)          # measured 0.8%
+    assert np.linalg.norm(out.p @ out.r.T) > 0.9 * np.linalg.norm(mt)   # the factor carries the signal

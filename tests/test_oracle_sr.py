@@ -142,3 +142,20 @@ def test_fp64_floor_is_exact():
         got = np.floor(np.float64(x) + k * 2.0 ** -24)
         exact = (Fraction(float(x)) + Fraction(k, 2 ** 24)).__floor__()
         assert got == exact, (x, k)
+
+
+def test_exact_integer_sums_floor_to_themselves():
+    # x + u landing exactly on an integer must give that integer (floor of an
+    # exact sum).  With beta = 0 and fp32 gradients m = g, and with 127 in the
+    # block, sc = 127/127 = 1 and x = m; x = 1 - u (exact in fp32, since u is a
+    # multiple of 2^-24 below 1) then sums to exactly 1 for every element
+    from oracle import rng
+    seed, step, tensor = 21, 4, 2
+    u = rng.rounding_uniforms(256, seed, step, tensor)
+    g = (1.0 - u).astype(np.float32)
+    g[0] = 127.0
+    assert np.array_equal(g[1:].astype(np.float64) + u[1:], np.ones(255))
+    r = codec.momentum_update(np.zeros(256, np.int8), np.zeros(1, np.float32), g, 0.0, grad_dtype="f32",
+                              rounding=codec.StochasticRounding(seed, step, tensor))
+    assert r.absmax[0] == 127.0
+    assert int(r.q8[0]) == 127 and np.all(r.q8[1:] == 1)
