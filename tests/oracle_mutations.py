@@ -37,34 +37,50 @@ MUTATIONS = {
                                      "block_sumsq = np.sum(np.abs(m64), axis=1)", CODEC),
     "inverse_norm_eps_inside_sqrt": ("oracle.codec", "(1.0 / (np.sqrt(S) + EPS))", "(1.0 / np.sqrt(S + EPS))",
                                      CODEC),
+    "normalize_divides": ("oracle.codec", "scaled = (g32 * scale[:, None])", "scaled = (g32 / scale[:, None])", CODEC),
+    "segment_tail_rejected": ("oracle.codec", "(end % QBLOCK and end != n)", "(end % QBLOCK)", CODEC),
+    "dequantize_over_128": ("oracle.codec", "(np.asarray(absmax, dtype=F32) / F32(127.0))",
+                            "(np.asarray(absmax, dtype=F32) / F32(128.0))", CODEC),
     # Newton-Schulz ("NVIDIA impulsa ... Megatron", section "Newton-Schulz distribuido")
     "ns_poly_sign_of_c": ("oracle.ns", "B = b * A + c * (A @ A)", "B = b * A - c * (A @ A)", NS),
     "ns_drops_a_term": ("oracle.ns", "X = a * X + B @ X", "X = B @ X", NS),
     "ns_update_on_the_right": ("oracle.ns", "X = a * X + B @ X", "X = a * X + X @ B", NS),
     "ns_gram_transposed": ("oracle.ns", "A = X @ X.T", "A = X.T @ X", NS),
+    "ns_inverse_norm_divides": ("oracle.ns", "X = X * float(inv_norm)", "X = X / float(inv_norm)", NS),
     # MuonBP ("MuonBP: Faster Muon via Block-Periodic Orthogonalization", section "整体框架")
     "muonbp_full_step_offset": ("oracle.muonbp", "return P != 0 and t % P == 0", "return P != 0 and t % P == 1", NS),
     "muonbp_learning_rates_swapped": ("oracle.muonbp", "eta = F32(eta_full if full else eta_block)",
                                       "eta = F32(eta_block if full else eta_full)", NS),
     "muonbp_shared_tile_norm": ("oracle.muonbp", "inv_norm=float(inv[g])", "inv_norm=float(inv[gbase])", NS),
+    "muonbp_tile_column_offset": ("oracle.muonbp", "r * cols + j * tw", "r * cols + j * th", NS),
     # MXFP8 carrier ("Quantized Muon Momentum", section "Wave18B MXFP8 Carrier Probe")
     "e4m3_subnormal_exponent": ("oracle.carrier", "2.0 ** (1 - 7)", "2.0 ** (0 - 7)", CARRIER),
     "e4m3_ties_to_odd": ("oracle.carrier", "(lo % 2 == 0)", "(lo % 2 == 1)", CARRIER),
     "e4m3_bias_8": ("oracle.carrier", "2.0 ** (e - 7)", "2.0 ** (e - 8)", CARRIER),
     "e8m0_not_minimal": ("oracle.carrier", "while amax > math.ldexp(E4M3_MAX, e)",
                          "while amax >= math.ldexp(E4M3_MAX, e)", CARRIER),
+    "carrier_scale_inverted": ("oracle.carrier", "127 - bytes_.astype(np.int64)", "bytes_.astype(np.int64) - 127",
+                               CARRIER),
+    "carrier_norm_without_root": ("oracle.carrier", "(math.sqrt(S) + codec.EPS)", "(S + codec.EPS)", CARRIER),
     # Philox4x32-10 (Salmon et al., SC'11) for the stochastic requantisation
     "philox_multiplier": ("oracle.rng", "M0 = 0xD2511F53\n", "M0 = 0xD2511F55\n", SR),
     "philox_key_bumped_before_round_one": ("oracle.rng", "if r > 0:", "if r >= 0:", SR),
     "philox_words_crossed": ("oracle.rng", "(p1 >> np.uint64(32)) ^ c1 ^ k0", "(p0 >> np.uint64(32)) ^ c1 ^ k0", SR),
     "sr_floor_replaced_by_rint": ("oracle.codec", "r = np.floor(x.astype(np.float64) + u)",
                                   "r = np.rint(x.astype(np.float64) + u - 0.5)", SR),
+    "sr_counter_tensor_word_is_step": ("oracle.rng", "ctr[:, 2] = np.uint64(tensor_index & _MASK)",
+                                       "ctr[:, 2] = np.uint64(step & _MASK)", SR),
+    "sr_uniform_scale_2_23": ("oracle.rng", "* 2.0 ** -24", "* 2.0 ** -23", SR),
     # GRASP ("4-bit-Muon-GRASP", the update equations and the grid quantisation)
     "grasp_grid_uses_max": ("oracle.grasp", "return np.minimum(rb, cb).astype(F32)",
                             "return np.maximum(rb, cb).astype(F32)", GRASP),
     "grasp_reconstruct_subtracts": ("oracle.grasp", "return (res + acc).astype(F32)",
                                     "return (res - acc).astype(F32)", GRASP),
     "grasp_residual_sign": ("oracle.grasp", "resid = mt - p @ r.T", "resid = mt + p @ r.T", GRASP),
+    "grasp_levels_2_pow_b_minus_1": ("oracle.grasp", "L = F32(2 ** (bits - 1) - 1)\n    nbr",
+                                     "L = F32(2 ** (bits - 1))\n    nbr", GRASP),
+    "grasp_nibbles_swapped": ("oracle.grasp", "(u[:, 0::2] | (u[:, 1::2] << 4))", "(u[:, 1::2] | (u[:, 0::2] << 4))",
+                              GRASP),
     "grasp_momentum_mu_on_gradient": ("oracle.grasp", "m = ((F32(mu) * m_prev).astype(F32) + g).astype(F32)",
                                       "m = (m_prev + (F32(mu) * g).astype(F32)).astype(F32)", GRASP),
 }

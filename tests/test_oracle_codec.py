@@ -328,3 +328,20 @@ def test_inverse_norm_adds_eps_to_the_norm():
     assert S.tolist() == [0.0, 2.0 ** -12]
     assert inv[0] == F32(1e7)
     assert inv[1] == F32(63.99959040262142)
+
+
+@pytest.mark.parametrize("q8_kind", ["int8", "uint8"])
+def test_dequantize_fixed_points(q8_kind):
+    # step 2's scale is absmax/127: with absmax 127 every code dequantises to
+    # itself, with absmax 254 to twice itself (both exact in fp32), with absmax
+    # 0 to zero, and the ends +-127 always give +-absmax
+    q = np.arange(-127, 128, dtype=np.int32)
+    q = np.concatenate([q, q[:1]])                          # 256 codes = one block
+    codes = codec.int_to_q8(q, q8_kind)
+    for amax, mult in ((127.0, 1.0), (254.0, 2.0), (0.0, 0.0)):
+        d = codec.dequantize(codes, np.array([amax], F32), q8_kind)
+        assert np.array_equal(d, (q * mult).astype(F32)), amax
+    for amax in (0.37, 1e-20, 3e30):
+        d = codec.dequantize(codes, np.array([amax], F32), q8_kind)
+        assert abs(d[0] + F32(amax)) <= F32(amax) * 2 ** -23     # code -127: two roundings of -absmax
+        assert abs(d[254] - F32(amax)) <= F32(amax) * 2 ** -23
