@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert name in exported, name
         assert hasattr(lib, name)
-    assert set(q.exported_symbols()) <= set(declared_symbols())
+    assert set(q.exported_symbols()) == set(declared_symbols())   # the binding covers the whole header
 
 
 def test_status_strings_and_version(lib):
@@ -246,3 +246,26 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     # the binding's structures have the sizes the C compiler gave them
     assert [C.sizeof(t) for t in (q.qmuon_tensor, q.qmuon_norm_segment, q.qmuon_ns_problem,
                                   q.qmuon_grasp_matrix)] == [40, 24, 64, 96]
+
+
+def _declared_arities():
+    # QMUON_API <ret> name(<params>);  -> number of parameters ("void" = 0)
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"QMUON_API\s+[\w\s\*]+?\b(qmuon_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    # every entry the binding sets up takes as many arguments as the header
+    # declares (ctypes would otherwise pass garbage or drop arguments)
+    arity = _declared_arities()
+    assert set(arity) == set(declared_symbols())
+    L = q.lib()
+    for name in q.exported_symbols():
+        fn = getattr(L, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == arity[name], (name, len(fn.argtypes), arity[name])
