@@ -93,3 +93,29 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "Mparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_clock_sampler_summarises_nvidia_smi_lines():
+    # the clocks record of the bench line from nvidia-smi's CSV rows (index,
+    # sm, max sm, power, active, hw_slowdown, hw_thermal, sw_thermal,
+    # sw_power_cap): median SM clock under load, the maximum, and every
+    # throttle reason seen active
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = bench.ClockSampler(0)
+    s.proc = _Done()
+    s.lines = ["0, 1965, 2070, 1100.5, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 1710, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 1800, 2070, 1250.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "[N/A] garbled line",
+               "0, 1500, 2070, 1400.0, 0x40, Not Active, Active, Not Active, Not Active"]
+    c = s.stop()
+    assert c["samples"] == 4 and c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == 1755.0                                   # median of 1965, 1710, 1800, 1500
+    assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler(0).stop()["reasons"] == ["nvidia-smi unavailable"]
