@@ -10,7 +10,9 @@ once per entry in a child process with ``QMUON_PLANT_ORACLE_MISTAKE`` set
 
 Changes that leave the mathematics intact are not listed: skipping ColNorm
 before the thin QR, for one, scales the columns of M_t Q by positive numbers
-and so gives the same positive-diagonal factor P.
+and so gives the same positive-diagonal factor P; nor does restoring the
+blocks outside every group after the in-place normalisation, whose scale
+there is already 1.
 """
 
 import importlib
@@ -37,6 +39,12 @@ MUTATIONS = {
                                      "block_sumsq = np.sum(np.abs(m64), axis=1)", CODEC),
     "inverse_norm_eps_inside_sqrt": ("oracle.codec", "(1.0 / (np.sqrt(S) + EPS))", "(1.0 / np.sqrt(S + EPS))",
                                      CODEC),
+    "bf16_ties_away": ("oracle.codec", "lsb = (u >> 16) & 1", "lsb = 1", CODEC),
+    "one_minus_beta_in_fp64": ("oracle.codec", "omb = F32(F32(1.0) - beta32)", "omb = F32(1.0 - float(beta))", CODEC),
+    "tail_padding_kept": ("oracle.codec", "m.reshape(-1)[numel:] = 0.0", "m.reshape(-1)[numel:] = 1.0", CODEC),
+    "zero_block_codes_not_forced": ("oracle.codec", "qn = np.where(amax[:, None] == 0, 0, qn)",
+                                    "qn = np.where(amax[:, None] == 0, 1, qn)", CODEC),
+    "segment_overlap_allowed": ("oracle.codec", "if np.any(arr[b0:b1] >= 0):", "if False:", CODEC),
     "normalize_divides": ("oracle.codec", "scaled = (g32 * scale[:, None])", "scaled = (g32 / scale[:, None])", CODEC),
     "segment_tail_rejected": ("oracle.codec", "(end % QBLOCK and end != n)", "(end % QBLOCK)", CODEC),
     "dequantize_over_128": ("oracle.codec", "(np.asarray(absmax, dtype=F32) / F32(127.0))",
@@ -52,6 +60,8 @@ MUTATIONS = {
     "muonbp_learning_rates_swapped": ("oracle.muonbp", "eta = F32(eta_full if full else eta_block)",
                                       "eta = F32(eta_block if full else eta_full)", NS),
     "muonbp_shared_tile_norm": ("oracle.muonbp", "inv_norm=float(inv[g])", "inv_norm=float(inv[gbase])", NS),
+    "muonbp_row_tile_offset": ("oracle.muonbp", "segs.append(codec.NormSegment(tensor_index, i * th * cols, th * cols, g))",
+                               "segs.append(codec.NormSegment(tensor_index, i * th, th * cols, g))", NS),
     "muonbp_tile_column_offset": ("oracle.muonbp", "r * cols + j * tw", "r * cols + j * th", NS),
     # MXFP8 carrier ("Quantized Muon Momentum", section "Wave18B MXFP8 Carrier Probe")
     "e4m3_subnormal_exponent": ("oracle.carrier", "2.0 ** (1 - 7)", "2.0 ** (0 - 7)", CARRIER),
@@ -59,6 +69,10 @@ MUTATIONS = {
     "e4m3_bias_8": ("oracle.carrier", "2.0 ** (e - 7)", "2.0 ** (e - 8)", CARRIER),
     "e8m0_not_minimal": ("oracle.carrier", "while amax > math.ldexp(E4M3_MAX, e)",
                          "while amax >= math.ldexp(E4M3_MAX, e)", CARRIER),
+    "e8m0_zero_block_byte": ("oracle.carrier", "return 127 if amax == 0.0 else 254", "return 0 if amax == 0.0 else 254",
+                             CARRIER),
+    "carrier_decode_scale_stride": ("oracle.carrier", "np.repeat(e8m0_value(scale_inv), SCALE_BLOCK, axis=1)",
+                                    "np.tile(e8m0_value(scale_inv), (1, SCALE_BLOCK))", CARRIER),
     "carrier_scale_inverted": ("oracle.carrier", "127 - bytes_.astype(np.int64)", "bytes_.astype(np.int64) - 127",
                                CARRIER),
     "carrier_norm_without_root": ("oracle.carrier", "(math.sqrt(S) + codec.EPS)", "(S + codec.EPS)", CARRIER),
@@ -79,6 +93,12 @@ MUTATIONS = {
     "grasp_residual_sign": ("oracle.grasp", "resid = mt - p @ r.T", "resid = mt + p @ r.T", GRASP),
     "grasp_levels_2_pow_b_minus_1": ("oracle.grasp", "L = F32(2 ** (bits - 1) - 1)\n    nbr",
                                      "L = F32(2 ** (bits - 1))\n    nbr", GRASP),
+    "grasp_dequant_step_times_level": ("oracle.grasp", "step = (d / L).astype(F32)", "step = (d * L).astype(F32)",
+                                       GRASP),
+    "grasp_row_max_over_whole_row": ("oracle.grasp", "rmax[bj] = a[:, bj * s_cols:(bj + 1) * s_cols].max(axis=1)",
+                                     "rmax[bj] = a.max(axis=1)", GRASP),
+    "grasp_qr_sign_not_fixed": ("oracle.grasp", "sgn = np.where(np.diag(rf) < 0, -1.0, 1.0)",
+                                "sgn = np.ones(rf.shape[0])", GRASP),
     "grasp_nibbles_swapped": ("oracle.grasp", "(u[:, 0::2] | (u[:, 1::2] << 4))", "(u[:, 1::2] | (u[:, 0::2] << 4))",
                               GRASP),
     "grasp_momentum_mu_on_gradient": ("oracle.grasp", "m = ((F32(mu) * m_prev).astype(F32) + g).astype(F32)",

@@ -181,6 +181,10 @@ def test_bf16_and_fp16_storage_match_torch():
     rng = np.random.default_rng(3)
     x = (rng.standard_normal(1 << 16) * 10 ** rng.uniform(-30, 30, 1 << 16)).astype(F32)
     x[:4] = [0.0, -0.0, 3.4e38, -1e-45]
+    # exact ties (low half 0x8000) above an even and an odd bf16, both signs
+    k = (np.arange(1, 4096, dtype=np.uint32) * 7919) % 0x7F7F
+    ties = ((k << 16) | 0x8000).view(F32)
+    x = np.concatenate([x, ties, -ties])
     ours = codec.bf16_bits_from_f32(x)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(ours, ref)

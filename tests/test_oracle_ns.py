@@ -121,21 +121,23 @@ def test_p1_is_muon_and_1x1_tiling_is_full():
         np.testing.assert_allclose(dW, 0.02 * got, rtol=1e-6, atol=2e-8)  # one fp32 ulp of |W|
 
 
-def test_block_step_is_per_tile_closed_form():
-    # tile widths must be multiples of 256; the second matrix has tall tiles
+@pytest.mark.parametrize("tr,tc", [(2, 4), (4, 1)])
+def test_block_step_is_per_tile_closed_form(tr, tc):
+    # tile widths must be multiples of 256 (or, for row tiles, tile sizes);
+    # the second matrix has tall tiles
     shapes = [(8, 1024), (600, 1024)]
     states, grads = _states(shapes, 5)
-    new, U, info = muonbp.muonbp_step(2, 5, states, grads, 0.95, 0.02, 0.00707, tile=(2, 4))
-    assert not info["full"] and info["n_groups"] == 16
+    new, U, info = muonbp.muonbp_step(2, 5, states, grads, 0.95, 0.02, 0.00707, tile=(tr, tc))
+    assert not info["full"] and info["n_groups"] == 2 * tr * tc
     g = 0
     for k, (r, c) in enumerate(shapes):
         res = codec.momentum_update(states[k].q8, states[k].absmax, grads[k], 0.95)
         M = res.m.reshape(r, c).astype(np.float64)
         Mb = codec.f32_from_bf16_bits(res.grad).reshape(r, c).astype(np.float64)
         got = codec.f32_from_bf16_bits(U[k]).astype(np.float64)
-        th, tw = r // 2, c // 4
-        for i in range(2):
-            for j in range(4):
+        th, tw = r // tr, c // tc
+        for i in range(tr):
+            for j in range(tc):
                 tile = M[i * th:(i + 1) * th, j * tw:(j + 1) * tw]
                 inv = 1.0 / (np.linalg.norm(tile) + 1e-7)     # the tile's own norm
                 assert abs(info["inv"][g] - inv) <= 1e-6 * inv
@@ -145,3 +147,18 @@ def test_block_step_is_per_tile_closed_form():
                 g += 1
         dW = states[k].weight.astype(np.float64) - new[k].weight
         np.testing.assert_allclose(dW, 0.00707 * got, rtol=1e-6, atol=2e-8)
+
+
+@pytest.mark.parametrize("rows,cols,tr,tc", [(8, 1024, 2, 4), (6, 512, 3, 1), (12, 768, 4, 3), (5, 256, 1, 1)])
+def test_tile_segments_cover_exactly_their_tiles(rows, cols, tr, tc):
+    # brute force: mark every element each segment names, and compare with
+    # the tile (i, j) the element's row and column put it in
+    segs = muonbp.tile_segments(rows, cols, tr, tc, tensor_index=3, group_base=10)
+    got = np.full(rows * cols, -1)
+    for s in segs:
+        assert s.tensor_index == 3
+        assert np.all(got[s.start:s.start + s.length] == -1)          # no element twice
+        got[s.start:s.start + s.length] = s.group_id
+    r, c = np.divmod(np.arange(rows * cols), cols)
+    expect = 10 + (r // (rows // tr)) * tc + c // (cols // tc)
+    np.testing.assert_array_equal(got, expect)
