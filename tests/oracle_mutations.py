@@ -45,6 +45,11 @@ MUTATIONS = {
     "zero_block_codes_not_forced": ("oracle.codec", "qn = np.where(amax[:, None] == 0, 0, qn)",
                                     "qn = np.where(amax[:, None] == 0, 1, qn)", CODEC),
     "segment_overlap_allowed": ("oracle.codec", "if np.any(arr[b0:b1] >= 0):", "if False:", CODEC),
+    "absmax_propagates_nan": ("oracle.codec", "amax = np.fmax.reduce(np.abs(m), axis=1", "amax = np.maximum.reduce(np.abs(m), axis=1",
+                              CODEC),
+    "nan_code_not_zeroed": ("oracle.codec", "r = np.where(np.isnan(r), 0.0, r)", "r = np.where(np.isnan(r), 127.0, r)",
+                            CODEC),
+    "group_sum_overwrites": ("oracle.codec", "S[g] += float(np.sum(bs[sel]))", "S[g] = float(np.sum(bs[sel]))", CODEC),
     "normalize_divides": ("oracle.codec", "scaled = (g32 * scale[:, None])", "scaled = (g32 / scale[:, None])", CODEC),
     "segment_tail_rejected": ("oracle.codec", "(end % QBLOCK and end != n)", "(end % QBLOCK)", CODEC),
     "dequantize_over_128": ("oracle.codec", "(np.asarray(absmax, dtype=F32) / F32(127.0))",
@@ -62,6 +67,7 @@ MUTATIONS = {
     "muonbp_shared_tile_norm": ("oracle.muonbp", "inv_norm=float(inv[g])", "inv_norm=float(inv[gbase])", NS),
     "muonbp_row_tile_offset": ("oracle.muonbp", "segs.append(codec.NormSegment(tensor_index, i * th * cols, th * cols, g))",
                                "segs.append(codec.NormSegment(tensor_index, i * th, th * cols, g))", NS),
+    "muonbp_group_base_step": ("oracle.muonbp", "gbase += tr * tc", "gbase += 1", NS),
     "muonbp_tile_column_offset": ("oracle.muonbp", "r * cols + j * tw", "r * cols + j * th", NS),
     # MXFP8 carrier ("Quantized Muon Momentum", section "Wave18B MXFP8 Carrier Probe")
     "e4m3_subnormal_exponent": ("oracle.carrier", "2.0 ** (1 - 7)", "2.0 ** (0 - 7)", CARRIER),

@@ -349,3 +349,19 @@ def test_dequantize_fixed_points(q8_kind):
         d = codec.dequantize(codes, np.array([amax], F32), q8_kind)
         assert abs(d[0] + F32(amax)) <= F32(amax) * 2 ** -23     # code -127: two roundings of -absmax
         assert abs(d[254] - F32(amax)) <= F32(amax) * 2 ** -23
+
+
+def test_nonfinite_momentum_readings():
+    # the readings for non-finite momenta: the absmax ignores NaN lanes (an
+    # all-NaN block gets 0), a NaN product gives code 0, and an infinity makes
+    # the absmax infinite and every code of its block 0.  beta = 0, so m = g
+    g = np.zeros(768, F32)
+    g[0], g[1], g[2] = np.nan, 2.0, -1.0          # block 0: NaN among finite values
+    g[256:512] = np.nan                           # block 1: NaN only
+    g[512], g[513] = np.inf, 3.0                  # block 2: an infinity
+    r = codec.momentum_update(np.zeros(768, np.int8), np.zeros(3, F32), g, 0.0, grad_dtype="f32")
+    assert r.absmax.tolist() == [2.0, 0.0, np.inf]
+    q = r.q8.astype(np.int32)
+    assert q[0] == 0 and q[1] == 127 and q[2] == -64          # -1 * 63.5 = -63.5 -> -64 (ties to even)
+    assert np.all(q[256:512] == 0) and np.all(q[512:] == 0)
+    assert np.isnan(r.block_sumsq[0]) and np.isnan(r.block_sumsq[1]) and r.block_sumsq[2] == np.inf
