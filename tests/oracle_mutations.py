@@ -50,6 +50,9 @@ MUTATIONS = {
     "nan_code_not_zeroed": ("oracle.codec", "r = np.where(np.isnan(r), 0.0, r)", "r = np.where(np.isnan(r), 127.0, r)",
                             CODEC),
     "group_sum_overwrites": ("oracle.codec", "S[g] += float(np.sum(bs[sel]))", "S[g] = float(np.sum(bs[sel]))", CODEC),
+    "segment_drops_partial_last_block": ("oracle.codec", "b0, b1 = s.start // QBLOCK, n_blocks(end)",
+                                         "b0, b1 = s.start // QBLOCK, end // QBLOCK", CODEC),
+    "eps_1e6": ("oracle.codec", "EPS = 1e-7", "EPS = 1e-6", CODEC),
     "normalize_divides": ("oracle.codec", "scaled = (g32 * scale[:, None])", "scaled = (g32 / scale[:, None])", CODEC),
     "segment_tail_rejected": ("oracle.codec", "(end % QBLOCK and end != n)", "(end % QBLOCK)", CODEC),
     "dequantize_over_128": ("oracle.codec", "(np.asarray(absmax, dtype=F32) / F32(127.0))",
@@ -59,6 +62,8 @@ MUTATIONS = {
     "ns_drops_a_term": ("oracle.ns", "X = a * X + B @ X", "X = B @ X", NS),
     "ns_update_on_the_right": ("oracle.ns", "X = a * X + B @ X", "X = a * X + X @ B", NS),
     "ns_gram_transposed": ("oracle.ns", "A = X @ X.T", "A = X.T @ X", NS),
+    "ns_coefficients_reversed": ("oracle.ns", "a, b, c = (float(v) for v in coeffs)",
+                                 "c, b, a = (float(v) for v in coeffs)", NS),
     "ns_inverse_norm_divides": ("oracle.ns", "X = X * float(inv_norm)", "X = X / float(inv_norm)", NS),
     # MuonBP ("MuonBP: Faster Muon via Block-Periodic Orthogonalization", section "整体框架")
     "muonbp_full_step_offset": ("oracle.muonbp", "return P != 0 and t % P == 0", "return P != 0 and t % P == 1", NS),
@@ -105,6 +110,10 @@ MUTATIONS = {
                                      "rmax[bj] = a.max(axis=1)", GRASP),
     "grasp_qr_sign_not_fixed": ("oracle.grasp", "sgn = np.where(np.diag(rf) < 0, -1.0, 1.0)",
                                 "sgn = np.ones(rf.shape[0])", GRASP),
+    "grasp_column_max_over_whole_column": ("oracle.grasp", "cmax[bi] = a[bi * s_rows:(bi + 1) * s_rows, :].max(axis=0)",
+                                           "cmax[bi] = a.max(axis=0)", GRASP),
+    "grasp_grid_truncates": ("oracle.grasp", "q = np.rint((x * sc).astype(F32))", "q = np.trunc((x * sc).astype(F32))",
+                             GRASP),
     "grasp_nibbles_swapped": ("oracle.grasp", "(u[:, 0::2] | (u[:, 1::2] << 4))", "(u[:, 1::2] | (u[:, 0::2] << 4))",
                               GRASP),
     "grasp_momentum_mu_on_gradient": ("oracle.grasp", "m = ((F32(mu) * m_prev).astype(F32) + g).astype(F32)",
