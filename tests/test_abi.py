@@ -6,6 +6,7 @@ import ctypes as C
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -269,3 +270,19 @@ def test_binding_signatures_match_the_header(lib):
         fn = getattr(L, name)
         assert fn.argtypes is not None, name
         assert len(fn.argtypes) == arity[name], (name, len(fn.argtypes), arity[name])
+
+
+def test_product_path_never_touches_the_oracle():
+    # the binding and the library sources name nothing of the oracle, and
+    # importing and loading the product leaves the oracle package unimported
+    pkg = os.path.join(ROOT, "memory_reduced_muon_gb300")
+    for dirpath, _, names in os.walk(pkg):
+        for n in names:
+            if n.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
+                text = open(os.path.join(dirpath, n)).read()
+                assert "oracle" not in text, os.path.join(dirpath, n)
+    code = ("import sys; sys.path.insert(0, sys.argv[1]); import memory_reduced_muon_gb300 as q; q.lib(); "
+            "print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))")
+    r = subprocess.run([sys.executable, "-c", code, ROOT], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-1000:]
+    assert r.stdout.strip() == "False"
