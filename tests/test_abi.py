@@ -286,3 +286,12 @@ def test_product_path_never_touches_the_oracle():
     r = subprocess.run([sys.executable, "-c", code, ROOT], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr[-1000:]
     assert r.stdout.strip() == "False"
+
+
+def test_oracle_shares_nothing_with_the_product():
+    # the oracle names neither the library, its binding nor CUDA
+    for n in sorted(os.listdir(os.path.join(ROOT, "oracle"))):
+        if n.endswith(".py"):
+            text = open(os.path.join(ROOT, "oracle", n)).read()
+            for word in ("memory_reduced_muon_gb300", "libqmuon", "qmuon_", "cuda", "ctypes"):
+                assert word not in text, (n, word)
