@@ -139,7 +139,10 @@ QMUON_API size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind whic
  *   group_inv_norm  D  [n_groups] fp32 1/(sqrt(sum)+1e-7), or NULL
  *   ws, ws_bytes    D  workspace of qmuon_workspace_size(plan, QMUON_WS_UPDATE)
  * q8 codes and absmax are bit-exact with the reference arithmetic (no FMA
- * contraction); sums are accumulated in fp64 across blocks. */
+ * contraction); sums are accumulated in fp64 across blocks.  Non-finite
+ * momenta: NaN lanes are ignored by the absmax (a block of NaN only gets 0),
+ * a NaN product quantises to code 0, and an infinity makes its block's absmax
+ * infinite and every code of that block 0. */
 QMUON_API qmuon_status qmuon_update_multi_normalize_groups(const qmuon_plan* plan, float beta,
                                                  int32_t normalize_mode, float* group_sumsq,
                                                  float* group_inv_norm, void* ws,
@@ -165,8 +168,9 @@ QMUON_API qmuon_status qmuon_update_multi_normalize_groups_sr(const qmuon_plan* 
  * update entries, the carrier over the plan, qmuon_step and
  * qmuon_step_from_host) adds to *counter, with an atomic add, the number of
  * 256-element blocks whose fp32 sum of m*m is not finite (a NaN or an
- * infinity in m, or squares that overflow fp32).  Such a block's codes and
- * its stored momentum are not meaningful, and neither is its group's norm.
+ * infinity in m, or squares that overflow fp32).  Such a block's codes
+ * follow the rules of qmuon_update_multi_normalize_groups but no longer
+ * represent its momentum, and its group's norm is not meaningful.
  * The caller zeroes and reads the counter.
  *   counter  D  one uint32, 4-byte aligned, or NULL to stop counting
  * Host-only: changes no device state.  QMUON_ERR_INVALID_ARGUMENT on a NULL
