@@ -249,7 +249,9 @@ typedef struct {
   void* grad;
 } qmuon_grasp_matrix;
 
-/* Workspace bytes of qmuon_grasp_step for these matrices (0 on bad input). */
+/* Workspace bytes of qmuon_grasp_step for these matrices: 0 for a NULL array,
+ * n <= 0, or any shape qmuon_grasp_step rejects (the state pointers are not
+ * looked at, so the size can be asked for before the state is allocated). */
 QMUON_API size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices, int32_t n);
 
 /* One GRASP momentum step of n matrices (H array of descriptors):

@@ -709,7 +709,13 @@ extern "C" size_t qmuon_grasp_workspace_size(const qmuon_grasp_matrix* matrices,
   using namespace qm;
   if (!matrices || n <= 0) return 0;
   size_t b = kWsHeader + table_bytes(n);
-  for (int32_t i = 0; i < n; ++i) b += prob_scratch_bytes(matrices[i]);
+  for (int32_t i = 0; i < n; ++i) {
+    // a shape qmuon_grasp_step rejects has no workspace size (the pointers
+    // may still be unset when the size is asked for)
+    const qmuon_grasp_matrix& m = matrices[i];
+    if (m.rows < kRank || m.cols <= 0 || m.cols % kS || m.rows > (1 << 28) || m.cols > (1 << 28)) return 0;
+    b += prob_scratch_bytes(m);
+  }
   return b;
 }
 

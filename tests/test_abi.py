@@ -306,3 +306,35 @@ def test_oracle_shares_nothing_with_the_product():
                 assert m.split(".")[0] not in ("memory_reduced_muon_gb300", "ctypes", "torch"), (n, m)
             if isinstance(node, ast.Attribute):
                 assert node.attr != "cuda", n
+
+
+def _grasp(rows, cols, base=FAKE, grad=None):
+    p = [base + 0x10000 * i for i in range(10)]
+    return q.qmuon_grasp_matrix(rows, cols, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8],
+                                p[9] if grad is None else grad)
+
+
+def test_grasp_rejects_on_host(lib):
+    L = q.lib()
+    INV, UNS = q.QMUON_ERR_INVALID_ARGUMENT, q.QMUON_ERR_UNSUPPORTED
+
+    def call(mats, ws=FAKE, ws_bytes=1 << 40):
+        arr = (q.qmuon_grasp_matrix * max(1, len(mats)))(*mats)
+        return L.qmuon_grasp_step(arr if mats else None, len(mats), 0.9, ws, ws_bytes, None)
+
+    assert call([]) == INV
+    assert call([_grasp(7, 64)]) == INV                  # fewer rows than the rank 8
+    assert call([_grasp(64, 96)]) == UNS                 # cols not a multiple of 64
+    assert call([_grasp(64, 0)]) == INV
+    assert call([_grasp(64, 64, grad=FAKE + 8)]) == INV  # gradient not 16-byte aligned
+    bad = _grasp(64, 64)
+    bad.r_cmax = None
+    assert call([bad]) == INV                            # a missing state array
+    assert call([_grasp(64, 64)], ws=FAKE + 16) == INV   # workspace not 256-byte aligned
+    need = q.qmuon_grasp_workspace_size([_grasp(64, 64), _grasp(100, 128)])
+    assert need > q.qmuon_grasp_workspace_size([_grasp(64, 64)]) > 0
+    assert call([_grasp(64, 64), _grasp(100, 128)], ws_bytes=need - 1) == q.QMUON_ERR_WORKSPACE_TOO_SMALL
+    assert q.qmuon_grasp_workspace_size([]) == 0
+    for rows, cols in ((7, 64), (64, 96), (64, 0), (-1, 64)):
+        assert q.qmuon_grasp_workspace_size([_grasp(64, 64), _grasp(rows, cols)]) == 0, (rows, cols)
+    assert q.qmuon_grasp_workspace_size([q.qmuon_grasp_matrix(64, 64)]) > 0   # pointers not needed
