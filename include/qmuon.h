@@ -292,7 +292,9 @@ typedef struct {
   const uint8_t* scale_inv;
 } qmuon_ns_problem;
 
-/* Workspace bytes for qmuon_newton_schulz_batched on these problems. */
+/* Workspace bytes for qmuon_newton_schulz_batched on these problems: 0 for a
+ * NULL array, n_problems <= 0, or any shape, stride or input kind the batched
+ * call rejects (pointers are not looked at). */
 QMUON_API size_t qmuon_ns_workspace_size(const qmuon_ns_problem* problems, int32_t n_problems);
 
 /* Quintic Newton-Schulz on a batch of independent matrices, in place:

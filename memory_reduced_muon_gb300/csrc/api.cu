@@ -578,6 +578,15 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan,
 // ---------------------------------------------------------------------------
 extern "C" size_t qmuon_ns_workspace_size(const qmuon_ns_problem* problems, int32_t n_problems) {
   if (!problems || n_problems <= 0) return 0;
+  for (int32_t i = 0; i < n_problems; ++i) {
+    // a shape the batched call rejects has no workspace size (the pointers
+    // may still be unset when the size is asked for)
+    const qmuon_ns_problem& p = problems[i];
+    if (p.rows <= 0 || p.cols <= 0 || p.rows > (1 << 30) || p.cols > (1 << 30) || p.ld < p.cols || p.ld % 8 ||
+        p.cols % 8 || (p.input != QMUON_NS_BF16 && p.input != QMUON_NS_MXFP8) ||
+        (p.input == QMUON_NS_MXFP8 && p.cols % 32))
+      return 0;
+  }
   return kWsHeader + ns::batch_workspace_bytes(problems, n_problems);
 }
 

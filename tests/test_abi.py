@@ -137,6 +137,10 @@ def test_newton_schulz_rejects_on_host(lib):
     assert call([q.ns_problem(FAKE + 8, 64, 64)]) == q.QMUON_ERR_INVALID_ARGUMENT
     assert call([ok], iters=0) == q.QMUON_ERR_INVALID_ARGUMENT
     assert call([ok], ws_bytes=100) == q.QMUON_ERR_WORKSPACE_TOO_SMALL
+    for bad in (q.ns_problem(FAKE, -5, 64), q.ns_problem(FAKE, 64, 60), q.ns_problem(FAKE, 64, 64, ld=32),
+                q.ns_problem(FAKE, 64, 48, input_kind=q.QMUON_NS_MXFP8), q.ns_problem(FAKE, 64, 64, input_kind=7)):
+        assert q.qmuon_ns_workspace_size([ok, bad]) == 0
+    assert q.qmuon_ns_workspace_size([q.ns_problem(None, 64, 64)]) > 0      # pointers not needed
     need = q.qmuon_ns_workspace_size([ok])
     # A, B (64x64 bf16) and two 64x64 scratch copies, plus the problem table
     assert need >= 4 * 64 * 64 * 2
