@@ -119,7 +119,8 @@ QMUON_API qmuon_status qmuon_plan_info(const qmuon_plan* plan, int64_t* n_blocks
 /* Which entry a workspace is sized for. */
 typedef enum { QMUON_WS_UPDATE = 0, QMUON_WS_STEP = 1 } qmuon_ws_kind;
 
-/* Bytes of device workspace the entry needs (0 on a NULL plan).  The
+/* Bytes of device workspace the entry needs (0 on a NULL plan or an unknown
+ * kind).  The
  * workspace is scratch: its contents between calls are unspecified, except
  * that it must not be shared by calls in flight at the same time. */
 QMUON_API size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind which);

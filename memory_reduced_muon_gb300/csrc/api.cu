@@ -396,7 +396,7 @@ UpdLaunch make_launch(const qmuon_plan* p, int layout, float beta, const UpdWs& 
 }  // namespace
 
 extern "C" size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind which) {
-  if (!plan) return 0;
+  if (!plan || (which != QMUON_WS_UPDATE && which != QMUON_WS_STEP)) return 0;
   size_t b = update_ws_bytes(plan);
   if (which == QMUON_WS_STEP) {
     const size_t a = ns::step_workspace_bytes(plan->tensors.data(), (int32_t)plan->tensors.size(), 1, 1);
