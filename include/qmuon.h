@@ -120,9 +120,9 @@ QMUON_API qmuon_status qmuon_plan_info(const qmuon_plan* plan, int64_t* n_blocks
 typedef enum { QMUON_WS_UPDATE = 0, QMUON_WS_STEP = 1 } qmuon_ws_kind;
 
 /* Bytes of device workspace the entry needs (0 on a NULL plan or an unknown
- * kind).  The
- * workspace is scratch: its contents between calls are unspecified, except
- * that it must not be shared by calls in flight at the same time. */
+ * kind).  The workspace is scratch: its contents between calls are
+ * unspecified, except that it must not be shared by calls in flight at the
+ * same time. */
 QMUON_API size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind which);
 
 /* The blockwise 8-bit momentum update over every tensor of the plan in one
