@@ -139,8 +139,9 @@ QMUON_API size_t qmuon_workspace_size(const qmuon_plan* plan, qmuon_ws_kind whic
  *   group_sumsq     D  [n_groups] fp32 sum of m*m per group, or NULL
  *   group_inv_norm  D  [n_groups] fp32 1/(sqrt(sum)+1e-7), or NULL
  *   ws, ws_bytes    D  workspace of qmuon_workspace_size(plan, QMUON_WS_UPDATE)
- * q8 codes and absmax are bit-exact with the reference arithmetic (no FMA
- * contraction); sums are accumulated in fp64 across blocks.  Non-finite
+ * The arithmetic is exactly the fp32 operation order above, one rounding per
+ * operation (no FMA contraction), so q8 codes and absmax are reproducible
+ * bit for bit; sums are accumulated in fp64 across blocks.  Non-finite
  * momenta: NaN lanes are ignored by the absmax (a block of NaN only gets 0),
  * a NaN product quantises to code 0, and an infinity makes its block's absmax
  * infinite and every code of that block 0. */
