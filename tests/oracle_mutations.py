@@ -53,6 +53,8 @@ MUTATIONS = {
     "segment_drops_partial_last_block": ("oracle.codec", "b0, b1 = s.start // QBLOCK, n_blocks(end)",
                                          "b0, b1 = s.start // QBLOCK, end // QBLOCK", CODEC),
     "eps_1e6": ("oracle.codec", "EPS = 1e-7", "EPS = 1e-6", CODEC),
+    "fp16_store_truncates": ("oracle.codec", "return np.asarray(m, dtype=F32).astype(np.float16)  # IEEE nearest-even",
+                             "return np.trunc(np.asarray(m, dtype=F32) * 1024).astype(np.float16) / 1024", CODEC),
     "normalize_divides": ("oracle.codec", "scaled = (g32 * scale[:, None])", "scaled = (g32 / scale[:, None])", CODEC),
     "segment_tail_rejected": ("oracle.codec", "(end % QBLOCK and end != n)", "(end % QBLOCK)", CODEC),
     "dequantize_over_128": ("oracle.codec", "(np.asarray(absmax, dtype=F32) / F32(127.0))",
@@ -73,6 +75,10 @@ MUTATIONS = {
     "muonbp_row_tile_offset": ("oracle.muonbp", "segs.append(codec.NormSegment(tensor_index, i * th * cols, th * cols, g))",
                                "segs.append(codec.NormSegment(tensor_index, i * th, th * cols, g))", NS),
     "muonbp_group_base_step": ("oracle.muonbp", "gbase += tr * tc", "gbase += 1", NS),
+    "muonbp_weight_step_sign": ("oracle.muonbp", "W = (s.weight.astype(F32) - (eta * u32).astype(F32)).astype(F32)",
+                                "W = (s.weight.astype(F32) + (eta * u32).astype(F32)).astype(F32)", NS),
+    "muonbp_update_applied_unrounded": ("oracle.muonbp", "u32 = codec.f32_from_bf16_bits(ub).reshape(s.rows, s.cols)",
+                                        "u32 = U.astype(F32)", NS),
     "muonbp_tile_column_offset": ("oracle.muonbp", "r * cols + j * tw", "r * cols + j * th", NS),
     # MXFP8 carrier ("Quantized Muon Momentum", section "Wave18B MXFP8 Carrier Probe")
     "e4m3_subnormal_exponent": ("oracle.carrier", "2.0 ** (1 - 7)", "2.0 ** (0 - 7)", CARRIER),
