@@ -354,10 +354,32 @@ QMUON_API qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, 
  * make that first call before any stream capture begins.  Every call uses the
  * same array (the call clears what must start at zero), so calls that may
  * overlap on the GPU -- on different streams or from different threads --
- * race on it; enqueue them in order on one stream. */
+ * race on it; enqueue them in order on one stream.
+ * A failure the kernel detects on the GPU (a bounded wait that expired,
+ * QMUON_ERR_TIMEOUT) cannot be returned by this asynchronous call: it is kept
+ * in the static array, carried over by later calls (the first one is kept),
+ * and reported by qmuon_noalloc_sync_status.  A call's outputs are valid only
+ * if the next qmuon_noalloc_sync_status returns QMUON_OK. */
 QMUON_API qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tensor, qmuon_q8_kind q8_kind,
                                                       qmuon_dtype grad_dtype, float beta, float* sumsq,
                                                       float* inv_norm, void* stream);
+
+/* Waits for `stream`, then reads the status that the kernels of
+ * qmuon_update_normalize_noalloc recorded in the static array of the current
+ * device since the last read, and clears it.  Returns QMUON_OK, the recorded
+ * status (qmuon_last_error names the kernel's site), or QMUON_ERR_CUDA if the
+ * stream or the read failed.  It synchronises the calling thread and
+ * allocates nothing.  The pages have no counterpart. */
+QMUON_API qmuon_status qmuon_noalloc_sync_status(void* stream);
+
+/* Writes `status` (a failure code, QMUON_ERR_INVALID_ARGUMENT ..
+ * QMUON_ERR_OUT_OF_MEMORY) and `site` into the static array's pending status
+ * on the current device, as a kernel would record them, so that a caller can
+ * test its handling of a failure reported through qmuon_noalloc_sync_status
+ * without making a kernel fail.  Synchronous; allocates nothing.  Returns
+ * QMUON_ERR_INVALID_ARGUMENT for QMUON_OK or an unknown code (nothing
+ * written).  The pages have no counterpart. */
+QMUON_API qmuon_status qmuon_noalloc_inject_status(qmuon_status status, uint32_t site);
 
 /* qmuon_step fed from host memory: the step's gradients are copied in, the
  * step runs, and its group sums are copied out, all enqueued without

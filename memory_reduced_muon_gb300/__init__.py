@@ -112,6 +112,8 @@ def lib() -> C.CDLL:
         "qmuon_step_from_host": (i32, [vp, i64, i32, f32, f32, f32, C.POINTER(vp), C.POINTER(f32), i32,
                                        C.POINTER(vp), vp, vp, vp, sz, vp, vp]),
         "qmuon_plan_set_nonfinite_counter": (i32, [vp, vp]),
+        "qmuon_noalloc_sync_status": (i32, [vp]),
+        "qmuon_noalloc_inject_status": (i32, [i32, C.c_uint32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -129,7 +131,7 @@ def exported_symbols() -> list:
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
             "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
             "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host",
-            "qmuon_plan_set_nonfinite_counter"]
+            "qmuon_plan_set_nonfinite_counter", "qmuon_noalloc_sync_status", "qmuon_noalloc_inject_status"]
 
 
 # --------------------------------------------------------------------------
@@ -349,6 +351,18 @@ def qmuon_update_normalize_noalloc(q8, absmax, grad, rows: int, cols: int, q8_ki
                                               DTYPES.get(grad_dtype, grad_dtype), float(beta), _ptr(sumsq),
                                               _ptr(inv_norm), _stream(stream))
     _check(st, "qmuon_update_normalize_noalloc")
+
+
+def qmuon_noalloc_sync_status(stream=None):
+    """Waits for the stream and raises if a kernel of the allocation-free
+    update recorded a failure since the last read (the record is cleared)."""
+    _check(lib().qmuon_noalloc_sync_status(_stream(stream)), "qmuon_noalloc_sync_status")
+
+
+def qmuon_noalloc_inject_status(status: int, site: int = 0):
+    """Records ``status`` as if a kernel of the allocation-free update had
+    failed at ``site`` (for testing a caller's failure handling)."""
+    _check(lib().qmuon_noalloc_inject_status(int(status), int(site)), "qmuon_noalloc_inject_status")
 
 
 def qmuon_step_prepare(plan: Plan, weights, ws, ws_bytes: Optional[int] = None):

@@ -135,25 +135,6 @@ qmuon_status validate_tensor(const qmuon_tensor& t, qmuon_dtype dt) {
   return QMUON_OK;
 }
 
-// Update launch geometry: whole waves of resident CTAs, at most kMaxChunk
-// blocks per CTA and at least 16 (one per half-warp).
-void update_geometry(int64_t nb, int sms, int per_sm, int32_t* grid, int64_t* chunk) {
-  const int64_t wave = (int64_t)std::max(1, sms) * std::max(1, per_sm);
-  int64_t g;
-  if (nb <= wave * 16) {
-    g = std::max<int64_t>(1, (nb + 15) / 16);
-  } else {
-    const int64_t waves = (nb + wave * kMaxChunk - 1) / (wave * kMaxChunk);
-    g = wave * waves;
-  }
-  int64_t c = (nb + g - 1) / g;
-  if (c < 1) c = 1;
-  g = (nb + c - 1) / c;
-  if (g < 1) g = 1;
-  *grid = (int32_t)g;
-  *chunk = c;
-}
-
 }  // namespace
 
 extern "C" qmuon_status qmuon_plan_create(const qmuon_tensor* tensors, int32_t n_tensors,

@@ -85,6 +85,28 @@ struct UpdLaunch {
   unsigned int* nonfinite;
 };
 
+// Update launch geometry: whole waves of resident CTAs, at most kMaxChunk
+// blocks per CTA and at least 16 (one per half-warp).  Every entry that
+// launches the update kernel takes its grid and chunk from here, so that the
+// per-CTA partial sums are formed over the same blocks in the same order.
+inline void update_geometry(int64_t nb, int sms, int per_sm, int32_t* grid, int64_t* chunk) {
+  const int64_t wave = (int64_t)(sms > 1 ? sms : 1) * (per_sm > 1 ? per_sm : 1);
+  int64_t g;
+  if (nb <= wave * 16) {
+    g = (nb + 15) / 16;
+    if (g < 1) g = 1;
+  } else {
+    const int64_t waves = (nb + wave * kMaxChunk - 1) / (wave * kMaxChunk);
+    g = wave * waves;
+  }
+  int64_t c = (nb + g - 1) / g;
+  if (c < 1) c = 1;
+  g = (nb + c - 1) / c;
+  if (g < 1) g = 1;
+  *grid = (int32_t)g;
+  *chunk = c;
+}
+
 // Record the detail of a failure for qmuon_last_error() (api.cu); returns
 // QMUON_ERR_CUDA (or `status`) for convenient `return set_error(...)`.
 qmuon_status set_error(const char* where, cudaError_t e, qmuon_status status = QMUON_ERR_CUDA);

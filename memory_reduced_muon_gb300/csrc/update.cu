@@ -30,6 +30,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstddef>
+#include <cstdio>
 #include <mutex>
 
 #include "qm_internal.h"
@@ -770,11 +772,20 @@ cudaError_t launch_scale_groups(const UpdLaunch& L, qmuon_dtype dt, const float*
 // a caller-provided workspace.  Host code cannot use the array's name as a
 // device address, so the address is looked up once per device with
 // cudaGetSymbolAddress (that device current) and passed to the kernel.
+//
+// A kernel records a failure (a bounded wait that expired) in the header's
+// error word, and its waits give up at once while that word is set.  So
+// before each launch a one-thread kernel moves a recorded status into a
+// pending pair of words (the first failure is kept) and clears the error word
+// and the ticket; qmuon_noalloc_sync_status reports the pending status, else
+// the error word, and clears both.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int kStaticSlots = 8192;  // partial-sum slots: one per CTA of the launch
 static __device__ __align__(256) unsigned char g_static_scratch[qm::kWsHeader + kStaticSlots * sizeof(double)];
+// the pending status and its site live in the header's spare words
+constexpr int kPendingStatus = 0, kPendingSite = 1;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
@@ -792,6 +803,26 @@ cudaError_t static_scratch(int dev, void** out) {
   }
   *out = g_static_addr[dev];
   return cudaSuccess;
+}
+
+// Carries a status recorded by the previous call into the pending words and
+// clears what the update kernel needs at zero: the error word and the ticket.
+__global__ void noalloc_carry_status_kernel(qm::WsHeader* h) {
+  if (h->error != 0u && h->pad[kPendingStatus] == 0u) {
+    h->pad[kPendingStatus] = h->error;
+    h->pad[kPendingSite] = h->error_info;
+  }
+  h->error = 0u;
+  h->error_info = 0u;
+  h->ticket = 0u;
+}
+
+qmuon_status current_device(const char* where, int* dev) {
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return qm::set_error(where, e);
+  if (*dev < 0 || *dev >= kMaxDevices)
+    return qm::set_error_what(where, "device ordinal beyond the static table", QMUON_ERR_UNSUPPORTED);
+  return QMUON_OK;
 }
 
 }  // namespace
@@ -818,26 +849,22 @@ extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tenso
     return QMUON_ERR_INVALID_ARGUMENT;
 
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (cudaGetDevice)", e);
-  if (dev < 0 || dev >= kMaxDevices)
-    return set_error_msg("qmuon_update_normalize_noalloc: device ordinal beyond the static table", QMUON_ERR_UNSUPPORTED);
+  qmuon_status st = current_device("qmuon_update_normalize_noalloc (device)", &dev);
+  if (st != QMUON_OK) return st;
   void* scratch = nullptr;
-  e = static_scratch(dev, &scratch);
+  cudaError_t e = static_scratch(dev, &scratch);
   if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (cudaGetSymbolAddress)", e);
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (SM count)", e);
   const int per_sm = update_blocks_per_sm(q8_kind, grad_dtype, false);
   if (per_sm <= 0) return set_error_msg("qmuon_update_normalize_noalloc: occupancy query failed", QMUON_ERR_CUDA);
 
-  // launch geometry: whole waves of resident CTAs, <= kMaxChunk blocks each
+  // the launch geometry of the planned entry point, so the sums are formed alike
   const int64_t nb = (n + kBlock - 1) / kBlock;
-  const int64_t wave = (int64_t)sms * per_sm;
-  int64_t g = (nb <= wave * 16) ? (nb + 15) / 16 : wave * ((nb + wave * kMaxChunk - 1) / (wave * kMaxChunk));
-  if (g < 1) g = 1;
-  const int64_t chunk = (nb + g - 1) / g;
-  g = (nb + chunk - 1) / chunk;
-  if (g > kStaticSlots)
+  int32_t grid = 0;
+  int64_t chunk = 0;
+  update_geometry(nb, sms, per_sm, &grid, &chunk);
+  if (grid > kStaticSlots)
     return set_error_msg("qmuon_update_normalize_noalloc: launch needs more partial-sum slots than the static "
                          "scratch array holds", QMUON_ERR_INVALID_ARGUMENT);
 
@@ -851,7 +878,7 @@ extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tenso
   L.n_tensors = 1;
   L.nb_total = nb;
   L.chunk = chunk;
-  L.grid = (int32_t)g;
+  L.grid = grid;
   L.beta = beta;
   L.layout.n_groups = (sumsq || inv_norm) ? 1 : 0;  // block_group null: one group, one slot per CTA
   L.header = static_cast<WsHeader*>(scratch);
@@ -859,9 +886,52 @@ extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tenso
   L.group_sumsq = sumsq;
   L.group_inv = inv_norm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the ticket must start at zero
-  e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
+  // the array keeps the previous call's contents: keep its status for
+  // qmuon_noalloc_sync_status, and start the error word and ticket at zero
+  noalloc_carry_status_kernel<<<1, 1, 0, s>>>(L.header);
+  e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, false, s);
   if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (launch)", e);
+  return QMUON_OK;
+}
+
+extern "C" qmuon_status qmuon_noalloc_sync_status(void* stream) {
+  using namespace qm;
+  int dev = 0;
+  qmuon_status st = current_device("qmuon_noalloc_sync_status (device)", &dev);
+  if (st != QMUON_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return set_error("qmuon_noalloc_sync_status (stream synchronize)", e);
+  // the symbol copies read and write the array on the current device and
+  // allocate nothing
+  WsHeader h{};
+  e = cudaMemcpyFromSymbol(&h, g_static_scratch, sizeof(h), 0, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error("qmuon_noalloc_sync_status (read header)", e);
+  const unsigned status = h.pad[kPendingStatus] ? h.pad[kPendingStatus] : h.error;
+  const unsigned site = h.pad[kPendingStatus] ? h.pad[kPendingSite] : h.error_info;
+  if (status == 0u) return QMUON_OK;
+  const unsigned zero[2] = {0u, 0u};
+  e = cudaMemcpyToSymbol(g_static_scratch, zero, sizeof(zero), offsetof(WsHeader, error), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbol(g_static_scratch, zero, sizeof(zero), offsetof(WsHeader, pad) + kPendingStatus * 4,
+                           cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return set_error("qmuon_noalloc_sync_status (clear header)", e);
+  char msg[128];
+  std::snprintf(msg, sizeof(msg), "qmuon_update_normalize_noalloc: kernel reported status %u at site 0x%x", status,
+                site);
+  return set_error_msg(msg, (qmuon_status)status);
+}
+
+extern "C" qmuon_status qmuon_noalloc_inject_status(qmuon_status status, uint32_t site) {
+  using namespace qm;
+  if ((int)status <= (int)QMUON_OK || (int)status > (int)QMUON_ERR_OUT_OF_MEMORY)
+    return set_error_msg("qmuon_noalloc_inject_status: not a failure status", QMUON_ERR_INVALID_ARGUMENT);
+  int dev = 0;
+  qmuon_status st = current_device("qmuon_noalloc_inject_status (device)", &dev);
+  if (st != QMUON_OK) return st;
+  const unsigned words[2] = {(unsigned)status, site};
+  const cudaError_t e = cudaMemcpyToSymbol(g_static_scratch, words, sizeof(words),
+                                           offsetof(WsHeader, pad) + kPendingStatus * 4, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return set_error("qmuon_noalloc_inject_status (write header)", e);
   return QMUON_OK;
 }

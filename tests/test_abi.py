@@ -110,6 +110,22 @@ def test_entries_reject_null_plan_and_bad_args(lib):
     assert L.qmuon_sync_status(FAKE + 16, None) == INV   # not 256-byte aligned
 
 
+def test_noalloc_status_calls_on_host(lib):
+    # the injector refuses a non-failure code before any CUDA call; with no
+    # usable device both status calls answer QMUON_ERR_CUDA with the detail
+    import torch
+    L = q.lib()
+    assert L.qmuon_noalloc_inject_status(q.QMUON_OK, 0) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert L.qmuon_noalloc_inject_status(99, 0) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert "not a failure status" in q.qmuon_last_error()
+    if torch.cuda.is_available():
+        return
+    assert L.qmuon_noalloc_sync_status(None) == q.QMUON_ERR_CUDA
+    assert q.qmuon_last_error().startswith("qmuon_noalloc_sync_status")
+    assert L.qmuon_noalloc_inject_status(q.QMUON_ERR_TIMEOUT, 7) == q.QMUON_ERR_CUDA
+    assert q.qmuon_last_error().startswith("qmuon_noalloc_inject_status")
+
+
 def test_carrier_rejects_on_host(lib):
     L = q.lib()
     t = _tensor(4, 48)   # 48 columns: not a multiple of 32
