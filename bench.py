@@ -40,6 +40,8 @@ import workloads  # noqa: E402
 METRIC = "qMuon update HBM GB/s + Newton-Schulz TFLOP/s; Mparams/s per optimizer step"
 UPDATE_BYTES_PER_ELEM = 1 + 2 + 1 + 2 + 8.0 / 256   # q8 r/w, bf16 grad r/w, absmax r/w
 MAX_BATCHES = 40   # pre-generated gradient batches (1.75 GB each at the default workload)
+L2_BYTES = 129 * 2 ** 20          # GB300 L2
+L2_FLUSH_BYTES = 512 * 2 ** 20    # a write that evicts it
 
 
 def load_peaks():
@@ -53,10 +55,9 @@ def load_peaks():
 
 def load_traffic():
     """Per-launch (or per-call) DRAM bytes from the committed ncu summaries
-    (``key = bytes`` lines in profiles/dram_traffic_llama8b_x4_muonbp.md and
-    profiles/grasp_llama8b_x4.md)."""
+    (``key = bytes`` lines in the profiles listed below)."""
     out = {}
-    for name in ("dram_traffic_llama8b_x4_muonbp.md", "grasp_llama8b_x4.md"):
+    for name in ("dram_traffic_llama8b_x4_muonbp.md", "grasp_llama8b_x4.md", "dram_traffic_update_rowscale4.md"):
         try:
             with open(os.path.join(ROOT, "profiles", name)) as f:
                 for line in f:
@@ -79,6 +80,22 @@ def step_ns_flops(w, full):
     for m in w.matrices:
         tot += tr * tc * ns_flops_of(m.rows // tr, m.cols // tc, w.iters)
     return tot
+
+
+def ns_executed_flops_of(rows, cols, iters):
+    """FLOPs the tensor cores execute for one matrix: 256 x 256 output tiles
+    (the symmetric products only those on or above the diagonal, SYRK) and
+    K loops in steps of 64."""
+    m, n = min(rows, cols), max(rows, cols)
+    tm, tn = -(-m // 256), -(-n // 256)
+    kpad = lambda k: -(-k // 64) * 64   # noqa: E731
+    sym = tm * (tm + 1) // 2
+    return iters * 2.0 * 256 * 256 * (sym * kpad(n) + sym * kpad(m) + tm * tn * kpad(m))
+
+
+def step_ns_executed(w, full):
+    tr, tc = (1, 1) if full else w.tile
+    return sum(tr * tc * ns_executed_flops_of(m.rows // tr, m.cols // tc, w.iters) for m in w.matrices)
 
 
 class ClockSampler:
@@ -166,58 +183,145 @@ def barrier(world):
 # the CPU oracle leg (cpu_baseline and --impl reference)
 # --------------------------------------------------------------------------
 
-def oracle_sample(w, budget_s=15.0, min_s=12.0):
-    """Time the oracle on a bounded sample of the workload's block step.
+CODEC_SLICE = 1 << 20   # elements per thread in one sample step of the oracle's codec
 
-    The momentum update (numpy, fp32 codec) runs on one whole matrix of each
-    shape and the Newton-Schulz (numpy, fp64) on one tile of each shape; the
-    per-parameter costs are added, weighted by how many parameters of the
-    workload have that shape.  Whole passes over the shapes repeat until
-    ``min_s`` seconds have gone by, and the costs are averaged over the
-    passes.  As a guard on slow hosts, the first pass stops after ``budget_s``
-    (the sample string then lists only the shapes measured).
-    Returns (Mparams/s, sample, cores, seconds)."""
-    import numpy as np
-    from oracle import codec, ns as ons
 
+def _block_tiles(w):
+    """(rows, cols, params of the workload with that matrix shape) per shape,
+    and the tile shape each one's block-step Newton-Schulz runs on."""
     shapes = {}
     for m in w.matrices:
         shapes[(m.rows, m.cols)] = shapes.get((m.rows, m.cols), 0) + m.numel
     tr, tc = w.tile if w.P != 1 else (1, 1)
-    rng = np.random.default_rng(0)
-    t_start = time.perf_counter()
-    sec_per_param = 0.0
-    passes = 0
-    done = []
-    while True:
-        done = []
-        for (rows, cols), weight in sorted(shapes.items(), key=lambda kv: kv[0][0] * kv[0][1]):
-            n = rows * cols
-            q8 = np.zeros(n, np.int8)
-            a = np.zeros((n + 255) // 256, np.float32)
-            g = codec.bf16_bits_from_f32(rng.standard_normal(n).astype(np.float32))
+    return [((r, c), wt, (r // tr, c // tc)) for (r, c), wt in sorted(shapes.items(), key=lambda kv: kv[0][0] * kv[0][1])]
+
+
+def _oracle_codec(n, beta, seed):
+    """The oracle's momentum update on n elements from a zero state; returns
+    its duration (the inputs are drawn first, untimed)."""
+    import numpy as np
+    from oracle import codec
+    rng = np.random.default_rng(seed)
+    q8 = np.zeros(n, np.int8)
+    a = np.zeros((n + 255) // 256, np.float32)
+    g = codec.bf16_bits_from_f32(rng.standard_normal(n).astype(np.float32))
+    t0 = time.perf_counter()
+    codec.momentum_update(q8, a, g, beta)
+    return time.perf_counter() - t0
+
+
+NS_SAMPLE_FLOPS = 4e11   # larger tiles are timed on a bounded one (m <= 1792, n <= 4096), scaled by FLOPs
+
+
+def _sample_tile(th, tw, iters):
+    if ns_flops_of(th, tw, iters) <= NS_SAMPLE_FLOPS:
+        return th, tw
+    m, n = min(min(th, tw), 1792), min(max(th, tw), 4096)
+    return (m, n) if th <= tw else (n, m)
+
+
+def _oracle_ns_tiles(w, seed):
+    """fp64 Newton-Schulz of the oracle on one tile of every shape (or on a
+    bounded tile of the same orientation, scaled by the FLOP count); returns
+    per shape (seconds for the tile, flops actually run, seconds measured)."""
+    import numpy as np
+    from oracle import ns as ons
+    rng = np.random.default_rng(seed)
+    out = []
+    for _, _, (th, tw) in _block_tiles(w):
+        sh, sw = _sample_tile(th, tw, w.iters)
+        M = rng.standard_normal((sh, sw))
+        t0 = time.perf_counter()
+        ons.newton_schulz(M, iters=w.iters)
+        dt = time.perf_counter() - t0
+        f_run = ns_flops_of(sh, sw, w.iters)
+        out.append((dt * ns_flops_of(th, tw, w.iters) / f_run, f_run, dt))
+    return out
+
+
+_SINGLE_CORE = r"""
+import sys, time, numpy as np
+sys.path.insert(0, sys.argv[1])
+from oracle import codec, ns
+n, rows, cols, iters = (int(x) for x in sys.argv[2:6])
+rng = np.random.default_rng(7)
+q8 = np.zeros(n, np.int8); a = np.zeros((n + 255) // 256, np.float32)
+g = codec.bf16_bits_from_f32(rng.standard_normal(n).astype(np.float32))
+t0 = time.perf_counter(); codec.momentum_update(q8, a, g, 0.95); tc = time.perf_counter() - t0
+M = rng.standard_normal((rows, cols))
+t0 = time.perf_counter(); ns.newton_schulz(M, iters=iters); tn = time.perf_counter() - t0
+print(tc, tn)
+"""
+
+
+def _per_param_seconds(w, codec_s_per_elem, tile_costs, fp64_flops_per_s):
+    """Seconds per parameter of one optimizer step averaged over the
+    workload's step schedule: the codec on every parameter, block-step
+    Newton-Schulz from the measured tiles (weighted by the shapes' parameter
+    counts), full-step Newton-Schulz from the measured fp64 rate."""
+    blocks = _block_tiles(w)
+    ns_block = sum(c[0] / (th * tw) * wt for c, (_, wt, (th, tw)) in zip(tile_costs, blocks)) / w.numel
+    if w.P == 1:
+        return codec_s_per_elem + ns_block
+    ns_full = step_ns_flops(w, True) / fp64_flops_per_s / w.numel
+    n_full = sum(1 for t in range(1, w.steps + 1) if w.P and t % w.P == 0)
+    return codec_s_per_elem + (ns_block * (w.steps - n_full) + ns_full * n_full) / w.steps
+
+
+def oracle_sample(w, steps=3, warmup=1):
+    """Time the oracle as it stands on bounded sample steps of the workload.
+
+    One sample step: the codec (numpy, fp32) on CODEC_SLICE elements in each
+    of `cores` threads at once, then fp64 Newton-Schulz on one block-step tile
+    of every matrix shape (numpy's BLAS on every core).  `warmup` untimed
+    steps, then `steps` timed ones.  The workload rate is extrapolated from
+    the per-parameter costs (``_per_param_seconds``): the codec's from the
+    threads' wall time, the block steps' Newton-Schulz from the tiles, the
+    full steps' from the tiles' fp64 FLOP rate.  A single-core figure comes
+    from one more run in a subprocess with one BLAS thread.
+    Returns a dict: value (all cores, Mparams/s), ms_per_step (measured
+    sample step), steps, cores, sample, single_core (Mparams/s)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    step_ms, codec_rates, tile_runs = [], [], []
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        for k in range(warmup + steps):
             t0 = time.perf_counter()
-            r = codec.momentum_update(q8, a, g, w.beta)
-            t_upd = (time.perf_counter() - t0) / n
-            th, tw = rows // tr, cols // tc
-            M = codec.f32_from_bf16_bits(r.grad).reshape(rows, cols)[:th, :tw].astype(np.float64)
-            t0 = time.perf_counter()
-            ons.newton_schulz(M, iters=w.iters)
-            t_ns = (time.perf_counter() - t0) / (th * tw)
-            sec_per_param += (t_upd + t_ns) * weight / w.numel
-            done.append(f"{rows}x{cols} (update) / {th}x{tw} (NS)")
-            if passes == 0 and time.perf_counter() - t_start > budget_s:
-                break
-        passes += 1
-        elapsed = time.perf_counter() - t_start
-        if len(done) < len(shapes) or elapsed >= min_s or elapsed + elapsed / passes > budget_s * 2:
-            break
-    sec_per_param /= passes
-    dt = time.perf_counter() - t_start
-    sample = (f"block step, {passes} pass(es), per shape: numpy fp32 codec on one whole matrix + fp64 Newton-Schulz "
-              f"on one {tr}x{tc} tile, per-parameter costs weighted by the workload's shape mix: " + "; ".join(done))
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return 1.0 / sec_per_param / 1e6, sample, cores, dt
+            durs = list(ex.map(lambda i: _oracle_codec(CODEC_SLICE, w.beta, 1000 * k + i), range(cores)))
+            tiles = _oracle_ns_tiles(w, k)
+            dt = time.perf_counter() - t0
+            if k >= warmup:
+                step_ms.append(dt * 1e3)
+                codec_rates.append(max(durs) / (cores * CODEC_SLICE))
+                tile_runs.append(tiles)
+    codec_s = statistics.median(codec_rates)
+    tile_costs = [(statistics.median(run[i][0] for run in tile_runs), tile_runs[0][i][1],
+                   statistics.median(run[i][2] for run in tile_runs)) for i in range(len(tile_runs[0]))]
+    fp64_rate = sum(c[1] for c in tile_costs) / sum(c[2] for c in tile_costs)
+    value = 1.0 / _per_param_seconds(w, codec_s, tile_costs, fp64_rate) / 1e6
+    # one core: the codec and the smallest tile's Newton-Schulz with one BLAS thread
+    single = None
+    try:
+        blocks = _block_tiles(w)
+        th, tw = _sample_tile(*blocks[0][2], w.iters)
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", _SINGLE_CORE, ROOT, str(CODEC_SLICE), str(th), str(tw),
+                            str(w.iters)], capture_output=True, text=True, env=env, timeout=300)
+        tc1, tn1 = (float(x) for x in r.stdout.split())
+        rate1 = ns_flops_of(th, tw, w.iters) / tn1
+        tiles1 = [(ns_flops_of(bt[0], bt[1], w.iters) / rate1,) for _, _, bt in blocks]
+        single = 1.0 / _per_param_seconds(w, tc1 / CODEC_SLICE, tiles1, rate1) / 1e6
+    except Exception:
+        single = None
+    tiles_desc = "; ".join(f"{th}x{tw}" for _, _, (th, tw) in _block_tiles(w))
+    sample = (f"{steps} timed sample steps after {warmup} untimed, each: the numpy fp32 codec on "
+              f"{CODEC_SLICE} elements in each of {cores} threads, then fp64 Newton-Schulz ({w.iters} iterations) "
+              f"on one tile of each shape ({tiles_desc}; tiles above {NS_SAMPLE_FLOPS:.0e} FLOPs timed on a bounded tile and scaled by FLOPs); the workload rate is extrapolated from these "
+              "per-parameter costs weighted by the shapes' parameter counts, full steps from the tiles' fp64 FLOP "
+              "rate; single_core: the same with one thread and one BLAS thread")
+    return {"value": value, "ms_per_step": statistics.mean(step_ms), "steps": steps, "cores": cores,
+            "sample": sample, "single_core": single, "fp64_gflops": fp64_rate / 1e9,
+            "codec_mparams_per_s_all_cores": 1.0 / codec_s / 1e6, "extrapolated": True}
 
 
 # --------------------------------------------------------------------------
@@ -333,8 +437,147 @@ def run_gpu_carrier(args, world, rank, local, w):
     flop = step_ns_flops(w, True)
     return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks,
                 per_step=[], upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes,
-                ns_ms={"full": ns_ms}, ns_flop={"full": flop}, e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
-                launches=(1 + 1 + 3 * w.iters) * args.steps, n_params=n_params, w=w)
+                ns_ms={"full": ns_ms}, ns_flop={"full": flop}, ns_exec={"full": step_ns_executed(w, True)},
+                e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
+                launches=(1 + 1 + 3 * w.iters) * args.steps, n_params=n_params, w=w,
+                l2=f"inputs larger than L2 ({sum(2 * m.numel for m in mats) / 1e9:.2f} GB of bf16 gradients and "
+                   f"{sum(m.numel for m in mats) / 1e9:.2f} GB of codes read per step)")
+
+
+def run_gpu_grouped(args, world, rank, local, w):
+    """Workloads 2 and 3: the grouped momentum update
+    (qmuon_update_multi_normalize_groups, deferred norms) over every matrix
+    with the workload's norm groups (its segments, or one group per matrix),
+    then, when the workload has Newton-Schulz, one batched call over its
+    problems (its row slices, each scaled by its own group's inverse norm),
+    in place in the gradient buffers.  These workloads update no weights."""
+    import memory_reduced_muon_gb300 as q
+
+    dev = torch.device("cuda", local)
+    mats = w.matrices
+    stream = torch.cuda.current_stream()
+    states = [workloads.zero_state(m, w.q8_kind, device=dev) for m in mats]
+    n_steps_total = max(args.warmup, 1) + args.steps
+    n_batches = min(n_steps_total, MAX_BATCHES)
+    batches = [[workloads.make_grad(w, i, b + 1, device=dev) for i in range(len(mats))] for b in range(n_batches)]
+    segs = ([(sg.tensor_index, sg.start, sg.length, sg.group_id) for sg in w.segments]
+            if w.segments is not None else None)
+    n_groups = w.groups
+    plans = [q.qmuon_plan_create([(st[0], st[1], g, m.rows, m.cols) for st, g, m in zip(states, grads, mats)],
+                                 w.q8_kind, "bf16", segments=segs, n_groups=n_groups if segs else 0)
+             for grads in batches]
+    ws = torch.empty(q.qmuon_workspace_size(plans[0]), dtype=torch.uint8, device=dev)
+    sums = torch.zeros(n_groups, dtype=torch.float32, device=dev)
+    inv = torch.zeros(n_groups, dtype=torch.float32, device=dev)
+
+    def group_of(t, row0):
+        if segs is None:
+            return t
+        for ti, start, _, gid in segs:
+            if ti == t and start == row0 * mats[t].cols:
+                return gid
+        raise ValueError("a Newton-Schulz slice that starts no norm segment")
+
+    slices = w.ns_slices if w.ns_slices is not None else [(i, 0, m.rows) for i, m in enumerate(mats)]
+
+    def problems(grads):
+        out = []
+        for t, row0, rows in slices:
+            cols = mats[t].cols
+            out.append(q.ns_problem(grads[t].data_ptr() + 2 * row0 * cols, rows, cols, ld=cols,
+                                    inv_norm=inv.data_ptr() + 4 * group_of(t, row0)))
+        return out
+
+    probs = [problems(grads) for grads in batches] if w.ns else None
+    ws_n = torch.empty(q.qmuon_ns_workspace_size(probs[0]), dtype=torch.uint8, device=dev) if w.ns else None
+
+    def step(t):
+        b = (t - 1) % n_batches
+        q.qmuon_update_multi_normalize_groups(plans[b], w.beta, 2, sums, inv, ws, stream=stream)
+        if w.ns:
+            q.qmuon_newton_schulz_batched(probs[b], w.iters, w.coeffs, ws_n, stream=stream)
+
+    t = 0
+    for _ in range(max(args.warmup, 1)):
+        t += 1
+        step(t)
+    q.qmuon_sync_status(ws, stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(str(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    q.qmuon_sync_status(ws, stream)
+    if w.ns:
+        q.qmuon_sync_status(ws_n, stream)
+    n_params = w.numel
+    # the update alone and the Newton-Schulz alone, on the last batch
+    reps = max(3, min(args.steps, 20))   # the per-kernel legs: a few calls back to back
+    b_last = (t - 1) % n_batches
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(reps):
+        q.qmuon_update_multi_normalize_groups(plans[b_last], w.beta, 2, sums, inv, ws, stream=stream)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    upd_ms = u0.elapsed_time(u1) / reps
+    upd_bytes = UPDATE_BYTES_PER_ELEM * n_params
+    ns_ms, ns_flop, ns_exec = {}, {}, {}
+    if w.ns:
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        for _ in range(3):
+            q.qmuon_newton_schulz_batched(probs[b_last], w.iters, w.coeffs, ws_n, stream=stream)
+        n1.record(stream)
+        torch.cuda.synchronize()
+        q.qmuon_sync_status(ws_n, stream)
+        ns_ms["full"] = n0.elapsed_time(n1) / 3
+        ns_flop["full"] = sum(ns_flops_of(rows, mats[ti].cols, w.iters) for ti, _, rows in slices)
+        ns_exec["full"] = sum(ns_executed_flops_of(rows, mats[ti].cols, w.iters) for ti, _, rows in slices)
+    # end to end: each step's gradients copied in from page-locked host memory
+    # (two batches alternate), the step, and its group sums copied back
+    h2d = sum(g.numel() * g.element_size() for g in batches[0])
+    host = []
+    for b in range(2):
+        buf = torch.empty(sum(g.numel() for g in batches[b % n_batches]), dtype=torch.bfloat16, pin_memory=True)
+        views, o = [], 0
+        for g in batches[b % n_batches]:
+            v = buf[o:o + g.numel()].view(g.shape)
+            v.copy_(g.cpu())
+            views.append(v)
+            o += g.numel()
+        host.append(views)
+    sums_host = torch.zeros(n_groups).pin_memory()
+    e2e_steps = max(2, args.steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for k in range(e2e_steps):
+        t += 1
+        b = (t - 1) % n_batches
+        for dst, src in zip(batches[b], host[k % 2]):
+            dst.copy_(src, non_blocking=True)
+        step(t)
+        sums_host.copy_(sums, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    q.qmuon_sync_status(ws, stream)
+    launches = (1 + (3 * w.iters + (1 if w.iters == 1 else 0) if w.ns else 0)) * args.steps
+    return dict(value=job_throughput(n_params, args.steps, world, ms), ms=ms, clocks=clocks, per_step=[],
+                upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes, ns_ms=ns_ms,
+                ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=world * n_params * e2e_steps / e2e_s / 1e6, h2d=h2d,
+                d2h=4 * n_groups, n_full=args.steps if w.ns else 0, launches=launches, n_params=n_params, w=w,
+                l2=f"inputs larger than L2 ({h2d / 1e9:.2f} GB of bf16 gradients per step)")
 
 
 def run_gpu(args, world, rank, local):
@@ -345,8 +588,12 @@ def run_gpu(args, world, rank, local):
     w = workloads.get(args.workload)
     if args.row_scale > 1:
         w.matrices = [workloads.Matrix(m.name, max(8, m.rows // args.row_scale), m.cols) for m in w.matrices]
+    if args.q8:
+        w.q8_kind = args.q8
     if w.carrier:
         return run_gpu_carrier(args, world, rank, local, w)
+    if w.segments is not None or not w.ns:
+        return run_gpu_grouped(args, world, rank, local, w)
     mats = w.matrices
     n_params = w.numel
     stream = torch.cuda.current_stream()
@@ -403,24 +650,34 @@ def run_gpu(args, world, rank, local):
         sel = f"{torch.cuda.get_device_properties(local).pci_domain_id:08X}:{bus:02X}:{torch.cuda.get_device_properties(local).pci_device_id:02X}.0"
     except Exception:
         sel = str(local)
+    # a step whose inputs fit in L2 is timed alone, with L2 flushed before it
+    # (a write larger than L2, outside the step's events)
+    step_bytes = sum(m.numel * (2 + 1 + 4) for m in mats)   # bf16 gradient, q8 state, fp32 weights
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if step_bytes < 2 * L2_BYTES else None
+    l2_note = (f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB write outside the step's CUDA events; "
+               f"the step's inputs are {step_bytes / 1e6:.1f} MB)" if flush is not None else
+               f"inputs larger than L2 ({sum(2 * m.numel for m in mats) / 1e9:.2f} GB of bf16 gradients per step)")
     sampler = ClockSampler(sel)
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     kinds = []
     for k in range(args.steps):
         t += 1
+        if flush is not None:
+            flush.zero_()
+        ev0[k].record(stream)
         step(t)
-        ev[k + 1].record(stream)
+        ev1[k].record(stream)
         kinds.append("full" if (w.P and t % w.P == 0) else "block")
-    e0, e1 = ev[0], ev[-1]
     torch.cuda.synchronize()
-    per_step = [{"kind": kinds[k], "step_ms": ev[k].elapsed_time(ev[k + 1])} for k in range(args.steps)]
+    per_step = [{"kind": kinds[k], "step_ms": ev0[k].elapsed_time(ev1[k])} for k in range(args.steps)]
     barrier(world)
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
+    # back-to-back steps: first event to last; flushed steps: the sum of the steps
+    ms = (ev0[0].elapsed_time(ev1[-1]) if flush is None else sum(p["step_ms"] for p in per_step))
     q.qmuon_sync_status(ws, stream)
     ms_max = max_over_ranks(ms, world)
     value = job_throughput(n_params, args.steps, world, ms_max)
@@ -430,7 +687,7 @@ def run_gpu(args, world, rank, local):
                                  w.q8_kind, "bf16")
     ws_u = torch.empty(q.qmuon_workspace_size(plan_u), dtype=torch.uint8, device=dev)
     inv_u = torch.zeros(len(mats), dtype=torch.float32, device=dev)
-    reps = max(3, args.steps)
+    reps = max(3, min(args.steps, 20))   # the per-kernel legs: a few calls back to back
     for _ in range(2):
         q.qmuon_update_multi_normalize_groups(plan_u, w.beta, 2, None, inv_u, ws_u, stream=stream)
     u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -468,7 +725,7 @@ def run_gpu(args, world, rank, local):
                     k += 1
         return probs
 
-    ns_ms, ns_flop = {}, {}
+    ns_ms, ns_flop, ns_exec = {}, {}, {}
     for full in ([False, True] if w.P != 1 else [True]):
         probs = ns_problems(full)
         ws_n = torch.empty(q.qmuon_ns_workspace_size(probs), dtype=torch.uint8, device=dev)
@@ -485,6 +742,7 @@ def run_gpu(args, world, rank, local):
         key = "full" if full else "block"
         ns_ms[key] = n0.elapsed_time(n1) / nrep
         ns_flop[key] = step_ns_flops(w, full)
+        ns_exec[key] = step_ns_executed(w, full)
         del ws_n
 
     # e2e through the host-fed entry: every step copies its gradients in from
@@ -534,7 +792,8 @@ def run_gpu(args, world, rank, local):
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
     return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
                 upd_sr_ms=upd_sr_ms, grasp_ms=grasp_ms,
-                ns_ms=ns_ms, ns_flop=ns_flop, e2e_value=e2e_value, h2d=h2d, d2h=d2h, n_full=n_full,
+                ns_ms=ns_ms, ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=e2e_value, h2d=h2d, d2h=d2h, n_full=n_full,
+                l2=l2_note,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
 
@@ -587,6 +846,8 @@ def main():
     ap.add_argument("--row-scale", type=int, default=1,
                     help="divide every matrix's row count, keeping its columns and tiles (profiling captures only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q8", choices=["int8", "uint8"], default=None,
+                    help="code kind of the 8-bit state (default: the workload's)")
     ap.add_argument("--measure-peaks", action="store_true",
                     help="time cuBLASLt FP8 (E4M3) and bf16 GEMMs at 8192^3 and print one JSON line, nothing else")
     args = ap.parse_args()
@@ -602,7 +863,7 @@ def main():
                5: "llama8b_x4_mxfp8"}[args.workload]
     config = {"workload": wl_name, "description": w.name, "params": w.numel, "matrices": len(w.matrices),
               "P": w.P, "tile": list(w.tile), "ns_iters": w.iters, "beta": w.beta,
-              "l2": "inputs larger than L2 (1.75 GB of bf16 gradients per step)", "parallelism": f"replicas x{world}"}
+              "q8": args.q8 or w.q8_kind, "parallelism": f"replicas x{world}"}
     if args.row_scale > 1:
         config["row_scale"] = f"rows / {args.row_scale} (profiling only, not a reported number)"
         config["params"] = sum(max(8, m.rows // args.row_scale) * m.cols for m in w.matrices)
@@ -610,12 +871,18 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        v, sample, cores, dt = oracle_sample(w, budget_s=20.0)
+        o = oracle_sample(w, steps=args.steps, warmup=args.warmup)
+        v = o["value"]
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "Mparams/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.numel / (v * 1e6) * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 codec / f64 NS",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": v, "unit": "Mparams/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "steps": o["steps"], "warmup": args.warmup, "ms_per_step": o["ms_per_step"],
+                "step": "one bounded sample step of the oracle (see cpu_baseline.sample); value is the workload "
+                        "rate extrapolated from the sample's per-parameter costs",
+                "extrapolated": True, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32 codec / f64 NS", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "Mparams/s", "cores": o["cores"], "kind": "oracle",
+                                 "sample": o["sample"], "single_core": o["single_core"],
+                                 "codec_mparams_per_s_all_cores": o["codec_mparams_per_s_all_cores"],
+                                 "fp64_gflops": o["fp64_gflops"]},
                 "e2e": {"value": v, "unit": "Mparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -623,22 +890,34 @@ def main():
     r = run_gpu(args, world, rank, local)
     if rank != 0:
         return
+    config["l2"] = r["l2"]
     peaks, peak_src = load_peaks()
     traffic = load_traffic()
     w = r["w"]
     # dominant kernel family: the Newton-Schulz GEMMs (block steps dominate a P=5 schedule)
     key = "block" if "block" in r["ns_ms"] else "full"
     ns_tflops = {k: r["ns_flop"][k] / (r["ns_ms"][k] / 1e3) / 1e12 for k in r["ns_ms"]}
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    roof = {"bound": "tensor", "kernel": f"ns_gemm ({key} step, 15 launches per call)",
-            "achieved": ns_tflops[key], "peak": peak_t, "unit": "TFLOP/s", "frac": ns_tflops[key] / peak_t,
-            "peak_source": f"bf16_tflops_sustained of {peak_src}",
-            "traffic": traffic.get(f"ns_{key}_bytes_per_call") if args.row_scale == 1 and args.workload == 4 else None,
-            "flops_per_call": r["ns_flop"][key], "ms_per_call": r["ns_ms"][key]}
-    upd_roof = {"bound": "hbm", "achieved": r["upd_gbs"], "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+    ns_exec_tflops = {k: r["ns_exec"][k] / (r["ns_ms"][k] / 1e3) / 1e12 for k in r["ns_ms"]}
+    # the Newton-Schulz call is timed alone (a few calls back to back): the burst peak
+    peak_t = float(peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained")))
+    upd_roof = {"bound": "hbm", "kernel": "update_kernel (one launch over every matrix)",
+                "achieved": r["upd_gbs"], "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": r["upd_gbs"] / float(peaks["hbm_gbs"]), "frac_of_8000": r["upd_gbs"] / 8000.0,
+                "peak_source": f"hbm_gbs of {peak_src}",
                 "bytes_per_launch": r["upd_bytes"], "ms_per_launch": r["upd_ms"],
                 "traffic": traffic.get("update_bytes_per_launch") if args.row_scale == 1 and args.workload == 4 else None}
+    if r["ns_ms"]:
+        roof = {"bound": "tensor", "kernel": f"ns_gemm ({key} step, {3 * w.iters} launches per call)",
+                "achieved": ns_tflops[key], "peak": peak_t, "unit": "TFLOP/s", "frac": ns_tflops[key] / peak_t,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}: the call is timed alone",
+                "flops_basis": "algorithmic 2(2nm^2+m^3) per matrix and iteration",
+                "achieved_executed": ns_exec_tflops[key], "frac_executed": ns_exec_tflops[key] / peak_t,
+                "executed_flops_per_call": r["ns_exec"][key],
+                "traffic": traffic.get(f"ns_{key}_bytes_per_call")
+                if args.row_scale == 1 and args.workload == 4 else None,
+                "flops_per_call": r["ns_flop"][key], "ms_per_call": r["ns_ms"][key]}
+    else:   # an update-only workload: the update kernel is the step
+        roof = upd_roof
     line = {"metric": METRIC, "value": r["value"], "unit": "Mparams/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (NS operands, fp32 accumulate); int8 state, fp32 codec",
@@ -663,9 +942,13 @@ def main():
                      "d2h_bytes_per_step": r["d2h"]} if r["e2e_value"] is not None else None),
             "gpu_launches": r["launches"]}
     if not args.no_cpu_baseline:
-        v, sample, cores, dt = oracle_sample(w, budget_s=15.0)
-        line["cpu_baseline"] = {"value": v, "unit": "Mparams/s", "cores": cores, "kind": "oracle", "sample": sample,
-                                "seconds": dt}
+        t0 = time.perf_counter()
+        o = oracle_sample(w, steps=3, warmup=1)
+        line["cpu_baseline"] = {"value": o["value"], "unit": "Mparams/s", "cores": o["cores"], "kind": "oracle",
+                                "sample": o["sample"], "single_core": o["single_core"],
+                                "codec_mparams_per_s_all_cores": o["codec_mparams_per_s_all_cores"],
+                                "fp64_gflops": o["fp64_gflops"], "extrapolated": True,
+                                "seconds": time.perf_counter() - t0}
     print(json.dumps(line))
 
 

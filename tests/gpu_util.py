@@ -69,3 +69,25 @@ class Guarded:
     def check(self, what=""):
         lo, hi = self.raw[:GUARD], self.raw[GUARD + self.nbytes:]
         assert bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all()), f"guard bytes overwritten {what}"
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """fp64 values rounded to bf16 (nearest even) and back."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy() \
+        .astype(np.float64)
+
+
+def one_iteration_reference(M: np.ndarray, coeffs, inv: float) -> np.ndarray:
+    """One Newton-Schulz iteration with the engine's rounding points: A and the
+    polynomial B = a I + b A + c A A (the a X term folded into B's diagonal)
+    are stored in bf16, the update is the single product B X; everything else
+    is fp64."""
+    a, b, c = coeffs
+    X = M * inv
+    tall = X.shape[0] > X.shape[1]
+    if tall:
+        X = X.T
+    A = bf16_round(X @ X.T)
+    B = bf16_round(a * np.eye(A.shape[0]) + b * A + c * (A @ A))
+    out = B @ X
+    return out.T if tall else out

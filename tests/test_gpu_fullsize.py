@@ -80,8 +80,9 @@ def _assert_ns(got: np.ndarray, ref: np.ndarray, what, fro=2e-2, cos=0.999):
 # the row-group slices
 # ---------------------------------------------------------------------------
 
-def test_grouped_qkv_mlp_full_size():
-    w = workloads.get(3)
+@pytest.mark.parametrize("q8_kind", ["int8", "uint8"])
+def test_grouped_qkv_mlp_full_size(q8_kind):
+    w = workloads.get(3, q8_kind=q8_kind)
     mats = w.matrices
     rng = np.random.default_rng(3)
     states = [workloads.random_state(m, 700 + i, w.q8_kind, device="cuda") for i, m in enumerate(mats)]
@@ -118,8 +119,9 @@ def test_grouped_qkv_mlp_full_size():
     # a 4096 x 14336 MLP matrix: its own group (7), orthogonalised whole
     r = codec.momentum_update(*whole[5], w.beta, q8_kind=w.q8_kind)
     np.testing.assert_allclose(sums[7].item(), float(np.sum(r.block_sumsq)), rtol=1e-5)
-    M = codec.f32_from_bf16_bits(r.grad).reshape(mats[5].rows, mats[5].cols).astype(np.float64)
-    _assert_ns(bf16_to_f64(grads[5]), ns.newton_schulz(M, inv_norm=float(inv[7].item())), "mlp0.down")
+    if q8_kind == "int8":   # the uint8 codes decode to the same momentum: one Newton-Schulz check serves both
+        M = codec.f32_from_bf16_bits(r.grad).reshape(mats[5].rows, mats[5].cols).astype(np.float64)
+        _assert_ns(bf16_to_f64(grads[5]), ns.newton_schulz(M, inv_norm=float(inv[7].item())), "mlp0.down")
 
 
 # ---------------------------------------------------------------------------

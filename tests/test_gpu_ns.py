@@ -18,30 +18,11 @@ import memory_reduced_muon_gb300 as q
 import workloads
 from oracle import codec, muonbp, ns
 
-from gpu_util import bf16_to_f64, min_row_cos, random_grad, rel_fro, to_oracle_grad
+from gpu_util import bf16_to_f64, min_row_cos, one_iteration_reference, random_grad, rel_fro, to_oracle_grad
 
 pytestmark = pytest.mark.gpu
 
 COEFFS = workloads.COEFFS
-
-
-def _bf16_round(x: np.ndarray) -> np.ndarray:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
-
-
-def _one_iteration_reference(M, coeffs, inv):
-    # the engine's rounding points: A and the polynomial B = a I + b A + c A A
-    # (the a X term folded into B's diagonal) are stored in bf16, the update
-    # is the single product B X; everything else here is fp64
-    a, b, c = coeffs
-    X = M * inv
-    tall = X.shape[0] > X.shape[1]
-    if tall:
-        X = X.T
-    A = _bf16_round(X @ X.T)
-    B = _bf16_round(a * np.eye(A.shape[0]) + b * A + c * (A @ A))
-    out = B @ X
-    return out.T if tall else out
 
 
 def _run_ns(mats, iters, coeffs, invs=None):
@@ -68,7 +49,7 @@ def test_single_iteration_products(coeffs):
         Mb = Mt.float().cpu().numpy().astype(np.float64)
         inv = 1.0 / np.linalg.norm(Mb)
         mats.append(Mt)
-        ref.append(_one_iteration_reference(Mb, coeffs, inv))
+        ref.append(one_iteration_reference(Mb, coeffs, inv))
     invs = [torch.tensor([1.0 / np.linalg.norm(bf16_to_f64(m))], dtype=torch.float32, device="cuda") for m in mats]
     _run_ns(mats, 1, coeffs, invs)
     for (r, c), Mt, R in zip(SHAPES, mats, ref):

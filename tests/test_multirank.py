@@ -61,8 +61,20 @@ def test_single_rank_helpers():
 
 
 def test_oracle_sample_leg():
-    v, sample, cores, dt = bench.oracle_sample(workloads.get(1), budget_s=5.0)
-    assert v > 0 and cores >= 1 and "512x512" in sample
+    o = bench.oracle_sample(workloads.get(1), steps=2, warmup=1)
+    assert o["value"] > 0 and o["cores"] >= 1 and "512x512" in o["sample"]
+    assert o["steps"] == 2 and o["ms_per_step"] > 0 and o["extrapolated"] is True
+    assert o["single_core"] is None or 0 < o["single_core"]
+
+
+def test_executed_flop_count_of_the_syrk_schedule():
+    # 256 x 256 tiles, symmetric products on and above the diagonal: on the
+    # MuonBP workload's block set 1.357e13 FLOPs per call, full set 6.05e13
+    w = workloads.get(4)
+    assert abs(bench.step_ns_executed(w, False) - 1.3572e13) / 1.3572e13 < 1e-3
+    assert abs(bench.step_ns_executed(w, True) - 6.0527e13) / 6.0527e13 < 1e-3
+    # one 256 x 256 tile per product at m = n = 256: 3 x 2 x 256^3 per iteration
+    assert bench.ns_executed_flops_of(256, 256, 1) == 3 * 2.0 * 256 ** 3
 
 
 def test_step_flop_count_matches_page_formula():
@@ -88,6 +100,7 @@ def test_reference_arm_prints_the_contract_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "Mparams/s" and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    assert d["extrapolated"] is True   # value: the workload rate from the timed sample steps
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
     assert d["config"]["workload"] == "single_512"
     cb = d["cpu_baseline"]

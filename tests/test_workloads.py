@@ -78,3 +78,13 @@ def test_states(q8_kind):
     assert int(vals.min()) >= -127 and int(vals.max()) <= 127
     la = torch.log(a)
     assert float(la.min()) >= -9.0 and float(la.max()) <= 3.0
+
+
+def test_code_kind_variant():
+    # the grouped workload names both code kinds: the uint8 variant differs
+    # from the default only in its state encoding
+    a, b = workloads.get(3), workloads.get(3, q8_kind="uint8")
+    assert a.q8_kind == "int8" and b.q8_kind == "uint8"
+    assert a.matrices == b.matrices and a.segments == b.segments and a.ns_slices == b.ns_slices
+    with pytest.raises(ValueError):
+        workloads.get(3, q8_kind="int4")

@@ -105,8 +105,19 @@ def _qkv_mlp() -> Tuple[List[Matrix], List[Segment], List[Tuple[int, int, int]]]
     return mats, segs, slices
 
 
-def get(key: int) -> Workload:
-    """The five synthetic workloads, numbered 1..5."""
+def get(key: int, q8_kind: Optional[str] = None) -> Workload:
+    """The five synthetic workloads, numbered 1..5; ``q8_kind`` ("int8" or
+    "uint8") replaces the workload's code kind (the grouped workload 3 names
+    both)."""
+    w = _get(key)
+    if q8_kind is not None:
+        if q8_kind not in ("int8", "uint8"):
+            raise ValueError(q8_kind)
+        w.q8_kind = q8_kind
+    return w
+
+
+def _get(key: int) -> Workload:
     if key == 1:
         return Workload(1, "one 512x512 matrix, grad N(0,1e-3^2), 3 steps, Frobenius normalise + 5 NS iterations",
                         [Matrix("w", 512, 512)], "normal_1e-3", steps=3)
