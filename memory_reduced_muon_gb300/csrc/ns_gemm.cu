@@ -393,9 +393,20 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* p, int n, float 
 template <int CG>
 __device__ __forceinline__ void decode_tile(const NsProb& P, int kind, int local, int& I, int& J) {
   if (kind >= G_UPDATE) {
+    // the update product's tiles in the order CTA groups take them up: the
+    // tiles that run at the same time share one panel of the X operand, read
+    // once from DRAM, while they walk the other operand, B (m x m), which L2
+    // holds.  A tall problem's X is the A operand (row panels: row-major
+    // order), a wide one's the B operand (column panels: column-major order).
     const int tn = P.tiles_n[G_UPDATE];
-    I = local / tn;
-    J = local % tn;
+    if (P.tall) {
+      I = local / tn;
+      J = local % tn;
+    } else {
+      const int tm = P.tiles[G_UPDATE] / tn;
+      I = local % tm;
+      J = local / tm;
+    }
     return;
   }
   const int TM = (P.m + 128 * CG - 1) / (128 * CG);
