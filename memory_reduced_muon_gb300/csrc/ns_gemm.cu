@@ -1107,6 +1107,7 @@ void count_tiles(int64_t rows, int64_t cols, int32_t tiles_n[3], int32_t tiles[3
 }
 
 constexpr int kMaxGroups = 512;   // schedule capacity: CTA groups per launch
+constexpr int kLightM = 768;      // problems with a short side up to this are DRAM-bound per tile
 
 // Device table of a problem set: the problems, then per product kind the
 // group starts [kMaxGroups + 1] and the schedule entries.
@@ -1225,6 +1226,40 @@ void build_schedule(const std::vector<NsProb>& probs, int groups_cap, Launchable
       lists[h.second].push_back(t.second);
       h.first += t.first;
       std::push_heap(heap.begin(), heap.end(), later);
+    }
+    // A group's load does not depend on the order of its tiles.  Tiles of
+    // problems with a short side above kLightM are bound by the tensor cores,
+    // those at or below it by DRAM (their K loops are short and every tile
+    // streams its own X panel); each group runs them interleaved in
+    // proportion to their cost, so that at any time the groups together
+    // draw on both instead of running one kind after the other.
+    for (auto& lst : lists) {
+      std::vector<TileRef> heavy, light;
+      int64_t ht = 0, lt = 0;
+      for (const TileRef& t : lst) {
+        const int64_t c = tile_cost(probs[t.prob], kind);
+        if (probs[t.prob].m > kLightM) {
+          heavy.push_back(t);
+          ht += c;
+        } else {
+          light.push_back(t);
+          lt += c;
+        }
+      }
+      if (heavy.empty() || light.empty()) continue;
+      lst.clear();
+      size_t i = 0, j = 0;
+      int64_t h = 0, l = 0;
+      while (i < heavy.size() || j < light.size()) {
+        // the kind whose done fraction of its cost is behind goes next
+        if (j == light.size() || (i < heavy.size() && h * lt <= l * ht)) {
+          h += tile_cost(probs[heavy[i].prob], kind);
+          lst.push_back(heavy[i++]);
+        } else {
+          l += tile_cost(probs[light[j].prob], kind);
+          lst.push_back(light[j++]);
+        }
+      }
     }
     S.start[kind].assign(1, 0);
     S.entries[kind].clear();
