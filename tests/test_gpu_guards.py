@@ -1,7 +1,8 @@
 """Guard bytes around every buffer each entry writes (an out-of-bounds write
 shows up as a changed guard byte): the update in all its modes and with
 stochastic requantisation, the multi-tensor carrier, Newton-Schulz on strided
-matrices (the columns between cols and the row stride are guards too), the
+matrices (the columns between cols and the row stride are guards too) and fed
+from an MXFP8 carrier (which it only reads), the
 MuonBP step on ragged shapes, the allocation-free update and the GRASP step.
 Shapes are chosen for ragged tails: sizes that are no multiple of 256, 32, the
 64 x 64 TMA box or the 256 x 256 tile."""
@@ -89,6 +90,37 @@ def test_newton_schulz_strided_stays_in_bounds(shape, ld):
     q.qmuon_newton_schulz_batched([prob], 5, COEFFS, ws)
     q.qmuon_sync_status(ws)
     buf.check(shape)
+    assert torch.equal(buf.t[:, cols:], gap), "columns between cols and the row stride were written"
+    assert bool(torch.isfinite(x.float()).all())
+
+
+@pytest.mark.parametrize("shape,ld", [((37, 96), 104), ((300, 544), 552), ((520, 160), 168), ((129, 224), 224)])
+def test_newton_schulz_from_carrier_stays_in_bounds(shape, ld):
+    # the carrier is only read (payload and scales unchanged, guards intact);
+    # the output goes to x alone, whose row-stride gap survives
+    rows, cols = shape
+    m = workloads.Matrix("t", rows, cols)
+    qs, a = workloads.zero_state(m, "int8", device="cuda")
+    g = random_grad(m.numel, "bf16", 77)
+    pay = Guarded((m.numel,), torch.uint8)
+    sca = Guarded((rows * (cols // 32),), torch.uint8)
+    inv = torch.zeros(1, device="cuda")
+    ws = torch.empty(q.qmuon_carrier_workspace_size(rows, cols), dtype=torch.uint8, device="cuda")
+    q.qmuon_update_mxfp8_carrier(qs, a, g, rows, cols, "int8", "bf16", 0.9, pay.t, sca.t, inv, ws)
+    torch.cuda.synchronize()
+    pay_before, sca_before = pay.t.clone(), sca.t.clone()
+    buf = Guarded((rows, ld), torch.bfloat16)
+    gap = torch.full((rows, ld - cols), 1234.0, dtype=torch.bfloat16, device="cuda")
+    buf.t[:, cols:] = gap
+    x = buf.t[:, :cols]
+    prob = q.ns_problem(x, rows, cols, ld=ld, inv_norm=inv, input_kind=q.QMUON_NS_MXFP8, payload=pay.t,
+                        scale_inv=sca.t)
+    ws2 = torch.empty(q.qmuon_ns_workspace_size([prob]), dtype=torch.uint8, device="cuda")
+    q.qmuon_newton_schulz_batched([prob], 5, COEFFS, ws2)
+    q.qmuon_sync_status(ws2)
+    for b in (buf, pay, sca):
+        b.check(shape)
+    assert torch.equal(pay.t, pay_before) and torch.equal(sca.t, sca_before)
     assert torch.equal(buf.t[:, cols:], gap), "columns between cols and the row stride were written"
     assert bool(torch.isfinite(x.float()).all())
 
