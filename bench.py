@@ -150,6 +150,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def audit_per_step(q, before, steps):
+    """The library's path and dtype tallies added by the timed steps, per step
+    (fields that moved only)."""
+    after = q.qmuon_get_counters()
+    return {k: (after[k] - before[k]) / steps for k in after if after[k] != before[k]}
+
+
 def dist_info():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -406,6 +413,7 @@ def run_gpu_carrier(args, world, rank, local, w):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
+    tallies = q.qmuon_get_counters()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -415,6 +423,7 @@ def run_gpu_carrier(args, world, rank, local, w):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
+    audit = audit_per_step(q, tallies, args.steps)
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     q.qmuon_sync_status(ws_n, stream)
     # the carrier update alone and the Newton-Schulz alone
@@ -435,7 +444,7 @@ def run_gpu_carrier(args, world, rank, local, w):
     n_params = w.numel
     upd_bytes = (1 + 2 + 1 + 1 + 1.0 / 32 + 8.0 / 256) * n_params
     flop = step_ns_flops(w, True)
-    return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks,
+    return dict(value=world * n_params * args.steps / (ms / 1e3) / 1e6, ms=ms, clocks=clocks, audit=audit,
                 per_step=[], upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes,
                 ns_ms={"full": ns_ms}, ns_flop={"full": flop}, ns_exec={"full": step_ns_executed(w, True)},
                 e2e_value=None, h2d=0, d2h=0, n_full=args.steps,
@@ -507,6 +516,7 @@ def run_gpu_grouped(args, world, rank, local, w):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
+    tallies = q.qmuon_get_counters()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -516,6 +526,7 @@ def run_gpu_grouped(args, world, rank, local, w):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
+    audit = audit_per_step(q, tallies, args.steps)
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     q.qmuon_sync_status(ws, stream)
     if w.ns:
@@ -573,7 +584,7 @@ def run_gpu_grouped(args, world, rank, local, w):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     q.qmuon_sync_status(ws, stream)
     launches = (1 + (3 * w.iters + (1 if w.iters == 1 else 0) if w.ns else 0)) * args.steps
-    return dict(value=job_throughput(n_params, args.steps, world, ms), ms=ms, clocks=clocks, per_step=[],
+    return dict(value=job_throughput(n_params, args.steps, world, ms), ms=ms, clocks=clocks, audit=audit, per_step=[],
                 upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes, ns_ms=ns_ms,
                 ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=world * n_params * e2e_steps / e2e_s / 1e6, h2d=h2d,
                 d2h=4 * n_groups, n_full=args.steps if w.ns else 0, launches=launches, n_params=n_params, w=w,
@@ -661,6 +672,7 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
+    tallies = q.qmuon_get_counters()
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     kinds = []
@@ -676,6 +688,7 @@ def run_gpu(args, world, rank, local):
     per_step = [{"kind": kinds[k], "step_ms": ev0[k].elapsed_time(ev1[k])} for k in range(args.steps)]
     barrier(world)
     clocks = sampler.stop()
+    audit = audit_per_step(q, tallies, args.steps)
     # back-to-back steps: first event to last; flushed steps: the sum of the steps
     ms = (ev0[0].elapsed_time(ev1[-1]) if flush is None else sum(p["step_ms"] for p in per_step))
     q.qmuon_sync_status(ws, stream)
@@ -790,7 +803,8 @@ def run_gpu(args, world, rank, local):
 
     # launches of our kernels per step: 1 update + 3 per Newton-Schulz iteration
     launches_per_step = 1 + 3 * w.iters + (1 if w.iters == 1 else 0)
-    return dict(value=value, ms=ms_max, clocks=clocks, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs, upd_bytes=upd_bytes,
+    return dict(value=value, ms=ms_max, clocks=clocks, audit=audit, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs,
+                upd_bytes=upd_bytes,
                 upd_sr_ms=upd_sr_ms, grasp_ms=grasp_ms,
                 ns_ms=ns_ms, ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=e2e_value, h2d=h2d, d2h=d2h, n_full=n_full,
                 l2=l2_note,
@@ -938,6 +952,7 @@ def main():
                                             if args.row_scale == 1 and args.workload == 4 else None}
                                            if r.get("upd_sr_ms") else None),
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
+            "audit_per_step": r.get("audit"),
             "e2e": ({"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
                      "d2h_bytes_per_step": r["d2h"]} if r["e2e_value"] is not None else None),
             "gpu_launches": r["launches"]}

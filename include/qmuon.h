@@ -426,6 +426,57 @@ QMUON_API qmuon_status qmuon_step_prepare(const qmuon_plan* plan, float* const* 
  * (QMUON_ERR_TIMEOUT when a bounded wait expired), then clear it. */
 QMUON_API qmuon_status qmuon_sync_status(void* ws, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Path and dtype audit.  "Quantized Muon Momentum", §Wave18B MXFP8 Carrier
+ * Probe, checks a run with counters: calls of the carrier update and the
+ * dtypes of the tensors it read and wrote (uint8 payload and scales, fp32
+ * inverse norm, the gradient's dtype), and whether a bf16 path was taken.
+ * The library keeps the same kind of tallies for every entry point that
+ * computes, process-wide: a caller can check which paths ran, for example
+ * that Newton-Schulz was fed from MXFP8 carriers and how many bytes of bf16
+ * the carrier expansion wrote on the way (ns_bf16_handoff_bytes; the
+ * expansion is the bf16 hand-off that the page's probe still needs).
+ *
+ * A call adds to the tallies once it has enqueued all of its work and is
+ * about to return QMUON_OK; a call that fails adds nothing.  They count what
+ * was enqueued, not what the GPU has finished.  Additions are relaxed atomic
+ * ones, so calls from several threads are all counted.  Per-tensor fields
+ * add one per non-empty tensor per call.
+ * ------------------------------------------------------------------------- */
+typedef struct qmuon_counters {
+  uint64_t update_calls;            /* qmuon_update_multi_normalize_groups(_sr), qmuon_update_normalize_noalloc */
+  uint64_t update_sr_calls;         /*   of those, with stochastic requantisation */
+  uint64_t carrier_calls;           /* qmuon_update_mxfp8_carrier(_multi) */
+  uint64_t ns_calls;                /* qmuon_newton_schulz_batched */
+  uint64_t step_block_calls;        /* qmuon_step and qmuon_step_from_host, block steps */
+  uint64_t step_full_calls;         /*   full steps */
+  uint64_t step_sr_calls;           /*   steps with stochastic requantisation */
+  uint64_t step_host_fed_calls;     /*   steps through qmuon_step_from_host */
+  uint64_t grasp_calls;             /* qmuon_grasp_step */
+  uint64_t grad_bf16_tensors;       /* gradients read by update, carrier, step and GRASP calls, by dtype */
+  uint64_t grad_fp16_tensors;
+  uint64_t grad_fp32_tensors;
+  uint64_t state_int8_tensors;      /* 8-bit blockwise states updated (update, carrier and step calls) */
+  uint64_t state_uint8_tensors;
+  uint64_t carrier_payload_u8_tensors;   /* E4M3 payloads written (uint8) */
+  uint64_t carrier_scale_u8_tensors;     /* E8M0 scale arrays written (uint8) */
+  uint64_t carrier_inv_norm_f32_values;  /* fp32 inverse norms written by carrier calls */
+  uint64_t ns_bf16_problems;        /* Newton-Schulz problems read as bf16 (batched calls and steps) */
+  uint64_t ns_mxfp8_problems;       /* Newton-Schulz problems read from MXFP8 carriers */
+  uint64_t ns_bf16_handoff_bytes;   /* bf16 bytes the carrier expansion wrote as Newton-Schulz input */
+  uint64_t weight_f32_tensors;      /* fp32 master weights updated by steps */
+  uint64_t grasp_matrices;          /* matrices whose 4-bit state qmuon_grasp_step updated */
+} qmuon_counters;
+
+/* Copies the tallies into `out`: the first min(out_bytes, sizeof(qmuon_counters))
+ * bytes, so a caller built against an older, shorter struct still reads its
+ * own fields.  Returns QMUON_ERR_INVALID_ARGUMENT for a NULL `out`.  Host
+ * only; no CUDA call. */
+QMUON_API qmuon_status qmuon_get_counters(qmuon_counters* out, size_t out_bytes);
+
+/* Sets every tally to zero.  Host only; no CUDA call. */
+QMUON_API void qmuon_reset_counters(void);
+
 /* Detail of the last non-OK status returned on the calling thread (which
  * call failed and the CUDA error string), or "" if none.  The pointer stays
  * valid until the next qmuon call on this thread. */

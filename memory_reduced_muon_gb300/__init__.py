@@ -73,6 +73,17 @@ class qmuon_grasp_matrix(C.Structure):
 
 GRASP_RANK, GRASP_BLOCK = 8, 64
 
+COUNTER_FIELDS = (
+    "update_calls", "update_sr_calls", "carrier_calls", "ns_calls", "step_block_calls", "step_full_calls",
+    "step_sr_calls", "step_host_fed_calls", "grasp_calls", "grad_bf16_tensors", "grad_fp16_tensors",
+    "grad_fp32_tensors", "state_int8_tensors", "state_uint8_tensors", "carrier_payload_u8_tensors",
+    "carrier_scale_u8_tensors", "carrier_inv_norm_f32_values", "ns_bf16_problems", "ns_mxfp8_problems",
+    "ns_bf16_handoff_bytes", "weight_f32_tensors", "grasp_matrices")
+
+
+class qmuon_counters(C.Structure):
+    _fields_ = [(f, C.c_uint64) for f in COUNTER_FIELDS]
+
 _lib_handle = None
 
 
@@ -114,6 +125,8 @@ def lib() -> C.CDLL:
         "qmuon_plan_set_nonfinite_counter": (i32, [vp, vp]),
         "qmuon_noalloc_sync_status": (i32, [vp]),
         "qmuon_noalloc_inject_status": (i32, [i32, C.c_uint32]),
+        "qmuon_get_counters": (i32, [C.POINTER(qmuon_counters), sz]),
+        "qmuon_reset_counters": (None, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -131,7 +144,8 @@ def exported_symbols() -> list:
             "qmuon_update_normalize_noalloc", "qmuon_step_prepare", "qmuon_update_multi_normalize_groups_sr",
             "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
             "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host",
-            "qmuon_plan_set_nonfinite_counter", "qmuon_noalloc_sync_status", "qmuon_noalloc_inject_status"]
+            "qmuon_plan_set_nonfinite_counter", "qmuon_noalloc_sync_status", "qmuon_noalloc_inject_status",
+            "qmuon_get_counters", "qmuon_reset_counters"]
 
 
 # --------------------------------------------------------------------------
@@ -363,6 +377,18 @@ def qmuon_noalloc_inject_status(status: int, site: int = 0):
     """Records ``status`` as if a kernel of the allocation-free update had
     failed at ``site`` (for testing a caller's failure handling)."""
     _check(lib().qmuon_noalloc_inject_status(int(status), int(site)), "qmuon_noalloc_inject_status")
+
+
+def qmuon_get_counters() -> dict:
+    """The library's path and dtype tallies (calls that returned OK, and the
+    tensors they read or wrote), field name -> count."""
+    c = qmuon_counters()
+    _check(lib().qmuon_get_counters(C.byref(c), C.sizeof(c)), "qmuon_get_counters")
+    return {f: int(getattr(c, f)) for f in COUNTER_FIELDS}
+
+
+def qmuon_reset_counters():
+    lib().qmuon_reset_counters()
 
 
 def qmuon_step_prepare(plan: Plan, weights, ws, ws_bytes: Optional[int] = None):

@@ -4,6 +4,7 @@
 // workspace carving and launches.  Every device computation happens in the
 // kernels of update.cu and ns_gemm.cu.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <memory>
@@ -85,10 +86,27 @@ qmuon_status qm::set_error_what(const char* where, const char* what, qmuon_statu
 }
 
 namespace {
-qmuon_status cuda_status(cudaError_t e, const char* where) {
-  return e == cudaSuccess ? QMUON_OK : set_error(where, e);
-}
+std::atomic<uint64_t> g_tally[T_COUNT];
 }  // namespace
+
+void qm::tally(Tally t, uint64_t v) { g_tally[t].fetch_add(v, std::memory_order_relaxed); }
+
+void qm::tally_grad_state(qmuon_dtype dt, qmuon_q8_kind q8, uint64_t tensors) {
+  tally(dt == QMUON_BF16 ? T_GRAD_BF16 : dt == QMUON_FP16 ? T_GRAD_FP16 : T_GRAD_FP32, tensors);
+  tally(q8 == QMUON_Q8_INT8 ? T_STATE_INT8 : T_STATE_UINT8, tensors);
+}
+
+extern "C" qmuon_status qmuon_get_counters(qmuon_counters* out, size_t out_bytes) {
+  if (!out) return QMUON_ERR_INVALID_ARGUMENT;
+  uint64_t v[T_COUNT];
+  for (int i = 0; i < T_COUNT; ++i) v[i] = g_tally[i].load(std::memory_order_relaxed);
+  std::memcpy(out, v, std::min(out_bytes, sizeof(v)));
+  return QMUON_OK;
+}
+
+extern "C" void qmuon_reset_counters(void) {
+  for (int i = 0; i < T_COUNT; ++i) g_tally[i].store(0, std::memory_order_relaxed);
+}
 
 // ---------------------------------------------------------------------------
 // the plan
@@ -123,6 +141,12 @@ struct qmuon_plan {
 };
 
 namespace {
+
+uint64_t nonempty_tensors(const qmuon_plan* plan) {
+  uint64_t k = 0;
+  for (const qmuon_tensor& T : plan->tensors) k += (T.rows * T.cols != 0) ? 1 : 0;
+  return k;
+}
 
 qmuon_status validate_tensor(const qmuon_tensor& t, qmuon_dtype dt) {
   if (t.rows < 0 || t.cols < 0) return QMUON_ERR_INVALID_ARGUMENT;
@@ -418,7 +442,11 @@ qmuon_status update_groups(const qmuon_plan* plan, float beta, int32_t normalize
   cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
   if (e == cudaSuccess && normalize_mode == 1) e = launch_scale_groups(L, plan->dt, inv, s);
-  return cuda_status(e, "qmuon_update_multi_normalize_groups (launch)");
+  if (e != cudaSuccess) return set_error("qmuon_update_multi_normalize_groups (launch)", e);
+  tally(T_UPDATE_CALLS);
+  if (sr) tally(T_UPDATE_SR_CALLS);
+  tally_grad_state(plan->dt, plan->q8, nonempty_tensors(plan));
+  return QMUON_OK;
 }
 
 }  // namespace
@@ -510,7 +538,13 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier(const qmuon_tensor* tensor, q
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(L.header, 0, kWsHeader, s);
   if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, true, s);
-  return cuda_status(e, "qmuon_update_mxfp8_carrier (launch)");
+  if (e != cudaSuccess) return set_error("qmuon_update_mxfp8_carrier (launch)", e);
+  tally(T_CARRIER_CALLS);
+  tally_grad_state(grad_dtype, q8_kind, 1);
+  tally(T_CARRIER_PAYLOAD_U8);
+  tally(T_CARRIER_SCALE_U8);
+  tally(T_CARRIER_INV_NORM_F32);
+  return QMUON_OK;
 }
 
 extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan, float beta, uint8_t* const* payloads,
@@ -550,7 +584,14 @@ extern "C" qmuon_status qmuon_update_mxfp8_carrier_multi(const qmuon_plan* plan,
     if (e == cudaSuccess) e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
     if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, true, s);
     // the pageable host table is staged by the copy before it returns
-    return cuda_status(e, "qmuon_update_mxfp8_carrier_multi (launch)");
+    if (e != cudaSuccess) return set_error("qmuon_update_mxfp8_carrier_multi (launch)", e);
+    const uint64_t k = nonempty_tensors(plan);
+    tally(T_CARRIER_CALLS);
+    tally_grad_state(plan->dt, plan->q8, k);
+    tally(T_CARRIER_PAYLOAD_U8, k);
+    tally(T_CARRIER_SCALE_U8, k);
+    tally(T_CARRIER_INV_NORM_F32, k);
+    return QMUON_OK;
   });
 }
 
@@ -588,8 +629,20 @@ extern "C" qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* prob
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t me = cudaMemsetAsync(b, 0, kWsHeader, s);
     if (me != cudaSuccess) return set_error("qmuon_newton_schulz_batched (memset)", me);
-    return ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
-                         b + kWsHeader, ws_bytes - kWsHeader, s);
+    const qmuon_status rs = ns::run_batch(problems, n_problems, iters, coeffs, reinterpret_cast<WsHeader*>(b),
+                                          b + kWsHeader, ws_bytes - kWsHeader, s);
+    if (rs != QMUON_OK) return rs;
+    tally(T_NS_CALLS);
+    for (int32_t i = 0; i < n_problems; ++i) {
+      const qmuon_ns_problem& p = problems[i];
+      if (p.input == QMUON_NS_MXFP8) {
+        tally(T_NS_MXFP8_PROBLEMS);
+        tally(T_NS_BF16_HANDOFF_BYTES, (uint64_t)p.rows * (uint64_t)p.cols * 2u);
+      } else {
+        tally(T_NS_BF16_PROBLEMS);
+      }
+    }
+    return QMUON_OK;
   });
 }
 
@@ -624,7 +677,15 @@ extern "C" qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P,
     cudaError_t e = cudaMemsetAsync(w.header, 0, kWsHeader, s);
     if (e == cudaSuccess) e = launch_update(L, plan->q8, plan->dt, false, s);
     if (e != cudaSuccess) return set_error("qmuon_step (update launch)", e);
-    return ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+    const qmuon_status rs = ns::run_step(tabs, iters, coeffs, full ? eta_full : eta_block, w.header, s);
+    if (rs != QMUON_OK) return rs;
+    const uint64_t k = nonempty_tensors(plan);
+    tally(full ? T_STEP_FULL_CALLS : T_STEP_BLOCK_CALLS);
+    if (plan->sr) tally(T_STEP_SR_CALLS);
+    tally_grad_state(plan->dt, plan->q8, k);
+    tally(T_NS_BF16_PROBLEMS, full ? k : k * (uint64_t)plan->tile_r * (uint64_t)plan->tile_c);
+    tally(T_WEIGHT_F32, k);
+    return QMUON_OK;
   });
 }
 
@@ -671,6 +732,7 @@ extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, 
   if (e == cudaSuccess) e = cudaEventRecord(mp->grads_free, s);
   if (e != cudaSuccess) return set_error("qmuon_step_from_host (read-back)", e);
   mp->grads_free_recorded = true;
+  tally(T_STEP_HOST_FED_CALLS);
   return QMUON_OK;
 }
 

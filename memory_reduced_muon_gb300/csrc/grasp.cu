@@ -794,6 +794,9 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     e = cudaGetLastError();
     // the pageable host tables are staged by the copies above before they return
     if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
+    tally(T_GRASP_CALLS);
+    tally(T_GRASP_MATRICES, (uint64_t)n);
+    tally(T_GRAD_BF16, (uint64_t)n);
     return QMUON_OK;
   });
 }

@@ -892,6 +892,8 @@ extern "C" qmuon_status qmuon_update_normalize_noalloc(const qmuon_tensor* tenso
   e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_update(L, q8_kind, grad_dtype, false, s);
   if (e != cudaSuccess) return set_error("qmuon_update_normalize_noalloc (launch)", e);
+  tally(T_UPDATE_CALLS);
+  tally_grad_state(grad_dtype, q8_kind, 1);
   return QMUON_OK;
 }
 

@@ -220,6 +220,7 @@ def test_cuda_failures_carry_detail(lib):
 _C_CALLER = r"""
 /* A plain C99 caller of the library: the header must compile as C, and the
  * entries must link and answer without a GPU. */
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 #include "qmuon.h"
@@ -237,6 +238,13 @@ int main(void) {
   if (sizeof(qmuon_tensor) != 40 || sizeof(qmuon_norm_segment) != 24 || sizeof(qmuon_ns_problem) != 64 ||
       sizeof(qmuon_grasp_matrix) != 96)
     return 6;
+  /* the audit tallies: no CUDA call, and the failed plan_create above added nothing */
+  qmuon_counters c;
+  memset(&c, 0xff, sizeof(c));
+  if (sizeof(qmuon_counters) != 176 || offsetof(qmuon_counters, grasp_matrices) != 168) return 7;
+  if (qmuon_get_counters(&c, sizeof(c)) != QMUON_OK || c.update_calls != 0 || c.grasp_matrices != 0) return 8;
+  qmuon_reset_counters();
+  if (qmuon_get_counters(NULL, sizeof(c)) != QMUON_ERR_INVALID_ARGUMENT) return 9;
   printf("%s\n", qmuon_version());
   return 0;
 }
@@ -266,7 +274,35 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     assert run.stdout.startswith("qmuon")
     # the binding's structures have the sizes the C compiler gave them
     assert [C.sizeof(t) for t in (q.qmuon_tensor, q.qmuon_norm_segment, q.qmuon_ns_problem,
-                                  q.qmuon_grasp_matrix)] == [40, 24, 64, 96]
+                                  q.qmuon_grasp_matrix, q.qmuon_counters)] == [40, 24, 64, 96, 176]
+
+
+def _header_counter_fields():
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct qmuon_counters {"):text.index("} qmuon_counters;")]
+    return re.findall(r"uint64_t\s+(\w+);", body)
+
+
+def test_counters_on_host(lib):
+    # the binding names the header's fields in the header's order
+    assert tuple(_header_counter_fields()) == q.COUNTER_FIELDS
+    L = q.lib()
+    q.qmuon_reset_counters()
+    assert set(q.qmuon_get_counters().values()) == {0}
+    # calls rejected on the host add nothing
+    t = _tensor(4, 48)
+    assert L.qmuon_update_mxfp8_carrier(C.byref(t), 0, 0, 0.9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) \
+        == q.QMUON_ERR_UNSUPPORTED
+    assert L.qmuon_update_normalize_noalloc(None, 0, 0, 0.9, None, None, None) == q.QMUON_ERR_INVALID_ARGUMENT
+    cf = (C.c_float * 3)(3.4445, -4.775, 2.0315)
+    arr = (q.qmuon_ns_problem * 1)(q.ns_problem(FAKE, 64, 60))
+    assert L.qmuon_newton_schulz_batched(arr, 1, 5, cf, FAKE, 1 << 30, None) == q.QMUON_ERR_UNSUPPORTED
+    assert set(q.qmuon_get_counters().values()) == {0}
+    # a shorter struct (an older caller's) receives only its own prefix
+    buf = (C.c_uint64 * 3)(7, 7, 7)
+    assert L.qmuon_get_counters(C.cast(buf, C.POINTER(q.qmuon_counters)), 16) == q.QMUON_OK
+    assert list(buf) == [0, 0, 7]
+    assert L.qmuon_get_counters(None, 176) == q.QMUON_ERR_INVALID_ARGUMENT
 
 
 def _declared_arities():
