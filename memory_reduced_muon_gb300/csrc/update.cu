@@ -101,11 +101,35 @@ __device__ __forceinline__ uint32_t to_offset_binary(uint32_t w) {
   return (QK == QMUON_Q8_INT8) ? (w ^ 0x80808080u) : w;
 }
 
-// float(q) for byte b of an offset-binary word, exactly: prmt builds the
-// fp32 pattern 0x4B0000uu = 2^23 + u, and subtracting 2^23 + 128 (both exact)
-// leaves u - 128 = q.
-__device__ __forceinline__ float code_to_float(uint32_t u, int b) {
-  return __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650u | (uint32_t)b)), 8388736.0f);
+// For byte b of an offset-binary word, prmt builds the fp32 pattern
+// 0x4B0000uu = 2^23 + u; subtracting 2^23 + 128 (both exact) leaves
+// u - 128 = q, so float(q) takes one prmt and one exact subtraction.
+__device__ __forceinline__ float code_bits(uint32_t u, int b) {
+  return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650u | (uint32_t)b));
+}
+
+// Packed fp32 pairs (one instruction for two lanes of arithmetic), each
+// component rounded to nearest exactly as the scalar __fmul_rn / __fsub_rn.
+// ptxas fuses a packed multiply whose only use is a packed add into a packed
+// FMA (one rounding instead of two), so a product that feeds an addition is
+// always added with the scalar __fadd_rn: those chains were checked bit for
+// bit against the scalar ones on the GPU (sub -> mul, mul -> scalar add,
+// mul -> max -> add, mul -> E4M3 conversion).
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "sub.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
 }
 
 // Four codes (their int32 low bytes, two's complement) into one stored word.
@@ -120,31 +144,23 @@ __device__ __forceinline__ uint32_t pack_codes(int q0, int q1, int q2, int q3) {
 // E8M0 exponent byte of a 32-element block: 127 + e with e the smallest
 // integer such that amax <= 448 * 2^e (448 = 1.75 * 2^8 is the largest E4M3
 // value), clamped to [0, 254]; 127 for amax == 0, 254 for amax == inf.
+// With amax = f * 2^E (f in [1, 2), biased exponent field ef = E + 127),
+// e = E - 8 + [f > 1.75], so the byte is ef - 8 + [mantissa > 0.75].  A
+// subnormal amax (ef = 0, below 2^-126) and any amax below 2^-119 give a
+// negative byte and clamp to 0, so no subnormal case is needed: the byte is
+// a few integer operations and selects, without branches.
 __device__ __forceinline__ int e8m0_of_amax(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const uint32_t ef = (b >> 23) & 0xFFu, mant = b & 0x7FFFFFu;
-  if (amax == 0.0f) return 127;
-  if (ef == 0xFFu) return 254;
-  int E;          // amax = f * 2^E with f in [1, 2)
-  bool above;     // f > 1.75
-  if (ef != 0) {
-    E = (int)ef - 127;
-    above = mant > 0x600000u;
-  } else {        // subnormal: amax = mant * 2^-149
-    const int p = 31 - __clz((int)mant);
-    E = p - 149;
-    above = ((uint64_t)mant << 2) > ((uint64_t)7u << p);
-  }
-  const int e = E - 8 + (above ? 1 : 0);
-  const int byte = 127 + e;
-  return byte < 0 ? 0 : (byte > 254 ? 254 : byte);
+  const uint32_t b = __float_as_uint(amax);   // amax >= 0: the sign bit is clear
+  const int ef = (int)(b >> 23);
+  const int byte = ef - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  const int clamped = byte < 0 ? 0 : (byte > 254 ? 254 : byte);
+  return b == 0u ? 127 : (ef == 0xFF ? 254 : clamped);
 }
 
-// 2^(127 - byte) as an fp32 (byte in [0, 254]: exponent in [-127, 127]).
+// 2^(127 - byte) as an fp32 (byte in [0, 254]: exponent in [-127, 127]); the
+// one subnormal power, 2^-127 (byte 254), is the pattern 0x00400000.
 __device__ __forceinline__ float pow2_from_e8m0(int byte) {
-  const int k = 127 - byte;
-  if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
-  return __uint_as_float(0x00400000u);  // 2^-127 (subnormal, exact)
+  return __uint_as_float(byte < 254 ? (uint32_t)(254 - byte) << 23 : 0x00400000u);
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
@@ -244,16 +260,24 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   const float s_old = __fdiv_rn(in.amax_old, 127.0f);
   float m[16];
   float amax = 0.0f, ss = 0.0f;
+  const float2 s_old2 = make_float2(s_old, s_old), beta2 = make_float2(beta, beta), omb2 = make_float2(omb, omb);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float old = __fmul_rn(code_to_float(u[i >> 2], i & 3), s_old);
-    const float g = Grad<DT>::get(in.g, i);
+  for (int i = 0; i < 16; i += 2) {
+    // elements i and i + 1 as packed pairs: old = (2^23 + u - (2^23 + 128)) * s_old, the subtraction exact
+    const float2 old = mul2_rn(sub2_rn(make_float2(code_bits(u[i >> 2], i & 3), code_bits(u[i >> 2], (i + 1) & 3)),
+                                       make_float2(8388736.0f, 8388736.0f)),
+                               s_old2);
     // (4) m = beta * old + (1 - beta) * g: two rounded products, one rounded sum
-    float mi = __fadd_rn(__fmul_rn(beta, old), __fmul_rn(omb, g));
-    if (!FULL && i >= in.valid) mi = 0.0f;
-    m[i] = mi;
-    amax = fmaxf(amax, fabsf(mi));
-    ss = fmaf(mi, mi, ss);
+    const float2 pb = mul2_rn(beta2, old);
+    const float2 pg = mul2_rn(omb2, make_float2(Grad<DT>::get(in.g, i), Grad<DT>::get(in.g, i + 1)));
+    float mi[2] = {__fadd_rn(pb.x, pg.x), __fadd_rn(pb.y, pg.y)};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (!FULL && i + j >= in.valid) mi[j] = 0.0f;
+      m[i + j] = mi[j];
+      amax = fmaxf(amax, fabsf(mi[j]));
+      ss = fmaf(mi[j], mi[j], ss);
+    }
   }
   // (6) block absmax and (9) block sum of squares across the half-warp
   float amax_l = amax;
@@ -275,12 +299,14 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
   const float sc = (amax == 0.0f) ? 0.0f : __fdiv_rn(127.0f, amax);
   uint32_t qo[4];
   if constexpr (!SR) {
-    auto code = [sc](float x) {
-      return (int)__float_as_uint(__fadd_rn(fmaxf(__fmul_rn(x, sc), -INFINITY), 12582912.0f));
-    };
+    const float2 sc2 = make_float2(sc, sc);
+    auto code = [](float x) { return (int)__float_as_uint(__fadd_rn(fmaxf(x, -INFINITY), 12582912.0f)); };
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
-      qo[w] = pack_codes<QK>(code(m[4 * w]), code(m[4 * w + 1]), code(m[4 * w + 2]), code(m[4 * w + 3]));
+    for (int w = 0; w < 4; ++w) {
+      const float2 lo = mul2_rn(make_float2(m[4 * w], m[4 * w + 1]), sc2);
+      const float2 hi = mul2_rn(make_float2(m[4 * w + 2], m[4 * w + 3]), sc2);
+      qo[w] = pack_codes<QK>(code(lo.x), code(lo.y), code(hi.x), code(hi.y));
+    }
   } else {
     // stochastic: q = clamp(floor(x + u), -127, 127) with x = m * sc and u the
     // top 24 bits of the element's Philox word over 2^24.  x + u rounded
@@ -342,12 +368,13 @@ __device__ __forceinline__ float compute_lane(const LaneIn<DT>& in, const UpdTen
     const float amax32 = fmaxf(amax_l, __shfl_xor_sync(hmask, amax_l, 1));
     const int byte = e8m0_of_amax(amax32);
     const float mult = pow2_from_e8m0(byte);
+    const float2 mult2 = make_float2(mult, mult);
     uint32_t pw[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const uint32_t lo = cvt_e4m3x2(__fmul_rn(m[4 * v], mult), __fmul_rn(m[4 * v + 1], mult));
-      const uint32_t hi = cvt_e4m3x2(__fmul_rn(m[4 * v + 2], mult), __fmul_rn(m[4 * v + 3], mult));
-      pw[v] = lo | (hi << 16);
+      const float2 a = mul2_rn(make_float2(m[4 * v], m[4 * v + 1]), mult2);
+      const float2 b = mul2_rn(make_float2(m[4 * v + 2], m[4 * v + 3]), mult2);
+      pw[v] = __byte_perm(cvt_e4m3x2(a.x, a.y), cvt_e4m3x2(b.x, b.y), 0x5410u);
     }
     if (FULL || in.valid == 16) {
       __stcs(reinterpret_cast<uint4*>(T.payload + e0), make_uint4(pw[0], pw[1], pw[2], pw[3]));
