@@ -878,6 +878,9 @@ def main():
     config = {"workload": wl_name, "description": w.name, "params": w.numel, "matrices": len(w.matrices),
               "P": w.P, "tile": list(w.tile), "ns_iters": w.iters, "beta": w.beta,
               "q8": args.q8 or w.q8_kind, "parallelism": f"replicas x{world}"}
+    if w.carrier:
+        config["ns_input"] = ("bf16-expanded: each MXFP8 carrier is expanded exactly to bf16 in one launch, and the "
+                              "products run on bf16 tensor cores (no block-scaled FP8 MMA)")
     if args.row_scale > 1:
         config["row_scale"] = f"rows / {args.row_scale} (profiling only, not a reported number)"
         config["params"] = sum(max(8, m.rows // args.row_scale) * m.cols for m in w.matrices)
