@@ -150,6 +150,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+E2E_MIN_STEPS = 60   # host-fed steps timed by the end-to-end leg of the MuonBP workload
+
+
 def audit_per_step(q, before, steps):
     """The library's path and dtype tallies added by the timed steps, per step
     (fields that moved only)."""
@@ -586,7 +589,7 @@ def run_gpu_grouped(args, world, rank, local, w):
     launches = (1 + (3 * w.iters + (1 if w.iters == 1 else 0) if w.ns else 0)) * args.steps
     return dict(value=job_throughput(n_params, args.steps, world, ms), ms=ms, clocks=clocks, audit=audit, per_step=[],
                 upd_ms=upd_ms, upd_gbs=upd_bytes / (upd_ms / 1e3) / 1e9, upd_bytes=upd_bytes, ns_ms=ns_ms,
-                ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=world * n_params * e2e_steps / e2e_s / 1e6, h2d=h2d,
+                ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=world * n_params * e2e_steps / e2e_s / 1e6, e2e_steps=e2e_steps, h2d=h2d,
                 d2h=4 * n_groups, n_full=args.steps if w.ns else 0, launches=launches, n_params=n_params, w=w,
                 l2=f"inputs larger than L2 ({h2d / 1e9:.2f} GB of bf16 gradients per step)")
 
@@ -764,7 +767,10 @@ def run_gpu(args, world, rank, local):
     # alternate, so step k+1's copies (on a copy stream) overlap step k's
     # kernels; the clock stops once the last read-back has landed.
     torch.cuda.synchronize()
-    e2e_steps = max(2, args.steps)
+    # at least 60 steps (about a second): a host-to-device stall of the box
+    # (two copies at 12-19 GB/s, seen on some boxes and not on others) then
+    # weighs in proportion instead of taking a third of a 20-step leg
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     h2d = sum(g.numel() * g.element_size() for g in grads)
     ngr = max(info["n_block_groups"], info["n_full_groups"])
     copy_stream = torch.cuda.Stream(device=dev)
@@ -806,7 +812,7 @@ def run_gpu(args, world, rank, local):
     return dict(value=value, ms=ms_max, clocks=clocks, audit=audit, per_step=per_step, upd_ms=upd_ms, upd_gbs=upd_gbs,
                 upd_bytes=upd_bytes,
                 upd_sr_ms=upd_sr_ms, grasp_ms=grasp_ms,
-                ns_ms=ns_ms, ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=e2e_value, h2d=h2d, d2h=d2h, n_full=n_full,
+                ns_ms=ns_ms, ns_flop=ns_flop, ns_exec=ns_exec, e2e_value=e2e_value, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h, n_full=n_full,
                 l2=l2_note,
                 launches=launches_per_step * args.steps, n_params=n_params, w=w)
 
@@ -957,7 +963,8 @@ def main():
             "roofline": roof, "roofline_update": upd_roof, "clocks": r["clocks"],
             "audit_per_step": r.get("audit"),
             "e2e": ({"value": r["e2e_value"], "unit": "Mparams/s", "h2d_bytes_per_step": r["h2d"],
-                     "d2h_bytes_per_step": r["d2h"]} if r["e2e_value"] is not None else None),
+                     "d2h_bytes_per_step": r["d2h"], "steps": r.get("e2e_steps", args.steps)}
+                    if r["e2e_value"] is not None else None),
             "gpu_launches": r["launches"]}
     if not args.no_cpu_baseline:
         t0 = time.perf_counter()
