@@ -145,20 +145,20 @@ __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
   const GraspProb& P = a.probs[blockIdx.x];
   const int64_t cols = P.m.cols;
   double ss[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+  // unrolled so that several rows' loads are in flight at once; the sums
+  // still run over j in order
+#pragma unroll 4
   for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
     float r[kRank];
     factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
+    float4* dst = reinterpret_cast<float4*>(P.rdeq + j * kRank);
+    dst[0] = make_float4(r[0], r[1], r[2], r[3]);
+    dst[1] = make_float4(r[4], r[5], r[6], r[7]);
 #pragma unroll
     for (int l = 0; l < kRank; ++l) ss[l] += (double)r[l] * (double)r[l];
   }
   block_sum8(ss, red);
   if (threadIdx.x < kRank) P.qinv[threadIdx.x] = ss[threadIdx.x] > 0.0 ? 1.0 / sqrt(ss[threadIdx.x]) : 0.0;
-  for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
-    float r[kRank];
-    factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
-#pragma unroll
-    for (int l = 0; l < kRank; ++l) P.rdeq[j * kRank + l] = r[l];
-  }
 }
 
 // The CTA's share of Z^T Z in fp64 (36 lower-triangle entries, row-major
