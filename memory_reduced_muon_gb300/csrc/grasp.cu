@@ -335,20 +335,28 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
 }
 
 // Cholesky of an 8 x 8 SPD matrix (lower factor, in place), one thread.
-__device__ bool chol8(double (&g)[kRank][kRank]) {
+// Fully unrolled so that the matrix stays in registers; each column divides
+// once (its diagonal's reciprocal, within one fp64 rounding of the quotients).
+__device__ __forceinline__ bool chol8(double (&g)[kRank][kRank]) {
+  bool ok = true;
+#pragma unroll
   for (int j = 0; j < kRank; ++j) {
     double d = g[j][j];
+#pragma unroll
     for (int k = 0; k < j; ++k) d -= g[j][k] * g[j][k];
-    if (!(d > 0.0)) return false;
-    d = sqrt(d);
+    ok = ok && (d > 0.0);
+    d = sqrt(ok ? d : 1.0);
     g[j][j] = d;
+    const double inv = 1.0 / d;
+#pragma unroll
     for (int i = j + 1; i < kRank; ++i) {
       double s = g[i][j];
+#pragma unroll
       for (int k = 0; k < j; ++k) s -= g[i][k] * g[j][k];
-      g[i][j] = s / d;
+      g[i][j] = s * inv;
     }
   }
-  return true;
+  return ok;
 }
 
 // ---------------------------------------------------------------------------
@@ -368,15 +376,18 @@ __global__ void __launch_bounds__(64) grasp_chol(GraspArgs a, WsHeader* hdr) {
   __syncthreads();
   if (threadIdx.x == 0) {
     double g[kRank][kRank];
-    int k = 0;
+#pragma unroll
     for (int u = 0; u < kRank; ++u)
-      for (int v = 0; v < kRank; ++v) g[u][v] = (v <= u) ? sG[k++] : 0.0;
+#pragma unroll
+      for (int v = 0; v < kRank; ++v) g[u][v] = (v <= u) ? sG[u * (u + 1) / 2 + v] : 0.0;
     if (!chol8(g)) {
       // rank-deficient M_t Q: no orthonormal factor
       if (atomicCAS(&hdr->error, 0u, (unsigned)QMUON_ERR_INVALID_ARGUMENT) == 0u) hdr->error_info = 0x2000u + blockIdx.x;
       return;
     }
+#pragma unroll
     for (int u = 0; u < kRank; ++u)
+#pragma unroll
       for (int v = 0; v < kRank; ++v) P.L[u * kRank + v] = g[u][v];
   }
 }
@@ -389,7 +400,8 @@ __global__ void __launch_bounds__(64) grasp_chol(GraspArgs a, WsHeader* hdr) {
 template <int PASS>
 __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* hdr) {
   __shared__ double sL[kRank][kRank];
-  __shared__ double red[2][36];
+  __shared__ double sInvD[kRank];         // 1 / L_uu
+  __shared__ double sZZ[36][kS + 1];      // PASS 0: each row's products z_u z_v
   __shared__ float sx[kS][kRank];
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
   const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
@@ -397,9 +409,13 @@ __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* 
   const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
   const int64_t rows = P.m.rows;
   sL[threadIdx.x >> 3][threadIdx.x & 7] = P.L[threadIdx.x];
+  if (threadIdx.x < kRank) sInvD[threadIdx.x] = 1.0 / P.L[threadIdx.x * (kRank + 1)];
   __syncthreads();
   const int64_t i = bi * kS + threadIdx.x;
   const bool live = i < rows;
+  // forward substitution; fp64 throughput is scarce here, so each row
+  // multiplies by the diagonal's reciprocal (within one fp64 rounding of
+  // the quotient) instead of dividing
   double z[kRank];
 #pragma unroll
   for (int u = 0; u < kRank; ++u) {
@@ -407,13 +423,26 @@ __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* 
     if (live) s = (PASS == 0) ? (double)P.y[i * kRank + u] : P.p1[i * kRank + u];
 #pragma unroll
     for (int v = 0; v < u; ++v) s -= sL[u][v] * z[v];
-    z[u] = live ? s / sL[u][u] : 0.0;
+    z[u] = live ? s * sInvD[u] : 0.0;
   }
   if (PASS == 0) {
     if (live)
 #pragma unroll
       for (int l = 0; l < kRank; ++l) P.p1[i * kRank + l] = z[l];
-    gram_share(z, live, 1, red, P.gpart + bi * 36);
+    // the strip's share of Z^T Z: each row's 36 products, then one thread per
+    // entry adds the 64 rows in order
+    int k = 0;
+#pragma unroll
+    for (int u = 0; u < kRank; ++u)
+#pragma unroll
+      for (int v = 0; v <= u; ++v, ++k) sZZ[k][threadIdx.x] = z[u] * z[v];
+    __syncthreads();
+    if (threadIdx.x < 36) {
+      double g = 0.0;
+#pragma unroll 8
+      for (int r = 0; r < kS; ++r) g += sZZ[threadIdx.x][r];
+      P.gpart[bi * 36 + threadIdx.x] = g;
+    }
   } else {
     const int nvalid = (rows - bi * kS) < kS ? (int)(rows - bi * kS) : kS;
     if (live) {
