@@ -97,6 +97,34 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return r;
 }
 
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "sub.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// comp_add on two independent sums at once, with Knuth's TwoSum (additions
+// and subtractions only, so no packed multiply can be fused into them).  The
+// error term it accumulates is the exact rounding error of the addition, the
+// same value comp_add's magnitude-ordered form computes, so the totals are
+// those of two comp_add calls.
+__device__ __forceinline__ void two_sum_add2(float2& sum, float2& comp, float2 v) {
+  const float2 t = add2_rn(sum, v);
+  const float2 bv = sub2_rn(t, sum);
+  comp = add2_rn(comp, add2_rn(sub2_rn(sum, sub2_rn(t, bv)), sub2_rn(v, bv)));
+  sum = t;
+}
+
 // Compensated (Neumaier) addition of a block's sum into a running total:
 // the strips add up to 224 blocks, and orth magnifies the error of Y when its
 // columns are nearly parallel.
@@ -516,11 +544,12 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const Ws
     if (c < nch) load(c);
     cp_async_commit();
   }
-  float acc[2][kRank], accc[2][kRank];
+  // sums of the thread's two columns as packed pairs (column 2 cp in .x,
+  // 2 cp + 1 in .y): each component rounds as fmaf and as the scalar
+  // compensated sum would
+  float2 acc[kRank], accc[kRank];
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int l = 0; l < kRank; ++l) acc[h][l] = accc[h][l] = 0.0f;
+  for (int l = 0; l < kRank; ++l) acc[l] = accc[l] = make_float2(0.0f, 0.0f);
   for (int64_t c = 0; c < nch; ++c) {
     if (c + kP2Stages - 1 < nch) load(c + kP2Stages - 1);
     cp_async_commit();
@@ -529,36 +558,32 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const Ws
     const unsigned char* st = p2smem + (c % kP2Stages) * kP2StageBytes;
     const uint32_t* sm = reinterpret_cast<const uint32_t*>(st);
     const float (*sp)[kRank] = reinterpret_cast<const float (*)[kRank]>(st + kP2Rows * kS * 2);
-    float ab[2][kRank];
+    float2 ab[kRank];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) ab[h][l] = 0.0f;
+    for (int l = 0; l < kRank; ++l) ab[l] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int r = 0; r < kP2Rows / (kThreads / 32); ++r) {
       const int li = rg * (kP2Rows / (kThreads / 32)) + r;
       const uint32_t w = sm[li * (kS / 2) + cp];
-      const float m0 = __uint_as_float(w << 16), m1 = __uint_as_float(w & 0xFFFF0000u);
+      const float2 m = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
       float pr[kRank];
       *reinterpret_cast<float4*>(pr) = *reinterpret_cast<const float4*>(&sp[li][0]);
       *reinterpret_cast<float4*>(pr + 4) = *reinterpret_cast<const float4*>(&sp[li][4]);
 #pragma unroll
-      for (int l = 0; l < kRank; ++l) {
-        ab[0][l] = fmaf(m0, pr[l], ab[0][l]);
-        ab[1][l] = fmaf(m1, pr[l], ab[1][l]);
-      }
+      for (int l = 0; l < kRank; ++l) ab[l] = fma2(m, make_float2(pr[l], pr[l]), ab[l]);
     }
+    // TwoSum's error term is the exact rounding error of the addition, as
+    // the magnitude-ordered form of comp_add computes it
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) comp_add(acc[h][l], accc[h][l], ab[h][l]);
+    for (int l = 0; l < kRank; ++l) two_sum_add2(acc[l], accc[l], ab[l]);
     __syncthreads();   // the stage is refilled by the next iteration's copies
   }
   cp_async_wait<0>();
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int l = 0; l < kRank; ++l) part[rg][2 * cp + h][l] = acc[h][l] + accc[h][l];
+  for (int l = 0; l < kRank; ++l) {
+    part[rg][2 * cp][l] = acc[l].x + accc[l].x;
+    part[rg][2 * cp + 1][l] = acc[l].y + accc[l].y;
+  }
   __syncthreads();
   __shared__ float sx[kS][kRank];
   if (t < kS) {
