@@ -28,7 +28,9 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstring>
+#include <type_traits>
 #include <vector>
 
 #include "qm_internal.h"
@@ -240,26 +242,60 @@ __device__ __forceinline__ void quantize_block8(const float (*x)[kRank], int nva
   }
 }
 
+// 16- and 8-byte asynchronous global -> shared copies; an invalid one
+// writes zeros (source size 0) and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(src), "r"(valid ? 8 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---------------------------------------------------------------------------
 // pass 1: one CTA per 64-row strip of a matrix, walking its column blocks in
-// chunks of four (256 columns: R and the residual's column steps for the
-// chunk are staged in shared memory by all threads between two barriers).
-// Thread t owns row t/4 of the strip and 16 consecutive columns (t % 4) * 16
-// of each block, and loads its four blocks' codes and gradient up front; Y
-// for the strip's rows is complete when the walk ends.
+// chunks of two (128 columns).  Each chunk's gradient tile, residual codes and
+// dequantised R rows arrive in shared memory by asynchronous copies through a
+// two-stage ring, one chunk ahead of the arithmetic; the rows' residual
+// maxima and the columns' residual steps come by plain loads one chunk ahead
+// too.  With nothing held in registers between chunks, three CTAs fit on an
+// SM.  Thread t owns row t/4 of the strip and 16 consecutive columns
+// (t % 4) * 16 of each block; Y for the strip's rows is complete when the
+// walk ends.
 // ---------------------------------------------------------------------------
-constexpr int kChunk = 4;   // column blocks per chunk
+constexpr int kChunk = 4;   // column blocks per chunk of pass 3
+constexpr int kC1 = 2;      // column blocks per chunk of pass 1
 
-// Shared rows of 8 floats for the chunk's 256 columns.  The four 16-column
-// groups a warp reads at once sit 16 * 8 = 128 floats apart, one bank apart
-// modulo 32: each group of 16 columns is shifted by 4 more floats so that
-// their float4 reads fall in different banks.
-constexpr int kPadStride = kChunk * kS * kRank + (kChunk * kS / 16) * 4;
+// Shared rows of 8 floats for a chunk's columns.  The four 16-column groups a
+// warp reads at once sit 16 * 8 = 128 floats apart, one bank apart modulo 32:
+// each group of 16 columns is shifted by 4 more floats so that their float4
+// reads fall in different banks.
 __device__ __forceinline__ int sidx(int col, int l) { return col * kRank + (col >> 4) * 4 + l; }
 
-__global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
-  __shared__ __align__(16) float sR[kPadStride];
-  __shared__ float sStepC[kChunk * kS];   // fl(cmax_j / 7) of the residual
+// One stage of pass 1's ring.  Row strides are padded so that the rows a warp
+// reads at once fall in different banks: 272 bytes for the gradient (8 rows x
+// 4 column groups of 16 bf16 read as 16-byte halves), 96 bytes for the codes
+// (4 rows x 4 groups of 8 bytes per half-warp).
+constexpr int kP1GStride = kC1 * kS * 2 + 16;                  // bytes per gradient row
+constexpr int kP1CStride = kC1 * kS / 2 + 32;                  // bytes per code row
+constexpr int kP1RFloats = kC1 * kS * kRank + (kC1 * kS / 16) * 4;
+struct P1Stage {
+  unsigned char g[kS * kP1GStride];
+  unsigned char codes[kS * kP1CStride];
+  float r[kP1RFloats];
+  float step_c[kC1 * kS];                                      // fl(cmax_j / 7) of the residual
+};
+static_assert(sizeof(P1Stage) % 16 == 0 && offsetof(P1Stage, codes) % 16 == 0 && offsetof(P1Stage, r) % 16 == 0,
+              "pass 1 stage fields must stay 16-byte aligned");
+constexpr int kP1Smem = 2 * (int)sizeof(P1Stage);
+
+__global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
+  extern __shared__ __align__(16) unsigned char p1smem[];
+  P1Stage* stage = reinterpret_cast<P1Stage*>(p1smem);
   const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
   const GraspProb& P = a.probs[pi];
   const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
@@ -268,77 +304,120 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   const int ti = t >> 2, tj = (t & 3) * 16;
   const int64_t i = bi * kS + ti;
   const bool live = i < rows;
+  const __nv_bfloat16* grad = static_cast<const __nv_bfloat16*>(P.m.grad);
+  const int64_t nch = (P.nbc + kC1 - 1) / kC1;
+
+  // chunk k's copies into stage k & 1 (NB blocks, a compile-time count so
+  // the index arithmetic is shifts and masks): rows past the matrix read as zeros
+  auto issue_nb = [&](auto nb_c, int64_t k) {
+    constexpr int NB = decltype(nb_c)::value;
+    P1Stage& st = stage[k & 1];
+    const int64_t j0 = k * kC1 * kS;
+    // gradient: 64 rows x NB * 8 segments of 16 bytes
+#pragma unroll 1
+    for (int q = 0; q < kS * NB * 8 / kThreads; ++q) {
+      const int e = t + q * kThreads;
+      const int row = e / (NB * 8), seg = e % (NB * 8);
+      const bool ok = bi * kS + row < rows;
+      cp_async16(st.g + row * kP1GStride + seg * 16, grad + (ok ? (bi * kS + row) * cols + j0 + seg * 8 : 0), ok);
+    }
+    // codes: 64 rows x NB * 4 pieces of 8 bytes (the code array is 8-byte aligned)
+#pragma unroll 1
+    for (int q = 0; q < kS * NB * 4 / kThreads; ++q) {
+      const int e = t + q * kThreads;
+      const int row = e / (NB * 4), seg = e % (NB * 4);
+      const bool ok = bi * kS + row < rows;
+      cp_async8(st.codes + row * kP1CStride + seg * 8,
+                P.m.res + (ok ? (bi * kS + row) * (cols / 2) + j0 / 2 + seg * 8 : 0), ok);
+    }
+    // dequantised R rows of the chunk's columns: NB * 64 rows of 8 floats, in halves
+    if (t < NB * kS * 2)
+      cp_async16(&st.r[sidx(t >> 1, (t & 1) * 4)], P.rdeq + (j0 + (t >> 1)) * kRank + (t & 1) * 4, true);
+  };
+  auto issue = [&](int64_t k) {
+    if (P.nbc - k * kC1 >= kC1) issue_nb(std::integral_constant<int, kC1>{}, k);
+    else issue_nb(std::integral_constant<int, 1>{}, k);
+  };
+  static_assert(kC1 == 2 && kS * 4 % kThreads == 0 && kS * 2 * 2 <= kThreads,
+                "pass 1's copy loops assume two-block chunks of 64 x 64 blocks and 256 threads");
+  // chunk k's residual maxima of this thread's row, and of column t (plain loads)
+  float rmax_next[kC1], cmax_next;
+  auto fetch = [&](int64_t k) {
+    const int64_t b0 = k * kC1;
+    const int nb = (P.nbc - b0) < kC1 ? (int)(P.nbc - b0) : kC1;
+#pragma unroll
+    for (int c = 0; c < kC1; ++c) rmax_next[c] = (live && c < nb) ? __ldg(P.m.res_rmax + (b0 + c) * rows + i) : 0.0f;
+    cmax_next = (t < nb * kS) ? __ldg(P.m.res_cmax + bi * cols + b0 * kS + t) : 0.0f;
+  };
+
   float p[kRank];
   if (live) factor_row(P.m.p, P.m.p_rmax, P.m.p_cmax, i, p);
   float y[kRank] = {0, 0, 0, 0, 0, 0, 0, 0}, yc[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int64_t b0 = 0; b0 < P.nbc; b0 += kChunk) {
-    const int nb = (P.nbc - b0) < kChunk ? (int)(P.nbc - b0) : kChunk;
-    // this thread's inputs for the chunk, in flight while the chunk is staged
-    uint2 codes[kChunk];
-    uint4 g0[kChunk], g1[kChunk];
-    float rmax[kChunk];
+  issue(0);
+  cp_async_commit();
+  fetch(0);
+  for (int64_t k = 0; k < nch; ++k) {
+    P1Stage& st = stage[k & 1];
+    const int64_t b0 = k * kC1;
+    const int nb = (P.nbc - b0) < kC1 ? (int)(P.nbc - b0) : kC1;
+    // this chunk's column steps (its stage was last read two chunks ago,
+    // before the barrier that ended that chunk) and row maxima
+    if (t < nb * kS) st.step_c[t] = __fdiv_rn(cmax_next, 7.0f);
+    float rmax[kC1];
+#pragma unroll
+    for (int c = 0; c < kC1; ++c) rmax[c] = rmax_next[c];
+    if (k + 1 < nch) {
+      issue(k + 1);   // into the other stage, free since the last chunk's closing barrier
+      fetch(k + 1);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();   // chunk k's copies of this thread have landed
+    __syncthreads();      // ... and every thread's, with the column steps
     if (live) {
 #pragma unroll
-      for (int c = 0; c < kChunk; ++c) {
+      for (int c = 0; c < kC1; ++c) {
         if (c >= nb) break;
         const int64_t bj = b0 + c;
-        codes[c] = __ldg(reinterpret_cast<const uint2*>(P.m.res + i * (cols / 2) + (bj * kS + tj) / 2));
-        const __nv_bfloat16* grow = static_cast<const __nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
-        g0[c] = *reinterpret_cast<const uint4*>(grow);
-        g1[c] = *reinterpret_cast<const uint4*>(grow + 8);
-        rmax[c] = __ldg(P.m.res_rmax + bj * rows + i);
+        const float step_r = __fdiv_rn(rmax[c], 7.0f);
+        const int cb = c * kS + tj;   // column of the chunk
+        const uint4 g0 = *reinterpret_cast<const uint4*>(st.g + ti * kP1GStride + cb * 2);
+        const uint4 g1 = *reinterpret_cast<const uint4*>(st.g + ti * kP1GStride + cb * 2 + 16);
+        const uint2 cwv = *reinterpret_cast<const uint2*>(st.codes + ti * kP1CStride + cb / 2);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const uint32_t cw[2] = {cwv.x, cwv.y};
+        uint32_t out[8];
+        float yb[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
+          const float res = __fmul_rn((float)nib, fminf(step_r, st.step_c[cb + e]));
+          float rr[kRank];
+          *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e, 0)]);
+          *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e, 4)]);
+          float acc = 0.0f;
+#pragma unroll
+          for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], rr[l]));
+          const float mprev = __fadd_rn(res, acc);
+          const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
+          const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
+          const __nv_bfloat16 mb = __float2bfloat16_rn(m);
+          const float mv = __bfloat162float(mb);
+          if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
+          else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
+#pragma unroll
+          for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, rr[l], yb[l]);
+        }
+#pragma unroll
+        for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
+        // M_t over the gradient (this chunk's gradient is already in shared memory)
+        __nv_bfloat16* grow = static_cast<__nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
+        *reinterpret_cast<uint4*>(grow) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(grow + 8) = make_uint4(out[4], out[5], out[6], out[7]);
       }
     }
-    __syncthreads();   // the previous chunk's shared data is no longer read
-    {
-      const int64_t j0 = b0 * kS;
-      const int ncol = nb * kS;
-      // half a row of R (a float4) per thread per pass
-      for (int e = t; e < ncol * kRank / 4; e += kThreads) {
-        const int col = e >> 1, h = (e & 1) * 4;
-        *reinterpret_cast<float4*>(&sR[sidx(col, h)]) = __ldg(reinterpret_cast<const float4*>(P.rdeq + j0 * kRank) + e);
-      }
-      if (t < ncol) sStepC[t] = __fdiv_rn(__ldg(P.m.res_cmax + bi * cols + j0 + t), 7.0f);
-    }
-    __syncthreads();
-    if (!live) continue;
-#pragma unroll
-    for (int c = 0; c < kChunk; ++c) {
-      if (c >= nb) break;
-      const int64_t bj = b0 + c;
-      const float step_r = __fdiv_rn(rmax[c], 7.0f);
-      const uint32_t gw[8] = {g0[c].x, g0[c].y, g0[c].z, g0[c].w, g1[c].x, g1[c].y, g1[c].z, g1[c].w};
-      const uint32_t cw[2] = {codes[c].x, codes[c].y};
-      const int cb = c * kS + tj;   // column of the chunk
-      uint32_t out[8];
-      float yb[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
-        const float res = __fmul_rn((float)nib, fminf(step_r, sStepC[cb + e]));
-        float rr[kRank];
-        *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&sR[sidx(cb + e, 0)]);
-        *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&sR[sidx(cb + e, 4)]);
-        float acc = 0.0f;
-#pragma unroll
-        for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], rr[l]));
-        const float mprev = __fadd_rn(res, acc);
-        const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
-        const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
-        const __nv_bfloat16 mb = __float2bfloat16_rn(m);
-        const float mv = __bfloat162float(mb);
-        if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
-        else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
-#pragma unroll
-        for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, rr[l], yb[l]);
-      }
-#pragma unroll
-      for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
-      __nv_bfloat16* grow = static_cast<__nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
-      *reinterpret_cast<uint4*>(grow) = make_uint4(out[0], out[1], out[2], out[3]);
-      *reinterpret_cast<uint4*>(grow + 8) = make_uint4(out[4], out[5], out[6], out[7]);
-    }
+    __syncthreads();   // stage k & 1 is refilled by chunk k + 2's copies
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int l = 0; l < kRank; ++l) y[l] += yc[l];
   // the 4 threads of a row add their sums of M_t R_{t-1} (fixed order); the
@@ -501,13 +580,6 @@ constexpr int kP2Stages = 4;
 constexpr int kP2StageBytes = kP2Rows * kS * 2 + kP2Rows * kRank * 4;   // M_t chunk + P rows
 constexpr int kP2Smem = kP2Stages * kP2StageBytes + (kThreads / 32) * kS * kRank * 4;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const WsHeader* hdr) {
   extern __shared__ __align__(16) unsigned char p2smem[];
@@ -835,10 +907,12 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     const int64_t tiles = ts[n];
     if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
     // the opt-in belongs to the current device, so it is made on every call
-    const cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
+    cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(grasp_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize, kP1Smem);
     if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
     grasp_colnorm<<<n, kThreads, 0, s>>>(a);
-    grasp_pass1<<<(unsigned)rs[n], kThreads, 0, s>>>(a);
+    grasp_pass1<<<(unsigned)rs[n], kThreads, kP1Smem, s>>>(a);
     grasp_chol<<<n, 64, 0, s>>>(a, hdr);
     grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
     grasp_chol<<<n, 64, 0, s>>>(a, hdr);
