@@ -677,23 +677,35 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const Ws
 }
 
 // ---------------------------------------------------------------------------
-// pass 3: residual M_t - P_t R_t^T and its 4-bit grid codes, one CTA per
-// 64-row x 256-column chunk (four 64 x 64 blocks).  Thread t owns rows
-// 2 (t / 8), 2 (t / 8) + 1 of the chunk and the 8 consecutive columns 8 (t % 8)
-// of each block, so each column's R row read from shared memory serves two
-// rows.  Per block: the row maxima by shuffles over the row's 8 threads, the
-// column maxima by a shuffle over the 4 row pairs a warp holds and then the 8
-// warps' values in shared memory.
+// pass 3: residual M_t - P_t R_t^T and its 4-bit grid codes, one CTA of 128
+// threads per 64-row x 256-column chunk (four 64 x 64 blocks).  The chunk's
+// M_t values come into shared memory by asynchronous copies when the CTA
+// starts, one commit group per block.  Thread t owns rows 4 (t / 8) ...
+// 4 (t / 8) + 3 of the chunk and the 8 consecutive columns 8 (t % 8) of each
+// block, so each column's R row read from shared memory serves four rows.
+// Per block: the row maxima by shuffles over the row's 8 threads, the column
+// maxima by a shuffle over the 4 row quads a warp holds and then the 4 warps'
+// values in shared memory.
 // ---------------------------------------------------------------------------
 // Shared rows of 8 floats for the chunk's 256 columns, padded so that the
 // eight columns a warp reads at once (8 apart) fall in different banks.
 constexpr int kPadStride8 = kChunk * kS * kRank + (kChunk * kS / 8) * 4;
 __device__ __forceinline__ int sidx8(int col, int l) { return col * kRank + (col >> 3) * 4 + l; }
 
-__global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
-  __shared__ __align__(16) float sR[kPadStride8];
-  __shared__ float wmax[kThreads / 32][kS];
-  __shared__ float sInvC[kS];
+constexpr int kP3Threads = 128;
+constexpr int kP3Warps = kP3Threads / 32;
+struct P3Smem {
+  unsigned char m[kChunk][kS][kS * 2];   // the chunk's M_t (bf16), block by block
+  float r[kPadStride8];                  // R_t rows of the chunk's columns
+  float wmax[kP3Warps][kS];              // per-warp column maxima of a block
+  float inv_c[kS];                       // fl(7 / cmax_j)
+};
+static_assert(offsetof(P3Smem, r) % 16 == 0, "pass 3 shared fields must stay 16-byte aligned");
+constexpr int kP3Smem = (int)sizeof(P3Smem);
+
+__global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
+  extern __shared__ __align__(16) unsigned char p3smem[];
+  P3Smem& S = *reinterpret_cast<P3Smem*>(p3smem);
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
   const int pi = find_prob(a.tile_start, a.n, blockIdx.x);
   const GraspProb& P = a.probs[pi];
@@ -703,86 +715,105 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const Ws
   const int nb = (P.nbc - b0) < kChunk ? (int)(P.nbc - b0) : kChunk;
   const int64_t rows = P.m.rows, cols = P.m.cols;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int rp = t >> 3, cg = t & 7;
-  const int64_t i0 = bi * kS + 2 * rp;
-  const bool live[2] = {i0 < rows, i0 + 1 < rows};
-  // the chunk's M_t values of this thread, in flight while R is staged
-  uint4 gv[kChunk][2];
+  const int rq = t >> 3, cg = t & 7;
+  const int64_t i0 = bi * kS + 4 * rq;
+  bool live[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) live[h] = i0 + h < rows;
+  const __nv_bfloat16* grad = static_cast<const __nv_bfloat16*>(P.m.grad);
+  // the chunk's M_t: block c is commit group c (64 rows x 8 segments of 16
+  // bytes, 4 per thread); rows past the matrix read as zeros
 #pragma unroll
   for (int c = 0; c < kChunk; ++c) {
-    if (c >= nb) break;
+    if (c < nb) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      if (live[h])
-        gv[c][h] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.m.grad) + (i0 + h) * cols +
-                                                   (b0 + c) * kS + 8 * cg);
+      for (int q = 0; q < kS * 8 / kP3Threads; ++q) {
+        const int e = t + q * kP3Threads;
+        const int row = e >> 3, seg = e & 7;
+        const bool ok = bi * kS + row < rows;
+        cp_async16(&S.m[c][row][seg * 16], grad + (ok ? (bi * kS + row) * cols + (b0 + c) * kS + seg * 8 : 0), ok);
+      }
+    }
+    cp_async_commit();
   }
-  for (int e = t; e < nb * kS * kRank / 4; e += kThreads)
-    *reinterpret_cast<float4*>(&sR[sidx8(e >> 1, (e & 1) * 4)]) =
+  for (int e = t; e < nb * kS * kRank / 4; e += kP3Threads)
+    *reinterpret_cast<float4*>(&S.r[sidx8(e >> 1, (e & 1) * 4)]) =
         __ldg(reinterpret_cast<const float4*>(P.r + b0 * kS * kRank) + e);
-  float p[2][kRank];
+  float p[4][kRank];
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
+  for (int h = 0; h < 4; ++h)
 #pragma unroll
     for (int l = 0; l < kRank; ++l) p[h][l] = live[h] ? P.p[(i0 + h) * kRank + l] : 0.0f;
-  __syncthreads();
 #pragma unroll
   for (int c = 0; c < kChunk; ++c) {
     if (c >= nb) break;
     const int64_t bj = b0 + c;
-    float res[2][8];
-    float rm[2] = {0.0f, 0.0f};
+    // block c's copies (commit groups 0..c) have landed, for every thread
+    if (c == 0) cp_async_wait<kChunk - 1>();
+    else if (c == 1) cp_async_wait<kChunk - 2>();
+    else if (c == 2) cp_async_wait<kChunk - 3>();
+    else cp_async_wait<0>();
+    __syncthreads();
+    float res[4][8];
+    float rm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     float cmx[8];
+    uint4 mw[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) mw[h] = *reinterpret_cast<const uint4*>(&S.m[c][4 * rq + h][cg * 16]);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int cb = c * kS + 8 * cg + k;
       float rr[kRank];
-      *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 0)]);
-      *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&sR[sidx8(cb, 4)]);
+      *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&S.r[sidx8(cb, 0)]);
+      *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&S.r[sidx8(cb, 4)]);
       cmx[k] = 0.0f;
-      // both rows' dot products P_i . R_j at once, each in the order of fmaf's chain
-      float2 acc2 = make_float2(0.0f, 0.0f);
+      // the rows' dot products P_i . R_j, row pairs at once, each in the order of fmaf's chain
+      float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int l = 0; l < kRank; ++l) acc2 = fma2(make_float2(p[0][l], p[1][l]), make_float2(rr[l], rr[l]), acc2);
+      for (int l = 0; l < kRank; ++l) {
+        a01 = fma2(make_float2(p[0][l], p[1][l]), make_float2(rr[l], rr[l]), a01);
+        a23 = fma2(make_float2(p[2][l], p[3][l]), make_float2(rr[l], rr[l]), a23);
+      }
+      const float acc[4] = {a01.x, a01.y, a23.x, a23.y};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 4; ++h) {
         float v = 0.0f;
         if (live[h]) {
-          const uint32_t w = (k >> 1) == 0 ? gv[c][h].x : (k >> 1) == 1 ? gv[c][h].y : (k >> 1) == 2 ? gv[c][h].z : gv[c][h].w;
+          const uint32_t w = (k >> 1) == 0 ? mw[h].x : (k >> 1) == 1 ? mw[h].y : (k >> 1) == 2 ? mw[h].z : mw[h].w;
           const float m = __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
-          v = m - (h == 0 ? acc2.x : acc2.y);
+          v = m - acc[h];
         }
         res[h][k] = v;
         rm[h] = fmaxf(rm[h], fabsf(v));
         cmx[k] = fmaxf(cmx[k], fabsf(v));
       }
     }
-    // row maxima over the block's 64 columns (the 8 threads of a row pair)
+    // row maxima over the block's 64 columns (the 8 threads of a row quad)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < 4; ++h) {
       rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 1));
       rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 2));
       rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 4));
     }
-    // column maxima: lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same columns of the warp's 8 rows
+    // column maxima: lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same columns of the warp's 16 rows
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       float v = cmx[k];
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      if (lane < 8) wmax[warp][8 * cg + k] = v;
+      if (lane < 8) S.wmax[warp][8 * cg + k] = v;
     }
     __syncthreads();
     if (t < kS) {
       float cm = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) cm = fmaxf(cm, wmax[w][t]);
+      for (int w = 0; w < kP3Warps; ++w) cm = fmaxf(cm, S.wmax[w][t]);
       P.m.res_cmax[bi * cols + bj * kS + t] = cm;
-      sInvC[t] = inv_level(cm, 7.0f);
+      S.inv_c[t] = inv_level(cm, 7.0f);
     }
     __syncthreads();
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < 4; ++h) {
       if (!live[h]) continue;
       const int64_t i = i0 + h;
       if (cg == 0) P.m.res_rmax[bj * rows + i] = rm[h];
@@ -790,13 +821,14 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass3(GraspArgs a, const Ws
       uint32_t cw = 0u;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int q = grid_code(res[h][k], grid_factor(ir, sInvC[8 * cg + k]), 7);
+        const int q = grid_code(res[h][k], grid_factor(ir, S.inv_c[8 * cg + k]), 7);
         cw |= (uint32_t)(q + 8) << (4 * k);
       }
       *reinterpret_cast<uint32_t*>(P.m.res + i * (cols / 2) + (bj * kS + 8 * cg) / 2) = cw;
     }
-    __syncthreads();   // wmax and sInvC are rewritten by the next block
+    __syncthreads();   // wmax and inv_c are rewritten by the next block
   }
+  cp_async_wait<0>();
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -910,6 +942,8 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     cudaError_t attr = cudaFuncSetAttribute(grasp_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(grasp_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize, kP1Smem);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(grasp_pass3, cudaFuncAttributeMaxDynamicSharedMemorySize, kP3Smem);
     if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
     grasp_colnorm<<<n, kThreads, 0, s>>>(a);
     grasp_pass1<<<(unsigned)rs[n], kThreads, kP1Smem, s>>>(a);
@@ -918,7 +952,7 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     grasp_chol<<<n, 64, 0, s>>>(a, hdr);
     grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
     grasp_pass2<<<(unsigned)cs[n], kThreads, kP2Smem, s>>>(a, hdr);
-    grasp_pass3<<<(unsigned)tiles, kThreads, 0, s>>>(a, hdr);
+    grasp_pass3<<<(unsigned)tiles, kP3Threads, kP3Smem, s>>>(a, hdr);
     e = cudaGetLastError();
     // the pageable host tables are staged by the copies above before they return
     if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
