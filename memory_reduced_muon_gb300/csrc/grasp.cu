@@ -387,25 +387,39 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
         const uint32_t cw[2] = {cwv.x, cwv.y};
         uint32_t out[8];
         float yb[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+        // four elements at a time with the rank loop outside, so that four
+        // independent reconstruction chains interleave; every sum keeps its
+        // order (each element's over l, each Y sum's over the elements)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
-          const float res = __fmul_rn((float)nib, fminf(step_r, st.step_c[cb + e]));
-          float rr[kRank];
-          *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e, 0)]);
-          *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e, 4)]);
-          float acc = 0.0f;
+        for (int e0 = 0; e0 < 16; e0 += 4) {
+          float rr[4][kRank], acc[4], mv[4];
 #pragma unroll
-          for (int l = 0; l < kRank; ++l) acc = __fadd_rn(acc, __fmul_rn(p[l], rr[l]));
-          const float mprev = __fadd_rn(res, acc);
-          const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
-          const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
-          const __nv_bfloat16 mb = __float2bfloat16_rn(m);
-          const float mv = __bfloat162float(mb);
-          if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
-          else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
+          for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<float4*>(rr[j]) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 0)]);
+            *reinterpret_cast<float4*>(rr[j] + 4) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 4)]);
+            acc[j] = 0.0f;
+          }
 #pragma unroll
-          for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv, rr[l], yb[l]);
+          for (int l = 0; l < kRank; ++l)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(p[l], rr[j][l]));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = e0 + j;
+            const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
+            const float res = __fmul_rn((float)nib, fminf(step_r, st.step_c[cb + e]));
+            const float mprev = __fadd_rn(res, acc[j]);
+            const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
+            const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
+            const __nv_bfloat16 mb = __float2bfloat16_rn(m);
+            mv[j] = __bfloat162float(mb);
+            if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
+            else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv[j], rr[j][l], yb[l]);
         }
 #pragma unroll
         for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
