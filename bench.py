@@ -151,6 +151,37 @@ class ClockSampler:
 
 
 E2E_MIN_STEPS = 60   # host-fed steps timed by the end-to-end leg of the MuonBP workload
+# gradient batches in flight in that leg: step k's copies start once step
+# k - E2E_DEPTH has finished with its buffers.  Three measured slower than two
+# on boxes whose host copies slow down (a larger page-locked footprint)
+E2E_DEPTH = 2
+
+
+_HOST_MAPS = []   # keeps the huge-page mappings of pinned_host_bf16 alive
+
+
+def pinned_host_bf16(n: int) -> torch.Tensor:
+    """A page-locked host bf16 buffer of n elements for the end-to-end leg,
+    backed by transparent huge pages where the host allows it (anonymous
+    mapping advised MADV_HUGEPAGE, then registered with cudaHostRegister):
+    on boxes whose host-to-device copies slow down, that leg measured about
+    7% faster than with torch's own page-locked allocation.  Falls back to
+    torch's allocation if any step fails."""
+    import mmap
+    try:
+        mm = mmap.mmap(-1, 2 * n, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        mm.madvise(mmap.MADV_HUGEPAGE)
+        arr = np.frombuffer(mm, dtype=np.uint16)
+        arr[:] = 0   # touch: the pages exist before they are registered
+        buf = torch.from_numpy(arr).view(torch.bfloat16)
+        r = torch.cuda.cudart().cudaHostRegister(buf.data_ptr(), 2 * n, 0)
+        status = int(r[0] if isinstance(r, tuple) else r)
+        if status == 0 and buf.is_pinned():
+            _HOST_MAPS.append(mm)
+            return buf
+    except Exception:
+        pass
+    return torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
 
 
 def audit_per_step(q, before, steps):
@@ -626,9 +657,9 @@ def run_gpu(args, world, rank, local):
     # pinned host copies of two gradient batches for the end-to-end leg, taken
     # before any step overwrites them
     host_pool = []
-    for b in range(2):   # one page-locked buffer per batch, a view per matrix
+    for b in range(E2E_DEPTH):   # one page-locked buffer per batch, a view per matrix
         src = batches[b % n_batches]
-        buf = torch.empty(sum(g.numel() for g in src), dtype=torch.bfloat16, pin_memory=True)
+        buf = pinned_host_bf16(sum(g.numel() for g in src))
         views, o = [], 0
         for g in src:
             v = buf[o:o + g.numel()].view(g.shape)
@@ -763,9 +794,9 @@ def run_gpu(args, world, rank, local):
 
     # e2e through the host-fed entry: every step copies its gradients in from
     # page-locked host memory and reads its group sums (the step's metric)
-    # back to host memory.  Two plans over the same state and weights
-    # alternate, so step k+1's copies (on a copy stream) overlap step k's
-    # kernels; the clock stops once the last read-back has landed.
+    # back to host memory.  E2E_DEPTH plans over the same state and weights
+    # take turns, so a step's copies (on a copy stream) overlap the kernels of
+    # the steps before it; the clock stops once the last read-back has landed.
     torch.cuda.synchronize()
     # at least 60 steps (about a second): a host-to-device stall of the box
     # (two copies at 12-19 GB/s, seen on some boxes and not on others) then
@@ -780,19 +811,20 @@ def run_gpu(args, world, rank, local):
     # run slower (about 30 ms instead of 18 in a probe of ten and ten)
     for k in range(max(10, args.warmup)):
         t += 1
-        q.qmuon_step_from_host(plans[(k % 2) % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights,
-                               w.coeffs, w.iters, host_pool[k % 2], sums_host[0], sums, ws, stream=stream,
+        q.qmuon_step_from_host(plans[(k % E2E_DEPTH) % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights,
+                               w.coeffs, w.iters, host_pool[k % E2E_DEPTH], sums_host[0], sums, ws, stream=stream,
                                copy_stream=copy_stream)
     torch.cuda.synchronize()
-    # the host runs at most two steps ahead of the GPU, as a training loop would
+    # the host runs at most E2E_DEPTH steps ahead of the GPU, as a training
+    # loop that prefetches its batches would
     done = [torch.cuda.Event() for _ in range(e2e_steps)]
     barrier(world)
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         t += 1
-        b = k % 2
-        if k >= 2:
-            done[k - 2].synchronize()
+        b = k % E2E_DEPTH
+        if k >= E2E_DEPTH:
+            done[k - E2E_DEPTH].synchronize()
         q.qmuon_step_from_host(plans[b % n_batches], t, w.P, w.beta, w.eta_full, w.eta_block, weights, w.coeffs,
                                w.iters, host_pool[b], sums_host[k], sums, ws, stream=stream, copy_stream=copy_stream)
         done[k].record(stream)
