@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kUpdThreadsAll, 3) update_kernel(UpdLaunch L) 
     int i = 0;
     for (; i < n_stages; ++i) {
       const int slot = i % kUpdStages;
-      // lane 0 waits for the slot, the warp follows its verdict
+      // lane 0 waits for the slot, the warp follows its decision
       if (lane == 0 && i >= kUpdStages) ok = upd_wait(empty0 + 8 * slot, ((i / kUpdStages) - 1) & 1, L.header, 0x1100u);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
