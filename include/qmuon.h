@@ -323,7 +323,14 @@ QMUON_API qmuon_status qmuon_newton_schulz_batched(const qmuon_ns_problem* probl
  *   t          1-based step index
  *   weights    H  n_tensors device pointers (D) to fp32 rows x cols master
  *                 weights, updated in place
- *   group_sumsq D [n groups of this step] fp32 sums of m*m, or NULL */
+ *   group_sumsq D [n groups of this step] fp32 sums of m*m, or NULL
+ * Once qmuon_step_prepare has built the plan's tables for these weights and
+ * this workspace (and one step has run in the process), a step is a
+ * workspace memset and kernel launches on `stream`, so it can be captured
+ * into a CUDA graph.  The step index is fixed in the captured launches: a
+ * captured period of P steps (t = 1 .. P) replays as any later period, with
+ * nearest requantisation (stochastic requantisation would replay the same
+ * random numbers). */
 QMUON_API qmuon_status qmuon_step(const qmuon_plan* plan, int64_t t, int32_t P, float beta,
                         float eta_full, float eta_block, float* const* weights,
                         const float coeffs[3], int32_t iters, float* group_sumsq, void* ws,

@@ -33,6 +33,8 @@
 #include <cstddef>
 #include <cstdio>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "qm_internal.h"
 
@@ -747,8 +749,24 @@ void* pick_kernel(qmuon_q8_kind q8, qmuon_dtype dt, bool carrier, bool sr = fals
 size_t upd_smem(qmuon_dtype dt) { return dt == QMUON_FP32 ? upd_smem_bytes<QMUON_FP32>() : upd_smem_bytes<QMUON_BF16>(); }
 
 // Dynamic shared memory above the 48 KB default needs an opt-in per kernel.
+// The shared-memory opt-in belongs to a (kernel, device) pair: it is set once
+// per pair, so that a step's launches make no other CUDA call (a step can be
+// captured into a CUDA graph).
 cudaError_t prepare_kernel(void* k, qmuon_dtype dt) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem(dt));
+  static std::mutex mu;
+  static std::set<std::pair<void*, int>> done;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({k, dev})) return cudaSuccess;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)upd_smem(dt));
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    done.insert({k, dev});
+  }
+  return e;
 }
 
 }  // namespace
