@@ -2,7 +2,9 @@
 groups sum to 0, so the inverse norm is 1 / (0 + 1e-7)), a plan of only
 empty tensors (rejected: a plan holds at least one block), and a tensor of more than 2^31 elements, whose blocks around
 element 2^31 and at its end are checked bit-exact against the oracle (64-bit
-element and block indexing)."""
+element and block indexing).  Failure reporting: a status recorded in a
+workspace header (injected from the host) comes back from qmuon_sync_status
+with its site, and is cleared by the read."""
 
 import numpy as np
 import pytest
@@ -108,3 +110,25 @@ def test_tensor_past_2_pow_31_elements():
         assert a[b].item() == r.absmax[0]
         np.testing.assert_array_equal(to_oracle_grad(g[b * 256:(b + 1) * 256], "bf16"), r.grad, err_msg=str(b))
     assert np.isfinite(sums.item()) and sums.item() > 0
+
+
+@pytest.mark.parametrize("status,site", [(q.QMUON_ERR_TIMEOUT, 0x1300), (q.QMUON_ERR_INVALID_ARGUMENT, 0x2003)])
+def test_sync_status_reports_and_clears_a_recorded_failure(status, site):
+    # a kernel records a failure as (status, site) in the workspace header's
+    # first two words; injected from the host here, with no kernel made to fail
+    ts = _tensors([(64, 256)], 40)
+    plan = q.qmuon_plan_create([(qs, a, g, m.rows, m.cols) for m, qs, a, g in ts], "int8", "bf16")
+    ws = torch.zeros(q.qmuon_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    q.qmuon_sync_status(ws)   # a clean header
+    ws[:8].view(torch.int32).copy_(torch.tensor([status, site], dtype=torch.int32))
+    with pytest.raises(q.QmuonError) as e:
+        q.qmuon_sync_status(ws)
+    assert e.value.status == status
+    assert f"0x{site:x}" in q.qmuon_last_error()
+    assert ws[:8].view(torch.int32).cpu().tolist() == [0, 0]   # cleared by the read
+    q.qmuon_sync_status(ws)
+    # the next call on the workspace starts from a clean header and succeeds
+    inv = torch.zeros(1, device="cuda")
+    ws[:8].view(torch.int32).copy_(torch.tensor([status, site], dtype=torch.int32))
+    q.qmuon_update_multi_normalize_groups(plan, 0.9, 2, None, inv, ws)
+    q.qmuon_sync_status(ws)
