@@ -59,8 +59,13 @@ struct GraspProb {
 struct GraspArgs {
   const GraspProb* probs;
   const int64_t* tile_start;  // [n + 1] prefix of pass 3's chunks (64 rows x 4 column blocks)
-  const int64_t* rstrip_start;  // [n + 1] prefix of 64-row strips
-  const int64_t* cstrip_start;  // [n + 1] prefix of 64-column strips
+  const int64_t* rstrip_start;  // [n + 1] prefix of 64-row strips, problems in rorder
+  const int64_t* cstrip_start;  // [n + 1] prefix of 64-column strips, problems in corder
+  // The order in which the grid deals each kind of strip: longest first (a
+  // row strip's length is its matrix's column count, a column strip's its row
+  // count), so that the longest strips do not start last and run alone
+  const int32_t* rorder;        // [n] problem at each position of the row-strip order
+  const int32_t* corder;        // [n] problem at each position of the column-strip order
   int32_t n;
   float mu;
 };
@@ -296,9 +301,9 @@ constexpr int kP1Smem = 2 * (int)sizeof(P1Stage);
 __global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
   extern __shared__ __align__(16) unsigned char p1smem[];
   P1Stage* stage = reinterpret_cast<P1Stage*>(p1smem);
-  const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
-  const GraspProb& P = a.probs[pi];
-  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
+  const int pk = find_prob(a.rstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[__ldg(a.rorder + pk)];
+  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pk);
   const int64_t rows = P.m.rows, cols = P.m.cols;
   const int t = threadIdx.x;
   const int ti = t >> 2, tj = (t & 3) * 16;
@@ -525,9 +530,9 @@ __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* 
   __shared__ double sZZ[36][kS + 1];      // PASS 0: each row's products z_u z_v
   __shared__ float sx[kS][kRank];
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
-  const int pi = find_prob(a.rstrip_start, a.n, blockIdx.x);
-  const GraspProb& P = a.probs[pi];
-  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pi);
+  const int pk = find_prob(a.rstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[__ldg(a.rorder + pk)];
+  const int64_t bi = blockIdx.x - __ldg(a.rstrip_start + pk);
   const int64_t rows = P.m.rows;
   sL[threadIdx.x >> 3][threadIdx.x & 7] = P.L[threadIdx.x];
   if (threadIdx.x < kRank) sInvD[threadIdx.x] = 1.0 / P.L[threadIdx.x * (kRank + 1)];
@@ -599,9 +604,9 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const Ws
   extern __shared__ __align__(16) unsigned char p2smem[];
   float (*part)[kS][kRank] = reinterpret_cast<float (*)[kS][kRank]>(p2smem + kP2Stages * kP2StageBytes);
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
-  const int pi = find_prob(a.cstrip_start, a.n, blockIdx.x);
-  const GraspProb& P = a.probs[pi];
-  const int64_t bj = blockIdx.x - __ldg(a.cstrip_start + pi);
+  const int pk = find_prob(a.cstrip_start, a.n, blockIdx.x);
+  const GraspProb& P = a.probs[__ldg(a.corder + pk)];
+  const int64_t bj = blockIdx.x - __ldg(a.cstrip_start + pk);
   const int64_t rows = P.m.rows, cols = P.m.cols;
   const int t = threadIdx.x;
   const int cp = t & 31, rg = t >> 5;   // column pair, row group (one per warp: P reads broadcast)
@@ -855,7 +860,8 @@ size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
 }
 
 size_t table_bytes(int32_t n) {
-  return align_up((size_t)n * sizeof(GraspProb), 256) + 3 * align_up((size_t)(n + 1) * 8, 256);
+  return align_up((size_t)n * sizeof(GraspProb), 256) + 3 * align_up((size_t)(n + 1) * 8, 256) +
+         2 * align_up((size_t)n * 4, 256);
 }
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -927,9 +933,16 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
       P.p1 = reinterpret_cast<double*>(carve((size_t)P.m.rows * kRank * 8));
       P.gpart = reinterpret_cast<double*>(carve((size_t)P.nbr * 36 * 8));
       P.L = reinterpret_cast<double*>(carve(kRank * kRank * 8));
-      ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks
-      rs[i + 1] = rs[i] + P.nbr;
-      cs[i + 1] = cs[i] + P.nbc;
+      ts[i + 1] = ts[i] + P.nbr * ((P.nbc + kChunk - 1) / kChunk);   // pass 3: 64 x 256 chunks (all alike)
+    }
+    // row strips longest (most columns) first, column strips longest (most rows) first
+    std::vector<int32_t> ro(n), co(n);
+    for (int32_t i = 0; i < n; ++i) ro[i] = co[i] = i;
+    std::stable_sort(ro.begin(), ro.end(), [&](int32_t x, int32_t y) { return hp[x].m.cols > hp[y].m.cols; });
+    std::stable_sort(co.begin(), co.end(), [&](int32_t x, int32_t y) { return hp[x].m.rows > hp[y].m.rows; });
+    for (int32_t k = 0; k < n; ++k) {
+      rs[k + 1] = rs[k] + hp[ro[k]].nbr;
+      cs[k + 1] = cs[k] + hp[co[k]].nbc;
     }
     GraspArgs a{};
     a.probs = reinterpret_cast<const GraspProb*>(table);
@@ -937,6 +950,9 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     a.tile_start = reinterpret_cast<const int64_t*>(pre);
     a.rstrip_start = reinterpret_cast<const int64_t*>(pre + align_up((size_t)(n + 1) * 8, 256));
     a.cstrip_start = reinterpret_cast<const int64_t*>(pre + 2 * align_up((size_t)(n + 1) * 8, 256));
+    a.rorder = reinterpret_cast<const int32_t*>(pre + 3 * align_up((size_t)(n + 1) * 8, 256));
+    a.corder = reinterpret_cast<const int32_t*>(pre + 3 * align_up((size_t)(n + 1) * 8, 256) +
+                                                align_up((size_t)n * 4, 256));
     a.n = n;
     a.mu = mu;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -949,6 +965,10 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
       e = cudaMemcpyAsync(const_cast<int64_t*>(a.rstrip_start), rs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(const_cast<int64_t*>(a.cstrip_start), cs.data(), (size_t)(n + 1) * 8, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int32_t*>(a.rorder), ro.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int32_t*>(a.corder), co.data(), (size_t)n * 4, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return set_error("qmuon_grasp_step (upload)", e);
     const int64_t tiles = ts[n];
     if (tiles > (int64_t)0x7FFFFFFF) return QMUON_ERR_UNSUPPORTED;
