@@ -774,7 +774,6 @@ __global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const 
     else cp_async_wait<0>();
     __syncthreads();
     float res[4][8];
-    float rm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     float cmx[8];
     uint4 mw[4];
 #pragma unroll
@@ -785,7 +784,6 @@ __global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const 
       float rr[kRank];
       *reinterpret_cast<float4*>(rr) = *reinterpret_cast<const float4*>(&S.r[sidx8(cb, 0)]);
       *reinterpret_cast<float4*>(rr + 4) = *reinterpret_cast<const float4*>(&S.r[sidx8(cb, 4)]);
-      cmx[k] = 0.0f;
       // the rows' dot products P_i . R_j, row pairs at once, each in the order of fmaf's chain
       float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -803,17 +801,33 @@ __global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const 
           v = m - acc[h];
         }
         res[h][k] = v;
-        rm[h] = fmaxf(rm[h], fabsf(v));
-        cmx[k] = fmaxf(cmx[k], fabsf(v));
       }
+      // fmaxf skips a NaN; a set of NaNs alone gives NaN, which the maxima
+      // against zero further down drop, as a running maximum from zero would
+      cmx[k] = fmaxf(fmaxf(fabsf(res[0][k]), fabsf(res[1][k])), fmaxf(fabsf(res[2][k]), fabsf(res[3][k])));
     }
-    // row maxima over the block's 64 columns (the 8 threads of a row quad)
+    // row maxima over the block's 64 columns, reduced and scattered over the
+    // 8 threads of a row quad: after the exchanges across lanes 4, 2 and 1
+    // apart, thread cg holds the maximum of row hr = 2 (cg >> 2 & 1) + (cg >> 1 & 1)
+    float rmh[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 1));
-      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 2));
-      rm[h] = fmaxf(rm[h], __shfl_xor_sync(0xffffffffu, rm[h], 4));
-    }
+    for (int h = 0; h < 4; ++h)
+      rmh[h] = fmaxf(fmaxf(fmaxf(fabsf(res[h][0]), fabsf(res[h][1])), fmaxf(fabsf(res[h][2]), fabsf(res[h][3]))),
+                     fmaxf(fmaxf(fabsf(res[h][4]), fabsf(res[h][5])), fmaxf(fabsf(res[h][6]), fabsf(res[h][7]))));
+    const bool hi2 = (cg & 4) != 0, hi1 = (cg & 2) != 0;
+    float k0 = hi2 ? rmh[2] : rmh[0], k1 = hi2 ? rmh[3] : rmh[1];
+    k0 = fmaxf(k0, __shfl_xor_sync(0xffffffffu, hi2 ? rmh[0] : rmh[2], 4));
+    k1 = fmaxf(k1, __shfl_xor_sync(0xffffffffu, hi2 ? rmh[1] : rmh[3], 4));
+    float rk = hi1 ? k1 : k0;
+    rk = fmaxf(rk, __shfl_xor_sync(0xffffffffu, hi1 ? k0 : k1, 2));
+    rk = fmaxf(rk, __shfl_xor_sync(0xffffffffu, rk, 1));
+    rk = fmaxf(rk, 0.0f);
+    const int hr = (hi2 ? 2 : 0) + (hi1 ? 1 : 0);
+    if ((cg & 1) == 0 && i0 + hr < rows) P.m.res_rmax[bj * rows + i0 + hr] = rk;
+    const float irr = inv_level(rk, 7.0f);
+    float ir[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) ir[h] = __shfl_sync(0xffffffffu, irr, (h >> 1) * 4 + (h & 1) * 2, 8);
     // column maxima: lanes l, l ^ 8, l ^ 16, l ^ 24 hold the same columns of the warp's 16 rows
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -823,25 +837,42 @@ __global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const 
       if (lane < 8) S.wmax[warp][8 * cg + k] = v;
     }
     __syncthreads();
+    int inf_c = 0;
     if (t < kS) {
       float cm = 0.0f;
 #pragma unroll
       for (int w = 0; w < kP3Warps; ++w) cm = fmaxf(cm, S.wmax[w][t]);
       P.m.res_cmax[bi * cols + bj * kS + t] = cm;
-      S.inv_c[t] = inv_level(cm, 7.0f);
+      const float icm = inv_level(cm, 7.0f);
+      S.inv_c[t] = icm;
+      inf_c = icm == INFINITY;
     }
-    __syncthreads();
+    const bool any_inf_c = __syncthreads_or(inf_c) != 0;
+    float ic[8];
+    *reinterpret_cast<float4*>(ic) = *reinterpret_cast<const float4*>(&S.inv_c[8 * cg]);
+    *reinterpret_cast<float4*>(ic + 4) = *reinterpret_cast<const float4*>(&S.inv_c[8 * cg + 4]);
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       if (!live[h]) continue;
       const int64_t i = i0 + h;
-      if (cg == 0) P.m.res_rmax[bj * rows + i] = rm[h];
-      const float ir = inv_level(rm[h], 7.0f);
-      uint32_t cw = 0u;
+      uint32_t cw;
+      if (!any_inf_c && ir[h] != INFINITY) {
+        // Every factor fl(7 / min(r, c)) is finite and |x| <= min(r, c), so
+        // fl(x * factor) <= 7 (1 + 2^-24) in magnitude: each code is already in
+        // [-7, 7] (a NaN converts to 0), and the codes are packed by a
+        // multiply-add chain modulo 2^32, offset by 8 per nibble at the end.
+        uint32_t acc = 0u;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int q = grid_code(res[h][k], grid_factor(ir, S.inv_c[8 * cg + k]), 7);
-        cw |= (uint32_t)(q + 8) << (4 * k);
+        for (int k = 7; k >= 0; --k)
+          acc = acc * 16u + (uint32_t)__float2int_rn(__fmul_rn(res[h][k], grid_factor(ir[h], ic[k])));
+        cw = acc + 0x88888888u;
+      } else {
+        cw = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int q = grid_code(res[h][k], grid_factor(ir[h], ic[k]), 7);
+          cw |= (uint32_t)(q + 8) << (4 * k);
+        }
       }
       *reinterpret_cast<uint32_t*>(P.m.res + i * (cols / 2) + (bj * kS + 8 * cg) / 2) = cw;
     }
