@@ -112,6 +112,17 @@ __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
+// A packed multiply, each half rounded as __fmul_rn rounds it.  Its results
+// feed scalar additions only: ptxas fuses a packed multiply whose single use
+// is a packed addition into a packed FMA, which would round once instead of twice.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
 __device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
   float2 r;
   asm("{\n\t.reg .b64 pa, pb, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
@@ -298,7 +309,7 @@ static_assert(sizeof(P1Stage) % 16 == 0 && offsetof(P1Stage, codes) % 16 == 0 &&
               "pass 1 stage fields must stay 16-byte aligned");
 constexpr int kP1Smem = 2 * (int)sizeof(P1Stage);
 
-__global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   extern __shared__ __align__(16) unsigned char p1smem[];
   P1Stage* stage = reinterpret_cast<P1Stage*>(p1smem);
   const int pk = find_prob(a.rstrip_start, a.n, blockIdx.x);
@@ -357,7 +368,12 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
 
   float p[kRank];
   if (live) factor_row(P.m.p, P.m.p_rmax, P.m.p_cmax, i, p);
-  float y[kRank] = {0, 0, 0, 0, 0, 0, 0, 0}, yc[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float2 pp[kRank / 2];
+#pragma unroll
+  for (int l2 = 0; l2 < kRank / 2; ++l2) pp[l2] = make_float2(p[2 * l2], p[2 * l2 + 1]);
+  float2 y2[kRank / 2], yc2[kRank / 2];
+#pragma unroll
+  for (int l2 = 0; l2 < kRank / 2; ++l2) y2[l2] = yc2[l2] = make_float2(0.0f, 0.0f);
   issue(0);
   cp_async_commit();
   fetch(0);
@@ -389,45 +405,68 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
         const uint4 g1 = *reinterpret_cast<const uint4*>(st.g + ti * kP1GStride + cb * 2 + 16);
         const uint2 cwv = *reinterpret_cast<const uint2*>(st.codes + ti * kP1CStride + cb / 2);
         const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const uint32_t cw[2] = {cwv.x, cwv.y};
+        // the residual codes as bytes: even elements' nibbles in lo, odd ones' in hi
+        const uint32_t lo[2] = {cwv.x & 0x0F0F0F0Fu, cwv.y & 0x0F0F0F0Fu};
+        const uint32_t hi[2] = {(cwv.x >> 4) & 0x0F0F0F0Fu, (cwv.y >> 4) & 0x0F0F0F0Fu};
         uint32_t out[8];
-        float yb[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float2 yb[kRank / 2];
+#pragma unroll
+        for (int l2 = 0; l2 < kRank / 2; ++l2) yb[l2] = make_float2(0.0f, 0.0f);
         // four elements at a time with the rank loop outside, so that four
         // independent reconstruction chains interleave; every sum keeps its
-        // order (each element's over l, each Y sum's over the elements)
+        // order (each element's over l, each Y sum's over the elements).  The
+        // products of ranks l and l + 1 are one packed multiply, each half
+        // rounded as fmul rounds it, and feed the scalar additions in order.
 #pragma unroll
         for (int e0 = 0; e0 < 16; e0 += 4) {
-          float rr[4][kRank], acc[4], mv[4];
+          float2 rr[4][kRank / 2];
+          float acc[4], m[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            *reinterpret_cast<float4*>(rr[j]) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 0)]);
-            *reinterpret_cast<float4*>(rr[j] + 4) = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 4)]);
+            const float4 r0 = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 0)]);
+            const float4 r1 = *reinterpret_cast<const float4*>(&st.r[sidx(cb + e0 + j, 4)]);
+            rr[j][0] = make_float2(r0.x, r0.y);
+            rr[j][1] = make_float2(r0.z, r0.w);
+            rr[j][2] = make_float2(r1.x, r1.y);
+            rr[j][3] = make_float2(r1.z, r1.w);
             acc[j] = 0.0f;
           }
 #pragma unroll
-          for (int l = 0; l < kRank; ++l)
+          for (int l2 = 0; l2 < kRank / 2; ++l2)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(p[l], rr[j][l]));
+            for (int j = 0; j < 4; ++j) {
+              const float2 pr = mul2_rn(pp[l2], rr[j][l2]);
+              acc[j] = __fadd_rn(__fadd_rn(acc[j], pr.x), pr.y);
+            }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int e = e0 + j;
-            const int nib = (int)((cw[e >> 3] >> (4 * (e & 7))) & 0xFu) - 8;
-            const float res = __fmul_rn((float)nib, fminf(step_r, st.step_c[cb + e]));
+            // 2^23 + nibble, exactly, then the code's offset of 8 taken off (exact)
+            const uint32_t src = (e & 1) ? hi[e >> 3] : lo[e >> 3];
+            const float nib = __fsub_rn(__uint_as_float(__byte_perm(src, 0x4B000000u, 0x7650u | ((e & 7) >> 1))),
+                                        8388616.0f);
+            const float res = __fmul_rn(nib, fminf(step_r, st.step_c[cb + e]));
             const float mprev = __fadd_rn(res, acc[j]);
             const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
-            const float m = __fadd_rn(__fmul_rn(a.mu, mprev), g);
-            const __nv_bfloat16 mb = __float2bfloat16_rn(m);
-            mv[j] = __bfloat162float(mb);
-            if (e & 1) out[e >> 1] |= (uint32_t)__bfloat16_as_ushort(mb) << 16;
-            else out[e >> 1] = (uint32_t)__bfloat16_as_ushort(mb);
+            m[j] = __fadd_rn(__fmul_rn(a.mu, mprev), g);
+          }
+          // M_t rounded to bf16 two elements at a time; Y takes the rounded values
+          float mv[4];
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            const __nv_bfloat162 mb = __floats2bfloat162_rn(m[2 * jp], m[2 * jp + 1]);
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(&mb);
+            out[(e0 >> 1) + jp] = w;
+            mv[2 * jp] = __uint_as_float(w << 16);
+            mv[2 * jp + 1] = __uint_as_float(w & 0xFFFF0000u);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int l = 0; l < kRank; ++l) yb[l] = fmaf(mv[j], rr[j][l], yb[l]);
+            for (int l2 = 0; l2 < kRank / 2; ++l2) yb[l2] = fma2(make_float2(mv[j], mv[j]), rr[j][l2], yb[l2]);
         }
 #pragma unroll
-        for (int l = 0; l < kRank; ++l) comp_add(y[l], yc[l], yb[l]);
+        for (int l2 = 0; l2 < kRank / 2; ++l2) two_sum_add2(y2[l2], yc2[l2], yb[l2]);
         // M_t over the gradient (this chunk's gradient is already in shared memory)
         __nv_bfloat16* grow = static_cast<__nv_bfloat16*>(P.m.grad) + i * cols + bj * kS + tj;
         *reinterpret_cast<uint4*>(grow) = make_uint4(out[0], out[1], out[2], out[3]);
@@ -437,8 +476,12 @@ __global__ void __launch_bounds__(kThreads, 3) grasp_pass1(GraspArgs a) {
     __syncthreads();   // stage k & 1 is refilled by chunk k + 2's copies
   }
   cp_async_wait<0>();
+  float y[kRank];
 #pragma unroll
-  for (int l = 0; l < kRank; ++l) y[l] += yc[l];
+  for (int l2 = 0; l2 < kRank / 2; ++l2) {
+    y[2 * l2] = y2[l2].x + yc2[l2].x;
+    y[2 * l2 + 1] = y2[l2].y + yc2[l2].y;
+  }
   // the 4 threads of a row add their sums of M_t R_{t-1} (fixed order); the
   // column scaling of Q is applied once, in fp64
 #pragma unroll
