@@ -58,7 +58,7 @@ constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 3
 // 128 x 256 output tile and loads all of A (128 rows) and B (256 rows) per
 // stage (48 KB); a CTA pair (CG = 2) owns 256 x 256, each CTA loading its
 // 128 rows of A and half of B (32 KB per stage per CTA).  The symmetric
-// products keep a staging buffer for coalesced (and mirrored) stores; the
+// products keep two staging buffers of one step each for their stores; the
 // update product stages its whole output tile in TMA box layout; the updates
 // that also move the weights keep two output slots of one step each and a
 // ring of weight chunks, two per step (one per column half), two steps deep
@@ -261,6 +261,8 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... all but the most recent group of this thread's bulk stores have read their shared memory
+__device__ __forceinline__ void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA) before a barrier hands the data to the storing thread.
@@ -430,7 +432,12 @@ struct TileGeom {
   int bcol0;         // first B row (output column) this CTA loads
   int M_, N_, K_;
   bool a_mn, b_mn;
-  bool mirror;       // symmetric product, tile strictly above the diagonal
+  // The symmetric matrices (the Gram A and the polynomial B) hold only their
+  // 256 x 256 tiles on or above the diagonal.  An operand read from one has
+  // the index of its 256-row tile here (else -1): its K blocks left of that
+  // tile lie below the diagonal and are read as the transposed block above
+  // it, by an MN-major box at swapped coordinates.
+  int a_sym, b_sym;
   const CUtensorMap* mapA;
   const CUtensorMap* mapB;
 };
@@ -446,7 +453,7 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int k, int r
   g.row0 = I * (128 * CG) + 128 * rank;
   g.col0 = J * BN;
   g.bcol0 = g.col0 + (CG == 2 ? 128 * rank : 0);
-  g.mirror = (CG == 2) ? (I < J) : (g.row0 + BM <= g.col0);
+  g.a_sym = g.b_sym = -1;
   if (KIND == G_GRAM) {
     g.M_ = P.m; g.N_ = P.m; g.K_ = P.n;
     g.mapA = g.mapB = &P.map_x[args.src];
@@ -455,16 +462,19 @@ __device__ __forceinline__ TileGeom tile_geom(const GemmArgs& args, int k, int r
     g.M_ = P.m; g.N_ = P.m; g.K_ = P.m;
     g.mapA = g.mapB = &P.map_a;
     g.a_mn = g.b_mn = false;
+    g.a_sym = I;
+    g.b_sym = J;
   } else if (!P.tall) {
     g.M_ = P.m; g.N_ = P.n; g.K_ = P.m;
     g.mapA = &P.map_b; g.a_mn = false;
     g.mapB = &P.map_x[args.src]; g.b_mn = true;
+    g.a_sym = I;
   } else {
     g.M_ = P.n; g.N_ = P.m; g.K_ = P.m;
     g.mapA = &P.map_x[args.src]; g.a_mn = false;
     g.mapB = &P.map_b; g.b_mn = false;
+    g.b_sym = J;
   }
-  if (KIND >= G_UPDATE) g.mirror = false;   // only the symmetric products mirror
   return g;
 }
 
@@ -570,15 +580,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           const uint32_t bar = full_l + 8 * s;
           const uint32_t sa = smem_u32(smem + s * SB), sb = sa + SA;
           const int k0 = kb * BK;
+          const bool amn = g.a_mn || g.a_sym > k0 / 256, bmn = g.b_mn || g.b_sym > k0 / 256;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int x = g.a_mn ? g.row0 + 64 * i : k0, y = g.a_mn ? k0 : g.row0 + 64 * i;
+            const int x = amn ? g.row0 + 64 * i : k0, y = amn ? k0 : g.row0 + 64 * i;
             if (CG == 2) tma_load_2d_pair(sa + i * kBox, g.mapA, bar, x, y);
             else tma_load_2d(sa + i * kBox, g.mapA, bar, x, y);
           }
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
-            const int x = g.b_mn ? g.bcol0 + 64 * j : k0, y = g.b_mn ? k0 : g.bcol0 + 64 * j;
+            const int x = bmn ? g.bcol0 + 64 * j : k0, y = bmn ? k0 : g.bcol0 + 64 * j;
             if (CG == 2) tma_load_2d_pair(sb + j * kBox, g.mapB, bar, x, y);
             else tma_load_2d(sb + j * kBox, g.mapB, bar, x, y);
           }
@@ -597,7 +608,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       bool ok = true;
       for (int tile = k_begin; tile < k_end && ok; ++tile, ++ti) {
         const TileGeom g = tile_geom<KIND, CG>(args, tile, 0);
-        const uint32_t idesc = make_idesc(g.a_mn, g.b_mn, 128 * CG);
         const int acc = ti & 1, use = ti >> 1;
         if (use > 0 && !mbar_wait(tempty0 + 8 * acc, (use - 1) & 1, args.hdr, 0x500u | KIND)) break;
         tc_fence_after();
@@ -611,10 +621,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * SB), sb = sa + SA;
+          // each stage's operands are K-major or MN-major as the producer loaded them
+          const bool amn = g.a_mn || g.a_sym > (kb * BK) / 256, bmn = g.b_mn || g.b_sym > (kb * BK) / 256;
+          const uint32_t idesc = make_idesc(amn, bmn, 128 * CG);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = g.a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
-            const uint64_t bd = g.b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
+            const uint64_t ad = amn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
+            const uint64_t bd = bmn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
             mma_bf16_cg<CG>(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_cg<CG>(empty0 + 8 * s);   // frees the stage (in every CTA of the group)
@@ -826,15 +839,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // symmetric products, in four steps of 64 columns: at step st, half h
         // of the epilogue warps takes column chunk c = 2 st + h.  The step's
         // 128 x 64 block is staged in TMA box layout (two 64 x 64 boxes,
-        // 128-byte swizzle) and, for tiles strictly above the diagonal, its
-        // 64 x 128 transpose as well; one thread TMA-stores both and, before
-        // the next step's writes, waits until the stores have read them.
+        // 128-byte swizzle) in one of two buffers, alternately; one thread
+        // TMA-stores it and, before a buffer is written again, waits until the
+        // stores of two steps ago have read it.  Only tiles on or above the
+        // diagonal are computed and stored: the readers of these matrices
+        // take the blocks below it transposed from above.
         const CUtensorMap* mo = (KIND == G_GRAM) ? &P.map_a : &P.map_b;
         const int m = g.M_;
         const int rl = quarter * 32 + lane;   // this thread's row of the tile
-        unsigned char* sd = side;             // direct: boxes of rows 0-63 and 64-127
-        unsigned char* stp = side + 2 * kBox;  // transposed: boxes of columns row0.. and row0 + 64..
-        const int jj = rl & 63;               // this thread's column within a transposed box
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
           const int c = 2 * st + ch;
@@ -872,8 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             for (int i = 0; i < 32; ++i)
               out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]) + (cb + i == r ? args.ca : 0.0f);
           }
-          // the staging is free once the previous step's stores have read it
-          if (ew == 0 && lane == 0 && (st > 0 || ti > 0)) bulk_wait_read_all();
+          // this step's buffer is free once the stores of two steps ago have read it
+          unsigned char* sd = side + (st & 1) * 2 * kBox;   // boxes of rows 0-63 and 64-127
+          if (ew == 0 && lane == 0 && (st > 0 || ti > 0)) bulk_wait_read_but1();
           __syncwarp();
           named_barrier_epilogue();
           unsigned char* drow = sd + (rl >> 6) * kBox + (rl & 63) * 128;
@@ -884,17 +897,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
                 make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
                            pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
           }
-          if (g.mirror) {
-            // element (row rl, column 32 ch + e) of the block is element
-            // (32 ch + e, rl) of the transpose
-            unsigned char* tb = stp + (rl >> 6) * kBox + ((jj & 7) << 1);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int i = 32 * ch + e;
-              *reinterpret_cast<__nv_bfloat16*>(tb + i * 128 + ((((jj >> 3) ^ (i & 7))) << 4)) =
-                  __float2bfloat16_rn(out[e]);
-            }
-          }
           fence_proxy_async_smem();
           named_barrier_epilogue();
           if (ew == 0 && lane == 0) {
@@ -902,10 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
             if (cs < m) {
 #pragma unroll
               for (int b = 0; b < 2; ++b) {
-                if (g.row0 + 64 * b < m) {
-                  tma_store_2d(mo, smem_u32(sd + b * kBox), cs, g.row0 + 64 * b);
-                  if (g.mirror) tma_store_2d(mo, smem_u32(stp + b * kBox), g.row0 + 64 * b, cs);
-                }
+                if (g.row0 + 64 * b < m) tma_store_2d(mo, smem_u32(sd + b * kBox), cs, g.row0 + 64 * b);
               }
             }
             bulk_commit();

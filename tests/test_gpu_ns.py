@@ -72,6 +72,33 @@ def test_five_iterations_vs_oracle(shape):
     assert min_row_cos(got, ref) >= 0.999
 
 
+def test_symmetric_products_read_only_their_upper_tiles():
+    # The Gram A and the polynomial B hold only their 256 x 256 tiles on or
+    # above the diagonal; the products that read them take the blocks below
+    # it transposed from above.  With every workspace byte set to 0xFF
+    # (a bf16 NaN) before the call, any read of a block that was never
+    # written would put NaNs into X.  Shapes with two to eight row tiles,
+    # wide and tall, ragged and exact, in one batch.
+    shapes = [(300, 520), (520, 304), (512, 2048), (2048, 1024), (1100, 1536)]
+    mats, refs, invs = [], [], []
+    for i, (r, c) in enumerate(shapes):
+        g = random_grad(r * c, "bf16", 90 + i).reshape(r, c)
+        M = bf16_to_f64(g)
+        inv = torch.tensor([1.0 / (np.linalg.norm(M) + 1e-7)], dtype=torch.float32, device="cuda")
+        refs.append(ns.newton_schulz(M, inv_norm=float(inv.item())))
+        mats.append(g)
+        invs.append(inv)
+    probs = [q.ns_problem(g, g.shape[0], g.shape[1], inv_norm=inv) for g, inv in zip(mats, invs)]
+    ws = torch.full((q.qmuon_ns_workspace_size(probs),), 0xFF, dtype=torch.uint8, device="cuda")
+    q.qmuon_newton_schulz_batched(probs, 5, COEFFS, ws)
+    q.qmuon_sync_status(ws)
+    for shape, g, ref in zip(shapes, mats, refs):
+        got = bf16_to_f64(g)
+        assert np.isfinite(got).all(), shape
+        assert rel_fro(got, ref) <= 2e-2, shape
+        assert min_row_cos(got, ref) >= 0.999, shape
+
+
 def test_batch_of_mixed_problems_and_strided_view():
     # one launch sequence over problems of different shapes, one of them a
     # column block of a wider matrix (row stride larger than its width)
