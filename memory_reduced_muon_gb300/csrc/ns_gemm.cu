@@ -550,6 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (CG == 2) cluster_sync_all();   // the peer's barriers exist before anyone signals them
   else __syncthreads();
   tc_fence_after();
+  // The products of a Newton-Schulz call are launched as programmatic
+  // dependents of one another: the next one may be scheduled on the SMs this
+  // grid leaves free and set up its barriers and tensor memory meanwhile.
+  // Until here nothing was read that an earlier kernel writes (the problem
+  // and tile tables come from the host before the call); past the wait, every
+  // earlier grid of the stream has completed and its writes are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
@@ -1354,13 +1362,17 @@ cudaError_t launch_gemm(int kind, const Launchable& L, const GemmArgs& a0, cudaS
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem_bytes_of(kind, kCG);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch (the kernel waits on griddepcontrol.wait
+  // before it touches anything an earlier kernel of the stream wrote)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
