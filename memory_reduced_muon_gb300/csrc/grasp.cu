@@ -183,10 +183,20 @@ __device__ __forceinline__ void factor_row(const int8_t* q, const float* rmax, c
   for (int l = 0; l < kRank; ++l) out[l] = __fmul_rn((float)b[l], grid_step(rm, __ldg(cm + l), 127.0f));
 }
 
+// The step's kernels are launched as programmatic dependents of one another
+// (launch_dep below): each first waits until every earlier grid of the stream
+// has completed and its writes are visible, then lets the next kernel be
+// scheduled, so that its launch overlaps this one's last wave.
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // R_{t-1} dequantised and the inverse norms of its columns, one CTA per matrix
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
+  grid_dep_sync();
   __shared__ double red[kThreads / 32 * kRank];
   const GraspProb& P = a.probs[blockIdx.x];
   const int64_t cols = P.m.cols;
@@ -310,6 +320,7 @@ static_assert(sizeof(P1Stage) % 16 == 0 && offsetof(P1Stage, codes) % 16 == 0 &&
 constexpr int kP1Smem = 2 * (int)sizeof(P1Stage);
 
 __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
+  grid_dep_sync();
   extern __shared__ __align__(16) unsigned char p1smem[];
   P1Stage* stage = reinterpret_cast<P1Stage*>(p1smem);
   const int pk = find_prob(a.rstrip_start, a.n, blockIdx.x);
@@ -534,6 +545,7 @@ __device__ __forceinline__ bool chol8(double (&g)[kRank][kRank]) {
 // factor L; one CTA per matrix.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(64) grasp_chol(GraspArgs a, WsHeader* hdr) {
+  grid_dep_sync();
   __shared__ double sG[36];
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
   const GraspProb& P = a.probs[blockIdx.x];
@@ -568,6 +580,7 @@ __global__ void __launch_bounds__(64) grasp_chol(GraspArgs a, WsHeader* hdr) {
 // (one 64-row block of P) is grid-quantised.
 template <int PASS>
 __global__ void __launch_bounds__(64) grasp_tsolve(GraspArgs a, const WsHeader* hdr) {
+  grid_dep_sync();
   __shared__ double sL[kRank][kRank];
   __shared__ double sInvD[kRank];         // 1 / L_uu
   __shared__ double sZZ[36][kS + 1];      // PASS 0: each row's products z_u z_v
@@ -644,6 +657,7 @@ constexpr int kP2Smem = kP2Stages * kP2StageBytes + (kThreads / 32) * kS * kRank
 
 
 __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const WsHeader* hdr) {
+  grid_dep_sync();
   extern __shared__ __align__(16) unsigned char p2smem[];
   float (*part)[kS][kRank] = reinterpret_cast<float (*)[kS][kRank]>(p2smem + kP2Stages * kP2StageBytes);
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
@@ -766,6 +780,7 @@ static_assert(offsetof(P3Smem, r) % 16 == 0, "pass 3 shared fields must stay 16-
 constexpr int kP3Smem = (int)sizeof(P3Smem);
 
 __global__ void __launch_bounds__(kP3Threads, 4) grasp_pass3(GraspArgs a, const WsHeader* hdr) {
+  grid_dep_sync();
   extern __shared__ __align__(16) unsigned char p3smem[];
   P3Smem& S = *reinterpret_cast<P3Smem*>(p3smem);
   if (*reinterpret_cast<const volatile unsigned*>(&hdr->error) != 0u) return;
@@ -933,6 +948,24 @@ size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
          align_up((size_t)m.rows * kRank * 8, 256) + align_up(nbr * 36 * 8, 256) + align_up(kRank * kRank * 8, 256);
 }
 
+// A launch that may start while the stream's previous kernel finishes: the
+// kernel itself waits for that kernel (grid_dep_sync) before it reads anything.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dep(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 size_t table_bytes(int32_t n) {
   return align_up((size_t)n * sizeof(GraspProb), 256) + 3 * align_up((size_t)(n + 1) * 8, 256) +
          2 * align_up((size_t)n * 4, 256);
@@ -1053,15 +1086,14 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(grasp_pass3, cudaFuncAttributeMaxDynamicSharedMemorySize, kP3Smem);
     if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
-    grasp_colnorm<<<n, kThreads, 0, s>>>(a);
-    grasp_pass1<<<(unsigned)rs[n], kThreads, kP1Smem, s>>>(a);
-    grasp_chol<<<n, 64, 0, s>>>(a, hdr);
-    grasp_tsolve<0><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
-    grasp_chol<<<n, 64, 0, s>>>(a, hdr);
-    grasp_tsolve<1><<<(unsigned)rs[n], 64, 0, s>>>(a, hdr);
-    grasp_pass2<<<(unsigned)cs[n], kThreads, kP2Smem, s>>>(a, hdr);
-    grasp_pass3<<<(unsigned)tiles, kP3Threads, kP3Smem, s>>>(a, hdr);
-    e = cudaGetLastError();
+    e = launch_dep(grasp_colnorm, (unsigned)n, kThreads, 0, s, a);
+    if (e == cudaSuccess) e = launch_dep(grasp_pass1, (unsigned)rs[n], kThreads, kP1Smem, s, a);
+    if (e == cudaSuccess) e = launch_dep(grasp_chol, (unsigned)n, 64, 0, s, a, hdr);
+    if (e == cudaSuccess) e = launch_dep(grasp_tsolve<0>, (unsigned)rs[n], 64, 0, s, a, (const WsHeader*)hdr);
+    if (e == cudaSuccess) e = launch_dep(grasp_chol, (unsigned)n, 64, 0, s, a, hdr);
+    if (e == cudaSuccess) e = launch_dep(grasp_tsolve<1>, (unsigned)rs[n], 64, 0, s, a, (const WsHeader*)hdr);
+    if (e == cudaSuccess) e = launch_dep(grasp_pass2, (unsigned)cs[n], kThreads, kP2Smem, s, a, (const WsHeader*)hdr);
+    if (e == cudaSuccess) e = launch_dep(grasp_pass3, (unsigned)tiles, kP3Threads, kP3Smem, s, a, (const WsHeader*)hdr);
     // the pageable host tables are staged by the copies above before they return
     if (e != cudaSuccess) return set_error("qmuon_grasp_step (launch)", e);
     tally(T_GRASP_CALLS);
