@@ -185,6 +185,22 @@ QMUON_API qmuon_status qmuon_plan_set_nonfinite_counter(qmuon_plan* plan, uint32
  * QMUON_ERR_INVALID_ARGUMENT on a NULL plan or enable not 0/1. */
 QMUON_API qmuon_status qmuon_plan_set_stochastic_rounding(qmuon_plan* plan, int32_t enable, uint64_t seed);
 
+/* How qmuon_step_from_host moves host gradients into the plan's buffers:
+ *   QMUON_INGEST_PULL (the default): gradients in page-locked host memory
+ *     that the device can address, 16-byte aligned, are read by a small
+ *     kernel's own loads over the host link (about 19 CTAs on 152 SMs); any
+ *     other gradient is copied with cudaMemcpyAsync;
+ *   QMUON_INGEST_COPY: every gradient is copied with cudaMemcpyAsync.
+ * Both move about 211 GB/s on GB300.  Copy-engine transfers were seen to
+ * stall for 70-120 ms every ~510 ms on some hosts, which the pull does not;
+ * the pull's host reads, in turn, slow Newton-Schulz kernels running beside
+ * them (a MuonBP block step by about 2.8 ms while it runs).  Host-only:
+ * changes no device state.  QMUON_ERR_INVALID_ARGUMENT on a NULL plan or an
+ * unknown mode.  The pages have no counterpart. */
+#define QMUON_INGEST_PULL 0
+#define QMUON_INGEST_COPY 1
+QMUON_API qmuon_status qmuon_plan_set_host_ingest(qmuon_plan* plan, int32_t mode);
+
 /* Workspace bytes of qmuon_update_mxfp8_carrier for a rows x cols tensor. */
 QMUON_API size_t qmuon_carrier_workspace_size(int64_t rows, int64_t cols);
 
@@ -393,7 +409,12 @@ QMUON_API qmuon_status qmuon_noalloc_inject_status(qmuon_status status, uint32_t
  * blocking the caller.  The copies into the plan's gradient buffers go on
  * copy_stream and start once this plan's previous qmuon_step_from_host has
  * finished with those buffers; the step runs on `stream` once the copies
- * have landed.  A caller that alternates two plans over the same q8 state
+ * have landed.  With the plan's default ingest mode (qmuon_plan_set_host_ingest),
+ * a gradient in page-locked host memory that the device can address
+ * (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped), 16-byte
+ * aligned, is read by a kernel's own loads over the host link; any other is
+ * moved by cudaMemcpyAsync (qmuon_counters host_pulled_bytes and
+ * host_copied_bytes count the two).  A caller that alternates two plans over the same q8 state
  * (the same q8/absmax pointers, different gradient buffers) therefore
  * overlaps step t+1's host->device copies with step t's kernels.  The
  * arithmetic and device outputs are those of qmuon_step.
@@ -473,6 +494,8 @@ typedef struct qmuon_counters {
   uint64_t ns_bf16_handoff_bytes;   /* bf16 bytes the carrier expansion wrote as Newton-Schulz input */
   uint64_t weight_f32_tensors;      /* fp32 master weights updated by steps */
   uint64_t grasp_matrices;          /* matrices whose 4-bit state qmuon_grasp_step updated */
+  uint64_t host_pulled_bytes;       /* host-fed gradient bytes read by the device's own loads (page-locked memory) */
+  uint64_t host_copied_bytes;       /* host-fed gradient bytes moved by cudaMemcpyAsync (other host memory) */
 } qmuon_counters;
 
 /* Copies the tallies into `out`: the first min(out_bytes, sizeof(qmuon_counters))

@@ -78,7 +78,7 @@ COUNTER_FIELDS = (
     "step_sr_calls", "step_host_fed_calls", "grasp_calls", "grad_bf16_tensors", "grad_fp16_tensors",
     "grad_fp32_tensors", "state_int8_tensors", "state_uint8_tensors", "carrier_payload_u8_tensors",
     "carrier_scale_u8_tensors", "carrier_inv_norm_f32_values", "ns_bf16_problems", "ns_mxfp8_problems",
-    "ns_bf16_handoff_bytes", "weight_f32_tensors", "grasp_matrices")
+    "ns_bf16_handoff_bytes", "weight_f32_tensors", "grasp_matrices", "host_pulled_bytes", "host_copied_bytes")
 
 
 class qmuon_counters(C.Structure):
@@ -106,6 +106,7 @@ def lib() -> C.CDLL:
         "qmuon_update_multi_normalize_groups": (i32, [vp, f32, i32, vp, vp, vp, sz, vp]),
         "qmuon_update_multi_normalize_groups_sr": (i32, [vp, f32, i32, C.c_uint64, i64, vp, vp, vp, sz, vp]),
         "qmuon_plan_set_stochastic_rounding": (i32, [vp, i32, C.c_uint64]),
+        "qmuon_plan_set_host_ingest": (i32, [vp, i32]),
         "qmuon_grasp_workspace_size": (sz, [C.POINTER(qmuon_grasp_matrix), i32]),
         "qmuon_grasp_step": (i32, [C.POINTER(qmuon_grasp_matrix), i32, f32, vp, sz, vp]),
         "qmuon_carrier_workspace_size": (sz, [i64, i64]),
@@ -145,7 +146,7 @@ def exported_symbols() -> list:
             "qmuon_plan_set_stochastic_rounding", "qmuon_update_mxfp8_carrier_multi",
             "qmuon_grasp_workspace_size", "qmuon_grasp_step", "qmuon_step_from_host",
             "qmuon_plan_set_nonfinite_counter", "qmuon_noalloc_sync_status", "qmuon_noalloc_inject_status",
-            "qmuon_get_counters", "qmuon_reset_counters"]
+            "qmuon_get_counters", "qmuon_reset_counters", "qmuon_plan_set_host_ingest"]
 
 
 # --------------------------------------------------------------------------
@@ -273,6 +274,15 @@ def qmuon_update_multi_normalize_groups_sr(plan: Plan, beta: float, normalize_mo
 def qmuon_plan_set_nonfinite_counter(plan: Plan, counter):
     """``counter``: a device uint32/int32 tensor of one element, or None."""
     _check(lib().qmuon_plan_set_nonfinite_counter(plan.handle, _ptr(counter)), "qmuon_plan_set_nonfinite_counter")
+
+
+QMUON_INGEST_PULL = 0
+QMUON_INGEST_COPY = 1
+
+
+def qmuon_plan_set_host_ingest(plan: Plan, mode: int):
+    """QMUON_INGEST_PULL (default) or QMUON_INGEST_COPY for qmuon_step_from_host."""
+    _check(lib().qmuon_plan_set_host_ingest(plan.handle, int(mode)), "qmuon_plan_set_host_ingest")
 
 
 def qmuon_plan_set_stochastic_rounding(plan: Plan, enable: bool, seed: int = 0):

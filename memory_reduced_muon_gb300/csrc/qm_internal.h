@@ -136,7 +136,8 @@ enum Tally {
   T_UPDATE_CALLS, T_UPDATE_SR_CALLS, T_CARRIER_CALLS, T_NS_CALLS, T_STEP_BLOCK_CALLS, T_STEP_FULL_CALLS,
   T_STEP_SR_CALLS, T_STEP_HOST_FED_CALLS, T_GRASP_CALLS, T_GRAD_BF16, T_GRAD_FP16, T_GRAD_FP32, T_STATE_INT8,
   T_STATE_UINT8, T_CARRIER_PAYLOAD_U8, T_CARRIER_SCALE_U8, T_CARRIER_INV_NORM_F32, T_NS_BF16_PROBLEMS,
-  T_NS_MXFP8_PROBLEMS, T_NS_BF16_HANDOFF_BYTES, T_WEIGHT_F32, T_GRASP_MATRICES, T_COUNT
+  T_NS_MXFP8_PROBLEMS, T_NS_BF16_HANDOFF_BYTES, T_WEIGHT_F32, T_GRASP_MATRICES, T_HOST_PULLED_BYTES,
+  T_HOST_COPIED_BYTES, T_COUNT
 };
 static_assert(sizeof(qmuon_counters) == T_COUNT * sizeof(uint64_t), "one tally per qmuon_counters field");
 void tally(Tally t, uint64_t v = 1);

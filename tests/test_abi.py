@@ -241,7 +241,9 @@ int main(void) {
   /* the audit tallies: no CUDA call, and the failed plan_create above added nothing */
   qmuon_counters c;
   memset(&c, 0xff, sizeof(c));
-  if (sizeof(qmuon_counters) != 176 || offsetof(qmuon_counters, grasp_matrices) != 168) return 7;
+  if (sizeof(qmuon_counters) != 192 || offsetof(qmuon_counters, grasp_matrices) != 168 ||
+      offsetof(qmuon_counters, host_copied_bytes) != 184)
+    return 7;
   if (qmuon_get_counters(&c, sizeof(c)) != QMUON_OK || c.update_calls != 0 || c.grasp_matrices != 0) return 8;
   qmuon_reset_counters();
   if (qmuon_get_counters(NULL, sizeof(c)) != QMUON_ERR_INVALID_ARGUMENT) return 9;
@@ -274,7 +276,7 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     assert run.stdout.startswith("qmuon")
     # the binding's structures have the sizes the C compiler gave them
     assert [C.sizeof(t) for t in (q.qmuon_tensor, q.qmuon_norm_segment, q.qmuon_ns_problem,
-                                  q.qmuon_grasp_matrix, q.qmuon_counters)] == [40, 24, 64, 96, 176]
+                                  q.qmuon_grasp_matrix, q.qmuon_counters)] == [40, 24, 64, 96, 192]
 
 
 def _header_counter_fields():
@@ -302,7 +304,12 @@ def test_counters_on_host(lib):
     buf = (C.c_uint64 * 3)(7, 7, 7)
     assert L.qmuon_get_counters(C.cast(buf, C.POINTER(q.qmuon_counters)), 16) == q.QMUON_OK
     assert list(buf) == [0, 0, 7]
-    assert L.qmuon_get_counters(None, 176) == q.QMUON_ERR_INVALID_ARGUMENT
+    assert L.qmuon_get_counters(None, 192) == q.QMUON_ERR_INVALID_ARGUMENT
+
+
+def test_host_ingest_mode_is_checked_on_host(lib):
+    L = q.lib()
+    assert L.qmuon_plan_set_host_ingest(None, q.QMUON_INGEST_COPY) == q.QMUON_ERR_INVALID_ARGUMENT
 
 
 def _declared_arities():

@@ -124,8 +124,10 @@ def test_counters_follow_every_path():
     q.qmuon_plan_set_stochastic_rounding(splan, True, 11)
     c0 = q.qmuon_get_counters()
     q.qmuon_step_from_host(splan, 3, 2, 0.95, 0.02, 0.01, weights, COEFFS, 5, host, hsum, sums, sws)
+    # torch's page-locked buffers are mapped: the step reads them with its own loads
     _expect(_delta(c0, q.qmuon_get_counters()), step_block_calls=1, step_sr_calls=1, step_host_fed_calls=1,
-            grad_bf16_tensors=2, state_int8_tensors=2, ns_bf16_problems=4, weight_f32_tensors=2)
+            grad_bf16_tensors=2, state_int8_tensors=2, ns_bf16_problems=4, weight_f32_tensors=2,
+            host_pulled_bytes=2 * sum(r * c for r, c in shapes))
     q.qmuon_sync_status(sws)
 
     # ---- GRASP on two matrices ----

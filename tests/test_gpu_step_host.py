@@ -117,3 +117,54 @@ def test_rejects_missing_host_gradient():
     with pytest.raises(q.QmuonError) as e:
         q.qmuon_step_from_host(plans[0], 1, 1, 0.9, 0.02, 0.02, weights, COEFFS, 5, [g0, 0], None, None, ws)
     assert e.value.status == q.QMUON_ERR_INVALID_ARGUMENT
+
+
+def test_page_locked_pull_and_copy_paths_in_one_step():
+    # page-locked 16-byte aligned gradients are read by the device's own loads
+    # (host_pulled_bytes), pageable ones and a page-locked view that starts 2
+    # bytes into its buffer are copied (host_copied_bytes); the step equals the
+    # oracle's where its arithmetic is exact, as with every gradient copied
+    shapes = [(256, 512), (128, 256), (64, 192)]
+    mats, states, weights, bufs, plans, host = _setup(shapes, (1, 1), 95)
+    ws = torch.empty(q.qmuon_workspace_size(plans[0], q.QMUON_WS_STEP), dtype=torch.uint8, device="cuda")
+    g = [random_grad(m.numel, "bf16", 700 + i).reshape(m.rows, m.cols).cpu() for i, m in enumerate(mats)]
+    pinned = g[0].pin_memory()
+    pageable = g[1].clone()
+    wide = torch.empty(mats[2].numel + 8, dtype=torch.bfloat16).pin_memory()
+    wide[1:1 + mats[2].numel] = g[2].reshape(-1)
+    shifted = wide[1:1 + mats[2].numel].view(mats[2].rows, mats[2].cols)
+    assert shifted.data_ptr() % 16 == 2
+    sums_h = torch.full((3,), -1.0)
+    w_before = [w.cpu().numpy() for w in weights]
+    before = q.qmuon_get_counters()
+    q.qmuon_step_from_host(plans[0], 1, 1, 0.9, 0.02, 0.02, weights, COEFFS, 5, [pinned, pageable, shifted], sums_h,
+                           None, ws)
+    q.qmuon_sync_status(ws)
+    after = q.qmuon_get_counters()
+    assert after["host_pulled_bytes"] - before["host_pulled_bytes"] == 2 * mats[0].numel
+    assert after["host_copied_bytes"] - before["host_copied_bytes"] == 2 * (mats[1].numel + mats[2].numel)
+    host, U, inf = muonbp.muonbp_step(1, 1, host, [to_oracle_grad(x, "bf16") for x in g], 0.9, 0.02, 0.02,
+                                      tile=(1, 1))
+    np.testing.assert_allclose(sums_h.numpy(), inf["S"], rtol=1e-5)
+    for i, m in enumerate(mats):
+        np.testing.assert_array_equal(states[i][0].cpu().numpy(), host[i].q8)
+        np.testing.assert_array_equal(states[i][1].cpu().numpy(), host[i].absmax)
+        u32 = bufs[0][i].float().cpu().numpy()
+        expect = (w_before[i] - (np.float32(0.02) * u32).astype(np.float32)).astype(np.float32)
+        np.testing.assert_array_equal(weights[i].cpu().numpy(), expect)
+
+    # the plan told to copy: the same page-locked buffers go through the copy engines
+    q.qmuon_plan_set_host_ingest(plans[0], q.QMUON_INGEST_COPY)
+    g2 = [random_grad(m.numel, "bf16", 710 + i).reshape(m.rows, m.cols).cpu().pin_memory() for i, m in enumerate(mats)]
+    before = q.qmuon_get_counters()
+    q.qmuon_step_from_host(plans[0], 2, 1, 0.9, 0.02, 0.02, weights, COEFFS, 5, g2, sums_h, None, ws)
+    q.qmuon_sync_status(ws)
+    after = q.qmuon_get_counters()
+    assert after["host_pulled_bytes"] == before["host_pulled_bytes"]
+    assert after["host_copied_bytes"] - before["host_copied_bytes"] == 2 * sum(m.numel for m in mats)
+    host, U, inf = muonbp.muonbp_step(2, 1, host, [to_oracle_grad(x, "bf16") for x in g2], 0.9, 0.02, 0.02,
+                                      tile=(1, 1))
+    np.testing.assert_allclose(sums_h.numpy(), inf["S"], rtol=1e-5)
+    for i, m in enumerate(mats):
+        np.testing.assert_array_equal(states[i][0].cpu().numpy(), host[i].q8)
+        np.testing.assert_array_equal(states[i][1].cpu().numpy(), host[i].absmax)
