@@ -57,13 +57,13 @@ constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 3
 // Shared memory per product kind and CTA group.  One CTA (CG = 1) owns a
 // 128 x 256 output tile and loads all of A (128 rows) and B (256 rows) per
 // stage (48 KB); a CTA pair (CG = 2) owns 256 x 256, each CTA loading its
-// 128 rows of A and half of B (32 KB per stage per CTA).  The symmetric
-// products keep two staging buffers of one step each for their stores; the
-// update product stages its whole output tile in TMA box layout; the updates
-// that also move the weights keep two output slots of one step each and a
-// ring of weight chunks, two per step (one per column half), two steps deep
-// (kind 3, for short K loops where the weights bound the tile) or one step
-// deep with a fifth operand stage (kind 4, for long K loops).
+// 128 rows of A and half of B (32 KB per stage per CTA).  The polynomial and
+// update products stage their output per epilogue warp (4 KB each, one
+// 32 x 64 TMA box at a time), the Gram in two buffers of one 64-column step
+// each; the updates that also move the weights keep two output slots of one
+// step each and a ring of weight chunks, two per step (one per column half),
+// two steps deep (kind 3, for short K loops where the weights bound the tile)
+// or one step deep with a fifth operand stage (kind 4, for long K loops).
 __host__ __device__ constexpr uint32_t stage_bytes_of(int cg) { return cg == 2 ? 4 * kBox : kStageBytes; }
 __host__ __device__ constexpr int w_depth_of(int kind) { return kind == 3 ? 2 : 1; }
 __host__ __device__ constexpr int stages_of(int kind, int cg) {
@@ -96,6 +96,7 @@ struct alignas(128) NsProb {
   CUtensorMap map_b;      // m x m polynomial
   CUtensorMap map_w;      // fp32 weights (stored orientation, 32 x 128 boxes), when w is set
   CUtensorMap map_x32[3]; // the X buffers with 32-row boxes: one epilogue warp's stores
+  CUtensorMap map_b32;    // B with 32-row boxes, likewise
   __nv_bfloat16* x[3];
   int64_t x_ld[3];
   __nv_bfloat16* a;
@@ -683,14 +684,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const int r = g.row0 + quarter * 32 + lane;   // this thread's output row
       const int acc = ti & 1, use = ti >> 1;
       // G_POLY: this thread's A values for the b A term (its row, the four
-      // 32-column chunks c = 2 st + h it will finish) are loaded before the
+      // 32-column chunks of its warp's half of the tile) are loaded before the
       // accumulator is ready, so their latency overlaps the tensor cores; a
       // chunk that crosses the matrix edge is read element by element when used
       uint4 apre[4][4];
       if (KIND == G_POLY) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int cb = g.col0 + (2 * j + ch) * 32;
+          const int cb = g.col0 + 128 * ch + 32 * j;
           if (r < g.M_ && cb + 32 <= g.M_) {
             const uint4* q = reinterpret_cast<const uint4*>(P.a + (int64_t)r * P.ab_ld + cb);
 #pragma unroll
@@ -704,13 +705,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       bool ok = mbar_wait(tfull0 + 8 * acc, use & 1, args.hdr, 0x400u | KIND);
       tc_fence_after();
       ok = ok && *reinterpret_cast<volatile unsigned*>(&args.hdr->error) == 0u;
-      // the update's staging is per warp: it is free again once this warp's
-      // stores of the previous tile have read it.  tcgen05.ld is
-      // warp-collective, so a warp continues or stops as one; the other
-      // products stage through shared barriers, and all their epilogue warps
-      // continue or stop together
-      if (KIND == G_UPDATE && lane == 0 && ti > 0) bulk_wait_read_all();
-      if (KIND == G_UPDATE ? !__all_sync(0xffffffffu, ok) : !epilogue_all(ok)) break;
+      // the staging of the update and polynomial products is per warp: it is
+      // free again once this warp's stores of the previous tile have read it.
+      // tcgen05.ld is warp-collective, so a warp continues or stops as one;
+      // the Gram and the weight passes stage through shared barriers, and all
+      // their epilogue warps continue or stop together
+      constexpr bool WARP_LOCAL = (KIND == G_UPDATE || KIND == G_POLY);
+      if (WARP_LOCAL && lane == 0 && ti > 0) bulk_wait_read_all();
+      if (WARP_LOCAL ? !__all_sync(0xffffffffu, ok) : !epilogue_all(ok)) break;
       float s_first = 1.0f;
       if (args.first && P.inv) {
         const float iv = *P.inv;
@@ -724,6 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // staging, one 32 x 64 TMA box at a time (128-byte swizzle: 16-byte
         // chunk q of row r at q ^ (r & 7)), by its own TMA stores.  The four
         // TMEM loads are in flight together.
+        const CUtensorMap* mo = &P.map_x32[args.dst];
         uint32_t v[4][32];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) tmem_ld32_async(tbase + (uint32_t)((4 * ch + cc) * 32), v[cc]);
@@ -764,7 +767,63 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           __syncwarp();
           if (lane == 0) {
             const int x = g.col0 + 128 * ch + 64 * b;
-            if (y < g.M_ && x < g.N_) tma_store_2d(&P.map_x32[args.dst], smem_u32(wst), x, y);
+            if (y < g.M_ && x < g.N_) tma_store_2d(mo, smem_u32(wst), x, y);
+            bulk_commit();
+          }
+        }
+      } else if (KIND == G_GRAM) {
+        // the Gram A = s1^2 (X X^T) on a SYRK tile, in four steps of 64
+        // columns: at step st, half h of the epilogue warps takes column chunk
+        // c = 2 st + h.  The step's 128 x 64 block is staged in TMA box layout
+        // (two 64 x 64 boxes, 128-byte swizzle) in one of two buffers,
+        // alternately; one thread TMA-stores it and, before a buffer is
+        // written again, waits until the stores of two steps ago have read
+        // it.  (Warp-local staging, as in the other products, measured 2%
+        // slower for these long-K tiles.)  Only tiles on or above the diagonal
+        // are computed and stored: the readers of A and B take the blocks
+        // below it transposed from above.
+        const CUtensorMap* mo = &P.map_a;
+        const int m = g.M_;
+        const int rl = quarter * 32 + lane;   // this thread's row of the tile
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const int c = 2 * st + ch;
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), v);
+          if (st == 3) {   // every TMEM read of this accumulator is done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (CG == 2) mbar_arrive_cluster(tempty_l + 8 * acc);
+              else mbar_arrive(tempty0 + 8 * acc);
+            }
+          }
+          float out[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
+          // this step's buffer is free once the stores of two steps ago have read it
+          unsigned char* sd = side + (st & 1) * 2 * kBox;   // boxes of rows 0-63 and 64-127
+          if (ew == 0 && lane == 0 && (st > 0 || ti > 0)) bulk_wait_read_but1();
+          __syncwarp();
+          named_barrier_epilogue();
+          unsigned char* drow = sd + (rl >> 6) * kBox + (rl & 63) * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = ch * 4 + t;
+            *reinterpret_cast<uint4*>(drow + ((q ^ (rl & 7)) << 4)) =
+                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
+                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
+          }
+          fence_proxy_async_smem();
+          named_barrier_epilogue();
+          if (ew == 0 && lane == 0) {
+            const int cs = g.col0 + 64 * st;
+            if (cs < m) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                if (g.row0 + 64 * b < m) tma_store_2d(mo, smem_u32(sd + b * kBox), cs, g.row0 + 64 * b);
+              }
+            }
             bulk_commit();
           }
         }
@@ -844,23 +903,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
         }
       } else {
-        // symmetric products, in four steps of 64 columns: at step st, half h
-        // of the epilogue warps takes column chunk c = 2 st + h.  The step's
-        // 128 x 64 block is staged in TMA box layout (two 64 x 64 boxes,
-        // 128-byte swizzle) in one of two buffers, alternately; one thread
-        // TMA-stores it and, before a buffer is written again, waits until the
-        // stores of two steps ago have read it.  Only tiles on or above the
-        // diagonal are computed and stored: the readers of these matrices
-        // take the blocks below it transposed from above.
-        const CUtensorMap* mo = (KIND == G_GRAM) ? &P.map_a : &P.map_b;
+        // B = a I + b A + c A^2 on a SYRK tile, warp by warp as above, one
+        // 32-column TMEM load at a time (the b A term's values already take
+        // 64 registers), two chunks to a 32 x 64 box.  Only tiles on or above
+        // the diagonal are computed and stored: the readers of A and B take
+        // the blocks below it transposed from above.
         const int m = g.M_;
-        const int rl = quarter * 32 + lane;   // this thread's row of the tile
+        unsigned char* wst = side + ew * 4096;
+        const int y = g.row0 + 32 * quarter;
+        // element (row r, column c) of B, with a on the diagonal (the a X
+        // term of the update)
+        auto poly = [&](float a, uint32_t acc_bits, int c) {
+          return args.cb * a + args.cc * __uint_as_float(acc_bits) + (c == r ? args.ca : 0.0f);
+        };
 #pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          const int c = 2 * st + ch;
+        for (int j = 0; j < 4; ++j) {   // 32-column chunk j of the warp's half
           uint32_t v[32];
-          tmem_ld32(tbase + (uint32_t)(c * 32), v);
-          if (st == 3) {   // every TMEM read of this accumulator is done
+          tmem_ld32(tbase + (uint32_t)((4 * ch + j) * 32), v);
+          if (j == 3) {   // every TMEM read of this accumulator is done
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -868,54 +928,48 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
               else mbar_arrive(tempty0 + 8 * acc);
             }
           }
-          float out[32];
-          if (KIND == G_GRAM) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) out[i] = s_first * __uint_as_float(v[i]);
-          } else {
+          if (j == 2) {   // the first box's store has read the staging
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          const int cb = g.col0 + 128 * ch + 32 * j;
+          const int h = j & 1;
+          if (r < m && cb < m && cb + 32 > m) {
+            // a chunk that crosses the matrix edge, read element by element
             float av[32];
-            const int cb = g.col0 + c * 32;
-            if (r < m && cb < m && cb + 32 > m) {
-              load_row32(P.a + (int64_t)r * P.ab_ld + cb, m - cb, av);   // the matrix edge
-            } else {
+            load_row32(P.a + (int64_t)r * P.ab_ld + cb, m - cb, av);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint4 u = apre[st][i];
-                av[8 * i + 0] = bf16_lo(u.x); av[8 * i + 1] = bf16_hi(u.x);
-                av[8 * i + 2] = bf16_lo(u.y); av[8 * i + 3] = bf16_hi(u.y);
-                av[8 * i + 4] = bf16_lo(u.z); av[8 * i + 5] = bf16_hi(u.z);
-                av[8 * i + 6] = bf16_lo(u.w); av[8 * i + 7] = bf16_hi(u.w);
-              }
+            for (int t = 0; t < 4; ++t) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                w[k] = pack_bf16(poly(av[8 * t + 2 * k], v[8 * t + 2 * k], cb + 8 * t + 2 * k),
+                                 poly(av[8 * t + 2 * k + 1], v[8 * t + 2 * k + 1], cb + 8 * t + 2 * k + 1));
+              *reinterpret_cast<uint4*>(wst + lane * 128 + (((4 * h + t) ^ (lane & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
             }
-            // a on the diagonal (row r, column cb + i): the a X term of the update
+          } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              out[i] = args.cb * av[i] + args.cc * __uint_as_float(v[i]) + (cb + i == r ? args.ca : 0.0f);
-          }
-          // this step's buffer is free once the stores of two steps ago have read it
-          unsigned char* sd = side + (st & 1) * 2 * kBox;   // boxes of rows 0-63 and 64-127
-          if (ew == 0 && lane == 0 && (st > 0 || ti > 0)) bulk_wait_read_but1();
-          __syncwarp();
-          named_barrier_epilogue();
-          unsigned char* drow = sd + (rl >> 6) * kBox + (rl & 63) * 128;
+            for (int t = 0; t < 4; ++t) {
+              const uint4 u = apre[j][t];
+              const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+              uint32_t w[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int q = ch * 4 + t;
-            *reinterpret_cast<uint4*>(drow + ((q ^ (rl & 7)) << 4)) =
-                make_uint4(pack_bf16(out[8 * t], out[8 * t + 1]), pack_bf16(out[8 * t + 2], out[8 * t + 3]),
-                           pack_bf16(out[8 * t + 4], out[8 * t + 5]), pack_bf16(out[8 * t + 6], out[8 * t + 7]));
-          }
-          fence_proxy_async_smem();
-          named_barrier_epilogue();
-          if (ew == 0 && lane == 0) {
-            const int cs = g.col0 + 64 * st;
-            if (cs < m) {
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                if (g.row0 + 64 * b < m) tma_store_2d(mo, smem_u32(sd + b * kBox), cs, g.row0 + 64 * b);
-              }
+              for (int k = 0; k < 4; ++k)
+                w[k] = pack_bf16(poly(bf16_lo(uw[k]), v[8 * t + 2 * k], cb + 8 * t + 2 * k),
+                                 poly(bf16_hi(uw[k]), v[8 * t + 2 * k + 1], cb + 8 * t + 2 * k + 1));
+              *reinterpret_cast<uint4*>(wst + lane * 128 + (((4 * h + t) ^ (lane & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
             }
-            bulk_commit();
+          }
+          if (h == 1) {   // the box (chunks j - 1 and j) is staged: store it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int x = g.col0 + 128 * ch + 32 * (j - 1);
+              if (y < m && x < m) tma_store_2d(&P.map_b32, smem_u32(wst), x, y);
+              bulk_commit();
+            }
           }
         }
       }
@@ -1152,7 +1206,9 @@ bool fill_problem(NsProb& P, void* x0, int64_t rows, int64_t cols, int64_t ld, c
     if (!encode_bf16(&P.map_x[i], P.x[i], rows, cols, P.x_ld[i]) ||
         !encode_bf16(&P.map_x32[i], P.x[i], rows, cols, P.x_ld[i], 32))
       return false;
-  if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld)) return false;
+  if (!encode_bf16(&P.map_a, P.a, m, m, P.ab_ld) || !encode_bf16(&P.map_b, P.b, m, m, P.ab_ld) ||
+      !encode_bf16(&P.map_b32, P.b, m, m, P.ab_ld, 32))
+    return false;
   if (w && !encode_w(&P.map_w, w, rows, cols, w_ld)) return false;
   count_tiles(rows, cols, P.tiles_n, P.tiles);
   return true;
