@@ -778,8 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         // (two 64 x 64 boxes, 128-byte swizzle) in one of two buffers,
         // alternately; one thread TMA-stores it and, before a buffer is
         // written again, waits until the stores of two steps ago have read
-        // it.  (Warp-local staging, as in the other products, measured 2%
-        // slower for these long-K tiles.)  Only tiles on or above the diagonal
+        // it.  (Warp-local staging, as in the other products, measured no
+        // better for these long-K tiles.)  Only tiles on or above the diagonal
         // are computed and stored: the readers of A and B take the blocks
         // below it transposed from above.
         const CUtensorMap* mo = &P.map_a;
