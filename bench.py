@@ -153,7 +153,7 @@ class ClockSampler:
 E2E_MIN_STEPS = 60   # host-fed steps timed by the end-to-end leg of the MuonBP workload
 # gradient batches in flight in that leg: step k's copies start once step
 # k - E2E_DEPTH has finished with its buffers.  Three measured slower than two
-# on boxes whose host copies slow down (a larger page-locked footprint)
+# on hosts whose copy-engine transfers stall (a larger page-locked footprint)
 E2E_DEPTH = 2
 
 
@@ -798,9 +798,10 @@ def run_gpu(args, world, rank, local):
     # take turns, so a step's copies (on a copy stream) overlap the kernels of
     # the steps before it; the clock stops once the last read-back has landed.
     torch.cuda.synchronize()
-    # at least 60 steps (about a second): a host-to-device stall of the box
-    # (two copies at 12-19 GB/s, seen on some boxes and not on others) then
-    # weighs in proportion instead of taking a third of a 20-step leg
+    # at least 60 steps (about a second): a periodic host-to-device stall of
+    # the host (copy-engine transfers at 12-19 GB/s for ~180 ms every ~510 ms,
+    # seen on some hosts and not on others) then weighs in proportion instead
+    # of taking a third of a 20-step leg
     e2e_steps = max(E2E_MIN_STEPS, args.steps)
     h2d = sum(g.numel() * g.element_size() for g in grads)
     ngr = max(info["n_block_groups"], info["n_full_groups"])

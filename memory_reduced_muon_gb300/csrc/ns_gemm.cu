@@ -50,7 +50,7 @@ constexpr uint32_t kStageA = 2 * kBox;          // 128 rows (or columns) x 64
 constexpr uint32_t kStageB = 4 * kBox;          // 256 x 64
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 fp32 accumulators
-constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // epilogue staging: half a CTA tile (symmetric steps) or 8 x 4 KB warp boxes
+constexpr uint32_t kStageOutBytes = 128 * 128 * 2;   // epilogue staging: two 64-column steps (Gram) or 8 x 4 KB warp boxes
 constexpr uint32_t kUSlotBytes = 2 * kBox;           // G_UPDATE_W: 128 x 64 output columns of one step
 constexpr uint32_t kWChunkBytes = 128 * 32 * 4;      // G_UPDATE_W: 128 rows x 32 fp32 weights (one TMA box)
 
