@@ -202,3 +202,32 @@ def test_steps_long_k():
     # full steps whose update tiles have K >= 2048 on average: the weight pass
     # with the one-step weight ring and five operand stages (a ragged shape too)
     _run_steps([(2048, 2304), (2100, 2056)], (1, 1), 1, 2, 110)
+
+
+@pytest.mark.parametrize("P,t", [(2, 1), (2, 2)])
+def test_step_results_do_not_depend_on_workspace_contents(P, t):
+    # a block step (t = 1) and a full step (t = 2) with every workspace byte
+    # set to 0xFF (bf16 NaN) before the call give bit-for-bit the outputs of
+    # the same step with a zeroed workspace: nothing reads a byte of the
+    # workspace that the call did not write first (the symmetric matrices'
+    # blocks below the diagonal among them)
+    shapes = [(512, 2048), (1100, 1536), (1024, 512)]
+    tile = (1, 2)
+    out = []
+    for fill in (0x00, 0xFF):
+        mats = [workloads.Matrix(f"m{i}", r, c) for i, (r, c) in enumerate(shapes)]
+        states = [workloads.random_state(m, 120 + i, device="cuda") for i, m in enumerate(mats)]
+        grads = [random_grad(m.numel, "bf16", 130 + i).reshape(m.rows, m.cols) for i, m in enumerate(mats)]
+        weights = [(torch.randn(m.rows, m.cols, device="cuda", generator=torch.Generator("cuda").manual_seed(140 + i))
+                    * 0.02).contiguous() for i, m in enumerate(mats)]
+        plan = q.qmuon_plan_create([(s[0], s[1], g, m.rows, m.cols) for s, g, m in zip(states, grads, mats)],
+                                   "int8", "bf16", tile=tile)
+        ws = torch.full((q.qmuon_workspace_size(plan, q.QMUON_WS_STEP),), fill, dtype=torch.uint8, device="cuda")
+        info = q.qmuon_plan_info(plan)
+        sums = torch.zeros(max(info["n_block_groups"], info["n_full_groups"]), device="cuda")
+        q.qmuon_step(plan, t, P, 0.95, 0.02, 0.01, weights, COEFFS, 5, sums, ws)
+        q.qmuon_sync_status(ws)
+        out.append([x.clone() for s in states for x in s] + [g.clone() for g in grads] +
+                   [w.clone() for w in weights] + [sums.clone()])
+    for a, b in zip(*out):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
