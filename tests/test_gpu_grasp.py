@@ -171,3 +171,26 @@ def test_grasp_rejects_bad_shapes():
     with pytest.raises(q.QmuonError) as e:
         q.qmuon_grasp_step([_desc(d, rows, cols)], 0.9, ws)
     assert e.value.status == q.QMUON_ERR_INVALID_ARGUMENT
+
+
+def test_grasp_step_does_not_depend_on_workspace_contents():
+    # the same warm step with every workspace byte zeroed and then set to 0xFF
+    # (NaN in every float scratch) leaves bit-identical states and M_t: each
+    # scratch value (strip shares, Gram sums, factors) is written before it is read
+    shapes = [(200, 320), (1000, 128), (1024, 2048), (9, 64)]
+    states, grads = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        st = grasp.initial_state(rows, cols, np.random.default_rng(60 + i).standard_normal((cols, 8)).astype(np.float32))
+        states.append(grasp.grasp_step(st, _grad(rows, cols, 80 + i), 0.9).state)
+        grads.append(_grad(rows, cols, 100 + i))
+    outs = []
+    for fill in (0x00, 0xFF):
+        devs = [_to_dev(st, g, *g.shape) for st, g in zip(states, grads)]
+        descs = [_desc(d, *g.shape) for d, g in zip(devs, grads)]
+        ws = torch.full((q.qmuon_grasp_workspace_size(descs),), fill, dtype=torch.uint8, device="cuda")
+        q.qmuon_grasp_step(descs, 0.9, ws)
+        q.qmuon_sync_status(ws)
+        outs.append(devs)
+    for da, db in zip(*outs):
+        for k in da:
+            assert torch.equal(da[k].contiguous().view(torch.uint8), db[k].contiguous().view(torch.uint8)), k
