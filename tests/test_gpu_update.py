@@ -273,3 +273,36 @@ def test_carrier_multi_rejects_unaligned_columns():
     with pytest.raises(q.QmuonError) as e:
         q.qmuon_update_mxfp8_carrier_multi(plan, 0.9, [pay], [sc], inv, ws)
     assert e.value.status == q.QMUON_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("entry", ["update", "carrier"])
+def test_update_and_carrier_do_not_depend_on_workspace_contents(entry):
+    # the same multi-tensor launch with the workspace zeroed and with every
+    # byte 0xFF (NaN partial sums, garbage tables) leaves bit-identical codes,
+    # absmax, momenta or carriers and group sums: each workspace value is
+    # written before it is read
+    shapes = [(64, 4096), (37, 96), (300, 1024), (5, 224), (2048, 300)]
+    if entry == "carrier":
+        shapes = [(r, c) for r, c in shapes if c % 32 == 0]
+    outs = []
+    for fill in (0x00, 0xFF):
+        states = _states(shapes, "int8", 300)
+        grads = [random_grad(r * c, "bf16", 310 + i) for i, (r, c) in enumerate(shapes)]
+        plan = q.qmuon_plan_create([(s, a, g, r, c) for (s, a), g, (r, c) in zip(states, grads, shapes)],
+                                   "int8", "bf16")
+        ws = torch.full((q.qmuon_workspace_size(plan),), fill, dtype=torch.uint8, device="cuda")
+        G = max(q.qmuon_plan_info(plan)["n_groups"], len(shapes))
+        sums = torch.zeros(G, device="cuda")
+        inv = torch.zeros(G, device="cuda")
+        extra = []
+        if entry == "update":
+            q.qmuon_update_multi_normalize_groups(plan, 0.9, 0, sums, inv, ws)
+        else:
+            pays = [torch.empty(r * c, dtype=torch.uint8, device="cuda") for r, c in shapes]
+            scs = [torch.empty(r * (c // 32), dtype=torch.uint8, device="cuda") for r, c in shapes]
+            q.qmuon_update_mxfp8_carrier_multi(plan, 0.9, pays, scs, inv, ws, group_sumsq=sums)
+            extra = pays + scs
+        q.qmuon_sync_status(ws)
+        outs.append([x for s in states for x in s] + grads + extra + [sums, inv])
+    for a, b in zip(*outs):
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
