@@ -781,8 +781,7 @@ extern "C" qmuon_status qmuon_step_from_host(const qmuon_plan* plan, int64_t t, 
   // page-locked, device-addressable, 16-byte aligned whole-vector buffers are
   // pulled by one kernel launch per kPullMax tensors; anything else is copied
   const int sms = plan->host_ingest == QMUON_INGEST_PULL ? sm_count_of_current_device() : 0;
-  HostPull pull;
-  pull.n = 0;
+  HostPull pull{};
   uint64_t pulled = 0, copied = 0;
   auto flush = [&]() -> cudaError_t {
     if (pull.n == 0) return cudaSuccess;
