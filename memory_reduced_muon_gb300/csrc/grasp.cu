@@ -41,12 +41,14 @@ namespace {
 constexpr int kRank = QMUON_GRASP_RANK;   // 8
 constexpr int kS = QMUON_GRASP_BLOCK;     // 64
 constexpr int kThreads = 256;
+constexpr int kNormCols = 1024;   // columns of R_{t-1} per CTA of the column-norm pass
 
 // Device copy of one matrix's description plus its workspace slices.
 struct GraspProb {
   qmuon_grasp_matrix m;
   int64_t nbr, nbc;          // row / column blocks
-  double* qinv;              // [8]         1 / (column norms of R_{t-1}): Q = R_{t-1} diag(qinv)
+  int64_t ncc;               // chunks of kNormCols columns
+  double* qpart;             // [ncc][8]    each chunk's sums of r_jl^2 (R_{t-1}); Q = R_{t-1} diag(1 / norms)
   float* rdeq;               // [cols][8]   R_{t-1} dequantised
   float* y;                  // [rows][8]   M_t Q
   float* p;                  // [rows][8]   P_t
@@ -131,24 +133,16 @@ __device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
-// comp_add on two independent sums at once, with Knuth's TwoSum (additions
-// and subtractions only, so no packed multiply can be fused into them).  The
-// error term it accumulates is the exact rounding error of the addition, the
-// same value comp_add's magnitude-ordered form computes, so the totals are
-// those of two comp_add calls.
+// Compensated (Neumaier) addition of a block's sum into a running total, on
+// two independent sums at once: the strips add up to 224 blocks, and the
+// orthogonalisation magnifies the error of Y when its columns are nearly
+// parallel.  Knuth's TwoSum (additions and subtractions only, so no packed
+// multiply can be fused into them) gives the exact rounding error of each
+// addition, the same value as the magnitude-ordered Fast2Sum.
 __device__ __forceinline__ void two_sum_add2(float2& sum, float2& comp, float2 v) {
   const float2 t = add2_rn(sum, v);
   const float2 bv = sub2_rn(t, sum);
   comp = add2_rn(comp, add2_rn(sub2_rn(sum, sub2_rn(t, bv)), sub2_rn(v, bv)));
-  sum = t;
-}
-
-// Compensated (Neumaier) addition of a block's sum into a running total:
-// the strips add up to 224 blocks, and orth magnifies the error of Y when its
-// columns are nearly parallel.
-__device__ __forceinline__ void comp_add(float& sum, float& c, float v) {
-  const float t = sum + v;
-  c += (fabsf(sum) >= fabsf(v)) ? ((sum - t) + v) : ((v - t) + sum);
   sum = t;
 }
 
@@ -198,13 +192,17 @@ __device__ __forceinline__ void grid_dep_sync() {
 __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
   grid_dep_sync();
   __shared__ double red[kThreads / 32 * kRank];
-  const GraspProb& P = a.probs[blockIdx.x];
+  // CTA (c, k): matrix k's columns c * kNormCols .. + kNormCols
+  const GraspProb& P = a.probs[blockIdx.y];
+  if ((int64_t)blockIdx.x >= P.ncc) return;
   const int64_t cols = P.m.cols;
+  const int64_t j0 = (int64_t)blockIdx.x * kNormCols;
+  const int64_t j1 = cols < j0 + kNormCols ? cols : j0 + kNormCols;
   double ss[kRank] = {0, 0, 0, 0, 0, 0, 0, 0};
   // unrolled so that several rows' loads are in flight at once; the sums
   // still run over j in order
 #pragma unroll 4
-  for (int64_t j = threadIdx.x; j < cols; j += kThreads) {
+  for (int64_t j = j0 + threadIdx.x; j < j1; j += kThreads) {
     float r[kRank];
     factor_row(P.m.r, P.m.r_rmax, P.m.r_cmax, j, r);
     float4* dst = reinterpret_cast<float4*>(P.rdeq + j * kRank);
@@ -214,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) grasp_colnorm(GraspArgs a) {
     for (int l = 0; l < kRank; ++l) ss[l] += (double)r[l] * (double)r[l];
   }
   block_sum8(ss, red);
-  if (threadIdx.x < kRank) P.qinv[threadIdx.x] = ss[threadIdx.x] > 0.0 ? 1.0 / sqrt(ss[threadIdx.x]) : 0.0;
+  if (threadIdx.x < kRank) P.qpart[blockIdx.x * kRank + threadIdx.x] = ss[threadIdx.x];
 }
 
 // The CTA's share of Z^T Z in fp64 (36 lower-triangle entries, row-major
@@ -487,6 +485,14 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
     __syncthreads();   // stage k & 1 is refilled by chunk k + 2's copies
   }
   cp_async_wait<0>();
+  // 1 / (the column norms of R_{t-1}): the chunks' sums, added in chunk order
+  __shared__ double s_qinv[kRank];
+  if (t < kRank) {
+    double v = 0.0;
+    for (int64_t c = 0; c < P.ncc; ++c) v += __ldg(P.qpart + c * kRank + t);
+    s_qinv[t] = v > 0.0 ? 1.0 / sqrt(v) : 0.0;
+  }
+  __syncthreads();
   float y[kRank];
 #pragma unroll
   for (int l2 = 0; l2 < kRank / 2; ++l2) {
@@ -499,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass1(GraspArgs a) {
   for (int l = 0; l < kRank; ++l) {
     y[l] += __shfl_xor_sync(0xffffffffu, y[l], 1);
     y[l] += __shfl_xor_sync(0xffffffffu, y[l], 2);
-    y[l] = (float)((double)y[l] * P.qinv[l]);
+    y[l] = (float)((double)y[l] * s_qinv[l]);
   }
   if ((t & 3) == 0 && live) {
     float4* dst = reinterpret_cast<float4*>(P.y + i * kRank);
@@ -720,8 +726,8 @@ __global__ void __launch_bounds__(kThreads, 2) grasp_pass2(GraspArgs a, const Ws
 #pragma unroll
       for (int l = 0; l < kRank; ++l) ab[l] = fma2(m, make_float2(pr[l], pr[l]), ab[l]);
     }
-    // TwoSum's error term is the exact rounding error of the addition, as
-    // the magnitude-ordered form of comp_add computes it
+    // compensated sums over the chunks (TwoSum's error term is the exact
+    // rounding error of each addition)
 #pragma unroll
     for (int l = 0; l < kRank; ++l) two_sum_add2(acc[l], accc[l], ab[l]);
     __syncthreads();   // the stage is refilled by the next iteration's copies
@@ -943,7 +949,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
   const size_t nbr = (size_t)(m.rows + kS - 1) / kS;
-  return 2 * align_up((size_t)m.cols * kRank * 4, 256) + align_up(kRank * 8, 256) +
+  const size_t ncc = (size_t)(m.cols + kNormCols - 1) / kNormCols;
+  return 2 * align_up((size_t)m.cols * kRank * 4, 256) + align_up(ncc * kRank * 8, 256) +
          2 * align_up((size_t)m.rows * kRank * 4, 256) +
          align_up((size_t)m.rows * kRank * 8, 256) + align_up(nbr * 36 * 8, 256) + align_up(kRank * kRank * 8, 256);
 }
@@ -951,10 +958,10 @@ size_t prob_scratch_bytes(const qmuon_grasp_matrix& m) {
 // A launch that may start while the stream's previous kernel finishes: the
 // kernel itself waits for that kernel (grid_dep_sync) before it reads anything.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_dep(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+cudaError_t launch_dep(void (*kern)(KArgs...), dim3 grid, unsigned block, size_t smem, cudaStream_t s,
                        Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -1032,7 +1039,8 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
         scratch += align_up(bytes, 256);
         return p;
       };
-      P.qinv = reinterpret_cast<double*>(carve(kRank * 8));
+      P.ncc = (P.m.cols + kNormCols - 1) / kNormCols;
+      P.qpart = reinterpret_cast<double*>(carve((size_t)P.ncc * kRank * 8));
       P.rdeq = carve((size_t)P.m.cols * kRank * 4);
       P.y = carve((size_t)P.m.rows * kRank * 4);
       P.p = carve((size_t)P.m.rows * kRank * 4);
@@ -1086,7 +1094,9 @@ extern "C" qmuon_status qmuon_grasp_step(const qmuon_grasp_matrix* matrices, int
     if (attr == cudaSuccess)
       attr = cudaFuncSetAttribute(grasp_pass3, cudaFuncAttributeMaxDynamicSharedMemorySize, kP3Smem);
     if (attr != cudaSuccess) return set_error("qmuon_grasp_step (shared memory attribute)", attr);
-    e = launch_dep(grasp_colnorm, (unsigned)n, kThreads, 0, s, a);
+    int64_t ncc_max = 1;
+    for (int32_t i = 0; i < n; ++i) ncc_max = hp[i].ncc > ncc_max ? hp[i].ncc : ncc_max;
+    e = launch_dep(grasp_colnorm, dim3((unsigned)ncc_max, (unsigned)n), kThreads, 0, s, a);
     if (e == cudaSuccess) e = launch_dep(grasp_pass1, (unsigned)rs[n], kThreads, kP1Smem, s, a);
     if (e == cudaSuccess) e = launch_dep(grasp_chol, (unsigned)n, 64, 0, s, a, hdr);
     if (e == cudaSuccess) e = launch_dep(grasp_tsolve<0>, (unsigned)rs[n], 64, 0, s, a, (const WsHeader*)hdr);
