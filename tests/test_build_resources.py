@@ -5,9 +5,9 @@ The update kernel runs 3 CTAs of 288 threads per SM, so it has at most 72
 registers a thread; the Newton-Schulz kernel runs one CTA of 10 warps per SM
 and is capped at 168.  A spill in their hot loops cost the update kernel a
 quarter of its bandwidth once, so the kernels that carry the bf16 and fp16
-paths and the Newton-Schulz products must not spill at all.  (The
-fp32-gradient update variants spill a little today; they are not on the
-benchmarked path.  GRASP's passes 1 and 3 have spill budgets below.)
+paths, the Newton-Schulz products and the GRASP passes must not spill at
+all.  (The fp32-gradient update variants spill a little today; they are not
+on the benchmarked path.)
 """
 
 import os
